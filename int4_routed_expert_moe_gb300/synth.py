@@ -1,0 +1,146 @@
+"""Seeded synthetic inputs for the routed INT4-expert MoE FFN.
+
+This module only draws random numbers and lays them out in arrays. It holds
+none of the method's arithmetic (no dequantisation, routing, activation or
+combine): both the CPU oracle and the CUDA library consume what it returns.
+
+Storage convention of one expert (the canonical form, consumed unchanged by the
+library's expert block):
+
+* ``qp_gate`` uint8 [I][H/2], ``qp_up`` uint8 [I][H/2], ``qp_down`` uint8 [H][I/2]
+  -- packed 4-bit codes of the weight matrices W_g [I][H], W_u [I][H],
+  W_d [H][I]; byte c of a row holds element 2c in its low nibble and element
+  2c+1 in its high nibble. Uniform random bytes give uniform codes 0..15.
+* ``s_*`` / ``z_*`` float16 [rows][cols/g] -- one scale and one zero point for
+  each run of g consecutive elements along a row (the reduction axis).
+
+Distributions follow the workloads the pages measure (OLMoE-like 64-expert
+top-8 layers, a 512-expert top-10 stack): activations N(0,1) in FP16, router
+logits FP32 (N(0,1), U(0,1), or Zipf-popular via the Gumbel-top-k trick),
+scales U(1e-3, 1e-2) in FP16, zero point 8.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# Workloads. Names say what they are; sizes are the ones each case runs at.
+WORKLOADS = {
+    "tiny_layer": dict(L=1, H=256, I=128, E=8, k=2, g=64, renorm=True, T=4,
+                       logits="normal"),
+    "olmoe_decode": dict(L=16, H=2048, I=1024, E=64, k=8, g=128, renorm=False,
+                         T=1, steps=128, logits="normal"),
+    "olmoe_partial": dict(L=16, H=2048, I=1024, E=64, k=8, g=128, renorm=False,
+                          T=1, steps=128, seqs=12, warm_seqs=1, C=30,
+                          decay=0.9, logits="zipf", alpha=1.0),
+    "olmoe_prefill": dict(L=16, H=2048, I=1024, E=64, k=8, g=128, renorm=False,
+                          T=512, logits="uniform", Ts=2048, Is=4096),
+    "large_fanout": dict(L=48, H=2048, I=512, E=512, k=10, g=128, renorm=True,
+                         T=(1, 16, 256), logits="zipf", alpha=1.1),
+}
+
+BASE_SEED = 20261202
+
+
+def rng_for(*key: int) -> np.random.Generator:
+    """Independent PCG64 stream for a tuple of integer keys."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(
+        [int(v) & 0xFFFFFFFF for v in key])))
+
+
+def expert_arrays(seed: int, layer: int, expert: int, H: int, I: int, g: int,
+                  zero: str = "eight", codes: str = "uniform") -> dict:
+    """Canonical arrays of one expert, seeded by (seed, layer, expert).
+
+    ``zero``: "eight" (z = 8.0), "int" (random integer 0..15) or "frac"
+    (random FP16 in [0, 15]). ``codes``: "uniform" random bytes.
+    """
+    r = rng_for(seed, layer, expert)
+
+    def packed(rows, cols):
+        return r.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+
+    def scales(rows, cols):
+        return r.uniform(1e-3, 1e-2, size=(rows, cols // g)).astype(np.float16)
+
+    def zeros(rows, cols):
+        shape = (rows, cols // g)
+        if zero == "eight":
+            return np.full(shape, 8.0, dtype=np.float16)
+        if zero == "int":
+            return r.integers(0, 16, size=shape).astype(np.float16)
+        if zero == "frac":
+            return r.uniform(0.0, 15.0, size=shape).astype(np.float16)
+        raise ValueError(zero)
+
+    out = {}
+    out["qp_gate"] = packed(I, H)
+    out["qp_up"] = packed(I, H)
+    out["qp_down"] = packed(H, I)
+    out["s_gate"], out["z_gate"] = scales(I, H), zeros(I, H)
+    out["s_up"], out["z_up"] = scales(I, H), zeros(I, H)
+    out["s_down"], out["z_down"] = scales(H, I), zeros(H, I)
+    return out
+
+
+def activations(seed: int, tag: int, T: int, H: int) -> np.ndarray:
+    """x ~ N(0,1) rounded to FP16, shape [T][H]."""
+    return rng_for(seed, 0x7A, tag).standard_normal((T, H)).astype(np.float16)
+
+
+def logits_normal(seed: int, tag: int, T: int, E: int) -> np.ndarray:
+    return rng_for(seed, 0x10, tag).standard_normal((T, E)).astype(np.float32)
+
+
+def logits_uniform(seed: int, tag: int, T: int, E: int) -> np.ndarray:
+    return rng_for(seed, 0x11, tag).uniform(0.0, 1.0, (T, E)).astype(np.float32)
+
+
+def zipf_ranks(seed: int, layer: int, E: int) -> np.ndarray:
+    """Popularity rank (1 = most popular) of every expert of a layer."""
+    perm = rng_for(seed, 0x20, layer).permutation(E)
+    ranks = np.empty(E, dtype=np.int64)
+    ranks[perm] = np.arange(1, E + 1)
+    return ranks
+
+
+def logits_zipf(seed: int, layer: int, tag: int, T: int, E: int,
+                alpha: float) -> np.ndarray:
+    """Logits whose top-k is a draw without replacement with P(e) ~ rank^-alpha.
+
+    l_e = -alpha * ln(rank_e) + G_e with G_e ~ Gumbel(0, 1) (Gumbel-top-k).
+    """
+    ranks = zipf_ranks(seed, layer, E)
+    gum = rng_for(seed, 0x21, layer, tag).gumbel(0.0, 1.0, (T, E))
+    return (-alpha * np.log(ranks)[None, :] + gum).astype(np.float32)
+
+
+def logits_for(wl: dict, seed: int, layer: int, tag: int, T: int) -> np.ndarray:
+    kind = wl["logits"]
+    E = wl["E"]
+    if kind == "normal":
+        return logits_normal(seed, layer * 1_000_003 + tag, T, E)
+    if kind == "uniform":
+        return logits_uniform(seed, layer * 1_000_003 + tag, T, E)
+    if kind == "zipf":
+        return logits_zipf(seed, layer, tag, T, E, wl["alpha"])
+    raise ValueError(kind)
+
+
+def shared_weights(seed: int, H: int, Is: int) -> dict:
+    """FP16 weights of the dense non-routed SwiGLU FFN, scaled to keep O(1) outputs."""
+    r = rng_for(seed, 0x30)
+    wg = (r.standard_normal((Is, H)) / np.sqrt(H)).astype(np.float16)
+    wu = (r.standard_normal((Is, H)) / np.sqrt(H)).astype(np.float16)
+    wd = (r.standard_normal((H, Is)) / np.sqrt(Is)).astype(np.float16)
+    return {"wg": wg, "wu": wu, "wd": wd}
+
+
+def pack_codes(q: np.ndarray) -> np.ndarray:
+    """Pack an explicit code matrix [rows][cols] (values 0..15) into bytes.
+
+    Test helper for hand-made cases: byte c = q[2c] | q[2c+1] << 4. This is the
+    storage convention, not the method.
+    """
+    q = np.asarray(q, dtype=np.uint8)
+    assert q.ndim == 2 and q.shape[1] % 2 == 0 and int(q.max(initial=0)) < 16
+    return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
