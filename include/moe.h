@@ -1,0 +1,264 @@
+/*
+ * int4_routed_expert_moe_gb300 -- C ABI of the routed INT4-expert MoE FFN
+ * for NVIDIA GB300 (sm_103a), one process on one GPU.
+ *
+ * What the library computes (sources are web pages, cited by title/section):
+ *   * "Horizon RunMap -- Prévia Técnica", "02 / A solução" and
+ *     "03 / Arquitetura": the router chooses the experts of each token; the
+ *     expert kernel combines compact expert weights and FP16 scales with FP16
+ *     activations and returns the result to the rest of the model, without
+ *     keeping an expanded expert on the GPU. The non-routed parts run in FP16.
+ *   * same page, "08 / Comportamento do modelo": W4A16 -- routed expert
+ *     weights INT4 with FP16 scales, FP16 activations, conversion inside the
+ *     kernel, FP32 accumulation with explicit rounding points.
+ *   * same page, "03 / Arquitetura", contract resident-qpacked-cache-v1
+ *     (ADR 0009): complete immutable source in host RAM, copies arrive at a
+ *     GPU position and are published as a whole new generation, an evicted
+ *     copy is reused only after its readers retire, capacity is fixed before
+ *     requests and init rejects a profile that is short of it, a failure
+ *     before publish keeps the previous generation.
+ *   * "Desenvolvedor do Strata cria mapa ao vivo de 24 576 especialistas MoE
+ *     em uma GTX 1070": hot experts stay in VRAM; eviction follows an access
+ *     counter whose old accesses lose weight.
+ *   * lucashiago.com.br "local" explainer, etapa 1: every block of weights
+ *     carries a scale and a zero point that rebuild it.
+ *
+ * Conventions for every call:
+ *   * Pointers documented "device" must point to GPU memory of the current
+ *     device; "host" pointers to CPU memory. The caller owns every buffer
+ *     passed in (allocate with any allocator); the library owns only the
+ *     residency handle and the CUDA events inside it.
+ *   * `stream` is a cudaStream_t (NULL = legacy default stream). GPU calls
+ *     only enqueue work on it and return; nothing synchronises the device
+ *     unless stated.
+ *   * Every call returns a moe_status (0 = MOE_OK). No call aborts, throws
+ *     or traps. moe_last_error() gives a thread-local detail string for the
+ *     last failure. An asynchronous CUDA error from earlier work is reported
+ *     by the next call that checks (MOE_ERR_CUDA).
+ *   * FP16 values are passed as their 16-bit patterns (IEEE binary16).
+ *
+ * Expert block (one expert, `moe_expert_block_bytes` bytes, 16-byte aligned
+ * segments, in this order; H = hidden, I = inter, g = group):
+ *   q_gate  uint8 [I][H/2]   codes of W_g [I][H]
+ *   q_up    uint8 [I][H/2]   codes of W_u [I][H]
+ *   q_down  uint8 [H][I/2]   codes of W_d [H][I]
+ *   s_gate  fp16  [I][H/g]   z_gate fp16 [I][H/g]
+ *   s_up    fp16  [I][H/g]   z_up   fp16 [I][H/g]
+ *   s_down  fp16  [H][I/g]   z_down fp16 [H][I/g]
+ * Byte c of a code row holds element 2c in its low nibble and element 2c+1
+ * in its high nibble; codes are unsigned 0..15. The weight is
+ *   W[n][c] = (q[n][c] - z[n][c/g]) * s[n][c/g],
+ * groups running along each row's reduction axis (H for gate/up, I for down).
+ * Bytes per expert = 3*H*I/2 + 3*(H*I/g)*4.
+ * Shape limits: H and I multiples of 64, g a multiple of 32 dividing H and I,
+ * H <= 8192, I <= 8192.
+ */
+#ifndef INT4_ROUTED_EXPERT_MOE_GB300_MOE_H
+#define INT4_ROUTED_EXPERT_MOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,         /* null pointer, bad enum, k > E, ...            */
+  MOE_ERR_SHAPE = -2,       /* shape outside the limits above                */
+  MOE_ERR_CAPACITY = -3,    /* residency capacity or workspace too small     */
+  MOE_ERR_CUDA = -4,        /* a CUDA runtime call failed                    */
+  MOE_ERR_NONFINITE = -5,   /* NaN / +inf router logits (host-side checks)   */
+  MOE_ERR_STATE = -6,       /* handle used in a state that forbids the call  */
+  MOE_ERR_TIMEOUT = -7,     /* a bounded device wait gave up                 */
+  MOE_ERR_INJECTED = -8,    /* failure injected by the residency test hook   */
+  MOE_ERR_UNSUPPORTED = -9  /* valid request this build does not implement   */
+} moe_status;
+
+typedef struct {
+  int32_t hidden; /* H */
+  int32_t inter;  /* I, the expert intermediate size */
+  int32_t group;  /* g, elements per scale/zero group */
+} moe_expert_shape;
+
+/* ---- diagnostics --------------------------------------------------------- */
+const char* moe_status_string(int status);
+/* Thread-local detail of the last failing call on this thread ("" if none). */
+const char* moe_last_error(void);
+/* Library ABI version, currently 1. */
+int moe_version(void);
+
+/* ---- expert block layout (host only) ------------------------------------- */
+/* Bytes of one expert block; 0 if the shape is invalid. */
+size_t moe_expert_block_bytes(const moe_expert_shape* shape);
+/* Byte offsets of the nine segments, in the order listed above. */
+int moe_expert_block_offsets(const moe_expert_shape* shape, size_t offsets_out[9]);
+/* Copy the nine canonical arrays (host) into one block (host). Copies only:
+ * the canonical arrays already have the block's element order. */
+int moe_pack_expert(const moe_expert_shape* shape,
+                    const uint8_t* q_gate, const uint8_t* q_up, const uint8_t* q_down,
+                    const uint16_t* s_gate, const uint16_t* z_gate,
+                    const uint16_t* s_up, const uint16_t* z_up,
+                    const uint16_t* s_down, const uint16_t* z_down,
+                    void* block_out);
+/* Inverse of moe_pack_expert (host -> host). */
+int moe_unpack_expert(const moe_expert_shape* shape, const void* block,
+                      uint8_t* q_gate, uint8_t* q_up, uint8_t* q_down,
+                      uint16_t* s_gate, uint16_t* z_gate,
+                      uint16_t* s_up, uint16_t* z_up,
+                      uint16_t* s_down, uint16_t* z_down);
+
+/* ---- routing --------------------------------------------------------------
+ * "02 / A solução": the router picks the experts of each token.
+ * logits  device fp32 [T][E]  (row-major)
+ * ids     device int32 [T][k] out: experts in (logit desc, index asc) order;
+ *         -0 == +0, so exact ties go to the lower index.
+ * weights device fp32 [T][k] out: p = softmax over all E logits;
+ *         w_j = p[id_j] / sum_j' p[id_j'] if renorm, else p[id_j].
+ * bad_tokens device int32 [1] or NULL: if non-NULL, incremented (atomically)
+ *         once per token whose logits hold NaN or +inf or are all -inf; such a
+ *         token gets ids -1 and weights 0 (moe_expert_forward skips id -1).
+ * Limits: 1 <= k <= E <= 4096, k <= 32, T >= 0 (T = 0 enqueues nothing).
+ */
+int moe_route(const float* logits, int T, int E, int k, int renorm,
+              int32_t* ids, float* weights, int32_t* bad_tokens, void* stream);
+
+/* ---- token sort -----------------------------------------------------------
+ * Groups the (token, choice) pairs p = t*k + j by expert for the grouped
+ * executor ("04 / Resultados": compact experts computed in groups).
+ * ids      device int32 [T][k]; ids outside [0, E) are dropped.
+ * offsets  device int32 [E+1] out: pairs of expert e are [offsets[e], offsets[e+1])
+ * pair_tok device int32 [T*k] out: token of each sorted pair
+ * pair_j   device int32 [T*k] out: choice index j of each sorted pair
+ * Order within an expert: ascending p (stable). Limits: E <= 1024, T*k <= 65536.
+ */
+int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* offsets,
+                   int32_t* pair_tok, int32_t* pair_j, void* stream);
+
+/* ---- routed expert FFN ----------------------------------------------------
+ * y[t] = sum_j w[t][j] * W_d (silu(W_g x_t) * (W_u x_t))  (+ y_shared[t])
+ * with the weights of expert ids[t][j] read from its INT4 block and converted
+ * inside the kernel ("03 / Arquitetura", "08 / Comportamento do modelo").
+ * x         device fp16 [T][H]
+ * ids       device int32 [T][k]; id -1 means "no expert" (contributes 0)
+ * weights   device fp32 [T][k]
+ * pool      device, n_slots expert blocks back to back ([n_slots][block])
+ * slot_of   device int32 [E]: slot of each expert, -1 if not resident
+ * y_shared  device fp16 [T][H] or NULL: added to the routed sum (the separate
+ *           FP16 non-routed path, "03 / Arquitetura")
+ * y         device fp16 [T][H] out (round to nearest even)
+ * workspace device, >= moe_forward_workspace_bytes(...) bytes, 256-aligned.
+ *           Its first 4 bytes are a sticky error word: bit 0 = an id mapped
+ *           to a slot outside [0, n_slots) (that pair contributed 0); bit 1 =
+ *           an id outside [-1, E). Read it with moe_workspace_flags.
+ * path      MOE_PATH_AUTO, MOE_PATH_GEMV (per-pair dequant-GEMV, for decode)
+ *           or MOE_PATH_GROUPED (token-sorted tensor-core grouped GEMM).
+ * Arithmetic: products in FP16 pairs of at most 8 terms, FP32 accumulation,
+ * the SwiGLU intermediate rounded to FP16 before the down projection.
+ */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2 };
+size_t moe_forward_workspace_bytes(const moe_expert_shape* shape, int T, int k,
+                                   int E, int path);
+int moe_expert_forward(const moe_expert_shape* shape, const void* x, int T,
+                       const int32_t* ids, const float* weights, int k, int E,
+                       const void* pool, const int32_t* slot_of, int n_slots,
+                       const void* y_shared, void* y, void* workspace,
+                       size_t workspace_bytes, int path, void* stream);
+/* Clear (zero) the workspace error word: enqueued on `stream`. */
+int moe_workspace_clear_flags(void* workspace, void* stream);
+/* Read the workspace error word into *flags_out: synchronises `stream`. */
+int moe_workspace_flags(const void* workspace, int32_t* flags_out, void* stream);
+
+/* ---- shared (non-routed) FP16 SwiGLU FFN ----------------------------------
+ * y = W_d (silu(W_g x) * (W_u x)) with FP16 weights ("03 / Arquitetura": the
+ * non-routed parts stay FP16).
+ * x  device fp16 [T][H]; wg, wu device fp16 [Is][H]; wd device fp16 [H][Is];
+ * y  device fp16 [T][H] out. workspace >= moe_shared_workspace_bytes(T, H, Is).
+ * Limits: H, Is multiples of 128.
+ */
+size_t moe_shared_workspace_bytes(int T, int H, int Is);
+int moe_shared_forward(const void* x, int T, int H, int Is, const void* wg,
+                       const void* wu, const void* wd, void* y, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* ---- residency manager ----------------------------------------------------
+ * Per-layer GPU slot pools fed from a complete, immutable host source
+ * ("03 / Arquitetura", ADR 0009) with eviction by decayed access counts
+ * (Strata page). One decode step of one layer:
+ *   1. every count c of the layer becomes c*decay, then gains 1 per id given;
+ *   2. N = distinct ids; |N| > slots is MOE_ERR_CAPACITY (nothing changes);
+ *   3. misses N \ resident, in ascending id order; when the resident set is
+ *      full the victim is argmin (count, id) over resident \ N; the miss
+ *      takes the lowest free slot (a spare) else the victim's slot;
+ *   4. each miss is copied host->device with cudaMemcpyAsync on the copy
+ *      stream, after the copy stream waited for every reader of the slot
+ *      enqueued so far on the compute stream;
+ *   5. the compute stream waits for the copies, then a one-block kernel
+ *      publishes the new slot table [E] of the layer (the new generation).
+ * Initial state: expert e in slot e for e < slots ("canonical initial
+ * placement"), counts 0, spare slots free.
+ */
+typedef struct {
+  int32_t layers;            /* L */
+  int32_t experts;           /* E per layer */
+  int32_t slots;             /* C: experts resident per layer (1..E) */
+  int32_t spares;            /* S: extra physical slots per layer (>= 0) */
+  int32_t max_ids_per_step;  /* upper bound on n passed to prepare */
+  int32_t dry_run;           /* 1: decide and trace only, no CUDA work */
+  uint64_t block_bytes;      /* bytes of one expert block */
+  double decay;              /* count decay per step, in (0, 1] */
+} moe_residency_cfg;
+
+typedef struct {
+  uint64_t steps, hits, misses, evictions, copies, h2d_bytes;
+} moe_residency_stats;
+
+typedef struct {
+  int64_t step;    /* prepare() calls made on this layer before this one */
+  int32_t layer;
+  int32_t expert;  /* the miss */
+  int32_t slot;    /* physical slot it was copied into */
+  int32_t victim;  /* evicted expert, -1 if none */
+} moe_residency_event;
+
+typedef struct moe_residency moe_residency;
+
+/* host_src: host [L][E][block_bytes], page-locked (cudaHostAlloc /
+ *   cudaHostRegister), owned by the caller, never written by the library,
+ *   must outlive the handle.
+ * dev_pool: device [L][slots+spares][block_bytes]; dev_slot_of: device
+ *   int32 [L][E]. Both owned by the caller. create() fills the pool with the
+ *   canonical placement and the slot table, synchronously.
+ * compute, copy: cudaStream_t. Capacity errors (slots > E, max_ids_per_step
+ *   distinct experts not fitting) return MOE_ERR_CAPACITY and no handle. */
+int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
+                         void* dev_pool, int32_t* dev_slot_of, void* compute,
+                         void* copy, moe_residency** out);
+/* host_ids: host int32 [n], the ids all tokens of this step need in `layer`
+ * (entries outside [0, E) are rejected with MOE_ERR_ARG, state unchanged). */
+int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, int n);
+/* layer = -1 sums over layers. */
+int moe_residency_get_stats(const moe_residency* r, int layer, moe_residency_stats* out);
+/* Copies up to `cap` events (all layers, in decision order); *n_out = total. */
+int moe_residency_trace(const moe_residency* r, moe_residency_event* buf,
+                        size_t cap, size_t* n_out);
+/* Host copy of the layer's current slot table [E] (what was last published). */
+int moe_residency_slot_table(const moe_residency* r, int layer, int32_t* host_out);
+/* Host copy of the layer's decayed counts [E]. */
+int moe_residency_counts(const moe_residency* r, int layer, double* host_out);
+/* Test hook: the nth copy enqueue from now (0-based) fails with
+ * MOE_ERR_INJECTED before it is issued; -1 disables. On such a failure the
+ * step is not published: counts, slot table and statistics keep their
+ * previous values, except that an expert whose slot was already overwritten
+ * by an earlier copy of the failed step (no spare was free) is marked absent
+ * and that removal is published. */
+int moe_residency_inject_copy_failure(moe_residency* r, int64_t nth_copy);
+/* Waits for the handle's copies, frees its events. NULL is a no-op. */
+void moe_residency_destroy(moe_residency* r);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INT4_ROUTED_EXPERT_MOE_GB300_MOE_H */

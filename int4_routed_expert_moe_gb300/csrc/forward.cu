@@ -1,0 +1,97 @@
+// ABI entry points of the routed expert FFN: argument checks and dispatch
+// between the decode dequant-GEMV kernels and the grouped tensor-core path.
+#include "common.h"
+#include "device.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// Pairs at or below this count take the GEMV path under MOE_PATH_AUTO.
+constexpr int kAutoGemvMaxPairs = 256;
+
+int pick_path(int path, int T, int k) {
+  if (path == MOE_PATH_AUTO) return (T * k <= kAutoGemvMaxPairs) ? MOE_PATH_GEMV : MOE_PATH_GROUPED;
+  return path;
+}
+
+__global__ void publish_kernel(int32_t* slot_of, SlotUpdates u) {
+  const int i = threadIdx.x;
+  if (i < u.n) slot_of[u.expert[i]] = u.slot[i];
+}
+
+}  // namespace
+
+int publish_slot_updates(int32_t* dev_slot_of_layer, const SlotUpdates& u, cudaStream_t st) {
+  if (u.n <= 0) return MOE_OK;
+  publish_kernel<<<1, kMaxSlotUpdates, 0, st>>>(dev_slot_of_layer, u);
+  return check_launch("publish_slot_updates");
+}
+
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_forward_workspace_bytes(const moe_expert_shape* s, int T, int k, int E, int path) {
+  if (!moe::valid_shape(s) || T < 0 || k < 1 || E < 1) return 0;
+  const int p = moe::pick_path(path, T, k);
+  if (p == MOE_PATH_GEMV) return moe::gemv_workspace_bytes(s->hidden, s->inter, T, k);
+  if (p == MOE_PATH_GROUPED) return moe::grouped_workspace_bytes(s->hidden, s->inter, T, k, E);
+  return 0;
+}
+
+int moe_expert_forward(const moe_expert_shape* s, const void* x, int T,
+                       const int32_t* ids, const float* weights, int k, int E,
+                       const void* pool, const int32_t* slot_of, int n_slots,
+                       const void* y_shared, void* y, void* workspace,
+                       size_t workspace_bytes, int path, void* stream) {
+  moe::clear_error();
+  if (!moe::valid_shape(s)) return moe::fail(MOE_ERR_SHAPE, "moe_expert_forward: invalid expert shape");
+  if (T < 0 || k < 1 || k > 32 || E < 1 || E > 4096 || n_slots < 1)
+    return moe::fail(MOE_ERR_ARG, "moe_expert_forward: bad T/k/E/n_slots (%d/%d/%d/%d)", T, k, E, n_slots);
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED)
+    return moe::fail(MOE_ERR_ARG, "moe_expert_forward: unknown path %d", path);
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !weights || !pool || !slot_of || !y || !workspace)
+    return moe::fail(MOE_ERR_ARG, "moe_expert_forward: NULL pointer");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 || reinterpret_cast<uintptr_t>(pool) % 256 ||
+      reinterpret_cast<uintptr_t>(x) % 16)
+    return moe::fail(MOE_ERR_ARG, "moe_expert_forward: workspace/pool must be 256-byte and x 16-byte aligned");
+  const int p = moe::pick_path(path, T, k);
+  const size_t need = moe_forward_workspace_bytes(s, T, k, E, p);
+  if (workspace_bytes < need)
+    return moe::fail(MOE_ERR_CAPACITY, "moe_expert_forward: workspace %zu < %zu bytes", workspace_bytes, need);
+  const moe::BlockLayout bl = moe::block_layout(s->hidden, s->inter, s->group);
+  moe::ForwardArgs a;
+  a.H = s->hidden; a.I = s->inter; a.g = s->group; a.T = T; a.k = k; a.E = E; a.n_slots = n_slots;
+  a.x = static_cast<const __half*>(x);
+  a.ids = ids; a.weights = weights;
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.block_bytes = bl.total;
+  a.off = moe::offsets_of(bl);
+  a.slot_of = slot_of;
+  a.y_shared = static_cast<const __half*>(y_shared);
+  a.y = static_cast<__half*>(y);
+  a.ws = workspace; a.ws_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (p == MOE_PATH_GEMV) return moe::gemv_forward(a);
+  return moe::grouped_forward(a);
+}
+
+int moe_workspace_clear_flags(void* workspace, void* stream) {
+  moe::clear_error();
+  if (!workspace) return moe::fail(MOE_ERR_ARG, "NULL workspace");
+  MOE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_workspace_flags(const void* workspace, int32_t* flags_out, void* stream) {
+  moe::clear_error();
+  if (!workspace || !flags_out) return moe::fail(MOE_ERR_ARG, "NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA_TRY(cudaMemcpyAsync(flags_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA_TRY(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+}  // extern "C"

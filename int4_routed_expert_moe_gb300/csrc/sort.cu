@@ -1,0 +1,134 @@
+// Token sort for the grouped executor: (token, choice) pairs grouped by
+// expert, stable in the pair index p = t*k + j.
+// "Horizon RunMap -- Prévia Técnica", "04 / Resultados": compact experts
+// computed in groups.
+//
+// One block of 32 warps. Warp w owns the contiguous pair segment
+// [w*seg, (w+1)*seg). Pass 1 counts, per warp and expert, the pairs of the
+// segment (warp match instead of atomics). Pass 2 turns the counts into
+// per-warp starting positions (prefix over warps, then an exclusive scan over
+// experts). Pass 3 re-walks each segment in order and scatters; ranks inside a
+// 32-pair chunk come from the match mask, so the order is stable.
+#include "common.h"
+#include "device.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kSortWarps = 32;
+
+__global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
+    const int32_t* __restrict__ ids, int P, int k, int E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ pair_tok, int32_t* __restrict__ pair_j) {
+  extern __shared__ __align__(16) int32_t sm[];
+  int32_t* cnt = sm;                          // [kSortWarps][E]
+  int32_t* total = sm + kSortWarps * E;       // [E + 1]
+  griddep_wait();
+  griddep_launch_dependents();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < kSortWarps * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int seg = (P + kSortWarps - 1) / kSortWarps;
+  const int p0 = warp * seg, p1 = min(P, p0 + seg);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  // Pass 1: per-warp histogram.
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < p1) {
+      e = ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned active = __ballot_sync(0xffffffffu, p < p1);
+    const unsigned peers = __match_any_sync(0xffffffffu, e) & active;
+    if (p < p1 && e >= 0 && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // Pass 2a: per expert, exclusive prefix over warps; totals per expert.
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+    total[e] = run;
+  }
+  __syncthreads();
+  // Pass 2b: exclusive scan of totals over experts (one warp, E <= 1024).
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int v = e < E ? total[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) total[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) total[E] = carry;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) offsets[e] = total[e];
+  // Pass 3: stable scatter.
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < p1) {
+      e = ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned active = __ballot_sync(0xffffffffu, p < p1);
+    const unsigned peers = __match_any_sync(0xffffffffu, e) & active;
+    int pos = 0;
+    if (p < p1 && e >= 0) pos = total[e] + cnt[warp * E + e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (p < p1 && e >= 0) {
+      pair_tok[pos] = p / k;
+      pair_j[pos] = p - (p / k) * k;
+      if ((peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
+                      int32_t* pair_tok, int32_t* pair_j, cudaStream_t st) {
+  const size_t smem = (size_t)(kSortWarps * E + E + 1) * sizeof(int32_t);
+  cudaError_t e = cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort smem attr: %s", cudaGetErrorString(e));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kSortWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, token_sort_kernel, ids, P, k, E, offsets, pair_tok, pair_j);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort launch: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* offsets,
+                              int32_t* pair_tok, int32_t* pair_j, void* stream) {
+  moe::clear_error();
+  if (T < 0 || k < 1 || E < 1 || E > 1024 || (long long)T * k > 65536)
+    return moe::fail(MOE_ERR_ARG, "moe_token_sort: need E <= 1024, T*k <= 65536 (T=%d k=%d E=%d)", T, k, E);
+  if (!ids || !offsets || (T > 0 && (!pair_tok || !pair_j)))
+    return moe::fail(MOE_ERR_ARG, "moe_token_sort: NULL pointer");
+  return moe::launch_token_sort(ids, T * k, k, E, offsets, pair_tok, pair_j,
+                                static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,93 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and its host-only calls (layout, pack/unpack, argument checks) behave."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from int4_routed_expert_moe_gb300 import synth
+from tests._lib import ROOT, binding
+
+moe = binding()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    import ctypes
+    lib = ctypes.CDLL(moe.lib_path())
+    names = header_functions()
+    assert len(names) >= 20
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(names) == set(moe.EXPORTED), set(names) ^ set(moe.EXPORTED)
+
+
+def test_status_strings_and_version():
+    assert moe.moe_version() == 1
+    assert moe.moe_status_string(0) == "MOE_OK"
+    assert moe.moe_status_string(-3) == "MOE_ERR_CAPACITY"
+    assert moe.moe_status_string(-99) == "MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("shape,want", [((256, 128, 64), 55296), ((2048, 1024, 128), 3342336),
+                                         ((2048, 512, 128), 1671168)])
+def test_block_bytes(shape, want):
+    assert moe.moe_expert_block_bytes(shape) == want
+    off = moe.moe_expert_block_offsets(shape)
+    assert off == sorted(off) and all(o % 16 == 0 for o in off)
+
+
+@pytest.mark.parametrize("shape", [(0, 128, 64), (256, 100, 64), (256, 128, 48), (256, 128, 96),
+                                   (16384, 128, 64)])
+def test_invalid_shapes(shape):
+    assert moe.moe_expert_block_bytes(shape) == 0
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_expert_block_offsets(shape)
+    assert ei.value.status == moe.MOE_ERR_SHAPE
+
+
+@pytest.mark.parametrize("zero", ["eight", "int", "frac"])
+def test_pack_unpack_round_trip(zero):
+    H, I, g = 256, 128, 64
+    arrs = synth.expert_arrays(3, 0, 5, H, I, g, zero=zero)
+    # every code value appears, at both nibble positions
+    arrs["qp_gate"][0, :16] = np.arange(16, dtype=np.uint8) * 17
+    blk = moe.moe_pack_expert((H, I, g), arrs)
+    assert blk.nbytes == moe.moe_expert_block_bytes((H, I, g))
+    back = moe.moe_unpack_expert((H, I, g), blk)
+    for n, a in arrs.items():
+        assert np.array_equal(back[n].view(np.uint8), a.view(np.uint8)), n
+    off = moe.moe_expert_block_offsets((H, I, g))
+    assert np.array_equal(blk[off[0]:off[1]].reshape(I, H // 2), arrs["qp_gate"])
+
+
+def test_gpu_entry_points_reject_bad_arguments_before_touching_the_gpu():
+    import ctypes
+    lib = moe._lib
+    # k > E, k = 0, E too large: rejected on the host.
+    assert lib.moe_route(None, 4, 8, 9, 1, None, None, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_route(None, 4, 8, 0, 1, None, None, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_route(None, 4, 5000, 2, 1, None, None, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_route(None, 0, 8, 2, 1, None, None, None, None) == moe.MOE_OK  # T = 0: no-op
+    assert lib.moe_token_sort(None, 4, 2, 2000, None, None, None, None) == moe.MOE_ERR_ARG
+    s = moe.moe_expert_shape(256, 128, 64)
+    bad = moe.moe_expert_shape(256, 100, 64)
+    assert lib.moe_expert_forward(ctypes.byref(bad), None, 1, None, None, 2, 8, None, None, 8,
+                                  None, None, None, 0, 0, None) == moe.MOE_ERR_SHAPE
+    assert lib.moe_expert_forward(ctypes.byref(s), None, 1, None, None, 2, 8, None, None, 8,
+                                  None, None, None, 0, 7, None) == moe.MOE_ERR_ARG
+    assert lib.moe_expert_forward(ctypes.byref(s), None, 0, None, None, 2, 8, None, None, 8,
+                                  None, None, None, 0, 0, None) == moe.MOE_OK
+    assert "path" in moe.moe_last_error() or moe.moe_last_error() == ""
+
+
+def test_workspace_sizes():
+    s = (2048, 1024, 128)
+    assert moe.moe_forward_workspace_bytes(s, 1, 8, 64, moe.MOE_PATH_GEMV) == 256 + 8 * 1024 * 4
+    assert moe.moe_forward_workspace_bytes((2048, 100, 128), 1, 8, 64) == 0

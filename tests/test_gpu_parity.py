@@ -1,0 +1,171 @@
+"""CUDA path vs the CPU oracle, called through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+import torch
+
+from int4_routed_expert_moe_gb300 import synth
+from oracle import moe_oracle
+from tests._lib import binding
+from tests.gpu_util import LayerPool, run_layer, tol_ok
+
+pytestmark = pytest.mark.gpu
+
+moe = binding() if torch.cuda.is_available() else None
+
+
+def _route_gpu(logits, k, renorm):
+    dev = torch.device("cuda")
+    T = logits.shape[0]
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    bad = torch.zeros(1, dtype=torch.int32, device=dev)
+    moe.moe_route(torch.from_numpy(np.ascontiguousarray(logits)).to(dev), k, renorm, ids, w, bad)
+    return ids.cpu().numpy(), w.cpu().numpy(), int(bad.item())
+
+
+@pytest.mark.parametrize("T,E,k,renorm,kind", [
+    (4, 8, 2, True, "normal"), (1, 64, 8, False, "normal"), (512, 64, 8, False, "uniform"),
+    (16, 512, 10, True, "zipf"), (256, 512, 10, True, "zipf"), (3, 64, 64, True, "normal"),
+    (7, 2000, 32, False, "normal"), (33, 100, 5, True, "normal"), (1, 1, 1, True, "normal"),
+])
+def test_route_matches_oracle(T, E, k, renorm, kind):
+    if kind == "zipf":
+        lg = synth.logits_zipf(5, 0, T, T, E, 1.1)
+    elif kind == "uniform":
+        lg = synth.logits_uniform(5, T, T, E)
+    else:
+        lg = synth.logits_normal(5, T * 7 + E, T, E)
+    ids, w, bad = _route_gpu(lg, k, renorm)
+    rids, rw = moe_oracle.route(lg, k, renorm)
+    assert bad == 0
+    assert np.array_equal(ids, rids)
+    assert np.allclose(w, rw, rtol=2e-6, atol=1e-9)
+
+
+def test_route_ties_and_nonfinite():
+    lg = np.array([[1, 3, 3, 2, 3, 0, 0, 0], [0, 0, 0, 0, 0, 0, 0, 0],
+                   [-np.inf, 1, -np.inf, 0, -np.inf, -np.inf, -np.inf, -np.inf],
+                   [-0.0, 0.0, -0.0, 0.0, -1, -1, -1, -1]], dtype=np.float32)
+    for renorm in (True, False):
+        ids, w, bad = _route_gpu(lg, 3, renorm)
+        rids, rw = moe_oracle.route(lg, 3, renorm)
+        assert bad == 0 and np.array_equal(ids, rids)
+        assert np.allclose(w, rw, rtol=2e-6, atol=1e-12)
+    bad_lg = np.array([[0, np.nan, 1, 2], [0, 1, 2, 3], [np.inf, 0, 0, 0],
+                       [-np.inf] * 4], dtype=np.float32)
+    ids, w, bad = _route_gpu(bad_lg, 2, True)
+    assert bad == 3
+    assert ids[0].tolist() == [-1, -1] and ids[2].tolist() == [-1, -1] and ids[3].tolist() == [-1, -1]
+    assert ids[1].tolist() == [3, 2] and np.all(w[0] == 0)
+
+
+@pytest.mark.parametrize("T,k,E", [(4, 2, 8), (512, 8, 64), (256, 10, 512), (1, 8, 64),
+                                   (4096, 16, 1024), (0, 8, 64), (1000, 3, 7)])
+def test_token_sort_matches_oracle(T, k, E):
+    r = np.random.default_rng(T + E)
+    ids = np.stack([r.permutation(E)[:k] for _ in range(T)]).astype(np.int32).reshape(T, k)
+    dev = torch.device("cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    pt = torch.full((max(1, T * k),), -7, dtype=torch.int32, device=dev)
+    pj = torch.full((max(1, T * k),), -7, dtype=torch.int32, device=dev)
+    moe.moe_token_sort(torch.from_numpy(ids).to(dev), E, off, pt, pj)
+    roff, rpt, rpj = moe_oracle.token_sort(ids, E)
+    assert np.array_equal(off.cpu().numpy(), roff)
+    if T:
+        assert np.array_equal(pt.cpu().numpy(), rpt)
+        assert np.array_equal(pj.cpu().numpy(), rpj)
+
+
+def test_token_sort_drops_invalid_ids():
+    ids = np.array([[1, -1], [3, 1], [9, 0]], dtype=np.int32)
+    dev = torch.device("cuda")
+    off = torch.empty(5, dtype=torch.int32, device=dev)
+    pt = torch.full((6,), -7, dtype=torch.int32, device=dev)
+    pj = torch.full((6,), -7, dtype=torch.int32, device=dev)
+    moe.moe_token_sort(torch.from_numpy(ids).to(dev), 4, off, pt, pj)
+    assert off.cpu().tolist() == [0, 1, 3, 3, 4]
+    assert pt.cpu().tolist()[:4] == [2, 0, 1, 1] and pj.cpu().tolist()[:4] == [1, 0, 1, 0]
+
+
+def _layer_case(shape, E, k, renorm, T, seed, zero="eight", path=moe and 1, shared=False,
+                logit_kind="normal"):
+    H, I, g = shape
+    lp = LayerPool(moe, seed, 0, shape, E, zero=zero)
+    x = synth.activations(seed, 1, T, H)
+    if logit_kind == "zipf":
+        lg = synth.logits_zipf(seed, 0, 3, T, E, 1.1)
+    elif logit_kind == "uniform":
+        lg = synth.logits_uniform(seed, 3, T, E)
+    else:
+        lg = synth.logits_normal(seed, 3, T, E)
+    ysh = synth.activations(seed, 2, T, H) if shared else None
+    y, ids, w, flags = run_layer(moe, lp, x, lg, k, renorm, path, y_shared=ysh)
+    ref = moe_oracle.moe_layer(x, lg, lp.arrays, k, renorm, g, y_shared=ysh)
+    assert flags == 0
+    assert np.array_equal(ids, ref["ids"])
+    ok, err, bound = tol_ok(y, ref["y"])
+    assert ok, (err, bound)
+    return y
+
+
+@pytest.mark.parametrize("zero", ["eight", "int", "frac"])
+@pytest.mark.parametrize("shared", [False, True])
+def test_gemv_tiny_layer(zero, shared):
+    _layer_case((256, 128, 64), 8, 2, True, 4, 31, zero=zero, path=1, shared=shared)
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_gemv_olmoe_layer(T):
+    _layer_case((2048, 1024, 128), 64, 8, False, T, 32, path=1)
+
+
+def test_gemv_large_fanout_layer_b16():
+    _layer_case((2048, 512, 128), 512, 10, True, 16, 33, path=1, logit_kind="zipf")
+
+
+@pytest.mark.parametrize("shape,E,k", [((512, 192, 64), 6, 3), ((1088, 320, 32), 5, 2),
+                                       ((8192, 64, 64), 3, 1)])
+def test_gemv_ragged_shapes(shape, E, k):
+    # H not a multiple of 1024 (partial lane loop), I not a multiple of the
+    # 8-row block, the largest H.
+    _layer_case(shape, E, k, False, 2, 34, zero="int", path=1)
+
+
+def test_gemv_deterministic():
+    a = _layer_case((2048, 1024, 128), 64, 8, False, 1, 35, path=1)
+    b = _layer_case((2048, 1024, 128), 64, 8, False, 1, 35, path=1)
+    assert np.array_equal(a, b)
+
+
+def test_gemv_absent_expert_flags_and_skips():
+    shape, E, k, T = (256, 128, 64), 8, 2, 4
+    lp = LayerPool(moe, 36, 0, shape, E)
+    lp.slot_of[3] = -1
+    x = synth.activations(36, 1, T, 256)
+    lg = np.zeros((T, E), np.float32)
+    lg[:, 3] = 5.0
+    lg[:, 1] = 4.0
+    y, ids, w, flags = run_layer(moe, lp, x, lg, k, True, 1)
+    assert flags & 1
+    # expert 3 contributes nothing: y = w1 * o_1
+    ref_ids, ref_w = moe_oracle.route(lg, k, True)
+    wg, wu, wd = moe_oracle.dequantize_expert(lp.arrays(1), 64)
+    for t in range(T):
+        j1 = list(ref_ids[t]).index(1)
+        want = ref_w[t, j1] * moe_oracle.expert_ffn(x[t], wg, wu, wd)
+        ok, err, bound = tol_ok(y[t], want)
+        assert ok, (t, err, bound)
+
+
+def test_gemv_bad_token_contributes_nothing():
+    shape, E, k, T = (256, 128, 64), 8, 2, 3
+    lp = LayerPool(moe, 37, 0, shape, E)
+    x = synth.activations(37, 1, T, 256)
+    lg = synth.logits_normal(37, 3, T, E)
+    lg[1, 4] = np.nan
+    y, ids, w, flags = run_layer(moe, lp, x, lg, k, True, 1)
+    assert flags == 0 and ids[1].tolist() == [-1, -1]
+    assert np.all(y[1] == 0)
+    ref = moe_oracle.moe_layer(x[[0, 2]], lg[[0, 2]], lp.arrays, k, True, 64)
+    ok, err, bound = tol_ok(y[[0, 2]], ref["y"])
+    assert ok

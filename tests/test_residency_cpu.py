@@ -1,0 +1,155 @@
+"""Residency manager decisions (host logic, dry-run mode: no GPU) against the
+oracle's policy model: bit-exact traces, counts, slot tables and statistics."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from int4_routed_expert_moe_gb300 import synth
+from oracle import moe_oracle
+from tests._lib import ROOT, binding
+
+moe = binding()
+
+
+def dry(E, C, S, decay, L=1, max_ids=8):
+    cfg = dict(layers=L, experts=E, slots=C, spares=S, max_ids_per_step=max_ids, dry_run=1,
+               block_bytes=4096, decay=decay)
+    return moe.moe_residency_create(cfg, None, None, None)
+
+
+def test_hand_trace_matches_golden():
+    c = json.load(open(os.path.join(ROOT, "tests", "golden", "residency_hand_trace.json")))
+    h = dry(c["E"], c["C"], c["S"], c["decay"], max_ids=1)
+    try:
+        for ids in c["steps"]:
+            moe.moe_residency_prepare(h, 0, ids)
+        tr = [[s, e, sl, v] for (s, l, e, sl, v) in moe.moe_residency_trace(h)]
+        assert tr == c["trace"]
+        assert moe.moe_residency_counts(h, 0, c["E"]).tolist() == c["counts_after"]
+        assert moe.moe_residency_slot_table(h, 0, c["E"]).tolist() == c["slot_of_after"]
+        st = moe.moe_residency_get_stats(h, 0)
+        assert (st["hits"], st["misses"], st["evictions"]) == (c["hits"], c["misses"], c["evictions"])
+        assert st["h2d_bytes"] == 0  # dry run copies nothing
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+@pytest.mark.parametrize("E,C,S,k,T,decay,alpha", [
+    (64, 30, 0, 8, 1, 0.9, 1.0),     # the OLMoE partial-residency shape
+    (64, 30, 2, 8, 1, 0.9, 1.0),     # with spare slots
+    (64, 40, 0, 8, 4, 0.9, 1.0),     # batched decode
+    (32, 12, 0, 4, 2, 1.0, 0.5),     # decay 1: plain counts
+    (64, 16, 1, 8, 1, 0.5, 0.0),     # uniform popularity
+])
+def test_policy_matches_oracle(E, C, S, k, T, decay, alpha):
+    L, steps = 2, 300
+    h = dry(E, C, S, decay, L=L, max_ids=T * k)
+    try:
+        per_layer = {l: [] for l in range(L)}
+        for step in range(steps):
+            for l in range(L):
+                lg = synth.logits_zipf(9, l, step, T, E, alpha)
+                ids, _ = moe_oracle.route(lg, k, False)
+                flat = ids.reshape(-1).tolist()
+                per_layer[l].append(flat)
+                moe.moe_residency_prepare(h, l, flat)
+        trace = moe.moe_residency_trace(h)
+        for l in range(L):
+            ref = moe_oracle.residency_sim(per_layer[l], E, C, S, decay)
+            got = [(s, e, sl, v) for (s, ll, e, sl, v) in trace if ll == l]
+            assert got == [tuple(t) for t in ref["trace"]]
+            assert moe.moe_residency_counts(h, l, E).tolist() == ref["counts"]  # bit-exact
+            assert moe.moe_residency_slot_table(h, l, E).tolist() == ref["slot_of"]
+            st = moe.moe_residency_get_stats(h, l)
+            assert (st["hits"], st["misses"], st["evictions"]) == (ref["hits"], ref["misses"], ref["evictions"])
+            assert st["steps"] == steps
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+def test_capacity_is_checked_at_init():
+    cfg = dict(layers=1, experts=64, slots=6, spares=0, max_ids_per_step=8, dry_run=1,
+               block_bytes=4096, decay=0.9)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_residency_create(cfg, None, None, None)
+    assert ei.value.status == moe.MOE_ERR_CAPACITY
+    cfg.update(slots=65)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_residency_create(cfg, None, None, None)
+    assert ei.value.status == moe.MOE_ERR_CAPACITY
+    cfg.update(slots=8, decay=0.0)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_residency_create(cfg, None, None, None)
+    assert ei.value.status == moe.MOE_ERR_ARG
+
+
+def test_rejected_steps_change_nothing():
+    h = dry(16, 4, 0, 0.9, max_ids=4)
+    try:
+        moe.moe_residency_prepare(h, 0, [5, 6])
+        before = (moe.moe_residency_counts(h, 0, 16).tolist(), moe.moe_residency_slot_table(h, 0, 16).tolist(),
+                  moe.moe_residency_get_stats(h, 0), moe.moe_residency_trace(h))
+        # More ids than max_ids_per_step, ids out of range: rejected whole.
+        for ids, status in (([1, 2, 3, 7, 9], moe.MOE_ERR_ARG), ([1, 16], moe.MOE_ERR_ARG),
+                            ([-1], moe.MOE_ERR_ARG), (list(range(9)), moe.MOE_ERR_ARG)):
+            with pytest.raises(moe.MoeError) as ei:
+                moe.moe_residency_prepare(h, 0, ids)
+            assert ei.value.status == status
+        after = (moe.moe_residency_counts(h, 0, 16).tolist(), moe.moe_residency_slot_table(h, 0, 16).tolist(),
+                 moe.moe_residency_get_stats(h, 0), moe.moe_residency_trace(h))
+        assert before == after
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prepare(h, 1, [0])  # layer out of range
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+def test_injected_failure_with_spares_keeps_previous_generation():
+    # Copies land in spare slots only, so a failure leaves every published
+    # expert intact: counts, slot table and statistics keep their values.
+    h = dry(16, 4, 4, 0.9, max_ids=4)
+    try:
+        moe.moe_residency_prepare(h, 0, [0, 1])
+        before = (moe.moe_residency_counts(h, 0, 16).tolist(), moe.moe_residency_slot_table(h, 0, 16).tolist(),
+                  moe.moe_residency_get_stats(h, 0))
+        moe.moe_residency_inject_copy_failure(h, 2)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_residency_prepare(h, 0, [8, 9, 10, 11])
+        assert ei.value.status == moe.MOE_ERR_INJECTED
+        after = (moe.moe_residency_counts(h, 0, 16).tolist(), moe.moe_residency_slot_table(h, 0, 16).tolist(),
+                 moe.moe_residency_get_stats(h, 0))
+        assert before == after
+        # The hook fires once; the retried step then succeeds as if fresh.
+        moe.moe_residency_prepare(h, 0, [8, 9, 10, 11])
+        ref = moe_oracle.residency_sim([[0, 1], [8, 9, 10, 11]], 16, 4, 4, 0.9)
+        assert moe.moe_residency_slot_table(h, 0, 16).tolist() == ref["slot_of"]
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+def test_injected_failure_in_place_marks_overwritten_victims_absent():
+    # No spares: the first two copies of the failed step reuse victims' slots
+    # in place; those victims can no longer be served and become absent. The
+    # rest of the previous generation and the counts are kept.
+    h = dry(16, 4, 0, 0.9, max_ids=4)
+    try:
+        before_table = moe.moe_residency_slot_table(h, 0, 16).tolist()  # experts 0..3 in slots 0..3
+        before_counts = moe.moe_residency_counts(h, 0, 16).tolist()
+        moe.moe_residency_inject_copy_failure(h, 2)
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prepare(h, 0, [8, 9, 10])
+        table = moe.moe_residency_slot_table(h, 0, 16).tolist()
+        # misses 8, 9 would have evicted 0 and 1 (lowest (count, id)); their slots were overwritten
+        assert table[0] == -1 and table[1] == -1
+        assert table[2:4] == before_table[2:4] and all(v == -1 for v in table[4:])
+        assert moe.moe_residency_counts(h, 0, 16).tolist() == before_counts
+        assert moe.moe_residency_get_stats(h, 0)["steps"] == 0
+        # The freed slots are used first by the next step.
+        moe.moe_residency_prepare(h, 0, [8, 9, 10])
+        t = moe.moe_residency_slot_table(h, 0, 16)
+        assert sorted(t[t >= 0].tolist()) == [0, 1, 2, 3]
+        assert t[8] >= 0 and t[9] >= 0 and t[10] >= 0
+    finally:
+        moe.moe_residency_destroy(h)
