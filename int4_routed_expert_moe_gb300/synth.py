@@ -144,3 +144,65 @@ def pack_codes(q: np.ndarray) -> np.ndarray:
     q = np.asarray(q, dtype=np.uint8)
     assert q.ndim == 2 and q.shape[1] % 2 == 0 and int(q.max(initial=0)) < 16
     return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+
+
+def block_segments(H: int, I: int, g: int) -> dict:
+    """Byte ranges of the nine arrays inside one expert block, in the order
+    the library's header documents (codes gate/up/down, then scale and zero
+    of gate, up, down). Sizes only; the values are the generator's."""
+    sizes = [("qp_gate", I * H // 2), ("qp_up", I * H // 2), ("qp_down", H * I // 2),
+             ("s_gate", I * (H // g) * 2), ("z_gate", I * (H // g) * 2),
+             ("s_up", I * (H // g) * 2), ("z_up", I * (H // g) * 2),
+             ("s_down", H * (I // g) * 2), ("z_down", H * (I // g) * 2)]
+    out, pos = {}, 0
+    for name, n in sizes:
+        out[name] = (pos, pos + n)
+        pos += n
+    out["total"] = pos
+    return out
+
+
+def device_pool(n_blocks: int, H: int, I: int, g: int, seed: int, device="cuda",
+                chunk: int = 64):
+    """A pool of n_blocks expert blocks generated on the device with torch's
+    CUDA generator (seeded): uniform code bytes, scales U(1e-3, 1e-2) in FP16,
+    zero points 8. Same distributions as expert_arrays; used where host
+    generation of many gigabytes would be too slow."""
+    import torch
+    seg = block_segments(H, I, g)
+    bb = seg["total"]
+    pool = torch.empty((n_blocks, bb), dtype=torch.uint8, device=device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    for b0 in range(0, n_blocks, chunk):
+        b1 = min(n_blocks, b0 + chunk)
+        blk = pool[b0:b1]
+        for name in ("qp_gate", "qp_up", "qp_down"):
+            a, b = seg[name]
+            blk[:, a:b] = torch.randint(0, 256, (b1 - b0, b - a), dtype=torch.uint8,
+                                        device=device, generator=gen)
+        for name in ("s_gate", "s_up", "s_down"):
+            a, b = seg[name]
+            s = torch.empty((b1 - b0, (b - a) // 2), dtype=torch.float32, device=device)
+            s.uniform_(1e-3, 1e-2, generator=gen)
+            blk[:, a:b] = s.to(torch.float16).view(torch.uint8)
+        for name in ("z_gate", "z_up", "z_down"):
+            a, b = seg[name]
+            blk[:, a:b] = torch.full((b1 - b0, (b - a) // 2), 8.0, dtype=torch.float16,
+                                     device=device).view(torch.uint8)
+    return pool
+
+
+def arrays_from_block(block, H: int, I: int, g: int) -> dict:
+    """Canonical arrays of one expert read out of a block's bytes (host numpy)."""
+    seg = block_segments(H, I, g)
+    b = np.asarray(block, dtype=np.uint8)
+    shp = {"qp_gate": (I, H // 2), "qp_up": (I, H // 2), "qp_down": (H, I // 2),
+           "s_gate": (I, H // g), "z_gate": (I, H // g), "s_up": (I, H // g),
+           "z_up": (I, H // g), "s_down": (H, I // g), "z_down": (H, I // g)}
+    out = {}
+    for name, shape in shp.items():
+        lo, hi = seg[name]
+        raw = b[lo:hi]
+        out[name] = raw.reshape(shape) if name.startswith("qp") else raw.view(np.float16).reshape(shape)
+    return out

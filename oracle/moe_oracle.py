@@ -64,11 +64,8 @@ def dequantize(packed: np.ndarray, scale: np.ndarray, zero: np.ndarray,
     s = np.asarray(scale, dtype=np.float64)
     z = np.asarray(zero, dtype=np.float64)
     assert cols % group == 0 and s.shape == (rows, cols // group) == z.shape
-    w = np.empty((rows, cols), dtype=np.float64)
-    for c in range(cols):
-        gi = c // group
-        w[:, c] = (q[:, c] - z[:, gi]) * s[:, gi]
-    return w
+    gi = np.arange(cols) // group  # the group of every column c
+    return (q - z[:, gi]) * s[:, gi]
 
 
 def dequantize_expert(arrs: dict, group: int) -> tuple:
