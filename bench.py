@@ -1,0 +1,489 @@
+"""Benchmark of the routed INT4-expert MoE FFN on GB300.
+
+Default workload: OLMoE-shaped decode -- 16 MoE layers, hidden 2048, 64
+experts per layer, top-8 without renormalisation, expert intermediate 1024,
+SwiGLU, INT4 group 128 with FP16 scale and zero point, one token per step,
+all experts resident. One step = one decode token through all 16 layers:
+per layer route (moe_route) then the routed expert FFN (moe_expert_forward),
+each layer reading the previous layer's output.
+
+Prints one JSON line (rank 0). Metric: MoE-layer decode tokens/s, with the
+expert-weight HBM GB/s and its fraction of the measured copy bandwidth in
+``roofline``. ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle legs run single-threaded; pin BLAS before numpy loads.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from int4_routed_expert_moe_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer decode tokens/s (expert-weight HBM GB/s in roofline)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=128)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="olmoe_decode", choices=["olmoe_decode"])
+    ap.add_argument("--graph-window", type=int, default=128)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples (every 50 ms) with host timestamps."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        self.windows = []
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.strip().split(", ") for r in self.f.read().splitlines() if r.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        import datetime
+        def ts(s):
+            try:
+                return datetime.datetime.strptime(s, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        inside = [r for r in rows if len(r) >= 9 and ts(r[0]) is not None and t0 <= ts(r[0]) <= t1]
+        used = inside if inside else [r for r in rows if len(r) >= 9]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in used if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in used if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(used), "samples_in_timed_region": len(inside)}
+
+
+class ExtEvents:
+    """CUDA events recorded as graph nodes (cudaEventRecordExternal), through
+    the CUDA runtime torch already loaded; used only for timing."""
+
+    def __init__(self, n):
+        import ctypes
+        self.ct = ctypes
+        self.rt = None
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                self.rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.rt is None:
+            raise RuntimeError("libcudart not found")
+        self.ev = []
+        for _ in range(n):
+            e = ctypes.c_void_p()
+            rc = self.rt.cudaEventCreate(ctypes.byref(e))
+            if rc != 0:
+                raise RuntimeError(f"cudaEventCreate: {rc}")
+            self.ev.append(e)
+
+    def record(self, i, stream_handle):
+        rc = self.rt.cudaEventRecordWithFlags(self.ev[i], self.ct.c_void_p(stream_handle), 1)
+        if rc != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags: {rc}")
+
+    def elapsed(self, i, j):
+        f = self.ct.c_float()
+        rc = self.rt.cudaEventElapsedTime(self.ct.byref(f), self.ev[i], self.ev[j])
+        if rc != 0:
+            raise RuntimeError(f"cudaEventElapsedTime: {rc}")
+        return f.value
+
+    def destroy(self):
+        for e in self.ev:
+            self.rt.cudaEventDestroy(e)
+
+
+def smi_index():
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    first = vis.split(",")[0].strip() if vis else ""
+    return first if first.isdigit() else str(torch.cuda.current_device())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return 6800.0, "fallback 6.8 TB/s"
+
+
+# --------------------------------------------------------------------------
+class DecodeWorkload:
+    """The OLMoE-shaped decode stack, resident on the device."""
+
+    def __init__(self, moe, seed, steps_total, rank=0):
+        wl = synth.WORKLOADS["olmoe_decode"]
+        self.moe = moe
+        self.L, self.H, self.I, self.E = wl["L"], wl["H"], wl["I"], wl["E"]
+        self.k, self.g, self.T, self.renorm = wl["k"], wl["g"], wl["T"], wl["renorm"]
+        self.shape = (self.H, self.I, self.g)
+        dev = torch.device("cuda")
+        self.bb = moe.moe_expert_block_bytes(self.shape)
+        assert self.bb == synth.block_segments(*self.shape)["total"]
+        # One pool per layer, expert e in slot e (all resident).
+        self.pool = synth.device_pool(self.L * self.E, self.H, self.I, self.g, seed + rank)
+        self.slot_of = torch.arange(self.E, dtype=torch.int32, device=dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed + 1000 + rank)
+        self.n = steps_total
+        self.x0 = torch.randn((steps_total, self.T, self.H), generator=gen, device=dev).half()
+        self.logits = torch.randn((steps_total, self.L, self.T, self.E), generator=gen, device=dev)
+        self.ids = torch.empty((self.L, self.T, self.k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((self.L, self.T, self.k), dtype=torch.float32, device=dev)
+        self.y = torch.empty((self.L, self.T, self.H), dtype=torch.float16, device=dev)
+        wsb = moe.moe_forward_workspace_bytes(self.shape, self.T, self.k, self.E, moe.MOE_PATH_GEMV)
+        self.ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+
+    def layer_pool(self, l):
+        return self.pool[l * self.E:(l + 1) * self.E]
+
+    def step(self, s, x0=None, logits=None):
+        moe = self.moe
+        for l in range(self.L):
+            lg = self.logits[s, l] if logits is None else logits[l]
+            moe.moe_route(lg, self.k, self.renorm, self.ids[l], self.w[l])
+            x = (self.x0[s] if x0 is None else x0) if l == 0 else self.y[l - 1]
+            moe.moe_expert_forward(self.shape, x, self.ids[l], self.w[l], self.E, self.layer_pool(l),
+                                   self.slot_of, self.E, None, self.y[l], self.ws, moe.MOE_PATH_GEMV)
+
+    def launches_per_step(self):
+        return self.L * 3  # route, gate/up GEMV, down GEMV
+
+    def expert_bytes_per_step(self):
+        # T = 1: the k chosen experts of every layer are read once each.
+        return self.L * self.k * self.bb
+
+
+def run_ours(args, world, rank, local):
+    from int4_routed_expert_moe_gb300 import moe
+    seed = synth.BASE_SEED + 1
+    K, W = args.steps, args.warmup
+    wl = DecodeWorkload(moe, seed, K + W, rank)
+    stream = torch.cuda.current_stream()
+    win = max(1, args.graph_window)
+
+    # Capture windows of `win` steps into CUDA graphs (warm-up windows first).
+    wl.step(0)  # eager pass: sets up kernel attributes before capture
+    torch.cuda.synchronize()
+
+    def capture(s0, s1):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in range(s0, s1):
+                wl.step(s)
+        return g
+
+    warm_graphs = [capture(s, min(W, s + win)) for s in range(0, W, win)]
+    timed_graphs = [capture(s, min(W + K, s + win)) for s in range(W, W + K, win)]
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(smi_index())
+    time.sleep(0.2)
+    for g in warm_graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    ev0.record(stream)
+    for g in timed_graphs:
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world)
+
+    # Dominant unit: the routed expert FFN call of one layer (the gate/up and
+    # down dequant-GEMV kernels). A separate graph of n_kt steps brackets each
+    # call with external event-record nodes on the launching stream; the
+    # average of those durations is the per-launch time of the roofline.
+    n_kt = min(K, 32)
+    ev = ExtEvents(2 * n_kt * wl.L)
+    g_kt = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_kt):
+        st = torch.cuda.current_stream().cuda_stream
+        for i, s in enumerate(range(W, W + n_kt)):
+            for l in range(wl.L):
+                moe.moe_route(wl.logits[s, l], wl.k, wl.renorm, wl.ids[l], wl.w[l])
+                x = wl.x0[s] if l == 0 else wl.y[l - 1]
+                ev.record(2 * (i * wl.L + l), st)
+                moe.moe_expert_forward(wl.shape, x, wl.ids[l], wl.w[l], wl.E, wl.layer_pool(l),
+                                       wl.slot_of, wl.E, None, wl.y[l], wl.ws, moe.MOE_PATH_GEMV)
+                ev.record(2 * (i * wl.L + l) + 1, st)
+    g_kt.replay()
+    torch.cuda.synchronize()
+    fwd_ms = [ev.elapsed(2 * j, 2 * j + 1) for j in range(n_kt * wl.L)]
+    ev.destroy()
+    fwd_avg_s = statistics.mean(fwd_ms) / 1e3
+    rows = sampler.stop()
+    clocks = ClockSampler.summarize(rows, t_host0, t_host1)
+
+    tokens = K * wl.T * world
+    value = tokens / (ms_max / 1e3)
+    bytes_per_launch = wl.k * wl.bb
+    peak, peak_src = measured_peaks()
+    achieved = bytes_per_launch / fwd_avg_s / 1e9
+    step_gbs = wl.expert_bytes_per_step() * K / (ms / 1e3) / 1e9
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; random-init INT4 experts of the OLMoE shape)",
+        "config": {"workload": "olmoe_decode", "layers": wl.L, "hidden": wl.H, "experts": wl.E,
+                   "top_k": wl.k, "inter": wl.I, "group": wl.g, "tokens_per_step": wl.T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "arithmetic": "INT4 weights, FP16 products (<= 8 terms), FP32 accumulation",
+                   "l2": "inputs larger than L2: 427.8 MB of expert weights per step from a 3.42 GB pool",
+                   "launch": f"CUDA graphs of {win} steps, PDL between kernels"},
+        "expert_hbm_gbs_step": round(step_gbs, 1),
+        "expert_hbm_frac_step": round(step_gbs / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "moe_expert_forward (gateup_gemv + down_gemv), one layer",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "bytes_per_launch": bytes_per_launch, "avg_launch_us": round(fwd_avg_s * 1e6, 3),
+                     "peak_source": peak_src,
+                     "timing": f"external event-record graph nodes around each call, "
+                               f"{n_kt} steps x {wl.L} layers, graph replay"},
+        "gpu_launches": wl.launches_per_step() * K,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(moe, wl, min(K, 256), W)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    return out
+
+
+def run_e2e(moe, wl, n, W):
+    """Same metric through the public API with host buffers: per step the
+    token's activations and the 16 layers' router logits are copied from
+    pinned host memory, the 16 layers run, and the output is read back."""
+    x_h = wl.x0[W:W + n].cpu().pin_memory()
+    lg_h = wl.logits[W:W + n].cpu().pin_memory()
+    x_d = torch.empty_like(wl.x0[0])
+    lg_d = torch.empty_like(wl.logits[0])
+    y_h = torch.empty((wl.T, wl.H), dtype=torch.float16).pin_memory()
+    stream = torch.cuda.current_stream()
+    for s in range(min(8, n)):  # warm-up
+        x_d.copy_(x_h[s], non_blocking=True)
+        lg_d.copy_(lg_h[s], non_blocking=True)
+        wl.step(0, x0=x_d, logits=lg_d)
+        y_h.copy_(wl.y[wl.L - 1], non_blocking=True)
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for s in range(n):
+        x_d.copy_(x_h[s], non_blocking=True)
+        lg_d.copy_(lg_h[s], non_blocking=True)
+        wl.step(0, x0=x_d, logits=lg_d)
+        y_h.copy_(wl.y[wl.L - 1], non_blocking=True)
+        stream.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(n * wl.T / dt, 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(x_h[0].numel() * 2 + lg_h[0].numel() * 4),
+            "d2h_bytes_per_step": int(y_h.numel() * 2), "steps": n,
+            "how": "eager moe_route + moe_expert_forward per layer via the binding, "
+                   "pinned H2D of x and logits, D2H of the last layer's y, sync per step"}
+
+
+def oracle_layer_sample(wl, s, l, x16, experts_from_device):
+    from oracle import moe_oracle
+    lg = wl.logits[s, l].cpu().numpy()
+    return moe_oracle.moe_layer(x16, lg, experts_from_device, wl.k, wl.renorm, wl.g)
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The oracle as it stands, on host cores, on a bounded sample: one decode
+    token through as many of the 16 layers as fit in ~budget_s (at least one),
+    fresh N(0,1) activations per layer. Expert arrays are read from the
+    device pool before the clock starts."""
+    from oracle import moe_oracle
+    t_total, layers = 0.0, 0
+    s = 0
+    for l in range(wl.L):
+        lg = wl.logits[s, l].cpu().numpy()
+        ids, _ = moe_oracle.route(lg, wl.k, wl.renorm)
+        pool = wl.layer_pool(l)
+        experts = {int(e): synth.arrays_from_block(pool[int(e)].cpu().numpy(), *wl.shape)
+                   for e in ids.reshape(-1)}
+        x16 = synth.activations(7, l, wl.T, wl.H)
+        t0 = time.perf_counter()
+        moe_oracle.moe_layer(x16, lg, experts, wl.k, wl.renorm, wl.g)
+        t_total += time.perf_counter() - t0
+        layers += 1
+        if t_total >= budget_s:
+            break
+    tokens = wl.T * layers / wl.L
+    return {"value": round(tokens / t_total, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 decode token through {layers} of {wl.L} layers ({layers * wl.k} experts "
+                      f"dequantised in FP64), {t_total:.1f} s single-threaded",
+            "cpu": cpu_model()}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# --------------------------------------------------------------------------
+def run_reference(args):
+    """The CPU oracle on the same workload and metric: each step is a bounded
+    sample -- one routed expert of one (token, layer) pair of the OLMoE decode
+    stack (routing plus FP64 dequantisation and SwiGLU FFN) -- i.e. 1/128 of a
+    decode token. Inputs are the seeded host generator's."""
+    from oracle import moe_oracle
+    wl = synth.WORKLOADS["olmoe_decode"]
+    H, I, E, k, g, L = wl["H"], wl["I"], wl["E"], wl["k"], wl["g"], wl["L"]
+    K, W = args.steps, args.warmup
+    seed = synth.BASE_SEED + 2
+
+    def one(s):
+        lg = synth.logits_normal(seed, s, 1, E)
+        ids, w = moe_oracle.route(lg, k, wl["renorm"])
+        e = int(ids[0, s % k])
+        arrs = synth.expert_arrays(seed, s % L, e, H, I, g)
+        x = synth.activations(seed, s, 1, H)[0]
+        t0 = time.perf_counter()
+        ids, w = moe_oracle.route(lg, k, wl["renorm"])
+        mats = moe_oracle.dequantize_expert(arrs, g)
+        o = w[0, s % k] * moe_oracle.expert_ffn(x, *mats)
+        return time.perf_counter() - t0, o
+
+    for s in range(W):
+        one(s)
+    total = 0.0
+    for s in range(W, W + K):
+        dt, _ = one(s)
+        total += dt
+    frac = 1.0 / (L * k)
+    value = K * frac / total
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": round(total / K * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "olmoe_decode", "layers": L, "hidden": H, "experts": E, "top_k": k,
+                       "inter": I, "group": g, "tokens_per_step": 1},
+            "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step one routed expert of one (token, layer) pair = 1/128 "
+                                       "of a decode token", "cpu": cpu_model()},
+            "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -40,19 +40,52 @@ __device__ __forceinline__ const uint8_t* expert_block(
 }
 
 // Load activations [n] (fp16, global) into shared memory in the pair order
-// of dot8_codes, and their 32-element chunk sums (FP32) into xsum.
+// of dot8_codes, and their 32-element chunk sums (FP32) into xsum. Each
+// thread takes 8 elements (one 16-byte load); the 4 threads of a chunk are
+// adjacent lanes and combine their sums with two shuffles. All threads run
+// the same number of iterations so the shuffles see full warps.
 __device__ __forceinline__ void stage_activations(const __half* __restrict__ src, int n,
                                                   __half* xs, float* xsum) {
-  for (int b = threadIdx.x; b < n / 8; b += blockDim.x) {
-    const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * b);
-    __half a[8];
-    *reinterpret_cast<uint4*>(a) = v;
-    store_perm8(xs + 8 * b, a);
-  }
-  for (int c = threadIdx.x; c < n / 32; c += blockDim.x) {
+  const int nb = n / 8;
+  for (int base = 0; base < nb; base += blockDim.x) {
+    const int b = base + threadIdx.x;
     float s = 0.0f;
-    for (int i = 0; i < 32; ++i) s += __half2float(src[32 * c + i]);
-    xsum[c] = s;
+    if (b < nb) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * b);
+      __half a[8];
+      *reinterpret_cast<uint4*>(a) = v;
+      store_perm8(xs + 8 * b, a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += __half2float(a[i]);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if (b < nb && (b & 3) == 0) xsum[b >> 2] = s;
+  }
+}
+
+// Same for FP32 intermediate values: round to FP16 (the explicit rounding
+// point before the down projection), stage in pair order, and sum the
+// rounded values per 32-element chunk.
+__device__ __forceinline__ void stage_rounded(const float* __restrict__ src, int n,
+                                              __half* xs, float* xsum) {
+  const int nb = n / 8;
+  for (int base = 0; base < nb; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    float s = 0.0f;
+    if (b < nb) {
+      const float4 v0 = *reinterpret_cast<const float4*>(src + 8 * b);
+      const float4 v1 = *reinterpret_cast<const float4*>(src + 8 * b + 4);
+      __half a[8] = {__float2half_rn(v0.x), __float2half_rn(v0.y), __float2half_rn(v0.z),
+                     __float2half_rn(v0.w), __float2half_rn(v1.x), __float2half_rn(v1.y),
+                     __float2half_rn(v1.z), __float2half_rn(v1.w)};
+      store_perm8(xs + 8 * b, a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += __half2float(a[i]);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if (b < nb && (b & 3) == 0) xsum[b >> 2] = s;
   }
 }
 
@@ -142,19 +175,8 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
                                      blockIdx.x == 0 ? flags : nullptr);
     wj[threadIdx.x] = wts[p];
   }
-  // Round h to FP16 in the pair order, then chunk sums of the rounded values.
-  const float* hsrc = hbuf + (size_t)t * k * I;
-  for (int b = threadIdx.x; b < k * I / 8; b += blockDim.x) {
-    __half a[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = __float2half_rn(hsrc[8 * b + i]);
-    store_perm8(hs + 8 * b, a);
-  }
-  for (int c = threadIdx.x; c < k * I / 32; c += blockDim.x) {
-    float s = 0.0f;
-    for (int i = 0; i < 32; ++i) s += __half2float(__float2half_rn(hsrc[32 * c + i]));
-    hsum[c] = s;
-  }
+  // h of the k pairs of token t: [k][I] floats, contiguous.
+  stage_rounded(hbuf + (size_t)t * k * I, k * I, hs, hsum);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * kWarps + warp;

@@ -127,7 +127,7 @@ extern "C" int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* 
   moe::clear_error();
   if (T < 0 || k < 1 || E < 1 || E > 1024 || (long long)T * k > 65536)
     return moe::fail(MOE_ERR_ARG, "moe_token_sort: need E <= 1024, T*k <= 65536 (T=%d k=%d E=%d)", T, k, E);
-  if (!ids || !offsets || (T > 0 && (!pair_tok || !pair_j)))
+  if (!offsets || (T > 0 && (!ids || !pair_tok || !pair_j)))
     return moe::fail(MOE_ERR_ARG, "moe_token_sort: NULL pointer");
   return moe::launch_token_sort(ids, T * k, k, E, offsets, pair_tok, pair_j,
                                 static_cast<cudaStream_t>(stream));

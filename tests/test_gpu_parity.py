@@ -63,7 +63,9 @@ def test_route_ties_and_nonfinite():
                                    (4096, 16, 1024), (0, 8, 64), (1000, 3, 7)])
 def test_token_sort_matches_oracle(T, k, E):
     r = np.random.default_rng(T + E)
-    ids = np.stack([r.permutation(E)[:k] for _ in range(T)]).astype(np.int32).reshape(T, k)
+    ids = np.zeros((T, k), dtype=np.int32)
+    for t in range(T):
+        ids[t] = r.permutation(E)[:k]
     dev = torch.device("cuda")
     off = torch.empty(E + 1, dtype=torch.int32, device=dev)
     pt = torch.full((max(1, T * k),), -7, dtype=torch.int32, device=dev)
@@ -87,7 +89,7 @@ def test_token_sort_drops_invalid_ids():
     assert pt.cpu().tolist()[:4] == [2, 0, 1, 1] and pj.cpu().tolist()[:4] == [1, 0, 1, 0]
 
 
-def _layer_case(shape, E, k, renorm, T, seed, zero="eight", path=moe and 1, shared=False,
+def _layer_case(shape, E, k, renorm, T, seed, zero="eight", path=1, shared=False,
                 logit_kind="normal"):
     H, I, g = shape
     lp = LayerPool(moe, seed, 0, shape, E, zero=zero)
