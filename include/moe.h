@@ -148,16 +148,28 @@ int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* offsets,
  * y_shared  device fp16 [T][H] or NULL: added to the routed sum (the separate
  *           FP16 non-routed path, "03 / Arquitetura")
  * y         device fp16 [T][H] out (round to nearest even)
- * workspace device, >= moe_forward_workspace_bytes(...) bytes, 256-aligned.
+ * workspace device, >= moe_forward_workspace_bytes(...) bytes, 256-aligned,
+ *           zero-filled before its first use (calls leave it reusable: the
+ *           synchronisation counters inside are reset by the call itself).
+ *           Calls sharing a workspace must be ordered (same stream).
  *           Its first 4 bytes are a sticky error word: bit 0 = an id mapped
  *           to a slot outside [0, n_slots) (that pair contributed 0); bit 1 =
- *           an id outside [-1, E). Read it with moe_workspace_flags.
- * path      MOE_PATH_AUTO, MOE_PATH_GEMV (per-pair dequant-GEMV, for decode)
- *           or MOE_PATH_GROUPED (token-sorted tensor-core grouped GEMM).
+ *           an id outside [-1, E); bit 2 = a bounded device wait expired (the
+ *           result is not valid). Read it with moe_workspace_flags.
+ * path      MOE_PATH_AUTO: GEMV up to 256 (token, choice) pairs, else grouped.
+ *           MOE_PATH_GEMV: decode dequant-GEMV. One persistent kernel (one
+ *             block per SM) streams each block's slice of the chosen experts
+ *             through shared memory with bulk async copies, computes gate/up
+ *             rows, publishes h per pair, and runs the down projection and
+ *             the top-k combine as soon as a pair's h is complete. Falls back
+ *             to the unfused kernels when its shared memory does not fit.
+ *           MOE_PATH_GROUPED: token-sorted tensor-core grouped GEMM.
+ *           MOE_PATH_GEMV_UNFUSED: the two-kernel dequant-GEMV (gate/up,
+ *             then down + combine), kept for comparison.
  * Arithmetic: products in FP16 pairs of at most 8 terms, FP32 accumulation,
  * the SwiGLU intermediate rounded to FP16 before the down projection.
  */
-enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2 };
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2, MOE_PATH_GEMV_UNFUSED = 3 };
 size_t moe_forward_workspace_bytes(const moe_expert_shape* shape, int T, int k,
                                    int E, int path);
 int moe_expert_forward(const moe_expert_shape* shape, const void* x, int T,

@@ -1,5 +1,7 @@
 // ABI entry points of the routed expert FFN: argument checks and dispatch
 // between the decode dequant-GEMV kernels and the grouped tensor-core path.
+#include <algorithm>
+
 #include "common.h"
 #include "device.cuh"
 #include "kernels.h"
@@ -13,6 +15,10 @@ constexpr int kAutoGemvMaxPairs = 256;
 int pick_path(int path, int T, int k) {
   if (path == MOE_PATH_AUTO) return (T * k <= kAutoGemvMaxPairs) ? MOE_PATH_GEMV : MOE_PATH_GROUPED;
   return path;
+}
+
+size_t gemv_ws(int H, int I, int T, int k) {
+  return std::max(fused_workspace_bytes(H, I, T, k), gemv_workspace_bytes(H, I, T, k));
 }
 
 __global__ void publish_kernel(int32_t* slot_of, SlotUpdates u) {
@@ -35,7 +41,7 @@ extern "C" {
 size_t moe_forward_workspace_bytes(const moe_expert_shape* s, int T, int k, int E, int path) {
   if (!moe::valid_shape(s) || T < 0 || k < 1 || E < 1) return 0;
   const int p = moe::pick_path(path, T, k);
-  if (p == MOE_PATH_GEMV) return moe::gemv_workspace_bytes(s->hidden, s->inter, T, k);
+  if (p == MOE_PATH_GEMV || p == MOE_PATH_GEMV_UNFUSED) return moe::gemv_ws(s->hidden, s->inter, T, k);
   if (p == MOE_PATH_GROUPED) return moe::grouped_workspace_bytes(s->hidden, s->inter, T, k, E);
   return 0;
 }
@@ -49,7 +55,8 @@ int moe_expert_forward(const moe_expert_shape* s, const void* x, int T,
   if (!moe::valid_shape(s)) return moe::fail(MOE_ERR_SHAPE, "moe_expert_forward: invalid expert shape");
   if (T < 0 || k < 1 || k > 32 || E < 1 || E > 4096 || n_slots < 1)
     return moe::fail(MOE_ERR_ARG, "moe_expert_forward: bad T/k/E/n_slots (%d/%d/%d/%d)", T, k, E, n_slots);
-  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED)
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED &&
+      path != MOE_PATH_GEMV_UNFUSED)
     return moe::fail(MOE_ERR_ARG, "moe_expert_forward: unknown path %d", path);
   if (T == 0) return MOE_OK;
   if (!x || !ids || !weights || !pool || !slot_of || !y || !workspace)
@@ -74,7 +81,13 @@ int moe_expert_forward(const moe_expert_shape* s, const void* x, int T,
   a.y = static_cast<__half*>(y);
   a.ws = workspace; a.ws_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
-  if (p == MOE_PATH_GEMV) return moe::gemv_forward(a);
+  if (p == MOE_PATH_GEMV) {
+    const int rc = moe::fused_forward(a);
+    if (rc != MOE_ERR_UNSUPPORTED) return rc;
+    moe::clear_error();  // shapes beyond the fused kernel's shared memory
+    return moe::gemv_forward(a);
+  }
+  if (p == MOE_PATH_GEMV_UNFUSED) return moe::gemv_forward(a);
   return moe::grouped_forward(a);
 }
 

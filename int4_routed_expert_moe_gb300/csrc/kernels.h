@@ -51,6 +51,10 @@ int gemv_forward(const ForwardArgs& a);
 int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
                       int32_t* pair_tok, int32_t* pair_j, cudaStream_t st);
 
+// Fused one-kernel decode path (persistent, one block per SM).
+size_t fused_workspace_bytes(int H, int I, int T, int k);
+int fused_forward(const ForwardArgs& a);
+
 size_t grouped_workspace_bytes(int H, int I, int T, int k, int E);
 int grouped_forward(const ForwardArgs& a);
 

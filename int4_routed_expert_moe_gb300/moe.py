@@ -28,7 +28,7 @@ MOE_ERR_TIMEOUT = -7
 MOE_ERR_INJECTED = -8
 MOE_ERR_UNSUPPORTED = -9
 
-MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GROUPED = 0, 1, 2
+MOE_PATH_AUTO, MOE_PATH_GEMV, MOE_PATH_GROUPED, MOE_PATH_GEMV_UNFUSED = 0, 1, 2, 3
 
 
 class MoeError(RuntimeError):

@@ -110,33 +110,70 @@ def _layer_case(shape, E, k, renorm, T, seed, zero="eight", path=1, shared=False
     return y
 
 
+GEMV_PATHS = [1, 3]  # fused one-kernel decode, unfused two-kernel decode
+
+
+@pytest.mark.parametrize("path", GEMV_PATHS)
 @pytest.mark.parametrize("zero", ["eight", "int", "frac"])
 @pytest.mark.parametrize("shared", [False, True])
-def test_gemv_tiny_layer(zero, shared):
-    _layer_case((256, 128, 64), 8, 2, True, 4, 31, zero=zero, path=1, shared=shared)
+def test_gemv_tiny_layer(zero, shared, path):
+    _layer_case((256, 128, 64), 8, 2, True, 4, 31, zero=zero, path=path, shared=shared)
 
 
+@pytest.mark.parametrize("path", GEMV_PATHS)
 @pytest.mark.parametrize("T", [1, 3])
-def test_gemv_olmoe_layer(T):
-    _layer_case((2048, 1024, 128), 64, 8, False, T, 32, path=1)
+def test_gemv_olmoe_layer(T, path):
+    _layer_case((2048, 1024, 128), 64, 8, False, T, 32, path=path)
 
 
-def test_gemv_large_fanout_layer_b16():
-    _layer_case((2048, 512, 128), 512, 10, True, 16, 33, path=1, logit_kind="zipf")
+@pytest.mark.parametrize("path", GEMV_PATHS)
+def test_gemv_large_fanout_layer_b16(path):
+    _layer_case((2048, 512, 128), 512, 10, True, 16, 33, path=path, logit_kind="zipf")
 
 
+@pytest.mark.parametrize("path", GEMV_PATHS)
 @pytest.mark.parametrize("shape,E,k", [((512, 192, 64), 6, 3), ((1088, 320, 32), 5, 2),
-                                       ((8192, 64, 64), 3, 1)])
-def test_gemv_ragged_shapes(shape, E, k):
-    # H not a multiple of 1024 (partial lane loop), I not a multiple of the
-    # 8-row block, the largest H.
-    _layer_case(shape, E, k, False, 2, 34, zero="int", path=1)
+                                       ((8192, 64, 64), 3, 1), ((2048, 1024, 128), 64, 8)])
+def test_gemv_ragged_shapes(shape, E, k, path):
+    # H not a multiple of 1024 (partial lane loop), I and H not multiples of
+    # the block count (ragged row slices), scale rows not 16-byte multiples,
+    # the largest H; and 16 tokens x 8 choices = 128 pairs (ring reuse).
+    T = 16 if shape == (2048, 1024, 128) else 2
+    _layer_case(shape, E, k, False, T, 34, zero="int", path=path)
 
 
-def test_gemv_deterministic():
-    a = _layer_case((2048, 1024, 128), 64, 8, False, 1, 35, path=1)
-    b = _layer_case((2048, 1024, 128), 64, 8, False, 1, 35, path=1)
+@pytest.mark.parametrize("path", GEMV_PATHS)
+def test_gemv_deterministic(path):
+    a = _layer_case((2048, 1024, 128), 64, 8, False, 1, 35, path=path)
+    b = _layer_case((2048, 1024, 128), 64, 8, False, 1, 35, path=path)
     assert np.array_equal(a, b)
+
+
+def test_gemv_fused_workspace_reuse_and_agreement():
+    # Several calls on one workspace (the fused kernel resets its counters),
+    # and the fused and unfused kernels agree to FP16 rounding.
+    shape, E, k, T = (2048, 1024, 128), 64, 8, 2
+    lp = LayerPool(moe, 38, 0, shape, E)
+    dev = torch.device("cuda")
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, T, k, E, 1), dtype=torch.uint8, device=dev)
+    outs = []
+    for rep in range(3):
+        x = torch.from_numpy(synth.activations(38, rep, T, 2048)).to(dev)
+        lg = torch.from_numpy(synth.logits_normal(38, rep, T, E)).to(dev)
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        moe.moe_route(lg, k, False, ids, w)
+        ys = []
+        for path in (1, 3):
+            y = torch.empty((T, 2048), dtype=torch.float16, device=dev)
+            moe.moe_expert_forward(shape, x, ids, w, E, lp.pool, lp.slot_of, E, None, y, ws, path)
+            ys.append(y.float().cpu().numpy())
+        assert moe.moe_workspace_flags(ws) == 0
+        ok, err, bound = tol_ok(ys[0], ys[1], rel=2e-3)
+        assert ok, (rep, err, bound)
+        outs.append(ys[0])
+    ws_words = ws[:4096].view(torch.int32).cpu().numpy()
+    assert np.all(ws_words[1:] == 0)  # exit counter and pair counters back to zero
 
 
 def test_gemv_absent_expert_flags_and_skips():
