@@ -208,7 +208,7 @@ class DecodeWorkload:
         self.shape = (self.H, self.I, self.g)
         dev = torch.device("cuda")
         self.bb = moe.moe_expert_block_bytes(self.shape)
-        assert self.bb == synth.block_segments(*self.shape)["total"]
+        assert self.bb == synth.block_layout(*self.shape)["total"]
         # One pool per layer, expert e in slot e (all resident).
         self.pool = synth.device_pool(self.L * self.E, self.H, self.I, self.g, seed + rank)
         self.slot_of = torch.arange(self.E, dtype=torch.int32, device=dev)
@@ -236,7 +236,7 @@ class DecodeWorkload:
                                    self.slot_of, self.E, None, self.y[l], self.ws, moe.MOE_PATH_GEMV)
 
     def launches_per_step(self):
-        return self.L * 3  # route, gate/up GEMV, down GEMV
+        return self.L * 3  # route, decode gate/up kernel, decode down kernel
 
     def expert_bytes_per_step(self):
         # T = 1: the k chosen experts of every layer are read once each.
@@ -285,8 +285,8 @@ def run_ours(args, world, rank, local):
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, world)
 
-    # Dominant unit: the routed expert FFN call of one layer (the gate/up and
-    # down dequant-GEMV kernels). A separate graph of n_kt steps brackets each
+    # Dominant unit: one moe_expert_forward call of the GEMV path (the gate/up
+    # and down streaming kernels, which overlap through PDL). A separate graph of n_kt steps brackets each
     # call with external event-record nodes on the launching stream; the
     # average of those durations is the per-launch time of the roofline.
     n_kt = min(K, 32)
@@ -330,7 +330,7 @@ def run_ours(args, world, rank, local):
                    "launch": f"CUDA graphs of {win} steps, PDL between kernels"},
         "expert_hbm_gbs_step": round(step_gbs, 1),
         "expert_hbm_frac_step": round(step_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "moe_expert_forward (gateup_gemv + down_gemv), one layer",
+        "roofline": {"bound": "hbm", "kernel": "moe_expert_forward GEMV path: decode_gateup_kernel + decode_down_kernel (overlapped via PDL), one layer",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": round(fwd_avg_s * 1e6, 3),

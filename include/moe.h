@@ -37,19 +37,23 @@
  *     by the next call that checks (MOE_ERR_CUDA).
  *   * FP16 values are passed as their 16-bit patterns (IEEE binary16).
  *
- * Expert block (one expert, `moe_expert_block_bytes` bytes, 16-byte aligned
- * segments, in this order; H = hidden, I = inter, g = group):
- *   q_gate  uint8 [I][H/2]   codes of W_g [I][H]
- *   q_up    uint8 [I][H/2]   codes of W_u [I][H]
- *   q_down  uint8 [H][I/2]   codes of W_d [H][I]
- *   s_gate  fp16  [I][H/g]   z_gate fp16 [I][H/g]
- *   s_up    fp16  [I][H/g]   z_up   fp16 [I][H/g]
- *   s_down  fp16  [H][I/g]   z_down fp16 [H][I/g]
- * Byte c of a code row holds element 2c in its low nibble and element 2c+1
- * in its high nibble; codes are unsigned 0..15. The weight is
+ * Expert block (one expert, `moe_expert_block_bytes` bytes; H = hidden,
+ * I = inter, g = group). Two sections of fixed-stride rows, so that the rows
+ * a kernel needs of one expert are one contiguous byte range:
+ *   gate/up section: I rows n, stride gu_row_bytes, each holding
+ *     [codes of W_g row n: H/2 bytes][codes of W_u row n: H/2 bytes]
+ *     [s_gate row n: H/g fp16][z_gate row n][s_up row n][z_up row n]
+ *   down section (at d_offset = I * gu_row_bytes): H rows m, stride
+ *     d_row_bytes, each holding
+ *     [codes of W_d row m: I/2 bytes][s_down row m: I/g fp16][z_down row m]
+ * Strides are the row contents rounded up to 16 bytes (moe_expert_block_layout
+ * gives every offset). Byte c of a code row holds element 2c in its low
+ * nibble and element 2c+1 in its high nibble; codes are unsigned 0..15. The
+ * weight is
  *   W[n][c] = (q[n][c] - z[n][c/g]) * s[n][c/g],
  * groups running along each row's reduction axis (H for gate/up, I for down).
- * Bytes per expert = 3*H*I/2 + 3*(H*I/g)*4.
+ * Without padding (H/g and I/g even) a block holds 3*H*I/2 + 3*(H*I/g)*4
+ * bytes, which is also the byte count every read of one expert moves.
  * Shape limits: H and I multiples of 64, g a multiple of 32 dividing H and I,
  * H <= 8192, I <= 8192.
  */
@@ -90,12 +94,25 @@ const char* moe_last_error(void);
 int moe_version(void);
 
 /* ---- expert block layout (host only) ------------------------------------- */
+typedef struct {
+  uint64_t total;        /* bytes of one expert block */
+  uint64_t d_offset;     /* byte offset of the down section (I * gu_row_bytes) */
+  uint32_t gu_row_bytes; /* stride of the I gate/up rows (multiple of 16) */
+  uint32_t d_row_bytes;  /* stride of the H down rows (multiple of 16) */
+  /* byte offsets inside a gate/up row */
+  uint32_t gu_q_gate, gu_q_up, gu_s_gate, gu_z_gate, gu_s_up, gu_z_up;
+  /* byte offsets inside a down row */
+  uint32_t d_q, d_s, d_z;
+} moe_block_layout;
+
 /* Bytes of one expert block; 0 if the shape is invalid. */
 size_t moe_expert_block_bytes(const moe_expert_shape* shape);
-/* Byte offsets of the nine segments, in the order listed above. */
-int moe_expert_block_offsets(const moe_expert_shape* shape, size_t offsets_out[9]);
-/* Copy the nine canonical arrays (host) into one block (host). Copies only:
- * the canonical arrays already have the block's element order. */
+/* Every offset of the block layout described above. */
+int moe_expert_block_layout(const moe_expert_shape* shape, moe_block_layout* out);
+/* Build one block (host) from the nine canonical arrays (host):
+ * q_gate, q_up uint8 [I][H/2]; q_down uint8 [H][I/2] (packed codes);
+ * s_gate, z_gate, s_up, z_up fp16 [I][H/g]; s_down, z_down fp16 [H][I/g].
+ * Padding bytes are zeroed. */
 int moe_pack_expert(const moe_expert_shape* shape,
                     const uint8_t* q_gate, const uint8_t* q_up, const uint8_t* q_down,
                     const uint16_t* s_gate, const uint16_t* z_gate,

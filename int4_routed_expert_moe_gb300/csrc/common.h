@@ -8,7 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -27,24 +27,31 @@ inline bool valid_shape(const moe_expert_shape* s) {
   return true;
 }
 
+// Expert block layout: gate/up rows [q_gate | q_up | s_gate | z_gate | s_up |
+// z_up] then down rows [q_down | s_down | z_down], strides rounded to 16.
 struct BlockLayout {
-  size_t q_gate, q_up, q_down, s_gate, z_gate, s_up, z_up, s_down, z_down, total;
+  size_t total, d_offset;
+  uint32_t gu_row, d_row;
+  uint32_t gu_q_gate, gu_q_up, gu_s_gate, gu_z_gate, gu_s_up, gu_z_up;
+  uint32_t d_q, d_s, d_z;
 };
 
 inline BlockLayout block_layout(int H, int I, int g) {
   BlockLayout b;
-  const size_t qgu = (size_t)I * H / 2, qd = (size_t)H * I / 2;
-  const size_t sgu = (size_t)I * (H / g) * 2, sd = (size_t)H * (I / g) * 2;
-  b.q_gate = 0;
-  b.q_up = b.q_gate + qgu;
-  b.q_down = b.q_up + qgu;
-  b.s_gate = b.q_down + qd;
-  b.z_gate = b.s_gate + sgu;
-  b.s_up = b.z_gate + sgu;
-  b.z_up = b.s_up + sgu;
-  b.s_down = b.z_up + sgu;
-  b.z_down = b.s_down + sd;
-  b.total = b.z_down + sd;
+  const uint32_t sgu = (uint32_t)(H / g) * 2u, sd = (uint32_t)(I / g) * 2u;
+  b.gu_q_gate = 0;
+  b.gu_q_up = (uint32_t)H / 2;
+  b.gu_s_gate = (uint32_t)H;
+  b.gu_z_gate = b.gu_s_gate + sgu;
+  b.gu_s_up = b.gu_z_gate + sgu;
+  b.gu_z_up = b.gu_s_up + sgu;
+  b.gu_row = (b.gu_z_up + sgu + 15u) & ~15u;
+  b.d_q = 0;
+  b.d_s = (uint32_t)I / 2;
+  b.d_z = b.d_s + sd;
+  b.d_row = (b.d_z + sd + 15u) & ~15u;
+  b.d_offset = (size_t)I * b.gu_row;
+  b.total = b.d_offset + (size_t)H * b.d_row;
   return b;
 }
 

@@ -117,12 +117,13 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
     return;
   }
   const int nch = H / 32;  // 16-byte chunks per row
-  const uint8_t* qg = blk + off.q_gate + (size_t)n * (H / 2);
-  const uint8_t* qu = blk + off.q_up + (size_t)n * (H / 2);
-  const __half* sg = reinterpret_cast<const __half*>(blk + off.s_gate) + (size_t)n * (H / g);
-  const __half* zg = reinterpret_cast<const __half*>(blk + off.z_gate) + (size_t)n * (H / g);
-  const __half* su = reinterpret_cast<const __half*>(blk + off.s_up) + (size_t)n * (H / g);
-  const __half* zu = reinterpret_cast<const __half*>(blk + off.z_up) + (size_t)n * (H / g);
+  const uint8_t* row = blk + (size_t)n * off.gu_row;
+  const uint8_t* qg = row + off.gu_q_gate;
+  const uint8_t* qu = row + off.gu_q_up;
+  const __half* sg = reinterpret_cast<const __half*>(row + off.gu_s_gate);
+  const __half* zg = reinterpret_cast<const __half*>(row + off.gu_z_gate);
+  const __half* su = reinterpret_cast<const __half*>(row + off.gu_s_up);
+  const __half* zu = reinterpret_cast<const __half*>(row + off.gu_z_up);
 
   uint4 wg[NIT], wu[NIT];
 #pragma unroll
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
         if (blk) {
           jj[u] = j;
           cc[u] = c;
-          w[u] = ld_stream_v4(blk + off.q_down + (size_t)m * (I / 2) + 16 * c);
+          w[u] = ld_stream_v4(blk + off.d_offset + (size_t)m * off.d_row + off.d_q + 16 * c);
         }
       }
     }
@@ -207,8 +208,9 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
         const int j = jj[u], c = cc[u];
         const uint8_t* blk = blks[j];
         const int gi = (32 * c) / g;
-        const float s = __half2float(reinterpret_cast<const __half*>(blk + off.s_down)[(size_t)m * (I / g) + gi]);
-        const float z = __half2float(reinterpret_cast<const __half*>(blk + off.z_down)[(size_t)m * (I / g) + gi]);
+        const uint8_t* drow = blk + off.d_offset + (size_t)m * off.d_row;
+        const float s = __half2float(reinterpret_cast<const __half*>(drow + off.d_s)[gi]);
+        const float z = __half2float(reinterpret_cast<const __half*>(drow + off.d_z)[gi]);
         const half2* hp = reinterpret_cast<const half2*>(hs + (size_t)j * I + 32 * c);
         const float d = dot32_codes(w[u], hp);
         acc += wj[j] * (s * (d - z * hsum[j * nch + c]));
@@ -243,12 +245,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 size_t gemv_workspace_bytes(int H, int I, int T, int k) {
   (void)H;
-  return kWorkspaceHeader + (size_t)T * k * I * sizeof(float);
+  return ws_scratch_offset(T * k) + (size_t)T * k * I * sizeof(float);
 }
 
 int gemv_forward(const ForwardArgs& a) {
   const int H = a.H, I = a.I, g = a.g, T = a.T, k = a.k;
-  float* hbuf = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + kWorkspaceHeader);
+  float* hbuf = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + ws_scratch_offset(T * k));
   int32_t* flags = static_cast<int32_t*>(a.ws);
   const size_t smem_a = (size_t)H * 2 + (size_t)(H / 32) * 4;
   const dim3 grid_a((I + kWarps - 1) / kWarps, T * k);

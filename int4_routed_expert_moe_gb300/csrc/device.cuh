@@ -30,14 +30,12 @@ __device__ __forceinline__ half2 u32_as_h2(uint32_t v) {
   return *reinterpret_cast<half2*>(&v);
 }
 
-// Dot product of the eight 4-bit codes of one 32-bit word (code i in bits
-// 4i..4i+3) with eight FP16 activations stored as the pairs
-// xp[0] = (x0, x4), xp[1] = (x1, x5), xp[2] = (x2, x6), xp[3] = (x3, x7).
-// A code q becomes the FP16 value 1024 + q (or 1024 + 16 q for the odd
-// nibbles) by OR-ing it into the exponent pattern of 1024; subtracting 1024
-// (or scaling by 1/16 and subtracting 64) gives q exactly. The four products
-// of each pair lane are summed in FP16 and the pair is widened to FP32.
-__device__ __forceinline__ float dot8_codes(uint32_t w, const half2* xp) {
+// Eight 4-bit codes of one 32-bit word (code i in bits 4i..4i+3) as four
+// FP16 pairs: q[0] = (c0, c4), q[1] = (c1, c5), q[2] = (c2, c6), q[3] = (c3, c7).
+// A code c becomes the FP16 value 1024 + c (or 1024 + 16 c for the odd
+// nibbles) by OR-ing it into the bit pattern of 1024; subtracting 1024 (or
+// scaling by 1/16 and subtracting 64) gives c exactly.
+__device__ __forceinline__ void codes_to_h2(uint32_t w, half2 (&q)[4]) {
   const uint32_t kMagic = 0x64006400u;  // (1024.0, 1024.0) in FP16
   const uint32_t t0 = (w & 0x000F000Fu) | kMagic;
   const uint32_t t1 = (w & 0x00F000F0u) | kMagic;
@@ -47,22 +45,33 @@ __device__ __forceinline__ float dot8_codes(uint32_t w, const half2* xp) {
   const half2 k1024 = __float2half2_rn(1024.0f);
   const half2 k16th = __float2half2_rn(0.0625f);
   const half2 km64 = __float2half2_rn(-64.0f);
-  const half2 q0 = __hsub2(u32_as_h2(t0), k1024);
-  const half2 q1 = __hfma2(u32_as_h2(t1), k16th, km64);
-  const half2 q2 = __hsub2(u32_as_h2(t2), k1024);
-  const half2 q3 = __hfma2(u32_as_h2(t3), k16th, km64);
-  half2 acc = __hmul2(q0, xp[0]);
-  acc = __hfma2(q1, xp[1], acc);
-  acc = __hfma2(q2, xp[2], acc);
-  acc = __hfma2(q3, xp[3], acc);
-  const float2 f = __half22float2(acc);
-  return f.x + f.y;
+  q[0] = __hsub2(u32_as_h2(t0), k1024);
+  q[1] = __hfma2(u32_as_h2(t1), k16th, km64);
+  q[2] = __hsub2(u32_as_h2(t2), k1024);
+  q[3] = __hfma2(u32_as_h2(t3), k16th, km64);
 }
 
-// Dot of 32 codes (16 bytes) with 32 activations pre-permuted in groups of 8.
+// Dot product of the 16 codes of two words with 16 FP16 activations stored
+// as pairs xp[0..7] (pair order of codes_to_h2, word by word). Each FP16
+// lane sums 8 products; the pair is then widened to FP32.
+__device__ __forceinline__ float dot16_codes(uint32_t w0, uint32_t w1, const half2* xp) {
+  half2 q[4];
+  codes_to_h2(w0, q);
+  half2 acc = __hmul2(q[0], xp[0]);
+  acc = __hfma2(q[1], xp[1], acc);
+  acc = __hfma2(q[2], xp[2], acc);
+  acc = __hfma2(q[3], xp[3], acc);
+  codes_to_h2(w1, q);
+  acc = __hfma2(q[0], xp[4], acc);
+  acc = __hfma2(q[1], xp[5], acc);
+  acc = __hfma2(q[2], xp[6], acc);
+  acc = __hfma2(q[3], xp[7], acc);
+  return __low2float(acc) + __high2float(acc);
+}
+
+// Dot of 32 codes (16 bytes) with 32 activations in pair order.
 __device__ __forceinline__ float dot32_codes(const uint4& w, const half2* xp) {
-  return (dot8_codes(w.x, xp) + dot8_codes(w.y, xp + 4)) +
-         (dot8_codes(w.z, xp + 8) + dot8_codes(w.w, xp + 12));
+  return dot16_codes(w.x, w.y, xp) + dot16_codes(w.z, w.w, xp + 8);
 }
 
 // Stores eight activations a[0..7] in the pair order dot8_codes reads.

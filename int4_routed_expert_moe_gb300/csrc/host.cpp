@@ -50,16 +50,62 @@ size_t moe_expert_block_bytes(const moe_expert_shape* s) {
   return moe::block_layout(s->hidden, s->inter, s->group).total;
 }
 
-int moe_expert_block_offsets(const moe_expert_shape* s, size_t off[9]) {
+int moe_expert_block_layout(const moe_expert_shape* s, moe_block_layout* out) {
   moe::clear_error();
-  if (!off) return moe::fail(MOE_ERR_ARG, "offsets_out is NULL");
+  if (!out) return moe::fail(MOE_ERR_ARG, "out is NULL");
   if (!moe::valid_shape(s)) return moe::fail(MOE_ERR_SHAPE, "invalid expert shape");
   const moe::BlockLayout b = moe::block_layout(s->hidden, s->inter, s->group);
-  const size_t v[9] = {b.q_gate, b.q_up, b.q_down, b.s_gate, b.z_gate,
-                       b.s_up, b.z_up, b.s_down, b.z_down};
-  for (int i = 0; i < 9; ++i) off[i] = v[i];
+  out->total = b.total;
+  out->d_offset = b.d_offset;
+  out->gu_row_bytes = b.gu_row;
+  out->d_row_bytes = b.d_row;
+  out->gu_q_gate = b.gu_q_gate;
+  out->gu_q_up = b.gu_q_up;
+  out->gu_s_gate = b.gu_s_gate;
+  out->gu_z_gate = b.gu_z_gate;
+  out->gu_s_up = b.gu_s_up;
+  out->gu_z_up = b.gu_z_up;
+  out->d_q = b.d_q;
+  out->d_s = b.d_s;
+  out->d_z = b.d_z;
   return MOE_OK;
 }
+
+}  // extern "C"
+
+namespace {
+// Direction-agnostic row copy between the canonical arrays and a block.
+template <bool kPack>
+void copy_rows(const moe_expert_shape* s, uint8_t* blk, uint8_t* qg, uint8_t* qu, uint8_t* qd,
+               uint8_t* sg, uint8_t* zg, uint8_t* su, uint8_t* zu, uint8_t* sd, uint8_t* zd) {
+  const int H = s->hidden, I = s->inter, g = s->group;
+  const moe::BlockLayout b = moe::block_layout(H, I, g);
+  const size_t q_gu = (size_t)H / 2, s_gu = (size_t)(H / g) * 2;
+  const size_t q_d = (size_t)I / 2, s_d = (size_t)(I / g) * 2;
+  auto mv = [](uint8_t* blk_part, uint8_t* arr_part, size_t n) {
+    if (kPack) std::memcpy(blk_part, arr_part, n);
+    else std::memcpy(arr_part, blk_part, n);
+  };
+  if (kPack) std::memset(blk, 0, b.total);
+  for (int n = 0; n < I; ++n) {
+    uint8_t* row = blk + (size_t)n * b.gu_row;
+    mv(row + b.gu_q_gate, qg + n * q_gu, q_gu);
+    mv(row + b.gu_q_up, qu + n * q_gu, q_gu);
+    mv(row + b.gu_s_gate, sg + n * s_gu, s_gu);
+    mv(row + b.gu_z_gate, zg + n * s_gu, s_gu);
+    mv(row + b.gu_s_up, su + n * s_gu, s_gu);
+    mv(row + b.gu_z_up, zu + n * s_gu, s_gu);
+  }
+  for (int m = 0; m < H; ++m) {
+    uint8_t* row = blk + b.d_offset + (size_t)m * b.d_row;
+    mv(row + b.d_q, qd + m * q_d, q_d);
+    mv(row + b.d_s, sd + m * s_d, s_d);
+    mv(row + b.d_z, zd + m * s_d, s_d);
+  }
+}
+}  // namespace
+
+extern "C" {
 
 int moe_pack_expert(const moe_expert_shape* s, const uint8_t* q_gate,
                     const uint8_t* q_up, const uint8_t* q_down,
@@ -72,19 +118,9 @@ int moe_pack_expert(const moe_expert_shape* s, const uint8_t* q_gate,
   if (!q_gate || !q_up || !q_down || !s_gate || !z_gate || !s_up || !z_up ||
       !s_down || !z_down || !block_out)
     return moe::fail(MOE_ERR_ARG, "NULL array");
-  const moe::BlockLayout b = moe::block_layout(s->hidden, s->inter, s->group);
-  uint8_t* o = static_cast<uint8_t*>(block_out);
-  const size_t qgu = b.q_up - b.q_gate, qd = b.s_gate - b.q_down;
-  const size_t sgu = b.z_gate - b.s_gate, sd = b.z_down - b.s_down;
-  std::memcpy(o + b.q_gate, q_gate, qgu);
-  std::memcpy(o + b.q_up, q_up, qgu);
-  std::memcpy(o + b.q_down, q_down, qd);
-  std::memcpy(o + b.s_gate, s_gate, sgu);
-  std::memcpy(o + b.z_gate, z_gate, sgu);
-  std::memcpy(o + b.s_up, s_up, sgu);
-  std::memcpy(o + b.z_up, z_up, sgu);
-  std::memcpy(o + b.s_down, s_down, sd);
-  std::memcpy(o + b.z_down, z_down, sd);
+  auto c = [](const void* p) { return const_cast<uint8_t*>(static_cast<const uint8_t*>(p)); };
+  copy_rows<true>(s, static_cast<uint8_t*>(block_out), c(q_gate), c(q_up), c(q_down), c(s_gate),
+                  c(z_gate), c(s_up), c(z_up), c(s_down), c(z_down));
   return MOE_OK;
 }
 
@@ -97,19 +133,9 @@ int moe_unpack_expert(const moe_expert_shape* s, const void* block,
   if (!q_gate || !q_up || !q_down || !s_gate || !z_gate || !s_up || !z_up ||
       !s_down || !z_down || !block)
     return moe::fail(MOE_ERR_ARG, "NULL array");
-  const moe::BlockLayout b = moe::block_layout(s->hidden, s->inter, s->group);
-  const uint8_t* i = static_cast<const uint8_t*>(block);
-  const size_t qgu = b.q_up - b.q_gate, qd = b.s_gate - b.q_down;
-  const size_t sgu = b.z_gate - b.s_gate, sd = b.z_down - b.s_down;
-  std::memcpy(q_gate, i + b.q_gate, qgu);
-  std::memcpy(q_up, i + b.q_up, qgu);
-  std::memcpy(q_down, i + b.q_down, qd);
-  std::memcpy(s_gate, i + b.s_gate, sgu);
-  std::memcpy(z_gate, i + b.z_gate, sgu);
-  std::memcpy(s_up, i + b.s_up, sgu);
-  std::memcpy(z_up, i + b.z_up, sgu);
-  std::memcpy(s_down, i + b.s_down, sd);
-  std::memcpy(z_down, i + b.z_down, sd);
+  auto c = [](void* p) { return static_cast<uint8_t*>(p); };
+  copy_rows<false>(s, const_cast<uint8_t*>(static_cast<const uint8_t*>(block)), q_gate, q_up,
+                   q_down, c(s_gate), c(z_gate), c(s_up), c(z_up), c(s_down), c(z_down));
   return MOE_OK;
 }
 

@@ -11,22 +11,30 @@
 
 namespace moe {
 
-// Byte offsets of the segments inside one expert block (see include/moe.h).
+// Expert block geometry passed to kernels (see include/moe.h).
 struct BlockOffsets {
-  unsigned long long q_gate, q_up, q_down, s_gate, z_gate, s_up, z_up, s_down, z_down;
+  unsigned long long d_offset;  // start of the down section
+  unsigned gu_row, d_row;       // row strides
+  unsigned gu_q_gate, gu_q_up, gu_s_gate, gu_z_gate, gu_s_up, gu_z_up;  // in a gate/up row
+  unsigned d_q, d_s, d_z;       // in a down row
 };
 
 inline BlockOffsets offsets_of(const BlockLayout& b) {
   BlockOffsets o;
-  o.q_gate = b.q_gate; o.q_up = b.q_up; o.q_down = b.q_down;
-  o.s_gate = b.s_gate; o.z_gate = b.z_gate; o.s_up = b.s_up; o.z_up = b.z_up;
-  o.s_down = b.s_down; o.z_down = b.z_down;
+  o.d_offset = b.d_offset;
+  o.gu_row = b.gu_row; o.d_row = b.d_row;
+  o.gu_q_gate = b.gu_q_gate; o.gu_q_up = b.gu_q_up; o.gu_s_gate = b.gu_s_gate;
+  o.gu_z_gate = b.gu_z_gate; o.gu_s_up = b.gu_s_up; o.gu_z_up = b.gu_z_up;
+  o.d_q = b.d_q; o.d_s = b.d_s; o.d_z = b.d_z;
   return o;
 }
 
 // The workspace starts with a 256-byte header; its first int32 is the sticky
-// error word.
+// error word, the second the fused decode kernel's exit counter. Then come the
+// fused kernel's per-pair counters [P] (256-byte rounded); every path keeps
+// its scratch after them, so counters stay zero between calls of any path.
 constexpr size_t kWorkspaceHeader = 256;
+inline size_t ws_scratch_offset(int P) { return kWorkspaceHeader + (((size_t)P * 4 + 255) / 256) * 256; }
 
 struct ForwardArgs {
   int H, I, g, T, k, E, n_slots;

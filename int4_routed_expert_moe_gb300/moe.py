@@ -41,6 +41,13 @@ class moe_expert_shape(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("group", ctypes.c_int32)]
 
 
+class moe_block_layout(ctypes.Structure):
+    _fields_ = [("total", ctypes.c_uint64), ("d_offset", ctypes.c_uint64),
+                ("gu_row_bytes", ctypes.c_uint32), ("d_row_bytes", ctypes.c_uint32)] + [
+        (n, ctypes.c_uint32) for n in ("gu_q_gate", "gu_q_up", "gu_s_gate", "gu_z_gate", "gu_s_up",
+                                        "gu_z_up", "d_q", "d_s", "d_z")]
+
+
 class moe_residency_cfg(ctypes.Structure):
     _fields_ = [("layers", ctypes.c_int32), ("experts", ctypes.c_int32),
                 ("slots", ctypes.c_int32), ("spares", ctypes.c_int32),
@@ -73,7 +80,7 @@ _SIGS = {
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_version": (_I, []),
     "moe_expert_block_bytes": (_SZ, [_SHAPE]),
-    "moe_expert_block_offsets": (_I, [_SHAPE, ctypes.POINTER(_SZ)]),
+    "moe_expert_block_layout": (_I, [_SHAPE, ctypes.POINTER(moe_block_layout)]),
     "moe_pack_expert": (_I, [_SHAPE] + [_P] * 10),
     "moe_unpack_expert": (_I, [_SHAPE] + [_P] * 10),
     "moe_route": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -158,11 +165,11 @@ def moe_expert_block_bytes(shape) -> int:
     return _lib.moe_expert_block_bytes(ctypes.byref(s))
 
 
-def moe_expert_block_offsets(shape) -> list:
+def moe_expert_block_layout(shape) -> dict:
     s = _shape(shape)
-    off = (ctypes.c_size_t * 9)()
-    _check(_lib.moe_expert_block_offsets(ctypes.byref(s), off), "moe_expert_block_offsets")
-    return list(off)
+    out = moe_block_layout()
+    _check(_lib.moe_expert_block_layout(ctypes.byref(s), ctypes.byref(out)), "moe_expert_block_layout")
+    return {n: int(getattr(out, n)) for n, _ in moe_block_layout._fields_}
 
 
 _ARRAY_ORDER = ("qp_gate", "qp_up", "qp_down", "s_gate", "z_gate", "s_up", "z_up",

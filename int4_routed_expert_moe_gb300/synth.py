@@ -146,63 +146,64 @@ def pack_codes(q: np.ndarray) -> np.ndarray:
     return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
 
 
-def block_segments(H: int, I: int, g: int) -> dict:
-    """Byte ranges of the nine arrays inside one expert block, in the order
-    the library's header documents (codes gate/up/down, then scale and zero
-    of gate, up, down). Sizes only; the values are the generator's."""
-    sizes = [("qp_gate", I * H // 2), ("qp_up", I * H // 2), ("qp_down", H * I // 2),
-             ("s_gate", I * (H // g) * 2), ("z_gate", I * (H // g) * 2),
-             ("s_up", I * (H // g) * 2), ("z_up", I * (H // g) * 2),
-             ("s_down", H * (I // g) * 2), ("z_down", H * (I // g) * 2)]
-    out, pos = {}, 0
-    for name, n in sizes:
-        out[name] = (pos, pos + n)
-        pos += n
-    out["total"] = pos
-    return out
+def block_layout(H: int, I: int, g: int) -> dict:
+    """Byte geometry of one expert block as the library's header documents it:
+    gate/up rows [q_gate | q_up | s_gate | z_gate | s_up | z_up] and down rows
+    [q_down | s_down | z_down], each row padded to 16 bytes. Sizes only."""
+    sgu, sd = (H // g) * 2, (I // g) * 2
+    gu = {"qp_gate": (0, H // 2), "qp_up": (H // 2, H), "s_gate": (H, H + sgu),
+          "z_gate": (H + sgu, H + 2 * sgu), "s_up": (H + 2 * sgu, H + 3 * sgu),
+          "z_up": (H + 3 * sgu, H + 4 * sgu)}
+    d = {"qp_down": (0, I // 2), "s_down": (I // 2, I // 2 + sd), "z_down": (I // 2 + sd, I // 2 + 2 * sd)}
+    gu_row = (H + 4 * sgu + 15) // 16 * 16
+    d_row = (I // 2 + 2 * sd + 15) // 16 * 16
+    return {"gu": gu, "d": d, "gu_row": gu_row, "d_row": d_row, "d_offset": I * gu_row,
+            "total": I * gu_row + H * d_row}
 
 
 def device_pool(n_blocks: int, H: int, I: int, g: int, seed: int, device="cuda",
                 chunk: int = 64):
     """A pool of n_blocks expert blocks generated on the device with torch's
     CUDA generator (seeded): uniform code bytes, scales U(1e-3, 1e-2) in FP16,
-    zero points 8. Same distributions as expert_arrays; used where host
-    generation of many gigabytes would be too slow."""
+    zero points 8, padding 0. Same distributions as expert_arrays; used where
+    host generation of many gigabytes would be too slow."""
     import torch
-    seg = block_segments(H, I, g)
-    bb = seg["total"]
-    pool = torch.empty((n_blocks, bb), dtype=torch.uint8, device=device)
+    lay = block_layout(H, I, g)
+    bb = lay["total"]
+    pool = torch.zeros((n_blocks, bb), dtype=torch.uint8, device=device)
     gen = torch.Generator(device=device)
     gen.manual_seed(int(seed))
     for b0 in range(0, n_blocks, chunk):
         b1 = min(n_blocks, b0 + chunk)
+        n = b1 - b0
         blk = pool[b0:b1]
-        for name in ("qp_gate", "qp_up", "qp_down"):
-            a, b = seg[name]
-            blk[:, a:b] = torch.randint(0, 256, (b1 - b0, b - a), dtype=torch.uint8,
-                                        device=device, generator=gen)
-        for name in ("s_gate", "s_up", "s_down"):
-            a, b = seg[name]
-            s = torch.empty((b1 - b0, (b - a) // 2), dtype=torch.float32, device=device)
-            s.uniform_(1e-3, 1e-2, generator=gen)
-            blk[:, a:b] = s.to(torch.float16).view(torch.uint8)
-        for name in ("z_gate", "z_up", "z_down"):
-            a, b = seg[name]
-            blk[:, a:b] = torch.full((b1 - b0, (b - a) // 2), 8.0, dtype=torch.float16,
-                                     device=device).view(torch.uint8)
+        sections = ((blk[:, :lay["d_offset"]].view(n, I, lay["gu_row"]), lay["gu"]),
+                    (blk[:, lay["d_offset"]:].view(n, H, lay["d_row"]), lay["d"]))
+        for view, fields in sections:
+            for name, (lo, hi) in fields.items():
+                rows = view.shape[1]
+                if name.startswith("qp"):
+                    view[:, :, lo:hi] = torch.randint(0, 256, (n, rows, hi - lo), dtype=torch.uint8,
+                                                      device=device, generator=gen)
+                elif name.startswith("s"):
+                    v = torch.empty((n, rows, (hi - lo) // 2), dtype=torch.float32, device=device)
+                    v.uniform_(1e-3, 1e-2, generator=gen)
+                    view[:, :, lo:hi] = v.to(torch.float16).view(torch.uint8)
+                else:
+                    view[:, :, lo:hi] = torch.full((n, rows, (hi - lo) // 2), 8.0, dtype=torch.float16,
+                                                   device=device).view(torch.uint8)
     return pool
 
 
 def arrays_from_block(block, H: int, I: int, g: int) -> dict:
     """Canonical arrays of one expert read out of a block's bytes (host numpy)."""
-    seg = block_segments(H, I, g)
+    lay = block_layout(H, I, g)
     b = np.asarray(block, dtype=np.uint8)
-    shp = {"qp_gate": (I, H // 2), "qp_up": (I, H // 2), "qp_down": (H, I // 2),
-           "s_gate": (I, H // g), "z_gate": (I, H // g), "s_up": (I, H // g),
-           "z_up": (I, H // g), "s_down": (H, I // g), "z_down": (H, I // g)}
+    gu = b[:lay["d_offset"]].reshape(I, lay["gu_row"])
+    d = b[lay["d_offset"]:lay["total"]].reshape(H, lay["d_row"])
     out = {}
-    for name, shape in shp.items():
-        lo, hi = seg[name]
-        raw = b[lo:hi]
-        out[name] = raw.reshape(shape) if name.startswith("qp") else raw.view(np.float16).reshape(shape)
+    for view, fields in ((gu, lay["gu"]), (d, lay["d"])):
+        for name, (lo, hi) in fields.items():
+            part = np.ascontiguousarray(view[:, lo:hi])
+            out[name] = part if name.startswith("qp") else part.view(np.float16)
     return out

@@ -35,12 +35,21 @@ def test_status_strings_and_version():
     assert moe.moe_status_string(-99) == "MOE_ERR_UNKNOWN"
 
 
-@pytest.mark.parametrize("shape,want", [((256, 128, 64), 55296), ((2048, 1024, 128), 3342336),
-                                         ((2048, 512, 128), 1671168)])
-def test_block_bytes(shape, want):
+@pytest.mark.parametrize("shape,want", [((256, 128, 64), 57344), ((2048, 1024, 128), 3342336),
+                                         ((2048, 512, 128), 1671168), ((192, 64, 64), 64 * 224 + 192 * 48)])
+def test_block_layout(shape, want):
+    # Unpadded shapes hold exactly 3*H*I/2 + 3*(H*I/g)*4 bytes; rows whose
+    # contents are not a 16-byte multiple are padded (tiny: down rows 72 -> 80).
+    H, I, g = shape
     assert moe.moe_expert_block_bytes(shape) == want
-    off = moe.moe_expert_block_offsets(shape)
-    assert off == sorted(off) and all(o % 16 == 0 for o in off)
+    lay = moe.moe_expert_block_layout(shape)
+    assert lay["total"] == want and lay["d_offset"] == I * lay["gu_row_bytes"]
+    assert lay["gu_row_bytes"] % 16 == 0 and lay["d_row_bytes"] % 16 == 0
+    assert lay["gu_q_up"] == H // 2 and lay["gu_s_gate"] == H and lay["d_s"] == I // 2
+    assert lay["gu_z_up"] + 2 * (H // g) <= lay["gu_row_bytes"]
+    assert lay["d_z"] + 2 * (I // g) <= lay["d_row_bytes"]
+    syn = synth.block_layout(H, I, g)
+    assert (syn["gu_row"], syn["d_row"], syn["total"]) == (lay["gu_row_bytes"], lay["d_row_bytes"], want)
 
 
 @pytest.mark.parametrize("shape", [(0, 128, 64), (256, 100, 64), (256, 128, 48), (256, 128, 96),
@@ -48,7 +57,7 @@ def test_block_bytes(shape, want):
 def test_invalid_shapes(shape):
     assert moe.moe_expert_block_bytes(shape) == 0
     with pytest.raises(moe.MoeError) as ei:
-        moe.moe_expert_block_offsets(shape)
+        moe.moe_expert_block_layout(shape)
     assert ei.value.status == moe.MOE_ERR_SHAPE
 
 
@@ -63,8 +72,14 @@ def test_pack_unpack_round_trip(zero):
     back = moe.moe_unpack_expert((H, I, g), blk)
     for n, a in arrs.items():
         assert np.array_equal(back[n].view(np.uint8), a.view(np.uint8)), n
-    off = moe.moe_expert_block_offsets((H, I, g))
-    assert np.array_equal(blk[off[0]:off[1]].reshape(I, H // 2), arrs["qp_gate"])
+    lay = moe.moe_expert_block_layout((H, I, g))
+    gu = blk[:lay["d_offset"]].reshape(I, lay["gu_row_bytes"])
+    assert np.array_equal(gu[:, :H // 2], arrs["qp_gate"])
+    assert np.array_equal(gu[:, H // 2:H], arrs["qp_up"])
+    # the generator's reader of block bytes agrees with the library's packer
+    back2 = synth.arrays_from_block(blk, H, I, g)
+    for n, a in arrs.items():
+        assert np.array_equal(back2[n].view(np.uint8), a.view(np.uint8)), n
 
 
 def test_gpu_entry_points_reject_bad_arguments_before_touching_the_gpu():
@@ -89,5 +104,5 @@ def test_gpu_entry_points_reject_bad_arguments_before_touching_the_gpu():
 
 def test_workspace_sizes():
     s = (2048, 1024, 128)
-    assert moe.moe_forward_workspace_bytes(s, 1, 8, 64, moe.MOE_PATH_GEMV) == 256 + 8 * 1024 * 4
+    assert moe.moe_forward_workspace_bytes(s, 1, 8, 64, moe.MOE_PATH_GEMV) == 512 + 8 * 1024 * 4
     assert moe.moe_forward_workspace_bytes((2048, 100, 128), 1, 8, 64) == 0

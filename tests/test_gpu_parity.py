@@ -172,8 +172,8 @@ def test_gemv_fused_workspace_reuse_and_agreement():
         ok, err, bound = tol_ok(ys[0], ys[1], rel=2e-3)
         assert ok, (rep, err, bound)
         outs.append(ys[0])
-    ws_words = ws[:4096].view(torch.int32).cpu().numpy()
-    assert np.all(ws_words[1:] == 0)  # exit counter and pair counters back to zero
+    ws_words = ws[:1024].view(torch.int32).cpu().numpy()
+    assert ws_words[1] == 0 and np.all(ws_words[64:64 + T * k] == 0)  # counters back to zero
 
 
 def test_gemv_absent_expert_flags_and_skips():
