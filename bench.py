@@ -230,13 +230,13 @@ class DecodeWorkload:
         moe = self.moe
         for l in range(self.L):
             lg = self.logits[s, l] if logits is None else logits[l]
-            moe.moe_route(lg, self.k, self.renorm, self.ids[l], self.w[l])
             x = (self.x0[s] if x0 is None else x0) if l == 0 else self.y[l - 1]
-            moe.moe_expert_forward(self.shape, x, self.ids[l], self.w[l], self.E, self.layer_pool(l),
-                                   self.slot_of, self.E, None, self.y[l], self.ws, moe.MOE_PATH_GEMV)
+            moe.moe_layer_forward(self.shape, x, lg, self.k, self.renorm, self.ids[l], self.w[l],
+                                  self.layer_pool(l), self.slot_of, self.E, None, self.y[l], self.ws,
+                                  moe.MOE_PATH_GEMV)
 
     def launches_per_step(self):
-        return self.L * 3  # route, decode gate/up kernel, decode down kernel
+        return self.L * 2  # decode gate/up kernel (routing inside), decode down kernel
 
     def expert_bytes_per_step(self):
         # T = 1: the k chosen experts of every layer are read once each.
@@ -285,7 +285,7 @@ def run_ours(args, world, rank, local):
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, world)
 
-    # Dominant unit: one moe_expert_forward call of the GEMV path (the gate/up
+    # Dominant unit: one moe_layer_forward call of the GEMV path (the gate/up
     # and down streaming kernels, which overlap through PDL). A separate graph of n_kt steps brackets each
     # call with external event-record nodes on the launching stream; the
     # average of those durations is the per-launch time of the roofline.
@@ -296,11 +296,11 @@ def run_ours(args, world, rank, local):
         st = torch.cuda.current_stream().cuda_stream
         for i, s in enumerate(range(W, W + n_kt)):
             for l in range(wl.L):
-                moe.moe_route(wl.logits[s, l], wl.k, wl.renorm, wl.ids[l], wl.w[l])
                 x = wl.x0[s] if l == 0 else wl.y[l - 1]
                 ev.record(2 * (i * wl.L + l), st)
-                moe.moe_expert_forward(wl.shape, x, wl.ids[l], wl.w[l], wl.E, wl.layer_pool(l),
-                                       wl.slot_of, wl.E, None, wl.y[l], wl.ws, moe.MOE_PATH_GEMV)
+                moe.moe_layer_forward(wl.shape, x, wl.logits[s, l], wl.k, wl.renorm, wl.ids[l], wl.w[l],
+                                      wl.layer_pool(l), wl.slot_of, wl.E, None, wl.y[l], wl.ws,
+                                      moe.MOE_PATH_GEMV)
                 ev.record(2 * (i * wl.L + l) + 1, st)
     g_kt.replay()
     torch.cuda.synchronize()
@@ -330,7 +330,7 @@ def run_ours(args, world, rank, local):
                    "launch": f"CUDA graphs of {win} steps, PDL between kernels"},
         "expert_hbm_gbs_step": round(step_gbs, 1),
         "expert_hbm_frac_step": round(step_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "moe_expert_forward GEMV path: decode_gateup_kernel + decode_down_kernel (overlapped via PDL), one layer",
+        "roofline": {"bound": "hbm", "kernel": "moe_layer_forward GEMV path: decode_gateup_kernel (routing inside) + decode_down_kernel (overlapped via PDL), one layer",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": round(fwd_avg_s * 1e6, 3),
@@ -374,7 +374,7 @@ def run_e2e(moe, wl, n, W):
     return {"value": round(n * wl.T / dt, 2), "unit": "tokens/s",
             "h2d_bytes_per_step": int(x_h[0].numel() * 2 + lg_h[0].numel() * 4),
             "d2h_bytes_per_step": int(y_h.numel() * 2), "steps": n,
-            "how": "eager moe_route + moe_expert_forward per layer via the binding, "
+            "how": "eager moe_layer_forward per layer via the binding, "
                    "pinned H2D of x and logits, D2H of the last layer's y, sync per step"}
 
 

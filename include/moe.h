@@ -42,10 +42,10 @@
  * a kernel needs of one expert are one contiguous byte range:
  *   gate/up section: I rows n, stride gu_row_bytes, each holding
  *     [codes of W_g row n: H/2 bytes][codes of W_u row n: H/2 bytes]
- *     [s_gate row n: H/g fp16][z_gate row n][s_up row n][z_up row n]
+ *     [H/g quads of fp16 (s_gate, z_gate, s_up, z_up), one per group]
  *   down section (at d_offset = I * gu_row_bytes): H rows m, stride
  *     d_row_bytes, each holding
- *     [codes of W_d row m: I/2 bytes][s_down row m: I/g fp16][z_down row m]
+ *     [codes of W_d row m: I/2 bytes][I/g pairs of fp16 (s_down, z_down)]
  * Strides are the row contents rounded up to 16 bytes (moe_expert_block_layout
  * gives every offset). Byte c of a code row holds element 2c in its low
  * nibble and element 2c+1 in its high nibble; codes are unsigned 0..15. The
@@ -99,10 +99,10 @@ typedef struct {
   uint64_t d_offset;     /* byte offset of the down section (I * gu_row_bytes) */
   uint32_t gu_row_bytes; /* stride of the I gate/up rows (multiple of 16) */
   uint32_t d_row_bytes;  /* stride of the H down rows (multiple of 16) */
-  /* byte offsets inside a gate/up row */
-  uint32_t gu_q_gate, gu_q_up, gu_s_gate, gu_z_gate, gu_s_up, gu_z_up;
-  /* byte offsets inside a down row */
-  uint32_t d_q, d_s, d_z;
+  /* byte offsets inside a gate/up row: codes, then the scale/zero quads */
+  uint32_t gu_q_gate, gu_q_up, gu_sz;
+  /* byte offsets inside a down row: codes, then the scale/zero pairs */
+  uint32_t d_q, d_sz;
 } moe_block_layout;
 
 /* Bytes of one expert block; 0 if the shape is invalid. */
@@ -194,6 +194,22 @@ int moe_expert_forward(const moe_expert_shape* shape, const void* x, int T,
                        const void* pool, const int32_t* slot_of, int n_slots,
                        const void* y_shared, void* y, void* workspace,
                        size_t workspace_bytes, int path, void* stream);
+/* ---- routed layer: routing + expert FFN in one call ----------------------
+ * The same result as moe_route(logits, ...) followed by
+ * moe_expert_forward(...): the router picks each token's experts and their
+ * weights ("02 / A solução") and the chosen INT4 experts run on x. On the
+ * GEMV path, when T * E * E <= 262144, the routing runs inside the expert
+ * kernels (every block ranks the logits itself, fixed-order reductions), so
+ * no separate routing kernel or id round trip sits between the layer's input
+ * and its weight stream; otherwise moe_route runs first.
+ * logits  device fp32 [T][E]; ids / weights device out [T][k] (the routing
+ * used, as moe_route defines it: NaN/+inf/all -inf tokens get ids -1).
+ * Other arguments as moe_expert_forward; limits as moe_route.
+ */
+int moe_layer_forward(const moe_expert_shape* shape, const void* x, const float* logits, int T,
+                      int E, int k, int renorm, int32_t* ids, float* weights, const void* pool,
+                      const int32_t* slot_of, int n_slots, const void* y_shared, void* y,
+                      void* workspace, size_t workspace_bytes, int path, void* stream);
 /* Clear (zero) the workspace error word: enqueued on `stream`. */
 int moe_workspace_clear_flags(void* workspace, void* stream);
 /* Read the workspace error word into *flags_out: synchronises `stream`. */

@@ -27,29 +27,25 @@ inline bool valid_shape(const moe_expert_shape* s) {
   return true;
 }
 
-// Expert block layout: gate/up rows [q_gate | q_up | s_gate | z_gate | s_up |
-// z_up] then down rows [q_down | s_down | z_down], strides rounded to 16.
+// Expert block layout: gate/up rows [q_gate | q_up | per-group quads
+// (s_gate, z_gate, s_up, z_up)] then down rows [q_down | per-group pairs
+// (s_down, z_down)], row strides rounded up to 16 bytes.
 struct BlockLayout {
   size_t total, d_offset;
   uint32_t gu_row, d_row;
-  uint32_t gu_q_gate, gu_q_up, gu_s_gate, gu_z_gate, gu_s_up, gu_z_up;
-  uint32_t d_q, d_s, d_z;
+  uint32_t gu_q_gate, gu_q_up, gu_sz;
+  uint32_t d_q, d_sz;
 };
 
 inline BlockLayout block_layout(int H, int I, int g) {
   BlockLayout b;
-  const uint32_t sgu = (uint32_t)(H / g) * 2u, sd = (uint32_t)(I / g) * 2u;
   b.gu_q_gate = 0;
   b.gu_q_up = (uint32_t)H / 2;
-  b.gu_s_gate = (uint32_t)H;
-  b.gu_z_gate = b.gu_s_gate + sgu;
-  b.gu_s_up = b.gu_z_gate + sgu;
-  b.gu_z_up = b.gu_s_up + sgu;
-  b.gu_row = (b.gu_z_up + sgu + 15u) & ~15u;
+  b.gu_sz = (uint32_t)H;
+  b.gu_row = (b.gu_sz + (uint32_t)(H / g) * 8u + 15u) & ~15u;
   b.d_q = 0;
-  b.d_s = (uint32_t)I / 2;
-  b.d_z = b.d_s + sd;
-  b.d_row = (b.d_z + sd + 15u) & ~15u;
+  b.d_sz = (uint32_t)I / 2;
+  b.d_row = (b.d_sz + (uint32_t)(I / g) * 4u + 15u) & ~15u;
   b.d_offset = (size_t)I * b.gu_row;
   b.total = b.d_offset + (size_t)H * b.d_row;
   return b;

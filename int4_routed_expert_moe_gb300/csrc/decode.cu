@@ -120,10 +120,7 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
   const uint8_t* row = blk + (size_t)n * off.gu_row;
   const uint8_t* qg = row + off.gu_q_gate;
   const uint8_t* qu = row + off.gu_q_up;
-  const __half* sg = reinterpret_cast<const __half*>(row + off.gu_s_gate);
-  const __half* zg = reinterpret_cast<const __half*>(row + off.gu_z_gate);
-  const __half* su = reinterpret_cast<const __half*>(row + off.gu_s_up);
-  const __half* zu = reinterpret_cast<const __half*>(row + off.gu_z_up);
+  const __half* sz = reinterpret_cast<const __half*>(row + off.gu_sz);  // quads per group
 
   uint4 wg[NIT], wu[NIT];
 #pragma unroll
@@ -144,8 +141,8 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
       const float du = dot32_codes(wu[it], xp);
       const int gi = (32 * c) / g;
       const float xsm = xsum[c];
-      ag += __half2float(sg[gi]) * (dg - __half2float(zg[gi]) * xsm);
-      au += __half2float(su[gi]) * (du - __half2float(zu[gi]) * xsm);
+      ag += __half2float(sz[4 * gi + 0]) * (dg - __half2float(sz[4 * gi + 1]) * xsm);
+      au += __half2float(sz[4 * gi + 2]) * (du - __half2float(sz[4 * gi + 3]) * xsm);
     }
   }
   ag = warp_sum(ag);
@@ -209,8 +206,9 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
         const uint8_t* blk = blks[j];
         const int gi = (32 * c) / g;
         const uint8_t* drow = blk + off.d_offset + (size_t)m * off.d_row;
-        const float s = __half2float(reinterpret_cast<const __half*>(drow + off.d_s)[gi]);
-        const float z = __half2float(reinterpret_cast<const __half*>(drow + off.d_z)[gi]);
+        const __half* dsz = reinterpret_cast<const __half*>(drow + off.d_sz);
+        const float s = __half2float(dsz[2 * gi]);
+        const float z = __half2float(dsz[2 * gi + 1]);
         const half2* hp = reinterpret_cast<const half2*>(hs + (size_t)j * I + 32 * c);
         const float d = dot32_codes(w[u], hp);
         acc += wj[j] * (s * (d - z * hsum[j * nch + c]));

@@ -13,6 +13,11 @@
 // with bulk async copies (cp.async.bulk, completion counted on mbarriers);
 // for one decode token the ring holds every pair, so the whole slice is
 // requested at once and HBM sees one deep stream.
+//   * Routing (optional, moe_layer_forward): each block ranks the router
+//     logits itself -- expert e is chosen at position r when exactly r
+//     experts precede it in (logit desc, index asc) order -- and computes the
+//     softmax weights with fixed-order reductions, so every block of both
+//     kernels derives identical ids and weights without waiting for another.
 //   * decode_gateup_kernel: h[p][n] = silu(W_g x_t)[n] * (W_u x_t)[n],
 //     rounded to FP16 (the explicit rounding point) into the workspace.
 //   * decode_down_kernel: launched while the first kernel runs; before
@@ -33,8 +38,11 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 8;                 // compute warps of each kernel
-constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
+constexpr int kWarps = 8;                   // compute warps of the down kernel
+constexpr int kThreads = (kWarps + 1) * 32;   // + one producer warp
+constexpr int kGateWarps = 16;              // compute warps of the gate/up kernel
+constexpr int kGateThreads = (kGateWarps + 1) * 32;
+constexpr int kPairsPerIter = kGateWarps / 8;  // gate/up: 8 warps per pair in flight
 constexpr int kMaxStages = 8;
 constexpr unsigned kMbarTries = 50000;     // bounded mbarrier waits (~1 s)
 
@@ -114,8 +122,12 @@ __host__ __device__ inline Stage stage_of(int rmax, uint32_t row_bytes) {
 
 struct DecodeParams {
   const __half* x;
-  const int32_t* ids;
-  const float* wts;
+  const float* logits;  // [T][E] when the kernels route themselves, else NULL
+  int renorm;
+  const int32_t* ids;   // [T][k] given ids (logits == NULL)
+  const float* wts;     // [T][k] given weights (logits == NULL)
+  int32_t* ids_out;     // routed ids / weights written by block 0 (nullable)
+  float* wts_out;
   const uint8_t* pool;
   unsigned long long block_bytes;
   BlockOffsets off;
@@ -126,22 +138,120 @@ struct DecodeParams {
   __half* hbuf;    // workspace: h [P][I]
   int H, I, g, T, k, E, n_slots, P, G, stages;
   Stage st;
-  uint32_t extra_off, bar_off, blk_off;  // shared-memory carve-up after the stages
+  uint32_t part_off, route_off, bar_off, blk_off;  // shared-memory carve-up after the stages
 };
 
-__device__ __forceinline__ const uint8_t* resolve(const DecodeParams& a, int p) {
-  const int e = a.ids[p];
+// Per-block routing state in shared memory.
+struct RouteSmem {
+  int32_t* ids;   // [P]
+  float* w;       // [P]
+  float* red;     // [32 + 4] reduction scratch
+  int32_t* bad;   // [4]: any NaN/+inf, count of -inf
+  float* lg;      // [E]   logits of the token being routed
+  int32_t* rank;  // [E]
+};
+
+__device__ __forceinline__ RouteSmem route_smem(const DecodeParams& a, uint8_t* sm) {
+  RouteSmem r;
+  uint8_t* b = sm + a.route_off;
+  r.ids = reinterpret_cast<int32_t*>(b);
+  r.w = reinterpret_cast<float*>(b + (size_t)a.P * 4);
+  r.red = reinterpret_cast<float*>(b + (size_t)a.P * 8);
+  r.bad = reinterpret_cast<int32_t*>(r.red + 36);
+  r.lg = reinterpret_cast<float*>(r.bad + 4);
+  r.rank = reinterpret_cast<int32_t*>(r.lg + a.E);
+  return r;
+}
+
+// Block-wide fixed-order sum of one value per thread (all threads call).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < nw; ++w) t += red[w];
+    red[nw] = t;
+  }
+  __syncthreads();
+  return red[nw];
+}
+
+// "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
+// experts of each token. Same definition as moe_route: top-k by (logit desc,
+// index asc), softmax over all E, optionally renormalised over the k; a
+// token with NaN/+inf logits or all -inf gets ids -1 and weights 0.
+__device__ void route_block(const DecodeParams& a, const RouteSmem& r) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  // Rank counts are split over threads: thread (e, part) counts the experts
+  // of one slice of j that precede e; integer sums, so the order is free.
+  const int parts = max(1, nt / a.E);
+  const int span = (a.E + parts - 1) / parts;
+  for (int t = 0; t < a.T; ++t) {
+    if (tid == 0) r.bad[0] = r.bad[1] = 0;
+    for (int e = tid; e < a.E; e += nt) {
+      r.lg[e] = a.logits[(size_t)t * a.E + e];
+      r.rank[e] = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < a.E * parts; i += nt) {
+      const int e = i % a.E, part = i / a.E;
+      const float v = r.lg[e];
+      if (part == 0) {
+        if (isnan(v) || v == INFINITY) atomicOr(&r.bad[0], 1);
+        if (v == -INFINITY) atomicAdd(&r.bad[1], 1);
+      }
+      int cnt = 0;
+      const int j1 = min(a.E, (part + 1) * span);
+      for (int j = part * span; j < j1; ++j) {
+        const float u = r.lg[j];
+        cnt += (u > v) || (u == v && j < e);
+      }
+      if (cnt) atomicAdd(&r.rank[e], cnt);
+    }
+    __syncthreads();
+    for (int e = tid; e < a.E; e += nt)
+      if (r.rank[e] < a.k) r.ids[t * a.k + r.rank[e]] = e;
+    __syncthreads();
+    const bool token_bad = r.bad[0] != 0 || r.bad[1] == a.E;
+    const float m = token_bad ? 0.0f : r.lg[r.ids[t * a.k]];
+    float part_sum = 0.0f;
+    if (!token_bad)
+      for (int e = tid; e < a.E; e += nt) part_sum += expf(r.lg[e] - m);
+    const float s_all = block_sum(part_sum, r.red);
+    if (tid == 0) {
+      float s_sel = 0.0f;
+      for (int j = 0; j < a.k; ++j)
+        if (!token_bad) s_sel += expf(r.lg[r.ids[t * a.k + j]] - m);
+      for (int j = 0; j < a.k; ++j) {
+        const int q = t * a.k + j;
+        if (token_bad) {
+          r.ids[q] = -1;
+          r.w[q] = 0.0f;
+        } else {
+          r.w[q] = expf(r.lg[r.ids[q]] - m) / (a.renorm ? s_sel : s_all);
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ const uint8_t* resolve(const DecodeParams& a, int e) {
   if (e < 0 || e >= a.E) return nullptr;
   const int s = a.slot_of[e];
   if (s < 0 || s >= a.n_slots) return nullptr;
   return a.pool + (size_t)s * a.block_bytes;
 }
 
-// Shared prologue: barriers, the expert block of every pair (resolved once,
-// all loads in flight together), unusable-id reporting from block 0.
+// Shared prologue: barriers, routing (or the given ids), the expert block of
+// every pair (resolved once), unusable-id reporting and routed outputs.
 __device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, uint64_t* full,
                                          uint64_t* empty, const uint8_t** blk_of, int empty_count,
-                                         bool report) {
+                                         bool writer) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -149,13 +259,27 @@ __device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, uin
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  const RouteSmem r = route_smem(a, sm);
+  if (a.logits) {
+    route_block(a, r);
+  } else {
+    for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
+      r.ids[p] = a.ids[p];
+      r.w[p] = a.wts[p];
+    }
+    __syncthreads();
+  }
   for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
-    const uint8_t* b = resolve(a, p);
+    const int e = r.ids[p];
+    const uint8_t* b = resolve(a, e);
     blk_of[p] = b;
-    if (report && !b) {
-      const int e = a.ids[p];
-      if (e != -1 && (e < 0 || e >= a.E)) atomicOr(a.flags, 2);
-      else if (e >= 0) atomicOr(a.flags, 1);
+    if (writer) {
+      if (!b) {
+        if (e != -1 && (e < 0 || e >= a.E)) atomicOr(a.flags, 2);
+        else if (e >= 0) atomicOr(a.flags, 1);
+      }
+      if (a.ids_out) a.ids_out[p] = e;
+      if (a.wts_out) a.wts_out[p] = r.w[p];
     }
   }
   __syncthreads();
@@ -181,11 +305,73 @@ __device__ __forceinline__ void produce(const DecodeParams& a, uint8_t* sm, uint
   }
 }
 
+// The activations of the current token in shared memory, in the pair order
+// of dot16_codes, 64 bytes per 32-element chunk; piece i (16 bytes) of chunk
+// cc sits at slot (i + cc/2) % 4 so that the 8 lanes of a quarter-warp, which
+// read chunks cc..cc+7, hit 8 different bank groups. xsum holds chunk sums.
+__device__ __forceinline__ int xslot(int cc, int i) { return cc * 4 + ((i + (cc >> 1)) & 3); }
+
+__device__ __forceinline__ void stage_x(const __half* __restrict__ src, int H, uint4* xs4, float* xsum,
+                                        int tid, int nthreads) {
+  for (int cc = tid; cc < H / 32; cc += nthreads) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + 32 * cc + 8 * i);
+      __half e[8];
+      *reinterpret_cast<uint4*>(e) = v;
+      uint4 o;
+      half2* oh = reinterpret_cast<half2*>(&o);
+      oh[0] = __halves2half2(e[0], e[4]);
+      oh[1] = __halves2half2(e[1], e[5]);
+      oh[2] = __halves2half2(e[2], e[6]);
+      oh[3] = __halves2half2(e[3], e[7]);
+      xs4[xslot(cc, i)] = o;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += __half2float(e[j]);
+    }
+    xsum[cc] = sum;
+  }
+}
+
+// Gate and up sums of one row for one lane (before the warp sum):
+// s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks cc = lane + 32 it.
+__device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffsets& off, int nch,
+                                            int lane, int g, const uint4* xs4, const float* xsum,
+                                            float& ag, float& au) {
+  const uint8_t* rg = row + off.gu_q_gate;
+  const uint8_t* ru = row + off.gu_q_up;
+  const uint2* sz = reinterpret_cast<const uint2*>(row + off.gu_sz);  // quads per group
+  for (int cc = lane; cc < nch; cc += 32) {
+    const uint4 wg = *reinterpret_cast<const uint4*>(rg + 16 * cc);
+    const uint4 wu = *reinterpret_cast<const uint4*>(ru + 16 * cc);
+    const uint2 q = sz[(32 * cc) / g];
+    uint4 xv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xv[i] = xs4[xslot(cc, i)];
+    const half2* x01 = reinterpret_cast<const half2*>(&xv[0]);
+    const half2* x23 = reinterpret_cast<const half2*>(&xv[2]);
+    half2 xa[8], xb[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xa[i] = x01[i]; xa[4 + i] = reinterpret_cast<const half2*>(&xv[1])[i];
+      xb[i] = x23[i]; xb[4 + i] = reinterpret_cast<const half2*>(&xv[3])[i];
+    }
+    const float dg = dot16_codes(wg.x, wg.y, xa) + dot16_codes(wg.z, wg.w, xb);
+    const float du = dot16_codes(wu.x, wu.y, xa) + dot16_codes(wu.z, wu.w, xb);
+    const float2 sgz = __half22float2(u32_as_h2(q.x));  // (s_gate, z_gate)
+    const float2 suz = __half22float2(u32_as_h2(q.y));  // (s_up, z_up)
+    const float xsm = xsum[cc];
+    ag += sgz.x * (dg - sgz.y * xsm);
+    au += suz.x * (du - suz.y * xsm);
+  }
+}
+
 // ---- kernel 1: gate/up dequant-GEMV + SwiGLU -------------------------------
 // Stage: the block's gate/up rows [R][gu_row] (codes, scales and zeros of
-// both projections per row).
-template <int kMaxXChunks>
-__global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(const DecodeParams a) {
+// both projections per row). Each iteration covers kPairsPerIter pairs of one
+// token: warp w takes row w % 8 (+8, ...) of pair p + w / 8.
+__global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const DecodeParams a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -194,79 +380,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(const Decode
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + a.bar_off);
   uint64_t* empty = full + kMaxStages;
   const uint8_t** blk_of = reinterpret_cast<const uint8_t**>(sm + a.blk_off);
-  griddep_wait();  // ids and x come from earlier kernels
-  prologue(a, sm, full, empty, blk_of, kWarps, c == 0);
-  // Let the down kernel start its weight prefetch now.
-  griddep_launch_dependents();
-  if (warp == kWarps) {
-    if (lane == 0) {
-      produce(a, sm, full, empty, blk_of, n0, n1, 0ull, a.off.gu_row);
-    }
+  uint4* xs4 = reinterpret_cast<uint4*>(sm + a.part_off);                    // [H/32][4]
+  float* xsum = reinterpret_cast<float*>(sm + a.part_off + (size_t)a.H * 2);  // [H/32]
+  griddep_wait();  // logits / ids and x come from earlier kernels
+  prologue(a, sm, full, empty, blk_of, 8, c == 0);
+  griddep_launch_dependents();  // the down kernel may start its prefetch
+  if (warp == kGateWarps) {
+    if (lane == 0) produce(a, sm, full, empty, blk_of, n0, n1, 0ull, a.off.gu_row);
     return;
   }
-  // Lane l handles the 32-element chunks l, l+32, ... of every row; its
-  // activations for those chunks stay in registers while the token lasts.
   const int nch = a.H / 32;
-  half2 xr[kMaxXChunks][16];
-  float xs[kMaxXChunks];
-  int gix[kMaxXChunks];
-#pragma unroll
-  for (int it = 0; it < kMaxXChunks; ++it) gix[it] = (32 * (lane + 32 * it)) / a.g;
+  const int sub = warp / 8, wr = warp % 8;  // pair offset in the iteration, row lane
   int cur_t = -1;
-  for (int p = 0; p < a.P; ++p) {
-    const int s = p % a.stages;
+  for (int p = 0; p < a.P;) {
     const int t = p / a.k;
+    int np = 1;  // pairs of token t in this iteration
+    while (np < kPairsPerIter && p + np < a.P && (p + np) / a.k == t) ++np;
     if (t != cur_t) {
-#pragma unroll
-      for (int it = 0; it < kMaxXChunks; ++it) {
-        const int cc = lane + 32 * it;
-        if (cc < nch) xs[it] = load_chunk<false>(a.x + (size_t)t * a.H + 32 * cc, xr[it]);
-      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");  // previous x no longer read
+      stage_x(a.x + (size_t)t * a.H, a.H, xs4, xsum, threadIdx.x, kGateWarps * 32);
+      asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");
       cur_t = t;
     }
-    if (!mbar_wait(&full[s], (p / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
-    const uint8_t* blk = blk_of[p];
-    const uint8_t* stg = sm + (size_t)s * a.st.bytes;
-    for (int r = warp; r < rows; r += kWarps) {
-      float hv = 0.0f;
-      if (blk) {
-        const uint8_t* row = stg + (size_t)r * a.off.gu_row;
-        const uint8_t* rg = row + a.off.gu_q_gate;
-        const uint8_t* ru = row + a.off.gu_q_up;
-        const __half* sg = reinterpret_cast<const __half*>(row + a.off.gu_s_gate);
-        const __half* zg = reinterpret_cast<const __half*>(row + a.off.gu_z_gate);
-        const __half* su = reinterpret_cast<const __half*>(row + a.off.gu_s_up);
-        const __half* zu = reinterpret_cast<const __half*>(row + a.off.gu_z_up);
+    if (sub < np) {
+      const int q = p + sub;
+      const int s = q % a.stages;
+      if (!mbar_wait(&full[s], (q / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
+      const uint8_t* blk = blk_of[q];
+      const uint8_t* stg = sm + (size_t)s * a.st.bytes;
+      for (int r = wr; r < rows; r += 8) {
         float ag = 0.0f, au = 0.0f;
-#pragma unroll
-        for (int it = 0; it < kMaxXChunks; ++it) {
-          const int cc = lane + 32 * it;
-          if (cc < nch) {
-            const uint4 wg = *reinterpret_cast<const uint4*>(rg + 16 * cc);
-            const uint4 wu = *reinterpret_cast<const uint4*>(ru + 16 * cc);
-            const float dg = dot32_codes(wg, xr[it]);
-            const float du = dot32_codes(wu, xr[it]);
-            const int gi = gix[it];
-            ag += __half2float(sg[gi]) * (dg - __half2float(zg[gi]) * xs[it]);
-            au += __half2float(su[gi]) * (du - __half2float(zu[gi]) * xs[it]);
-          }
-        }
+        if (blk) gate_up_row(stg + (size_t)r * a.off.gu_row, a.off, nch, lane, a.g, xs4, xsum, ag, au);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           ag += __shfl_xor_sync(0xffffffffu, ag, o);
           au += __shfl_xor_sync(0xffffffffu, au, o);
         }
-        hv = silu_f(ag) * au;
+        if (lane == 0) a.hbuf[(size_t)q * a.I + n0 + r] = __float2half_rn(blk ? silu_f(ag) * au : 0.0f);
       }
-      if (lane == 0) a.hbuf[(size_t)p * a.I + n0 + r] = __float2half_rn(hv);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    p += np;
   }
 }
 
 // ---- kernel 2: down dequant-GEMV + top-k weighted combine -------------------
-// Stage: the block's down rows [R][d_row] (codes, scales, zeros per row).
+// Stage: the block's down rows [R][d_row] (codes, then scale/zero pairs).
 // Warp w computes the block's rows for pairs w, w+8, ...
 template <int kMaxHChunks>
 __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodeParams a) {
@@ -278,14 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodePa
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + a.bar_off);
   uint64_t* empty = full + kMaxStages;
   const uint8_t** blk_of = reinterpret_cast<const uint8_t**>(sm + a.blk_off);
-  float* part = reinterpret_cast<float*>(sm + a.extra_off);  // [P][rows]
-  // ids, slot_of and the pool are final before the gate/up kernel signalled
-  // (it passed its own griddepcontrol.wait), so the prefetch may start now.
+  float* part = reinterpret_cast<float*>(sm + a.part_off);  // [P][rows]
+  // Inputs the prefetch needs (logits or ids, slot_of, the pool) are final:
+  // the gate/up kernel passed its own griddepcontrol.wait before signalling.
   prologue(a, sm, full, empty, blk_of, 1, false);
+  const RouteSmem rt = route_smem(a, sm);
   if (warp == kWarps) {
-    if (lane == 0) {
-      produce(a, sm, full, empty, blk_of, m0, m1, a.off.d_offset, a.off.d_row);
-    }
+    if (lane == 0) produce(a, sm, full, empty, blk_of, m0, m1, a.off.d_offset, a.off.d_row);
     griddep_launch_dependents();
     return;
   }
@@ -316,16 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodePa
           const int r = r0 + u;
           if (r < rows) {
             const uint8_t* row = stg + (size_t)r * a.off.d_row;
-            const __half* sd = reinterpret_cast<const __half*>(row + a.off.d_s);
-            const __half* zd = reinterpret_cast<const __half*>(row + a.off.d_z);
+            const uint32_t* sz = reinterpret_cast<const uint32_t*>(row + a.off.d_sz);  // pairs per group
 #pragma unroll
             for (int it = 0; it < kMaxHChunks; ++it) {
               const int cc = lane + 32 * it;
               if (cc < nch) {
                 const uint4 w = *reinterpret_cast<const uint4*>(row + a.off.d_q + 16 * cc);
+                const float2 s2 = __half22float2(u32_as_h2(sz[gix[it]]));  // (s, z)
                 const float d = dot32_codes(w, hr[it]);
-                const int gi = gix[it];
-                v[u] += __half2float(sd[gi]) * (d - __half2float(zd[gi]) * hsum[it]);
+                v[u] += s2.x * (d - s2.y * hsum[it]);
               }
             }
           }
@@ -354,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodePa
     float v = 0.0f;
     for (int j = 0; j < a.k; ++j) {
       const int q = t * a.k + j;
-      v += a.wts[q] * part[q * rows + r];
+      v += rt.w[q] * part[q * rows + r];
     }
     if (a.y_shared) v += __half2float(a.y_shared[(size_t)t * a.H + m0 + r]);
     a.y[(size_t)t * a.H + m0 + r] = __float2half_rn(v);
@@ -364,12 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodePa
 int g_num_sms = 0;
 
 template <typename K>
-cudaError_t launch(K kern, const DecodeParams& a, size_t smem, cudaStream_t st) {
+cudaError_t launch(K kern, const DecodeParams& a, size_t smem, int threads, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.G);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -380,14 +538,18 @@ cudaError_t launch(K kern, const DecodeParams& a, size_t smem, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Carve-up: stages | extra | barriers | block table. Returns total bytes.
-size_t carve(DecodeParams& a, size_t extra, size_t budget) {
-  const size_t tail = 2 * kMaxStages * 8 + (size_t)a.P * 8 + 64;
-  if (extra + tail + 2 * (size_t)a.st.bytes > budget) return 0;
-  a.stages = (int)std::min<size_t>(kMaxStages, (budget - extra - tail) / a.st.bytes);
+// Carve-up: stages | part | route | barriers | block table. Returns total bytes.
+size_t carve(DecodeParams& a, size_t part, size_t budget) {
+  const size_t route = (size_t)a.P * 8 + 40 * 4 + (a.logits ? (size_t)a.E * 8 : 0);
+  const size_t tail = ((part + 15) & ~(size_t)15) + ((route + 15) & ~(size_t)15) + 2 * kMaxStages * 8 +
+                      (size_t)a.P * 8 + 64;
+  if (tail + 2 * (size_t)a.st.bytes > budget) return 0;
+  a.stages = (int)std::min<size_t>(kMaxStages, (budget - tail) / a.st.bytes);
   size_t o = (size_t)a.stages * a.st.bytes;
-  a.extra_off = (uint32_t)o;
-  o = (o + extra + 15) & ~(size_t)15;
+  a.part_off = (uint32_t)o;
+  o = (o + part + 15) & ~(size_t)15;
+  a.route_off = (uint32_t)o;
+  o = (o + route + 15) & ~(size_t)15;
   a.bar_off = (uint32_t)o;
   o += 2 * kMaxStages * 8;
   a.blk_off = (uint32_t)o;
@@ -407,7 +569,8 @@ size_t fused_workspace_bytes(int H, int I, int T, int k) {
 constexpr size_t kGateupBudget = 140 * 1024;
 constexpr size_t kDownBudget = 80 * 1024;
 
-int fused_forward(const ForwardArgs& fa) {
+int fused_forward_routed(const ForwardArgs& fa, const float* logits, int renorm, int32_t* ids_out,
+                         float* wts_out) {
   if (g_num_sms == 0) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -421,6 +584,7 @@ int fused_forward(const ForwardArgs& fa) {
   a.P = fa.T * fa.k;
   a.G = g_num_sms;
   a.x = fa.x; a.ids = fa.ids; a.wts = fa.weights; a.pool = fa.pool; a.block_bytes = fa.block_bytes;
+  a.logits = logits; a.renorm = renorm; a.ids_out = ids_out; a.wts_out = wts_out;
   a.off = fa.off; a.slot_of = fa.slot_of; a.y_shared = fa.y_shared; a.y = fa.y;
   uint8_t* ws = static_cast<uint8_t*>(fa.ws);
   a.flags = reinterpret_cast<int32_t*>(ws);
@@ -429,19 +593,20 @@ int fused_forward(const ForwardArgs& fa) {
 
   DecodeParams ag = a;
   ag.st = stage_of(rgu, a.off.gu_row);
-  const size_t smem_g = carve(ag, 0, kGateupBudget);
+  const size_t smem_g = carve(ag, (size_t)a.H * 2 + (size_t)(a.H / 32) * 4, kGateupBudget);
   DecodeParams ad = a;
   ad.st = stage_of(rdn, a.off.d_row);
   const size_t smem_d = carve(ad, (size_t)a.P * rdn * 4, kDownBudget);
   if (!smem_g || !smem_d) return fail(MOE_ERR_UNSUPPORTED, "streamed decode: shapes exceed shared memory");
   cudaError_t e;
-  if (xc <= 2) e = launch(decode_gateup_kernel<2>, ag, smem_g, fa.stream);
-  else e = launch(decode_gateup_kernel<4>, ag, smem_g, fa.stream);
+  e = launch(decode_gateup_kernel, ag, smem_g, kGateThreads, fa.stream);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode gate/up launch: %s", cudaGetErrorString(e));
-  if (hc <= 1) e = launch(decode_down_kernel<1>, ad, smem_d, fa.stream);
-  else e = launch(decode_down_kernel<2>, ad, smem_d, fa.stream);
+  if (hc <= 1) e = launch(decode_down_kernel<1>, ad, smem_d, kThreads, fa.stream);
+  else e = launch(decode_down_kernel<2>, ad, smem_d, kThreads, fa.stream);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode down launch: %s", cudaGetErrorString(e));
   return MOE_OK;
 }
+
+int fused_forward(const ForwardArgs& fa) { return fused_forward_routed(fa, nullptr, 0, nullptr, nullptr); }
 
 }  // namespace moe

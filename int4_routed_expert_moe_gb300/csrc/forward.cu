@@ -91,6 +91,51 @@ int moe_expert_forward(const moe_expert_shape* s, const void* x, int T,
   return moe::grouped_forward(a);
 }
 
+int moe_layer_forward(const moe_expert_shape* s, const void* x, const float* logits, int T, int E,
+                      int k, int renorm, int32_t* ids, float* weights, const void* pool,
+                      const int32_t* slot_of, int n_slots, const void* y_shared, void* y,
+                      void* workspace, size_t workspace_bytes, int path, void* stream) {
+  moe::clear_error();
+  if (!moe::valid_shape(s)) return moe::fail(MOE_ERR_SHAPE, "moe_layer_forward: invalid expert shape");
+  if (T < 0 || E < 1 || E > 4096 || k < 1 || k > 32 || k > E || n_slots < 1)
+    return moe::fail(MOE_ERR_ARG, "moe_layer_forward: bad T/E/k/n_slots (%d/%d/%d/%d)", T, E, k, n_slots);
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GROUPED &&
+      path != MOE_PATH_GEMV_UNFUSED)
+    return moe::fail(MOE_ERR_ARG, "moe_layer_forward: unknown path %d", path);
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !ids || !weights || !pool || !slot_of || !y || !workspace)
+    return moe::fail(MOE_ERR_ARG, "moe_layer_forward: NULL pointer");
+  const int p = moe::pick_path(path, T, k);
+  if (p == MOE_PATH_GEMV && (long long)T * E * E <= 262144) {
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 || reinterpret_cast<uintptr_t>(pool) % 256 ||
+        reinterpret_cast<uintptr_t>(x) % 16)
+      return moe::fail(MOE_ERR_ARG, "moe_layer_forward: workspace/pool must be 256-byte and x 16-byte aligned");
+    const size_t need = moe_forward_workspace_bytes(s, T, k, E, p);
+    if (workspace_bytes < need)
+      return moe::fail(MOE_ERR_CAPACITY, "moe_layer_forward: workspace %zu < %zu bytes", workspace_bytes, need);
+    const moe::BlockLayout bl = moe::block_layout(s->hidden, s->inter, s->group);
+    moe::ForwardArgs a;
+    a.H = s->hidden; a.I = s->inter; a.g = s->group; a.T = T; a.k = k; a.E = E; a.n_slots = n_slots;
+    a.x = static_cast<const __half*>(x);
+    a.ids = ids; a.weights = weights;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.block_bytes = bl.total;
+    a.off = moe::offsets_of(bl);
+    a.slot_of = slot_of;
+    a.y_shared = static_cast<const __half*>(y_shared);
+    a.y = static_cast<__half*>(y);
+    a.ws = workspace; a.ws_bytes = workspace_bytes;
+    a.stream = static_cast<cudaStream_t>(stream);
+    const int rc = moe::fused_forward_routed(a, logits, renorm, ids, weights);
+    if (rc != MOE_ERR_UNSUPPORTED) return rc;
+    moe::clear_error();
+  }
+  int rc = moe_route(logits, T, E, k, renorm, ids, weights, nullptr, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_expert_forward(s, x, T, ids, weights, k, E, pool, slot_of, n_slots, y_shared, y,
+                            workspace, workspace_bytes, path, stream);
+}
+
 int moe_workspace_clear_flags(void* workspace, void* stream) {
   moe::clear_error();
   if (!workspace) return moe::fail(MOE_ERR_ARG, "NULL workspace");

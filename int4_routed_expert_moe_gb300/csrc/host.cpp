@@ -61,13 +61,9 @@ int moe_expert_block_layout(const moe_expert_shape* s, moe_block_layout* out) {
   out->d_row_bytes = b.d_row;
   out->gu_q_gate = b.gu_q_gate;
   out->gu_q_up = b.gu_q_up;
-  out->gu_s_gate = b.gu_s_gate;
-  out->gu_z_gate = b.gu_z_gate;
-  out->gu_s_up = b.gu_s_up;
-  out->gu_z_up = b.gu_z_up;
+  out->gu_sz = b.gu_sz;
   out->d_q = b.d_q;
-  out->d_s = b.d_s;
-  out->d_z = b.d_z;
+  out->d_sz = b.d_sz;
   return MOE_OK;
 }
 
@@ -86,21 +82,32 @@ void copy_rows(const moe_expert_shape* s, uint8_t* blk, uint8_t* qg, uint8_t* qu
     if (kPack) std::memcpy(blk_part, arr_part, n);
     else std::memcpy(arr_part, blk_part, n);
   };
+  (void)s_gu;
+  (void)s_d;
+  const int ggu = H / g, gd = I / g;
   if (kPack) std::memset(blk, 0, b.total);
   for (int n = 0; n < I; ++n) {
     uint8_t* row = blk + (size_t)n * b.gu_row;
     mv(row + b.gu_q_gate, qg + n * q_gu, q_gu);
     mv(row + b.gu_q_up, qu + n * q_gu, q_gu);
-    mv(row + b.gu_s_gate, sg + n * s_gu, s_gu);
-    mv(row + b.gu_z_gate, zg + n * s_gu, s_gu);
-    mv(row + b.gu_s_up, su + n * s_gu, s_gu);
-    mv(row + b.gu_z_up, zu + n * s_gu, s_gu);
+    for (int gi = 0; gi < ggu; ++gi) {
+      uint8_t* quad = row + b.gu_sz + (size_t)gi * 8;
+      const size_t e = ((size_t)n * ggu + gi) * 2;
+      mv(quad + 0, sg + e, 2);
+      mv(quad + 2, zg + e, 2);
+      mv(quad + 4, su + e, 2);
+      mv(quad + 6, zu + e, 2);
+    }
   }
   for (int m = 0; m < H; ++m) {
     uint8_t* row = blk + b.d_offset + (size_t)m * b.d_row;
     mv(row + b.d_q, qd + m * q_d, q_d);
-    mv(row + b.d_s, sd + m * s_d, s_d);
-    mv(row + b.d_z, zd + m * s_d, s_d);
+    for (int gi = 0; gi < gd; ++gi) {
+      uint8_t* pr = row + b.d_sz + (size_t)gi * 4;
+      const size_t e = ((size_t)m * gd + gi) * 2;
+      mv(pr + 0, sd + e, 2);
+      mv(pr + 2, zd + e, 2);
+    }
   }
 }
 }  // namespace

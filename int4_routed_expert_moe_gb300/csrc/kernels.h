@@ -15,17 +15,16 @@ namespace moe {
 struct BlockOffsets {
   unsigned long long d_offset;  // start of the down section
   unsigned gu_row, d_row;       // row strides
-  unsigned gu_q_gate, gu_q_up, gu_s_gate, gu_z_gate, gu_s_up, gu_z_up;  // in a gate/up row
-  unsigned d_q, d_s, d_z;       // in a down row
+  unsigned gu_q_gate, gu_q_up, gu_sz;  // in a gate/up row (sz: quads s_g, z_g, s_u, z_u)
+  unsigned d_q, d_sz;                  // in a down row (sz: pairs s_d, z_d)
 };
 
 inline BlockOffsets offsets_of(const BlockLayout& b) {
   BlockOffsets o;
   o.d_offset = b.d_offset;
   o.gu_row = b.gu_row; o.d_row = b.d_row;
-  o.gu_q_gate = b.gu_q_gate; o.gu_q_up = b.gu_q_up; o.gu_s_gate = b.gu_s_gate;
-  o.gu_z_gate = b.gu_z_gate; o.gu_s_up = b.gu_s_up; o.gu_z_up = b.gu_z_up;
-  o.d_q = b.d_q; o.d_s = b.d_s; o.d_z = b.d_z;
+  o.gu_q_gate = b.gu_q_gate; o.gu_q_up = b.gu_q_up; o.gu_sz = b.gu_sz;
+  o.d_q = b.d_q; o.d_sz = b.d_sz;
   return o;
 }
 
@@ -62,6 +61,10 @@ int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
 // Fused one-kernel decode path (persistent, one block per SM).
 size_t fused_workspace_bytes(int H, int I, int T, int k);
 int fused_forward(const ForwardArgs& a);
+// Same, with routing done inside the kernels from logits [T][E]; routed ids
+// and weights are written to ids_out / wts_out when non-NULL.
+int fused_forward_routed(const ForwardArgs& a, const float* logits, int renorm, int32_t* ids_out,
+                         float* wts_out);
 
 size_t grouped_workspace_bytes(int H, int I, int T, int k, int E);
 int grouped_forward(const ForwardArgs& a);

@@ -44,8 +44,7 @@ class moe_expert_shape(ctypes.Structure):
 class moe_block_layout(ctypes.Structure):
     _fields_ = [("total", ctypes.c_uint64), ("d_offset", ctypes.c_uint64),
                 ("gu_row_bytes", ctypes.c_uint32), ("d_row_bytes", ctypes.c_uint32)] + [
-        (n, ctypes.c_uint32) for n in ("gu_q_gate", "gu_q_up", "gu_s_gate", "gu_z_gate", "gu_s_up",
-                                        "gu_z_up", "d_q", "d_s", "d_z")]
+        (n, ctypes.c_uint32) for n in ("gu_q_gate", "gu_q_up", "gu_sz", "d_q", "d_sz")]
 
 
 class moe_residency_cfg(ctypes.Structure):
@@ -87,6 +86,7 @@ _SIGS = {
     "moe_token_sort": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_forward_workspace_bytes": (_SZ, [_SHAPE, _I, _I, _I, _I]),
     "moe_expert_forward": (_I, [_SHAPE, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
+    "moe_layer_forward": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
     "moe_workspace_clear_flags": (_I, [_P, _P]),
     "moe_workspace_flags": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_shared_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -264,6 +264,23 @@ def moe_expert_forward(shape, x: torch.Tensor, ids: torch.Tensor, weights: torch
         _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True),
         _dev(y, torch.float16, "y", T * H), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), path, _stream(stream)), "moe_expert_forward")
+
+
+def moe_layer_forward(shape, x: torch.Tensor, logits: torch.Tensor, k: int, renorm: bool,
+                      ids: torch.Tensor, weights: torch.Tensor, pool: torch.Tensor,
+                      slot_of: torch.Tensor, n_slots: int, y_shared: torch.Tensor | None,
+                      y: torch.Tensor, workspace: torch.Tensor, path: int = MOE_PATH_AUTO,
+                      stream=None) -> None:
+    H, I, g = shape
+    T, E = logits.shape
+    s = _shape(shape)
+    bb = moe_expert_block_bytes(shape)
+    _check(_lib.moe_layer_forward(
+        ctypes.byref(s), _dev(x, torch.float16, "x", T * H), _dev(logits, torch.float32, "logits"), T, E,
+        k, int(bool(renorm)), _dev(ids, torch.int32, "ids", T * k), _dev(weights, torch.float32, "weights", T * k),
+        _dev(pool, torch.uint8, "pool", n_slots * bb), _dev(slot_of, torch.int32, "slot_of", E), n_slots,
+        _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True), _dev(y, torch.float16, "y", T * H),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), path, _stream(stream)), "moe_layer_forward")
 
 
 def moe_workspace_clear_flags(workspace: torch.Tensor, stream=None) -> None:

@@ -148,16 +148,17 @@ def pack_codes(q: np.ndarray) -> np.ndarray:
 
 def block_layout(H: int, I: int, g: int) -> dict:
     """Byte geometry of one expert block as the library's header documents it:
-    gate/up rows [q_gate | q_up | s_gate | z_gate | s_up | z_up] and down rows
-    [q_down | s_down | z_down], each row padded to 16 bytes. Sizes only."""
-    sgu, sd = (H // g) * 2, (I // g) * 2
-    gu = {"qp_gate": (0, H // 2), "qp_up": (H // 2, H), "s_gate": (H, H + sgu),
-          "z_gate": (H + sgu, H + 2 * sgu), "s_up": (H + 2 * sgu, H + 3 * sgu),
-          "z_up": (H + 3 * sgu, H + 4 * sgu)}
-    d = {"qp_down": (0, I // 2), "s_down": (I // 2, I // 2 + sd), "z_down": (I // 2 + sd, I // 2 + 2 * sd)}
-    gu_row = (H + 4 * sgu + 15) // 16 * 16
-    d_row = (I // 2 + 2 * sd + 15) // 16 * 16
-    return {"gu": gu, "d": d, "gu_row": gu_row, "d_row": d_row, "d_offset": I * gu_row,
+    gate/up rows [q_gate | q_up | per-group quads (s_gate, z_gate, s_up, z_up)]
+    and down rows [q_down | per-group pairs (s_down, z_down)], each row padded
+    to 16 bytes. Sizes only."""
+    ggu, gd = H // g, I // g
+    gu_row = (H + 8 * ggu + 15) // 16 * 16
+    d_row = (I // 2 + 4 * gd + 15) // 16 * 16
+    return {"gu_codes": {"qp_gate": (0, H // 2), "qp_up": (H // 2, H)},
+            "gu_sz": (H, ggu, ("s_gate", "z_gate", "s_up", "z_up")),
+            "d_codes": {"qp_down": (0, I // 2)},
+            "d_sz": (I // 2, gd, ("s_down", "z_down")),
+            "gu_row": gu_row, "d_row": d_row, "d_offset": I * gu_row,
             "total": I * gu_row + H * d_row}
 
 
@@ -177,21 +178,22 @@ def device_pool(n_blocks: int, H: int, I: int, g: int, seed: int, device="cuda",
         b1 = min(n_blocks, b0 + chunk)
         n = b1 - b0
         blk = pool[b0:b1]
-        sections = ((blk[:, :lay["d_offset"]].view(n, I, lay["gu_row"]), lay["gu"]),
-                    (blk[:, lay["d_offset"]:].view(n, H, lay["d_row"]), lay["d"]))
-        for view, fields in sections:
-            for name, (lo, hi) in fields.items():
-                rows = view.shape[1]
-                if name.startswith("qp"):
-                    view[:, :, lo:hi] = torch.randint(0, 256, (n, rows, hi - lo), dtype=torch.uint8,
-                                                      device=device, generator=gen)
-                elif name.startswith("s"):
-                    v = torch.empty((n, rows, (hi - lo) // 2), dtype=torch.float32, device=device)
+        sections = ((blk[:, :lay["d_offset"]].view(n, I, lay["gu_row"]), lay["gu_codes"], lay["gu_sz"]),
+                    (blk[:, lay["d_offset"]:].view(n, H, lay["d_row"]), lay["d_codes"], lay["d_sz"]))
+        for view, codes, (start, groups, names) in sections:
+            rows = view.shape[1]
+            for lo, hi in codes.values():
+                view[:, :, lo:hi] = torch.randint(0, 256, (n, rows, hi - lo), dtype=torch.uint8,
+                                                  device=device, generator=gen)
+            vals = torch.empty((n, rows, groups, len(names)), dtype=torch.float16, device=device)
+            for i, name in enumerate(names):
+                if name.startswith("s"):
+                    v = torch.empty((n, rows, groups), dtype=torch.float32, device=device)
                     v.uniform_(1e-3, 1e-2, generator=gen)
-                    view[:, :, lo:hi] = v.to(torch.float16).view(torch.uint8)
+                    vals[:, :, :, i] = v.to(torch.float16)
                 else:
-                    view[:, :, lo:hi] = torch.full((n, rows, (hi - lo) // 2), 8.0, dtype=torch.float16,
-                                                   device=device).view(torch.uint8)
+                    vals[:, :, :, i] = 8.0
+            view[:, :, start:start + groups * len(names) * 2] = vals.view(torch.uint8).view(n, rows, -1)
     return pool
 
 
@@ -202,8 +204,12 @@ def arrays_from_block(block, H: int, I: int, g: int) -> dict:
     gu = b[:lay["d_offset"]].reshape(I, lay["gu_row"])
     d = b[lay["d_offset"]:lay["total"]].reshape(H, lay["d_row"])
     out = {}
-    for view, fields in ((gu, lay["gu"]), (d, lay["d"])):
-        for name, (lo, hi) in fields.items():
-            part = np.ascontiguousarray(view[:, lo:hi])
-            out[name] = part if name.startswith("qp") else part.view(np.float16)
+    for view, codes, (start, groups, names) in ((gu, lay["gu_codes"], lay["gu_sz"]),
+                                                (d, lay["d_codes"], lay["d_sz"])):
+        for name, (lo, hi) in codes.items():
+            out[name] = np.ascontiguousarray(view[:, lo:hi])
+        sz = np.ascontiguousarray(view[:, start:start + groups * len(names) * 2]).view(np.float16)
+        sz = sz.reshape(view.shape[0], groups, len(names))
+        for i, name in enumerate(names):
+            out[name] = np.ascontiguousarray(sz[:, :, i])
     return out

@@ -45,9 +45,9 @@ def test_block_layout(shape, want):
     lay = moe.moe_expert_block_layout(shape)
     assert lay["total"] == want and lay["d_offset"] == I * lay["gu_row_bytes"]
     assert lay["gu_row_bytes"] % 16 == 0 and lay["d_row_bytes"] % 16 == 0
-    assert lay["gu_q_up"] == H // 2 and lay["gu_s_gate"] == H and lay["d_s"] == I // 2
-    assert lay["gu_z_up"] + 2 * (H // g) <= lay["gu_row_bytes"]
-    assert lay["d_z"] + 2 * (I // g) <= lay["d_row_bytes"]
+    assert lay["gu_q_up"] == H // 2 and lay["gu_sz"] == H and lay["d_sz"] == I // 2
+    assert lay["gu_sz"] + 8 * (H // g) <= lay["gu_row_bytes"]
+    assert lay["d_sz"] + 4 * (I // g) <= lay["d_row_bytes"]
     syn = synth.block_layout(H, I, g)
     assert (syn["gu_row"], syn["d_row"], syn["total"]) == (lay["gu_row_bytes"], lay["d_row_bytes"], want)
 
@@ -106,3 +106,21 @@ def test_workspace_sizes():
     s = (2048, 1024, 128)
     assert moe.moe_forward_workspace_bytes(s, 1, 8, 64, moe.MOE_PATH_GEMV) == 512 + 8 * 1024 * 4
     assert moe.moe_forward_workspace_bytes((2048, 100, 128), 1, 8, 64) == 0
+
+
+@pytest.mark.parametrize("shape", [(256, 128, 64), (2048, 512, 128), (192, 64, 64)])
+def test_device_pool_generator_layout_matches_library(shape):
+    # The generator's device-side pool (run here on the CPU device) and its
+    # reader agree with the library's unpacker byte for byte.
+    H, I, g = shape
+    pool = synth.device_pool(2, H, I, g, seed=3, device="cpu").numpy()
+    for b in range(2):
+        lib = moe.moe_unpack_expert(shape, pool[b])
+        syn = synth.arrays_from_block(pool[b], H, I, g)
+        for n in lib:
+            assert np.array_equal(lib[n].view(np.uint8), syn[n].view(np.uint8)), n
+        for n in ("s_gate", "s_up", "s_down"):
+            v = lib[n].astype(np.float64)
+            assert v.min() >= 9e-4 and v.max() <= 1.01e-2
+        for n in ("z_gate", "z_up", "z_down"):
+            assert np.all(lib[n] == 8.0)

@@ -2,7 +2,7 @@
 
 The OLMoE-shaped decode stack that bench.py times: 16 layers x 64 experts of
 hidden 2048 / intermediate 1024, generated on the device. For sampled layers
-the same moe_route + moe_expert_forward calls bench.py makes run on fresh
+the same moe_layer_forward call bench.py makes run on fresh
 N(0,1) activations, and the oracle recomputes the layer from the expert
 blocks read back from the pool (inputs, read before the kernels run)."""
 import numpy as np
@@ -30,9 +30,8 @@ def test_bench_decode_workload_sampled_layers():
                    for e in ids_ref.reshape(-1)}
         x16 = synth.activations(99, l, wl.T, wl.H)
         x = torch.from_numpy(x16).to(dev)
-        moe.moe_route(lg, wl.k, wl.renorm, wl.ids[l], wl.w[l])
-        moe.moe_expert_forward(wl.shape, x, wl.ids[l], wl.w[l], wl.E, pool, wl.slot_of, wl.E, None,
-                               wl.y[l], wl.ws, moe.MOE_PATH_GEMV)
+        moe.moe_layer_forward(wl.shape, x, lg, wl.k, wl.renorm, wl.ids[l], wl.w[l], pool, wl.slot_of,
+                              wl.E, None, wl.y[l], wl.ws, moe.MOE_PATH_GEMV)
         torch.cuda.synchronize()
         assert moe.moe_workspace_flags(wl.ws) == 0
         ref = moe_oracle.moe_layer(x16, lg.cpu().numpy(), experts, wl.k, wl.renorm, wl.g)

@@ -208,3 +208,50 @@ def test_gemv_bad_token_contributes_nothing():
     ref = moe_oracle.moe_layer(x[[0, 2]], lg[[0, 2]], lp.arrays, k, True, 64)
     ok, err, bound = tol_ok(y[[0, 2]], ref["y"])
     assert ok
+
+
+def _layer_forward_case(shape, E, k, renorm, T, seed, logits=None, shared=False, path=1):
+    H, I, g = shape
+    lp = LayerPool(moe, seed, 0, shape, E)
+    dev = torch.device("cuda")
+    x16 = synth.activations(seed, 1, T, H)
+    lg = synth.logits_normal(seed, 3, T, E) if logits is None else logits
+    ysh = synth.activations(seed, 2, T, H) if shared else None
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float16, device=dev)
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, T, k, E, path), dtype=torch.uint8, device=dev)
+    moe.moe_layer_forward(shape, torch.from_numpy(x16).to(dev), torch.from_numpy(lg).to(dev), k, renorm,
+                          ids, w, lp.pool, lp.slot_of, E,
+                          None if ysh is None else torch.from_numpy(ysh).to(dev), y, ws, path)
+    assert moe.moe_workspace_flags(ws) == 0
+    good = [t for t in range(T) if np.all(np.isfinite(lg[t]) | (lg[t] == -np.inf)) and not np.all(lg[t] == -np.inf)]
+    ref = moe_oracle.moe_layer(x16[good], lg[good], lp.arrays, k, renorm, g,
+                               y_shared=None if ysh is None else ysh[good])
+    got_ids = ids.cpu().numpy()
+    assert np.array_equal(got_ids[good], ref["ids"])
+    assert np.allclose(w.cpu().numpy()[good], ref["weights"], rtol=2e-6, atol=1e-9)
+    ok, err, bound = tol_ok(y.float().cpu().numpy()[good], ref["y"])
+    assert ok, (err, bound)
+    return got_ids, y.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("shape,E,k,renorm,T,shared", [
+    ((256, 128, 64), 8, 2, True, 4, True),          # tiny, shared path added
+    ((2048, 1024, 128), 64, 8, False, 1, False),    # OLMoE decode: routing inside the kernels
+    ((2048, 1024, 128), 64, 8, False, 3, False),
+    ((2048, 512, 128), 512, 10, True, 1, False),    # large fan-out, in-kernel routing (E^2 = 2^18)
+    ((2048, 512, 128), 512, 10, True, 16, False),   # routing kernel first (T*E^2 too large)
+])
+def test_layer_forward_matches_oracle(shape, E, k, renorm, T, shared):
+    _layer_forward_case(shape, E, k, renorm, T, 40 + T, shared=shared)
+
+
+def test_layer_forward_ties_and_bad_tokens():
+    E = 8
+    lg = np.array([[1, 3, 3, 2, 3, 0, 0, 0], [0, 0, 0, 0, 0, 0, 0, 0],
+                   [-np.inf, 1, -np.inf, 0, -np.inf, -np.inf, -np.inf, -np.inf],
+                   [0, np.nan, 1, 2, 0, 0, 0, 0], [-np.inf] * 8], dtype=np.float32)
+    ids, y = _layer_forward_case((256, 128, 64), E, 3, False, 5, 44, logits=lg)
+    assert ids[3].tolist() == [-1, -1, -1] and ids[4].tolist() == [-1, -1, -1]
+    assert np.all(y[3] == 0) and np.all(y[4] == 0)
