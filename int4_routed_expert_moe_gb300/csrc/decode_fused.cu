@@ -38,11 +38,19 @@
 namespace moe {
 namespace {
 
+// Warp counts: registers are granted to a block in units of four warps, so
+// 16 + 12 warps of the two kernels fit one SM together (64K registers).
 constexpr int kWarps = 8;                   // compute warps of the down kernel
 constexpr int kThreads = (kWarps + 1) * 32;   // + one producer warp
-constexpr int kGateWarps = 16;              // compute warps of the gate/up kernel
+constexpr int kGateWarps = 15;              // compute warps of the gate/up kernel
 constexpr int kGateThreads = (kGateWarps + 1) * 32;
-constexpr int kPairsPerIter = kGateWarps / 8;  // gate/up: 8 warps per pair in flight
+constexpr int kSub0 = 8;                    // gate/up: warps 0..7 take even pairs, 8..14 odd pairs
+constexpr int kPairsPerIter = 2;
+// Stage ownership: a stage must always be drained by the same warp (down) or
+// sub-group (gate/up) so that no consumer waits on a phase two fills ahead
+// (an mbarrier parity test cannot tell those apart). With an even stage
+// count, stage q % S of pair q is drained by sub-group q & 1 (gate/up) and by
+// warp (q % S) % kWarps (down), each in increasing q.
 constexpr int kMaxStages = 8;
 constexpr unsigned kMbarTries = 50000;     // bounded mbarrier waits (~1 s)
 
@@ -82,30 +90,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-// 32 FP16 values (64 bytes) into the pair order of codes_to_h2, with their sum.
-template <bool kCoherent>
-__device__ __forceinline__ float load_chunk(const __half* src, half2 (&xp)[16]) {
-  float sum = 0.0f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 v;
-    if (kCoherent) {
-      asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(src + 8 * q) : "memory");
-    } else {
-      v = *reinterpret_cast<const uint4*>(src + 8 * q);
-    }
-    __half e[8];
-    *reinterpret_cast<uint4*>(e) = v;
-    xp[4 * q + 0] = __halves2half2(e[0], e[4]);
-    xp[4 * q + 1] = __halves2half2(e[1], e[5]);
-    xp[4 * q + 2] = __halves2half2(e[2], e[6]);
-    xp[4 * q + 3] = __halves2half2(e[3], e[7]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sum += __half2float(e[i]);
-  }
-  return sum;
-}
 
 // ---- shared-memory stages -------------------------------------------------
 __host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -118,6 +102,32 @@ __host__ __device__ inline Stage stage_of(int rmax, uint32_t row_bytes) {
   Stage st;
   st.bytes = align16((uint32_t)rmax * row_bytes);
   return st;
+}
+
+// 32 FP16 values (64 bytes, read through L2) as the scaled pairs of
+// dot16_scaled; returns their sum, and 2^(24-s) in back.
+__device__ __forceinline__ float load_scaled_chunk(const __half* src, half2 (&xp)[16], float& back) {
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(src + 8 * q) : "memory");
+    const __half* e = reinterpret_cast<const __half*>(&r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * q + i] = __half2float(e[i]);
+  }
+  float sum = 0.0f, amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    sum += v[i];
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const int sh = chunk_shift(amax);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) scaled_perm8(v + 8 * q, sh, xp + 4 * q);
+  back = ldexpf(1.0f, 24 - sh);
+  return sum;
 }
 
 struct DecodeParams {
@@ -222,17 +232,19 @@ __device__ void route_block(const DecodeParams& a, const RouteSmem& r) {
     if (!token_bad)
       for (int e = tid; e < a.E; e += nt) part_sum += expf(r.lg[e] - m);
     const float s_all = block_sum(part_sum, r.red);
-    if (tid == 0) {
-      float s_sel = 0.0f;
-      for (int j = 0; j < a.k; ++j)
-        if (!token_bad) s_sel += expf(r.lg[r.ids[t * a.k + j]] - m);
-      for (int j = 0; j < a.k; ++j) {
-        const int q = t * a.k + j;
+    // Warp 0: lane j < k owns choice j; the selected sum in fixed lane order.
+    if (tid < 32) {
+      const int q = t * a.k + tid;
+      const float ej = (tid < a.k && !token_bad) ? expf(r.lg[r.ids[q]] - m) : 0.0f;
+      float s_sel = ej;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s_sel += __shfl_xor_sync(0xffffffffu, s_sel, o);
+      if (tid < a.k) {
         if (token_bad) {
           r.ids[q] = -1;
           r.w[q] = 0.0f;
         } else {
-          r.w[q] = expf(r.lg[r.ids[q]] - m) / (a.renorm ? s_sel : s_all);
+          r.w[q] = ej / (a.renorm ? s_sel : s_all);
         }
       }
     }
@@ -305,32 +317,39 @@ __device__ __forceinline__ void produce(const DecodeParams& a, uint8_t* sm, uint
   }
 }
 
-// The activations of the current token in shared memory, in the pair order
-// of dot16_codes, 64 bytes per 32-element chunk; piece i (16 bytes) of chunk
+// The activations of the current token in shared memory as the scaled pairs
+// of dot16_scaled, 64 bytes per 32-element chunk; piece i (16 bytes) of chunk
 // cc sits at slot (i + cc/2) % 4 so that the 8 lanes of a quarter-warp, which
-// read chunks cc..cc+7, hit 8 different bank groups. xsum holds chunk sums.
+// read chunks cc..cc+7, hit 8 different bank groups. Per chunk: xsum = sum of
+// the (unscaled) FP16 values, xback = 2^(24-s).
 __device__ __forceinline__ int xslot(int cc, int i) { return cc * 4 + ((i + (cc >> 1)) & 3); }
 
 __device__ __forceinline__ void stage_x(const __half* __restrict__ src, int H, uint4* xs4, float* xsum,
-                                        int tid, int nthreads) {
+                                        float* xback, int tid, int nthreads) {
   for (int cc = tid; cc < H / 32; cc += nthreads) {
-    float sum = 0.0f;
+    float v[32];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + 32 * cc + 8 * i);
-      __half e[8];
-      *reinterpret_cast<uint4*>(e) = v;
-      uint4 o;
-      half2* oh = reinterpret_cast<half2*>(&o);
-      oh[0] = __halves2half2(e[0], e[4]);
-      oh[1] = __halves2half2(e[1], e[5]);
-      oh[2] = __halves2half2(e[2], e[6]);
-      oh[3] = __halves2half2(e[3], e[7]);
-      xs4[xslot(cc, i)] = o;
+      const uint4 raw = *reinterpret_cast<const uint4*>(src + 32 * cc + 8 * i);
+      const __half* e = reinterpret_cast<const __half*>(&raw);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sum += __half2float(e[j]);
+      for (int j = 0; j < 8; ++j) v[8 * i + j] = __half2float(e[j]);
+    }
+    float sum = 0.0f, amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      sum += v[j];
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    const int sh = chunk_shift(amax);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 o;
+      scaled_perm8(v + 8 * i, sh, reinterpret_cast<half2*>(&o));
+      xs4[xslot(cc, i)] = o;
     }
     xsum[cc] = sum;
+    xback[cc] = ldexpf(1.0f, 24 - sh);
   }
 }
 
@@ -338,7 +357,7 @@ __device__ __forceinline__ void stage_x(const __half* __restrict__ src, int H, u
 // s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks cc = lane + 32 it.
 __device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffsets& off, int nch,
                                             int lane, int g, const uint4* xs4, const float* xsum,
-                                            float& ag, float& au) {
+                                            const float* xback, float& ag, float& au) {
   const uint8_t* rg = row + off.gu_q_gate;
   const uint8_t* ru = row + off.gu_q_up;
   const uint2* sz = reinterpret_cast<const uint2*>(row + off.gu_sz);  // quads per group
@@ -349,16 +368,11 @@ __device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffse
     uint4 xv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) xv[i] = xs4[xslot(cc, i)];
-    const half2* x01 = reinterpret_cast<const half2*>(&xv[0]);
-    const half2* x23 = reinterpret_cast<const half2*>(&xv[2]);
-    half2 xa[8], xb[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      xa[i] = x01[i]; xa[4 + i] = reinterpret_cast<const half2*>(&xv[1])[i];
-      xb[i] = x23[i]; xb[4 + i] = reinterpret_cast<const half2*>(&xv[3])[i];
-    }
-    const float dg = dot16_codes(wg.x, wg.y, xa) + dot16_codes(wg.z, wg.w, xb);
-    const float du = dot16_codes(wu.x, wu.y, xa) + dot16_codes(wu.z, wu.w, xb);
+    const half2* xa = reinterpret_cast<const half2*>(&xv[0]);  // pieces 0, 1 are contiguous
+    const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
+    const float back = xback[cc];
+    const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
+    const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
     const float2 sgz = __half22float2(u32_as_h2(q.x));  // (s_gate, z_gate)
     const float2 suz = __half22float2(u32_as_h2(q.y));  // (s_up, z_up)
     const float xsm = xsum[cc];
@@ -382,15 +396,18 @@ __global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const De
   const uint8_t** blk_of = reinterpret_cast<const uint8_t**>(sm + a.blk_off);
   uint4* xs4 = reinterpret_cast<uint4*>(sm + a.part_off);                    // [H/32][4]
   float* xsum = reinterpret_cast<float*>(sm + a.part_off + (size_t)a.H * 2);  // [H/32]
+  float* xback = xsum + a.H / 32;                                             // [H/32]
   griddep_wait();  // logits / ids and x come from earlier kernels
-  prologue(a, sm, full, empty, blk_of, 8, c == 0);
+  prologue(a, sm, full, empty, blk_of, 1, c == 0);
   griddep_launch_dependents();  // the down kernel may start its prefetch
   if (warp == kGateWarps) {
     if (lane == 0) produce(a, sm, full, empty, blk_of, n0, n1, 0ull, a.off.gu_row);
     return;
   }
   const int nch = a.H / 32;
-  const int sub = warp / 8, wr = warp % 8;  // pair offset in the iteration, row lane
+  const int sub = warp < kSub0 ? 0 : 1;                  // pair offset in the iteration
+  const int wr = warp - sub * kSub0;                     // row lane within the sub-group
+  const int nsub = sub ? kGateWarps - kSub0 : kSub0;     // warps of the sub-group
   int cur_t = -1;
   for (int p = 0; p < a.P;) {
     const int t = p / a.k;
@@ -398,19 +415,19 @@ __global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const De
     while (np < kPairsPerIter && p + np < a.P && (p + np) / a.k == t) ++np;
     if (t != cur_t) {
       asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");  // previous x no longer read
-      stage_x(a.x + (size_t)t * a.H, a.H, xs4, xsum, threadIdx.x, kGateWarps * 32);
+      stage_x(a.x + (size_t)t * a.H, a.H, xs4, xsum, xback, threadIdx.x, kGateWarps * 32);
       asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");
       cur_t = t;
     }
-    if (sub < np) {
-      const int q = p + sub;
+    const int q = (p & 1) == sub ? p : p + 1;  // this sub-group's pair, if any
+    if (q < p + np) {
       const int s = q % a.stages;
       if (!mbar_wait(&full[s], (q / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
       const uint8_t* blk = blk_of[q];
       const uint8_t* stg = sm + (size_t)s * a.st.bytes;
-      for (int r = wr; r < rows; r += 8) {
+      for (int r = wr; r < rows; r += nsub) {
         float ag = 0.0f, au = 0.0f;
-        if (blk) gate_up_row(stg + (size_t)r * a.off.gu_row, a.off, nch, lane, a.g, xs4, xsum, ag, au);
+        if (blk) gate_up_row(stg + (size_t)r * a.off.gu_row, a.off, nch, lane, a.g, xs4, xsum, xback, ag, au);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           ag += __shfl_xor_sync(0xffffffffu, ag, o);
@@ -418,8 +435,10 @@ __global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const De
         }
         if (lane == 0) a.hbuf[(size_t)q * a.I + n0 + r] = __float2half_rn(blk ? silu_f(ag) * au : 0.0f);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // The sub-group has finished reading the stage: one arrival frees it.
+      if (sub == 0) asm volatile("bar.sync 2, %0;" ::"n"(kSub0 * 32) : "memory");
+      else asm volatile("bar.sync 3, %0;" ::"n"((kGateWarps - kSub0) * 32) : "memory");
+      if (wr == 0 && lane == 0) mbar_arrive(&empty[s]);
     }
     p += np;
   }
@@ -454,17 +473,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodePa
   int gix[kMaxHChunks];
 #pragma unroll
   for (int it = 0; it < kMaxHChunks; ++it) gix[it] = (32 * (lane + 32 * it)) / a.g;
-  for (int q = warp; q < a.P; q += kWarps) {
+  for (int q = 0; q < a.P; ++q) {
     const int s = q % a.stages;
+    if (s % kWarps != warp) continue;
     const uint8_t* blk = blk_of[q];
     if (!mbar_wait(&full[s], (q / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
     if (blk && rows > 0) {
       half2 hr[kMaxHChunks][16];
-      float hsum[kMaxHChunks];
+      float hsum[kMaxHChunks], hback[kMaxHChunks];
 #pragma unroll
       for (int it = 0; it < kMaxHChunks; ++it) {
         const int cc = lane + 32 * it;
-        if (cc < nch) hsum[it] = load_chunk<true>(a.hbuf + (size_t)q * a.I + 32 * cc, hr[it]);
+        if (cc < nch) hsum[it] = load_scaled_chunk(a.hbuf + (size_t)q * a.I + 32 * cc, hr[it], hback[it]);
       }
       const uint8_t* stg = sm + (size_t)s * a.st.bytes;
       for (int r0 = 0; r0 < rows; r0 += 8) {
@@ -482,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodePa
               if (cc < nch) {
                 const uint4 w = *reinterpret_cast<const uint4*>(row + a.off.d_q + 16 * cc);
                 const float2 s2 = __half22float2(u32_as_h2(sz[gix[it]]));  // (s, z)
-                const float d = dot32_codes(w, hr[it]);
+                const float d = (dot16_scaled(w.x, w.y, hr[it]) + dot16_scaled(w.z, w.w, hr[it] + 8)) * hback[it];
                 v[u] += s2.x * (d - s2.y * hsum[it]);
               }
             }
@@ -525,6 +545,12 @@ template <typename K>
 cudaError_t launch(K kern, const DecodeParams& a, size_t smem, int threads, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // Ask for the full shared-memory carveout so that a block of the other
+  // decode kernel fits on the same SM (the down kernel prefetches while the
+  // gate/up kernel runs).
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.G);
   cfg.blockDim = dim3(threads);
@@ -544,7 +570,7 @@ size_t carve(DecodeParams& a, size_t part, size_t budget) {
   const size_t tail = ((part + 15) & ~(size_t)15) + ((route + 15) & ~(size_t)15) + 2 * kMaxStages * 8 +
                       (size_t)a.P * 8 + 64;
   if (tail + 2 * (size_t)a.st.bytes > budget) return 0;
-  a.stages = (int)std::min<size_t>(kMaxStages, (budget - tail) / a.st.bytes);
+  a.stages = (int)std::min<size_t>(kMaxStages, (budget - tail) / a.st.bytes) & ~1;  // even
   size_t o = (size_t)a.stages * a.st.bytes;
   a.part_off = (uint32_t)o;
   o = (o + part + 15) & ~(size_t)15;
@@ -593,7 +619,7 @@ int fused_forward_routed(const ForwardArgs& fa, const float* logits, int renorm,
 
   DecodeParams ag = a;
   ag.st = stage_of(rgu, a.off.gu_row);
-  const size_t smem_g = carve(ag, (size_t)a.H * 2 + (size_t)(a.H / 32) * 4, kGateupBudget);
+  const size_t smem_g = carve(ag, (size_t)a.H * 2 + (size_t)(a.H / 32) * 8, kGateupBudget);
   DecodeParams ad = a;
   ad.st = stage_of(rdn, a.off.d_row);
   const size_t smem_d = carve(ad, (size_t)a.P * rdn * 4, kDownBudget);

@@ -74,6 +74,48 @@ __device__ __forceinline__ float dot32_codes(const uint4& w, const half2* xp) {
   return dot16_codes(w.x, w.y, xp) + dot16_codes(w.z, w.w, xp + 8);
 }
 
+// Scaled-activation dot products. A 4-bit code c masked into the low bits of
+// an FP16 pattern is the FP16 subnormal c * 2^-24 exactly (and the odd nibble,
+// masked in place, 16c * 2^-24), so no bias has to be removed. The
+// activations of a 32-element chunk are pre-scaled by an exact power of two
+// 2^s (odd-nibble pairs by 2^(s-4)) chosen so that max|x| * 2^s < 2^15; every
+// product c * x * 2^(s-24) is then an FP16 normal well inside range. The
+// caller multiplies the FP32 result by 2^(24-s).
+//   xp[0] = (x0, x4) 2^s, xp[1] = (x1, x5) 2^(s-4),
+//   xp[2] = (x2, x6) 2^s, xp[3] = (x3, x7) 2^(s-4)   (per 8-element word)
+__device__ __forceinline__ half2 dot8_scaled(uint32_t w, const half2* xp, half2 acc) {
+  const uint32_t w8 = w >> 8;
+  acc = __hfma2(u32_as_h2(w & 0x000F000Fu), xp[0], acc);
+  acc = __hfma2(u32_as_h2(w & 0x00F000F0u), xp[1], acc);
+  acc = __hfma2(u32_as_h2(w8 & 0x000F000Fu), xp[2], acc);
+  acc = __hfma2(u32_as_h2(w8 & 0x00F000F0u), xp[3], acc);
+  return acc;
+}
+
+// 16 codes (two words); each FP16 lane sums 8 products, then FP32.
+__device__ __forceinline__ float dot16_scaled(uint32_t w0, uint32_t w1, const half2* xp) {
+  half2 acc = __float2half2_rn(0.0f);
+  acc = dot8_scaled(w0, xp, acc);
+  acc = dot8_scaled(w1, xp + 4, acc);
+  return __low2float(acc) + __high2float(acc);
+}
+
+// Exponent s for a chunk whose largest magnitude is amax: amax * 2^s < 2^15.
+__device__ __forceinline__ int chunk_shift(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e;
+  frexpf(amax, &e);  // amax = m 2^e, m in [0.5, 1)
+  return 15 - e;
+}
+
+// Eight activations a[0..7] as the four scaled pairs dot8_scaled reads.
+__device__ __forceinline__ void scaled_perm8(const float* a, int s, half2* out) {
+  out[0] = __floats2half2_rn(ldexpf(a[0], s), ldexpf(a[4], s));
+  out[1] = __floats2half2_rn(ldexpf(a[1], s - 4), ldexpf(a[5], s - 4));
+  out[2] = __floats2half2_rn(ldexpf(a[2], s), ldexpf(a[6], s));
+  out[3] = __floats2half2_rn(ldexpf(a[3], s - 4), ldexpf(a[7], s - 4));
+}
+
 // Stores eight activations a[0..7] in the pair order dot8_codes reads.
 __device__ __forceinline__ void store_perm8(__half* dst, const __half* a) {
   half2* d = reinterpret_cast<half2*>(dst);
