@@ -210,6 +210,31 @@ int moe_layer_forward(const moe_expert_shape* shape, const void* x, const float*
                       int E, int k, int renorm, int32_t* ids, float* weights, const void* pool,
                       const int32_t* slot_of, int n_slots, const void* y_shared, void* y,
                       void* workspace, size_t workspace_bytes, int path, void* stream);
+/* ---- routed layer without any device allocation --------------------------
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: code running inside another component's
+ * CUDA stream capture (cudaMalloc is not permitted during capture), plugins
+ * and serving runtimes whose host framework owns every device allocation,
+ * and deployments with a fixed, pre-planned memory budget.
+ * Same arguments and result as moe_layer_forward on the MOE_PATH_GEMV path,
+ * minus the workspace: the scratch it needs (an error word and the FP16
+ * SwiGLU intermediate of every (token, choice) pair) lives in a 1 MiB array
+ * compiled into the library, held by every GPU that loads the library until
+ * the process exits. The call allocates nothing (no cudaMalloc/cudaFree).
+ * Limits: T*k*inter*2 bytes plus a header of at most 1.3 KiB <= 1 MiB, else
+ * MOE_ERR_CAPACITY; H <= 4096 and inter <= 2048 (the streamed decode
+ * kernels), else MOE_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture. Every call shares the one array: calls that overlap on
+ * the GPU (different streams, or other threads) race and corrupt each
+ * other's results; order them on one stream. Device-side error bits are not
+ * reported (unusable ids contribute nothing, as in moe_expert_forward).
+ */
+int moe_layer_forward_noalloc(const moe_expert_shape* shape, const void* x, const float* logits,
+                              int T, int E, int k, int renorm, int32_t* ids, float* weights,
+                              const void* pool, const int32_t* slot_of, int n_slots,
+                              const void* y_shared, void* y, void* stream);
 /* Clear (zero) the workspace error word: enqueued on `stream`. */
 int moe_workspace_clear_flags(void* workspace, void* stream);
 /* Read the workspace error word into *flags_out: synchronises `stream`. */

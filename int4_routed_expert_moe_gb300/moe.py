@@ -87,6 +87,7 @@ _SIGS = {
     "moe_forward_workspace_bytes": (_SZ, [_SHAPE, _I, _I, _I, _I]),
     "moe_expert_forward": (_I, [_SHAPE, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
     "moe_layer_forward": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
+    "moe_layer_forward_noalloc": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P]),
     "moe_workspace_clear_flags": (_I, [_P, _P]),
     "moe_workspace_flags": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_shared_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -281,6 +282,23 @@ def moe_layer_forward(shape, x: torch.Tensor, logits: torch.Tensor, k: int, reno
         _dev(pool, torch.uint8, "pool", n_slots * bb), _dev(slot_of, torch.int32, "slot_of", E), n_slots,
         _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True), _dev(y, torch.float16, "y", T * H),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), path, _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_noalloc(shape, x: torch.Tensor, logits: torch.Tensor, k: int, renorm: bool,
+                              ids: torch.Tensor, weights: torch.Tensor, pool: torch.Tensor,
+                              slot_of: torch.Tensor, n_slots: int, y_shared: torch.Tensor | None,
+                              y: torch.Tensor, stream=None) -> None:
+    """moe_layer_forward without a workspace (scratch is a fixed array inside the library)."""
+    H, I, g = shape
+    T, E = logits.shape
+    s = _shape(shape)
+    bb = moe_expert_block_bytes(shape)
+    _check(_lib.moe_layer_forward_noalloc(
+        ctypes.byref(s), _dev(x, torch.float16, "x", T * H), _dev(logits, torch.float32, "logits"), T, E,
+        k, int(bool(renorm)), _dev(ids, torch.int32, "ids", T * k), _dev(weights, torch.float32, "weights", T * k),
+        _dev(pool, torch.uint8, "pool", n_slots * bb), _dev(slot_of, torch.int32, "slot_of", E), n_slots,
+        _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True), _dev(y, torch.float16, "y", T * H),
+        _stream(stream)), "moe_layer_forward_noalloc")
 
 
 def moe_workspace_clear_flags(workspace: torch.Tensor, stream=None) -> None:
