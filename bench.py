@@ -42,10 +42,12 @@ METRIC = "MoE-layer decode tokens/s (expert-weight HBM GB/s in roofline)"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=512)
-    ap.add_argument("--warmup", type=int, default=128)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="olmoe_decode", choices=["olmoe_decode"])
+    ap.add_argument("--workload", default="olmoe_decode",
+                    choices=["olmoe_decode", "olmoe_partial", "large_fanout_b1", "large_fanout_b16",
+                             "large_fanout_b256"])
     ap.add_argument("--graph-window", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -246,7 +248,8 @@ class DecodeWorkload:
 def run_ours(args, world, rank, local):
     from int4_routed_expert_moe_gb300 import moe
     seed = synth.BASE_SEED + 1
-    K, W = args.steps, args.warmup
+    K = args.steps or 512
+    W = args.warmup if args.warmup is not None else 128
     wl = DecodeWorkload(moe, seed, K + W, rank)
     stream = torch.cuda.current_stream()
     win = max(1, args.graph_window)
@@ -347,6 +350,162 @@ def run_ours(args, world, rank, local):
     return out
 
 
+def base_line(metric, value, unit, world, K, W, ms, config, hib=True):
+    return {"metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(ms / K, 5), "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded; random-init INT4 experts)", "config": config}
+
+
+def run_partial(args, world, rank):
+    """OLMoE shape with partial residency: 30 of 64 slots per layer, decayed
+    counts (0.9 per step), Zipf(1.0) popularity per layer; per layer and step
+    the router runs on the GPU, its ids reach the host, the residency manager
+    decides and streams misses from pinned host RAM on a side stream, then the
+    experts run from the managed pool. Timed: K decode steps after W."""
+    from int4_routed_expert_moe_gb300 import moe
+    wl = synth.WORKLOADS["olmoe_partial"]
+    L, H, I, E, k, g, C = wl["L"], wl["H"], wl["I"], wl["E"], wl["k"], wl["g"], wl["C"]
+    shape = (H, I, g)
+    K = args.steps or wl["seqs"] * wl["steps"]
+    W = args.warmup if args.warmup is not None else wl["warm_seqs"] * wl["steps"]
+    dev = torch.device("cuda")
+    bb = moe.moe_expert_block_bytes(shape)
+    seed = synth.BASE_SEED + 3 + rank
+    src = torch.empty((L, E, bb), dtype=torch.uint8).pin_memory()
+    for l in range(L):  # generated on the device, kept as the pinned host source
+        src[l].copy_(synth.device_pool(E, H, I, g, seed * 100 + l))
+    pool = torch.zeros((L, C, bb), dtype=torch.uint8, device=dev)
+    slot_of = torch.full((L, E), -1, dtype=torch.int32, device=dev)
+    copy = torch.cuda.Stream()
+    h = moe.moe_residency_create(dict(layers=L, experts=E, slots=C, spares=0, max_ids_per_step=k,
+                                      block_bytes=bb, decay=wl["decay"]), src, pool, slot_of,
+                                 torch.cuda.current_stream(), copy)
+    n = W + K
+    ranks = np.stack([synth.zipf_ranks(seed, l, E) for l in range(L)])  # [L][E]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    gum = -torch.log(-torch.log(torch.rand((n, L, 1, E), generator=gen, device=dev).clamp_min(1e-20)))
+    logits = (-wl["alpha"] * torch.log(torch.from_numpy(ranks).float().to(dev)))[None, :, None, :] + gum
+    x0 = torch.randn((n, 1, H), generator=gen, device=dev).half()
+    ids = torch.empty((L, 1, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, 1, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, 1, H), dtype=torch.float16, device=dev)
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, 1, k, E, moe.MOE_PATH_GEMV), dtype=torch.uint8,
+                     device=dev)
+    ids_host = torch.empty((k,), dtype=torch.int32).pin_memory()
+
+    def step(s):
+        for l in range(L):
+            moe.moe_route(logits[s, l], k, wl["renorm"], ids[l], w[l])
+            ids_host.copy_(ids[l].view(-1), non_blocking=True)
+            torch.cuda.current_stream().synchronize()  # the step's ids reach the host
+            moe.moe_residency_prepare(h, l, ids_host.numpy())
+            x = x0[s] if l == 0 else y[l - 1]
+            moe.moe_expert_forward(shape, x, ids[l], w[l], E, pool[l], slot_of[l], C, None, y[l], ws,
+                                   moe.MOE_PATH_GEMV)
+
+    try:
+        for s in range(W):
+            step(s)
+        torch.cuda.synchronize()
+        st0 = moe.moe_residency_get_stats(h)
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        t0 = time.perf_counter()
+        for s in range(W, W + K):
+            step(s)
+        ev1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+        st1 = moe.moe_residency_get_stats(h)
+        assert moe.moe_workspace_flags(ws) == 0
+    finally:
+        moe.moe_residency_destroy(h)
+    hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
+    h2d = st1["h2d_bytes"] - st0["h2d_bytes"]
+    out = base_line(METRIC, K * world / (ms / 1e3), "tokens/s", world, K, W, ms,
+                    {"workload": "olmoe_partial", "layers": L, "hidden": H, "experts": E, "top_k": k,
+                     "inter": I, "group": g, "slots": C, "decay": wl["decay"], "zipf_alpha": wl["alpha"],
+                     "tokens_per_step": 1,
+                     "launch": "eager; per layer: route, D2H of ids, host decision, H2D misses, experts"})
+    out["residency"] = {"hit_rate": round(hits / max(1, hits + misses), 4), "misses_per_token": round(misses / K, 3),
+                        "h2d_gb": round(h2d / 1e9, 3), "h2d_gbs": round(h2d / (ms / 1e3) / 1e9, 2),
+                        "wall_s": round(wall, 3)}
+    return out
+
+
+def run_fanout(args, world, rank, T):
+    """Large fan-out stack: 48 layers x 512 experts (hidden 2048, inter 512,
+    top-10 renormalised, Zipf(1.1) popularity), ~41 GB of INT4 experts all
+    resident; T tokens per step through all 48 layers."""
+    from int4_routed_expert_moe_gb300 import moe
+    wl = synth.WORKLOADS["large_fanout"]
+    L, H, I, E, k, g = wl["L"], wl["H"], wl["I"], wl["E"], wl["k"], wl["g"]
+    shape = (H, I, g)
+    K = args.steps or 64
+    W = args.warmup if args.warmup is not None else 8
+    dev = torch.device("cuda")
+    bb = moe.moe_expert_block_bytes(shape)
+    seed = synth.BASE_SEED + 5 + rank
+    pool = synth.device_pool(L * E, H, I, g, seed, chunk=256)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+    n = W + K
+    ranks = np.stack([synth.zipf_ranks(seed, l, E) for l in range(L)])
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    base = (-wl["alpha"] * torch.log(torch.from_numpy(ranks).float().to(dev)))[:, None, :]
+    x0 = torch.randn((n, T, H), generator=gen, device=dev).half()
+    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, T, H), dtype=torch.float16, device=dev)
+    path = moe.MOE_PATH_GEMV
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, T, k, E, path), dtype=torch.uint8, device=dev)
+    n_lg = n + 4
+    logits = torch.empty((n_lg, L, T, E), device=dev)  # drawn before the timed region
+    for s in range(n_lg):
+        u = torch.rand((L, T, E), generator=gen, device=dev).clamp_min(1e-20)
+        logits[s] = base - torch.log(-torch.log(u))
+    uniq = []
+
+    def step(s, count=False):
+        for l in range(L):
+            x = x0[s % n] if l == 0 else y[l - 1]
+            moe.moe_layer_forward(shape, x, logits[s, l], k, wl["renorm"], ids[l], w[l],
+                                  pool[l * E:(l + 1) * E], slot_of, E, None, y[l], ws, path)
+        if count:
+            uniq.append(sum(len(torch.unique(ids[l])) for l in range(L)))
+
+    for s in range(W):
+        step(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for s in range(W, W + K):
+        step(s)
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    for s in range(4):  # distinct experts per step, counted outside the timed region
+        step(W + s, count=True)
+    u_mean = float(np.mean(uniq))
+    peak, peak_src = measured_peaks()
+    gbs = u_mean * bb * K / (ms / 1e3) / 1e9
+    out = base_line(METRIC, K * T * world / (ms / 1e3), "tokens/s", world, K, W, ms,
+                    {"workload": f"large_fanout_b{T}", "layers": L, "hidden": H, "experts": E, "top_k": k,
+                     "inter": I, "group": g, "tokens_per_step": T, "zipf_alpha": wl["alpha"],
+                     "launch": "eager moe_layer_forward per layer",
+                     "l2": "inputs larger than L2: 41 GB pool"})
+    out["expert_hbm_gbs_step"] = round(gbs, 1)
+    out["expert_hbm_frac_step"] = round(gbs / peak, 4)
+    out["unique_experts_per_step"] = round(u_mean, 1)
+    return out
+
+
 def run_e2e(moe, wl, n, W):
     """Same metric through the public API with host buffers: per step the
     token's activations and the 16 layers' router logits are copied from
@@ -432,7 +591,8 @@ def run_reference(args):
     from oracle import moe_oracle
     wl = synth.WORKLOADS["olmoe_decode"]
     H, I, E, k, g, L = wl["H"], wl["I"], wl["E"], wl["k"], wl["g"], wl["L"]
-    K, W = args.steps, args.warmup
+    K = args.steps or 512
+    W = args.warmup if args.warmup is not None else 128
     seed = synth.BASE_SEED + 2
 
     def one(s):
@@ -477,7 +637,12 @@ def main():
         return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
-    out = run_ours(args, world, rank, local)
+    if args.workload == "olmoe_partial":
+        out = run_partial(args, world, rank)
+    elif args.workload.startswith("large_fanout_b"):
+        out = run_fanout(args, world, rank, int(args.workload.split("_b")[1]))
+    else:
+        out = run_ours(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
