@@ -126,7 +126,7 @@ __device__ __forceinline__ float load_scaled_chunk(const __half* src, half2 (&xp
   const int sh = chunk_shift(amax);
 #pragma unroll
   for (int q = 0; q < 4; ++q) scaled_perm8(v + 8 * q, sh, xp + 4 * q);
-  back = ldexpf(1.0f, 24 - sh);
+  back = pow2f(24 - sh);
   return sum;
 }
 
@@ -153,65 +153,101 @@ struct DecodeParams {
 
 // Per-block routing state in shared memory.
 struct RouteSmem {
-  int32_t* ids;   // [P]
-  float* w;       // [P]
-  float* red;     // [32 + 4] reduction scratch
-  int32_t* bad;   // [4]: any NaN/+inf, count of -inf
-  float* lg;      // [E]   logits of the token being routed
-  int32_t* rank;  // [E]
+  int32_t* ids;    // [P]
+  float* w;        // [P]
+  float* exsel;    // [P]   exp(logit - max) of each chosen expert
+  float* sall;     // [T]   softmax denominator per token
+  float* red;      // [ceil(E/32)] sums of exp over 32-expert slices
+  int32_t* bad;    // [4]:  any NaN/+inf, count of -inf, max key
+  float* lg;       // [E]   logits of the token being routed
+  int32_t* rank;   // [E]
+  int32_t* slot;   // [E]   copy of slot_of (when slot_tab)
 };
+
+// Experts up to this count get a shared-memory copy of slot_of.
+constexpr int kSlotTableMax = 1024;
+
+__host__ __device__ inline size_t route_smem_bytes(int P, int T, int E, bool routing) {
+  return (size_t)P * 12 + (size_t)T * 4 + (size_t)(4 + (E + 31) / 32) * 4 + (routing ? (size_t)E * 8 : 0) +
+         (E <= kSlotTableMax ? (size_t)E * 4 : 0);
+}
 
 __device__ __forceinline__ RouteSmem route_smem(const DecodeParams& a, uint8_t* sm) {
   RouteSmem r;
   uint8_t* b = sm + a.route_off;
   r.ids = reinterpret_cast<int32_t*>(b);
-  r.w = reinterpret_cast<float*>(b + (size_t)a.P * 4);
-  r.red = reinterpret_cast<float*>(b + (size_t)a.P * 8);
-  r.bad = reinterpret_cast<int32_t*>(r.red + 36);
+  r.w = reinterpret_cast<float*>(r.ids + a.P);
+  r.exsel = r.w + a.P;
+  r.sall = r.exsel + a.P;
+  r.red = r.sall + a.T;
+  r.bad = reinterpret_cast<int32_t*>(r.red + (a.E + 31) / 32);
   r.lg = reinterpret_cast<float*>(r.bad + 4);
-  r.rank = reinterpret_cast<int32_t*>(r.lg + a.E);
+  r.rank = reinterpret_cast<int32_t*>(r.lg + (a.logits ? a.E : 0));
+  r.slot = r.rank + (a.logits ? a.E : 0);
   return r;
 }
 
-// Block-wide fixed-order sum of one value per thread (all threads call).
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.0f;
-    for (int w = 0; w < nw; ++w) t += red[w];
-    red[nw] = t;
+// Order-preserving int key of a float that is not NaN (for atomicMax).
+__device__ __forceinline__ int32_t float_key(float v) {
+  const int32_t b = __float_as_int(v);
+  return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float key_float(int32_t k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
+__device__ __forceinline__ const uint8_t* resolve_slot(const DecodeParams& a, int e, int s) {
+  if (e < 0 || e >= a.E || s < 0 || s >= a.n_slots) return nullptr;
+  return a.pool + (size_t)s * a.block_bytes;
+}
+
+// Expert block of expert e, with unusable-id reporting by the writer block.
+__device__ __forceinline__ const uint8_t* resolve_report(const DecodeParams& a, const RouteSmem& r, int e,
+                                                         bool table, bool writer) {
+  const int s = (e < 0 || e >= a.E) ? -1 : (table ? r.slot[e] : a.slot_of[e]);
+  const uint8_t* b = resolve_slot(a, e, s);
+  if (writer && !b) {
+    if (e != -1 && (e < 0 || e >= a.E)) atomicOr(a.flags, 2);
+    else if (e >= 0) atomicOr(a.flags, 1);
   }
-  __syncthreads();
-  return red[nw];
+  return b;
 }
 
 // "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
 // experts of each token. Same definition as moe_route: top-k by (logit desc,
 // index asc), softmax over all E, optionally renormalised over the k; a
 // token with NaN/+inf logits or all -inf gets ids -1 and weights 0.
-__device__ void route_block(const DecodeParams& a, const RouteSmem& r) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  // Rank counts are split over threads: thread (e, part) counts the experts
-  // of one slice of j that precede e; integer sums, so the order is free.
+// Per token: (A) logits to shared memory; (B) rank counts split over threads
+// (thread (e, part) counts the experts of one slice of j that precede e;
+// integer sums, so the order is free) and the maximum logit; (C) the chosen
+// experts, their blocks and exp(logit - max), and the sum of exp over each
+// slice of 32 experts (one warp, fixed tree); the slice sums are then added
+// in slice order, so the denominator does not depend on the block size.
+// Three block barriers per token. The weights are formed afterwards by warp
+// 0 (finish_weights).
+__device__ void route_block(const DecodeParams& a, const RouteSmem& r, const uint8_t** blk_of, bool table,
+                            bool writer) {
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  const int nslices = (a.E + 31) / 32;
   const int parts = max(1, nt / a.E);
   const int span = (a.E + parts - 1) / parts;
   for (int t = 0; t < a.T; ++t) {
-    if (tid == 0) r.bad[0] = r.bad[1] = 0;
+    // (A)
+    if (tid == 0) {
+      r.bad[0] = r.bad[1] = 0;
+      r.bad[2] = float_key(-INFINITY);
+    }
     for (int e = tid; e < a.E; e += nt) {
       r.lg[e] = a.logits[(size_t)t * a.E + e];
       r.rank[e] = 0;
+      if (t == 0 && table) r.slot[e] = a.slot_of[e];
     }
     __syncthreads();
+    // (B)
     for (int i = tid; i < a.E * parts; i += nt) {
       const int e = i % a.E, part = i / a.E;
       const float v = r.lg[e];
       if (part == 0) {
         if (isnan(v) || v == INFINITY) atomicOr(&r.bad[0], 1);
+        else atomicMax(&r.bad[2], float_key(v));
         if (v == -INFINITY) atomicAdd(&r.bad[1], 1);
       }
       int cnt = 0;
@@ -223,44 +259,62 @@ __device__ void route_block(const DecodeParams& a, const RouteSmem& r) {
       if (cnt) atomicAdd(&r.rank[e], cnt);
     }
     __syncthreads();
-    for (int e = tid; e < a.E; e += nt)
-      if (r.rank[e] < a.k) r.ids[t * a.k + r.rank[e]] = e;
-    __syncthreads();
+    // (C)
     const bool token_bad = r.bad[0] != 0 || r.bad[1] == a.E;
-    const float m = token_bad ? 0.0f : r.lg[r.ids[t * a.k]];
-    float part_sum = 0.0f;
-    if (!token_bad)
-      for (int e = tid; e < a.E; e += nt) part_sum += expf(r.lg[e] - m);
-    const float s_all = block_sum(part_sum, r.red);
-    // Warp 0: lane j < k owns choice j; the selected sum in fixed lane order.
-    if (tid < 32) {
-      const int q = t * a.k + tid;
-      const float ej = (tid < a.k && !token_bad) ? expf(r.lg[r.ids[q]] - m) : 0.0f;
-      float s_sel = ej;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s_sel += __shfl_xor_sync(0xffffffffu, s_sel, o);
-      if (tid < a.k) {
-        if (token_bad) {
-          r.ids[q] = -1;
-          r.w[q] = 0.0f;
-        } else {
-          r.w[q] = ej / (a.renorm ? s_sel : s_all);
+    const float m = key_float(r.bad[2]);
+    for (int base = warp * 32; base < a.E; base += nt) {  // warp-uniform: one slice
+      const int e = base + lane;
+      float ex = 0.0f;
+      if (e < a.E) {
+        ex = token_bad ? 0.0f : expf(r.lg[e] - m);
+        const int rk = r.rank[e];
+        if (rk < a.k) {
+          const int q = t * a.k + rk;
+          const int id = token_bad ? -1 : e;
+          r.ids[q] = id;
+          r.exsel[q] = ex;
+          blk_of[q] = resolve_report(a, r, id, table, writer);
+          if (writer && a.ids_out) a.ids_out[q] = id;
         }
       }
+      ex = warp_sum(ex);
+      if (lane == 0) r.red[base / 32] = ex;
     }
     __syncthreads();
+    if (tid == 0) {
+      float s_all = 0.0f;
+      for (int i = 0; i < nslices; ++i) s_all += r.red[i];
+      r.sall[t] = s_all;
+    }
   }
 }
 
-__device__ __forceinline__ const uint8_t* resolve(const DecodeParams& a, int e) {
-  if (e < 0 || e >= a.E) return nullptr;
-  const int s = a.slot_of[e];
-  if (s < 0 || s >= a.n_slots) return nullptr;
-  return a.pool + (size_t)s * a.block_bytes;
+// Warp 0 after route_block: w[q] = exp(l - max) / (sum over all E, or over
+// the k chosen, in choice order); 0 for a token without a routing.
+__device__ __forceinline__ void finish_weights(const DecodeParams& a, const RouteSmem& r, bool writer) {
+  __syncwarp();
+  for (int q = threadIdx.x; q < a.P; q += 32) {
+    const int t = q / a.k;
+    float wq = 0.0f;
+    if (r.ids[q] >= 0) {
+      float den = r.sall[t];
+      if (a.renorm) {
+        den = 0.0f;
+        for (int j = 0; j < a.k; ++j) den += r.exsel[t * a.k + j];
+      }
+      wq = r.exsel[q] / den;
+    }
+    r.w[q] = wq;
+    if (writer && a.wts_out) a.wts_out[q] = wq;
+  }
+  __syncwarp();
 }
 
 // Shared prologue: barriers, routing (or the given ids), the expert block of
-// every pair (resolved once), unusable-id reporting and routed outputs.
+// every pair (resolved once), unusable-id reporting and routed outputs. On
+// return blk_of and ids are visible to the whole block; w is complete in
+// warp 0 (which forms it when the block routes itself) and becomes visible
+// to the other warps at their next barrier with warp 0.
 __device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, uint64_t* full,
                                          uint64_t* empty, const uint8_t** blk_of, int empty_count,
                                          bool writer) {
@@ -272,29 +326,27 @@ __device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, uin
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   const RouteSmem r = route_smem(a, sm);
+  const bool table = a.E <= kSlotTableMax;
   if (a.logits) {
-    route_block(a, r);
+    route_block(a, r, blk_of, table, writer);
+    if (threadIdx.x < 32) finish_weights(a, r, writer);
   } else {
     for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
       r.ids[p] = a.ids[p];
       r.w[p] = a.wts[p];
     }
+    if (table)
+      for (int e = threadIdx.x; e < a.E; e += blockDim.x) r.slot[e] = a.slot_of[e];
+    __syncthreads();
+    for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
+      blk_of[p] = resolve_report(a, r, r.ids[p], table, writer);
+      if (writer) {
+        if (a.ids_out) a.ids_out[p] = r.ids[p];
+        if (a.wts_out) a.wts_out[p] = r.w[p];
+      }
+    }
     __syncthreads();
   }
-  for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
-    const int e = r.ids[p];
-    const uint8_t* b = resolve(a, e);
-    blk_of[p] = b;
-    if (writer) {
-      if (!b) {
-        if (e != -1 && (e < 0 || e >= a.E)) atomicOr(a.flags, 2);
-        else if (e >= 0) atomicOr(a.flags, 1);
-      }
-      if (a.ids_out) a.ids_out[p] = e;
-      if (a.wts_out) a.wts_out[p] = r.w[p];
-    }
-  }
-  __syncthreads();
 }
 
 // Producer loop of one kernel: for each pair, wait for the stage to be free,
@@ -349,35 +401,40 @@ __device__ __forceinline__ void stage_x(const __half* __restrict__ src, int H, u
       xs4[xslot(cc, i)] = o;
     }
     xsum[cc] = sum;
-    xback[cc] = ldexpf(1.0f, 24 - sh);
+    xback[cc] = pow2f(24 - sh);
   }
 }
 
 // Gate and up sums of one row for one lane (before the warp sum):
 // s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks cc = lane + 32 it.
+// gq / xo: the lane's group index and activation slots per chunk, computed
+// once per kernel.
+template <int NC>
 __device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffsets& off, int nch,
-                                            int lane, int g, const uint4* xs4, const float* xsum,
-                                            const float* xback, float& ag, float& au) {
-  const uint8_t* rg = row + off.gu_q_gate;
-  const uint8_t* ru = row + off.gu_q_up;
+                                            int lane, const int* gq, const int* xo, const uint4* xs4,
+                                            const float* xsum, const float* xback, float& ag, float& au) {
   const uint2* sz = reinterpret_cast<const uint2*>(row + off.gu_sz);  // quads per group
-  for (int cc = lane; cc < nch; cc += 32) {
-    const uint4 wg = *reinterpret_cast<const uint4*>(rg + 16 * cc);
-    const uint4 wu = *reinterpret_cast<const uint4*>(ru + 16 * cc);
-    const uint2 q = sz[(32 * cc) / g];
-    uint4 xv[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) xv[i] = xs4[xslot(cc, i)];
-    const half2* xa = reinterpret_cast<const half2*>(&xv[0]);  // pieces 0, 1 are contiguous
-    const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
-    const float back = xback[cc];
-    const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
-    const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
-    const float2 sgz = __half22float2(u32_as_h2(q.x));  // (s_gate, z_gate)
-    const float2 suz = __half22float2(u32_as_h2(q.y));  // (s_up, z_up)
-    const float xsm = xsum[cc];
-    ag += sgz.x * (dg - sgz.y * xsm);
-    au += suz.x * (du - suz.y * xsm);
+  for (int it = 0; it < NC; ++it) {
+    const int cc = lane + 32 * it;
+    if (cc < nch) {
+      const uint4 wg = *reinterpret_cast<const uint4*>(row + off.gu_q_gate + 16 * cc);
+      const uint4 wu = *reinterpret_cast<const uint4*>(row + off.gu_q_up + 16 * cc);
+      const uint2 q = sz[gq[it]];
+      uint4 xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs4[xo[4 * it + i]];
+      const half2* xa = reinterpret_cast<const half2*>(&xv[0]);  // pieces 0, 1 are contiguous
+      const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
+      const float back = xback[cc];
+      const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
+      const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
+      const float2 sgz = __half22float2(u32_as_h2(q.x));  // (s_gate, z_gate)
+      const float2 suz = __half22float2(u32_as_h2(q.y));  // (s_up, z_up)
+      const float xsm = xsum[cc];
+      ag += sgz.x * (dg - sgz.y * xsm);
+      au += suz.x * (du - suz.y * xsm);
+    }
   }
 }
 
@@ -385,7 +442,8 @@ __device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffse
 // Stage: the block's gate/up rows [R][gu_row] (codes, scales and zeros of
 // both projections per row). Each iteration covers kPairsPerIter pairs of one
 // token: warp w takes row w % 8 (+8, ...) of pair p + w / 8.
-__global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const DecodeParams a) {
+template <int NC>
+__global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const DecodeParams a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -405,6 +463,14 @@ __global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const De
     return;
   }
   const int nch = a.H / 32;
+  int gq[NC], xo[4 * NC];
+#pragma unroll
+  for (int it = 0; it < NC; ++it) {
+    const int cc = lane + 32 * it;
+    gq[it] = (32 * cc) / a.g;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xo[4 * it + i] = xslot(cc, i);
+  }
   const int sub = warp < kSub0 ? 0 : 1;                  // pair offset in the iteration
   const int wr = warp - sub * kSub0;                     // row lane within the sub-group
   const int nsub = sub ? kGateWarps - kSub0 : kSub0;     // warps of the sub-group
@@ -427,7 +493,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const De
       const uint8_t* stg = sm + (size_t)s * a.st.bytes;
       for (int r = wr; r < rows; r += nsub) {
         float ag = 0.0f, au = 0.0f;
-        if (blk) gate_up_row(stg + (size_t)r * a.off.gu_row, a.off, nch, lane, a.g, xs4, xsum, xback, ag, au);
+        if (blk) gate_up_row<NC>(stg + (size_t)r * a.off.gu_row, a.off, nch, lane, gq, xo, xs4, xsum, xback, ag, au);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           ag += __shfl_xor_sync(0xffffffffu, ag, o);
@@ -448,7 +514,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) decode_gateup_kernel(const De
 // Stage: the block's down rows [R][d_row] (codes, then scale/zero pairs).
 // Warp w computes the block's rows for pairs w, w+8, ...
 template <int kMaxHChunks>
-__global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(const DecodeParams a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_down_kernel(const DecodeParams a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -566,7 +632,7 @@ cudaError_t launch(K kern, const DecodeParams& a, size_t smem, int threads, cuda
 
 // Carve-up: stages | part | route | barriers | block table. Returns total bytes.
 size_t carve(DecodeParams& a, size_t part, size_t budget) {
-  const size_t route = (size_t)a.P * 8 + 40 * 4 + (a.logits ? (size_t)a.E * 8 : 0);
+  const size_t route = route_smem_bytes(a.P, a.T, a.E, a.logits != nullptr);
   const size_t tail = ((part + 15) & ~(size_t)15) + ((route + 15) & ~(size_t)15) + 2 * kMaxStages * 8 +
                       (size_t)a.P * 8 + 64;
   if (tail + 2 * (size_t)a.st.bytes > budget) return 0;
@@ -625,7 +691,8 @@ int fused_forward_routed(const ForwardArgs& fa, const float* logits, int renorm,
   const size_t smem_d = carve(ad, (size_t)a.P * rdn * 4, kDownBudget);
   if (!smem_g || !smem_d) return fail(MOE_ERR_UNSUPPORTED, "streamed decode: shapes exceed shared memory");
   cudaError_t e;
-  e = launch(decode_gateup_kernel, ag, smem_g, kGateThreads, fa.stream);
+  if (xc <= 2) e = launch(decode_gateup_kernel<2>, ag, smem_g, kGateThreads, fa.stream);
+  else e = launch(decode_gateup_kernel<4>, ag, smem_g, kGateThreads, fa.stream);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode gate/up launch: %s", cudaGetErrorString(e));
   if (hc <= 1) e = launch(decode_down_kernel<1>, ad, smem_d, kThreads, fa.stream);
   else e = launch(decode_down_kernel<2>, ad, smem_d, kThreads, fa.stream);

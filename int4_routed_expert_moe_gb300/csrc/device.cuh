@@ -101,19 +101,25 @@ __device__ __forceinline__ float dot16_scaled(uint32_t w0, uint32_t w1, const ha
 }
 
 // Exponent s for a chunk whose largest magnitude is amax: amax * 2^s < 2^15.
+// (Clamped to [-100, 100] so that 2^s, 2^(s-4) and 2^(24-s) stay FP32 normals.)
 __device__ __forceinline__ int chunk_shift(float amax) {
   if (!(amax > 0.0f)) return 0;
   int e;
   frexpf(amax, &e);  // amax = m 2^e, m in [0.5, 1)
-  return 15 - e;
+  return max(-100, min(100, 15 - e));
 }
 
-// Eight activations a[0..7] as the four scaled pairs dot8_scaled reads.
+// 2^e as an FP32 value built from its exponent bits (|e| <= 126).
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Eight activations a[0..7] as the four scaled pairs dot8_scaled reads; the
+// power-of-two products are exact in FP32, then rounded once to FP16.
 __device__ __forceinline__ void scaled_perm8(const float* a, int s, half2* out) {
-  out[0] = __floats2half2_rn(ldexpf(a[0], s), ldexpf(a[4], s));
-  out[1] = __floats2half2_rn(ldexpf(a[1], s - 4), ldexpf(a[5], s - 4));
-  out[2] = __floats2half2_rn(ldexpf(a[2], s), ldexpf(a[6], s));
-  out[3] = __floats2half2_rn(ldexpf(a[3], s - 4), ldexpf(a[7], s - 4));
+  const float m0 = pow2f(s), m1 = pow2f(s - 4);
+  out[0] = __floats2half2_rn(a[0] * m0, a[4] * m0);
+  out[1] = __floats2half2_rn(a[1] * m1, a[5] * m1);
+  out[2] = __floats2half2_rn(a[2] * m0, a[6] * m0);
+  out[3] = __floats2half2_rn(a[3] * m1, a[7] * m1);
 }
 
 // Stores eight activations a[0..7] in the pair order dot8_codes reads.
