@@ -174,17 +174,29 @@ int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* offsets,
  *           an id outside [-1, E); bit 2 = a bounded device wait expired (the
  *           result is not valid). Read it with moe_workspace_flags.
  * path      MOE_PATH_AUTO: GEMV up to 256 (token, choice) pairs, else grouped.
- *           MOE_PATH_GEMV: decode dequant-GEMV. One persistent kernel (one
- *             block per SM) streams each block's slice of the chosen experts
- *             through shared memory with bulk async copies, computes gate/up
- *             rows, publishes h per pair, and runs the down projection and
- *             the top-k combine as soon as a pair's h is complete. Falls back
- *             to the unfused kernels when its shared memory does not fit.
- *           MOE_PATH_GROUPED: token-sorted tensor-core grouped GEMM.
- *           MOE_PATH_GEMV_UNFUSED: the two-kernel dequant-GEMV (gate/up,
- *             then down + combine), kept for comparison.
- * Arithmetic: products in FP16 pairs of at most 8 terms, FP32 accumulation,
- * the SwiGLU intermediate rounded to FP16 before the down projection.
+ *           MOE_PATH_GEMV: decode dequant-GEMV. Two streaming kernels (one
+ *             block per SM each) chained with programmatic dependent launch:
+ *             the first streams each block's rows of the chosen experts'
+ *             gate/up sections through shared memory with bulk async copies
+ *             and writes h = silu(gate) * up per pair; the second, started
+ *             while the first runs, prefetches the down rows, then computes
+ *             the down projection and the top-k combine. Falls back to the
+ *             unfused kernels when its shared memory does not fit (H > 4096
+ *             or I > 2048).
+ *           MOE_PATH_GROUPED: token-sorted tensor-core grouped GEMM: pairs
+ *             sorted by expert, tiles of up to 128 pairs; tcgen05 MMAs with
+ *             the expert rows as the 128-row operand (expanded from INT4 to
+ *             FP16 in shared memory) and the gathered activations as the
+ *             pair operand, FP32 accumulation in tensor memory; then the
+ *             down GEMM and a fixed-order combine. Limits: E <= 1024,
+ *             T*k <= 65536; y and y_shared 16-byte aligned.
+ *           MOE_PATH_GEMV_UNFUSED: the two-kernel dequant-GEMV without the
+ *             shared-memory streaming, kept for comparison.
+ * Arithmetic: GEMV paths form products in FP16 pairs of at most 8 terms with
+ * FP32 accumulation; the grouped path expands each weight to FP16
+ * (q - z) * s (one rounding for an integer zero point) and accumulates in
+ * FP32 in the tensor cores. All paths round the SwiGLU intermediate to FP16
+ * before the down projection.
  */
 enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2, MOE_PATH_GEMV_UNFUSED = 3 };
 size_t moe_forward_workspace_bytes(const moe_expert_shape* shape, int T, int k,
