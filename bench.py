@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 from int4_routed_expert_moe_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer decode tokens/s (expert-weight HBM GB/s in roofline)"
+METRIC_PREFILL = "MoE-layer prefill tokens/s (tensor-core TFLOP/s in roofline)"
 
 
 def parse():
@@ -46,8 +47,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="olmoe_decode",
-                    choices=["olmoe_decode", "olmoe_partial", "large_fanout_b1", "large_fanout_b16",
-                             "large_fanout_b256"])
+                    choices=["olmoe_decode", "olmoe_partial", "olmoe_prefill", "large_fanout_b1",
+                             "large_fanout_b16", "large_fanout_b256"])
     ap.add_argument("--graph-window", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -196,6 +197,18 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     return 6800.0, "fallback 6.8 TB/s"
+
+
+def measured_tensor_peak(sustained):
+    """Dense FP16 tensor peak in TFLOP/s: the measured cuBLAS bf16 figure
+    (FP16 and BF16 run at the same nominal rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d[key]), f"measured (MEASURED_PEAKS.json {key}; fp16 = bf16 nominal rate)"
+    return (1700.0, "fallback 1.7 PFLOP/s sustained") if sustained else (1900.0, "fallback 1.9 PFLOP/s")
 
 
 # --------------------------------------------------------------------------
@@ -506,6 +519,138 @@ def run_fanout(args, world, rank, T):
     return out
 
 
+def run_prefill(args, world, rank):
+    """OLMoE-shaped prefill: 512 tokens through 16 routed layers (uniform
+    router logits, 4096 (token, choice) pairs per layer over all 64 experts),
+    grouped tensor-core path, layers chained; then the non-routed FP16 SwiGLU
+    FFN of 2048 tokens (H 2048, Is 4096) as its own leg."""
+    from int4_routed_expert_moe_gb300 import moe
+    wl = synth.WORKLOADS["olmoe_prefill"]
+    L, H, I, E, k, g, T = wl["L"], wl["H"], wl["I"], wl["E"], wl["k"], wl["g"], wl["T"]
+    Ts, Is = wl["Ts"], wl["Is"]
+    shape = (H, I, g)
+    K = args.steps or 20
+    W = max(3, args.warmup if args.warmup is not None else 3)
+    dev = torch.device("cuda")
+    seed = synth.BASE_SEED + 4 + rank
+    pool = synth.device_pool(L * E, H, I, g, seed)
+    bb = moe.moe_expert_block_bytes(shape)
+    slot_of = torch.arange(E, dtype=torch.int32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    n = W + K
+    x0 = torch.randn((n, T, H), generator=gen, device=dev).half()
+    logits = torch.rand((n, L, T, E), generator=gen, device=dev)
+    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, T, H), dtype=torch.float16, device=dev)
+    path = moe.MOE_PATH_GROUPED
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, T, k, E, path), dtype=torch.uint8, device=dev)
+
+    def layer(s, l):
+        x = x0[s] if l == 0 else y[l - 1]
+        moe.moe_layer_forward(shape, x, logits[s, l], k, wl["renorm"], ids[l], w[l], pool[l * E:(l + 1) * E],
+                              slot_of, E, None, y[l], ws, path)
+
+    def step(s):
+        for l in range(L):
+            layer(s, l)
+
+    step(0)  # eager: kernel attributes, tensor-map entry point
+    torch.cuda.synchronize()
+    graphs = []
+    for s in range(n):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            step(s)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(smi_index())
+    time.sleep(0.2)
+    for s in range(W):
+        graphs[s].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    ev0.record()
+    for s in range(W, n):
+        graphs[s].replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    assert moe.moe_workspace_flags(ws) == 0
+
+    # Per-layer call durations (external event nodes around each call).
+    n_kt = min(K, 4)
+    ev = ExtEvents(2 * n_kt * L)
+    g_kt = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_kt):
+        st = torch.cuda.current_stream().cuda_stream
+        for i in range(n_kt):
+            for l in range(L):
+                ev.record(2 * (i * L + l), st)
+                layer(W + i, l)
+                ev.record(2 * (i * L + l) + 1, st)
+    g_kt.replay()
+    torch.cuda.synchronize()
+    layer_ms = statistics.mean(ev.elapsed(2 * j, 2 * j + 1) for j in range(n_kt * L))
+    ev.destroy()
+
+    # Shared FFN leg.
+    sw = {kk: torch.from_numpy(v).to(dev) for kk, v in synth.shared_weights(seed, H, Is).items()}
+    xs = torch.randn((Ts, H), generator=gen, device=dev).half()
+    ys = torch.empty((Ts, H), dtype=torch.float16, device=dev)
+    wss = torch.zeros(moe.moe_shared_workspace_bytes(Ts, H, Is), dtype=torch.uint8, device=dev)
+    moe.moe_shared_forward(xs, sw["wg"], sw["wu"], sw["wd"], ys, wss)
+    torch.cuda.synchronize()
+    reps = 20
+    g_sh = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_sh):
+        for _ in range(reps):
+            moe.moe_shared_forward(xs, sw["wg"], sw["wu"], sw["wd"], ys, wss)
+    for _ in range(3):
+        g_sh.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g_sh.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sh_s = e0.elapsed_time(e1) / 1e3 / reps
+    assert moe.moe_workspace_flags(wss) == 0
+    rows = sampler.stop()
+    clocks = ClockSampler.summarize(rows, t_host0, t_host1)
+
+    P = T * k
+    flops_layer = 6.0 * H * I * P
+    peak_t, peak_t_src = measured_tensor_peak(sustained=True)
+    peak_h, peak_h_src = measured_peaks()
+    achieved = flops_layer / (layer_ms / 1e3) / 1e12
+    weight_gbs = E * bb / (layer_ms / 1e3) / 1e9
+    sh_flops = 6.0 * Ts * H * Is
+    out = base_line(METRIC_PREFILL, K * T * world / (ms / 1e3), "tokens/s", world, K, W, ms,
+                    {"workload": "olmoe_prefill", "layers": L, "hidden": H, "experts": E, "top_k": k,
+                     "inter": I, "group": g, "tokens_per_step": T, "logits": "uniform",
+                     "l2": "inputs larger than L2: 3.42 GB of expert weights per step",
+                     "launch": "one CUDA graph per step (16 x (route + 6 grouped-path kernels))"})
+    out["roofline"] = {"bound": "tensor", "kernel": "moe_layer_forward grouped path, one layer (route, sort, "
+                                                    "tiles, gather, tcgen05 gate/up GEMM, tcgen05 down GEMM, combine)",
+                       "achieved": round(achieved, 1), "peak": peak_t, "unit": "TFLOP/s",
+                       "frac": round(achieved / peak_t, 4), "traffic": None,
+                       "flops_per_launch": flops_layer, "avg_launch_us": round(layer_ms * 1e3, 2),
+                       "peak_source": peak_t_src,
+                       "weight_gbs": round(weight_gbs, 1), "weight_hbm_frac": round(weight_gbs / peak_h, 4),
+                       "timing": f"external event-record graph nodes around each call, {n_kt} steps x {L} layers"}
+    out["shared_ffn"] = {"tokens": Ts, "hidden": H, "inter": Is, "us_per_call": round(sh_s * 1e6, 2),
+                         "tflops": round(sh_flops / sh_s / 1e12, 1),
+                         "frac_of_tensor_peak": round(sh_flops / sh_s / 1e12 / peak_t, 4)}
+    out["gpu_launches"] = (L * 7) * K
+    out["clocks"] = clocks
+    return out
+
+
 def run_e2e(moe, wl, n, W):
     """Same metric through the public API with host buffers: per step the
     token's activations and the 16 layers' router logits are copied from
@@ -639,6 +784,8 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
     if args.workload == "olmoe_partial":
         out = run_partial(args, world, rank)
+    elif args.workload == "olmoe_prefill":
+        out = run_prefill(args, world, rank)
     elif args.workload.startswith("large_fanout_b"):
         out = run_fanout(args, world, rank, int(args.workload.split("_b")[1]))
     else:

@@ -256,8 +256,14 @@ int moe_workspace_flags(const void* workspace, int32_t* flags_out, void* stream)
  * y = W_d (silu(W_g x) * (W_u x)) with FP16 weights ("03 / Arquitetura": the
  * non-routed parts stay FP16).
  * x  device fp16 [T][H]; wg, wu device fp16 [Is][H]; wd device fp16 [H][Is];
- * y  device fp16 [T][H] out. workspace >= moe_shared_workspace_bytes(T, H, Is).
- * Limits: H, Is multiples of 128.
+ * y  device fp16 [T][H] out. workspace >= moe_shared_workspace_bytes(T, H, Is),
+ *    256-aligned, zero-filled before its first use; its first 4 bytes are the
+ *    sticky error word (bit 2: a bounded device wait expired), then h [T][Is].
+ * Two tcgen05 GEMM kernels (gate/up with the SwiGLU epilogue, then down):
+ * operands by TMA, FP32 accumulation in tensor memory, h and y rounded to
+ * FP16. Limits: H, Is positive multiples of 64 (<= 65536); x, weights and y
+ * 16-byte aligned. Errors: MOE_ERR_ARG (shape, NULL, alignment),
+ * MOE_ERR_CAPACITY (workspace too small), MOE_ERR_CUDA.
  */
 size_t moe_shared_workspace_bytes(int T, int H, int Is);
 int moe_shared_forward(const void* x, int T, int H, int Is, const void* wg,

@@ -71,96 +71,95 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, con
 namespace {
 
 constexpr int BM = 128;  // weight rows per tile (MMA M)
-constexpr int BK = 64;   // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int BK = 64;   // K elements per pipeline step (one 128-byte swizzle row)
 constexpr int BN = 128;  // sorted pairs per tile at most (MMA N)
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 expand + epilogue
-constexpr int kDqWarps = 8;
-
-// Stage layouts (offsets inside a stage; every stage starts 1024-aligned).
-constexpr uint32_t kTileBytes = BM * BK * 2;  // one FP16 operand tile, 16 KB
+// Warp roles: 0 codes TMA, 1 TMEM + MMA issue (accumulator 0), 2 activation
+// TMA, 3 MMA issue (accumulator 1), 4..19 expand codes to FP16 and run the
+// epilogue. One thread issues a tcgen05.mma about every 120 cycles whatever
+// its N, so two issuing threads with an accumulator each double the rate at
+// the small N of a single expert's pairs. The expansion is a chain of short
+// dependent steps per warp; sixteen expand warps (four per SM sub-partition)
+// keep the issue slots busy.
+constexpr int kDqWarps = 16;
+constexpr int kThreads = (4 + kDqWarps) * 32;
 constexpr uint32_t kCodeBytes = BM * 32;      // codes of 128 rows x 64 elements
-constexpr uint32_t kSzBytes = BM * 32;        // 32 bytes of scale/zero per row
-// gate/up: A_gate | A_up | B | codes_gate | codes_up | quads
-constexpr uint32_t kGuAg = 0, kGuAu = kTileBytes, kGuB = 2 * kTileBytes, kGuCg = 3 * kTileBytes,
-                   kGuCu = kGuCg + kCodeBytes, kGuQ = kGuCu + kCodeBytes, kGuStage = kGuQ + kSzBytes;
-// down: A | B | codes | pairs
-constexpr uint32_t kDnA = 0, kDnB = kTileBytes, kDnC = 2 * kTileBytes, kDnQ = kDnC + kCodeBytes,
-                   kDnStage = kDnQ + kSzBytes;
-constexpr int kGuStages = 3, kDnStages = 4;
-constexpr uint32_t kCtrlBytes = 1024;
-constexpr size_t kGuSmem = (size_t)kGuStages * kGuStage + kCtrlBytes + 1024;
-constexpr size_t kDnSmem = (size_t)kDnStages * kDnStage + kCtrlBytes + 1024;
-static_assert(kGuStage % 1024 == 0 && kDnStage % 1024 == 0, "stages must keep 1024-byte alignment");
+constexpr uint32_t kSzBytes = BM * 32;        // 32 bytes of scale/zero entries per row
+constexpr uint32_t kXBytes = BN * BK * 2;     // activation tile, up to 128 pairs
+
+// Ring geometry per kernel (NPROJ = 2: gate and up; 1: down). Three rings:
+// codes in shared memory (freed as soon as the expand warps hold them in
+// registers), activations in shared memory and the expanded FP16 weights in
+// tensor memory (both freed when the MMAs reading them complete). Keeping the
+// expanded operand out of shared memory leaves its bandwidth to the TMA
+// writes and the activation reads of the MMAs.
+template <int NPROJ>
+struct Geo {
+  static constexpr int SC = 8;
+  static constexpr int SX = NPROJ == 2 ? 6 : 8;
+  static constexpr int SA = 4;
+  static constexpr uint32_t kC = NPROJ * kCodeBytes + kSzBytes;
+  static constexpr uint32_t offX = 0, offC = SX * kXBytes, offCtrl = offC + SC * kC;
+  static constexpr size_t smem = (size_t)offCtrl + 1024 + 1024;
+  static constexpr uint32_t kSzEntry = NPROJ == 2 ? 8 : 4;  // bytes of one group's scale/zero entry
+  static constexpr int kGAlign = NPROJ == 2 ? 2 : 4;         // entries per 16 bytes
+  // Tensor memory: two accumulators in columns [0, 2*BN) (gate and up; or
+  // the even and odd K slices of the down projection), then SA stages of the
+  // expanded operand, 32 columns (64 FP16 of K) per projection.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t colA(int sa, int p) { return 2 * BN + (uint32_t)(sa * NPROJ + p) * 32u; }
+  static_assert(2 * BN + SA * NPROJ * 32 <= (int)kTmemCols, "tensor memory budget");
+  static_assert(kC % 1024 == 0, "ring slots keep 1024-byte alignment");
+  // Each ring slot must always be drained by the same expand warps (step kt
+  // is taken by the warps with kt % 4 == j), so no waiter can see a phase two
+  // fills ahead.
+  static_assert(SC % 4 == 0 && SA % 4 == 0, "slot ownership of the interleaved expand warps");
+};
 
 // Position of element e (0..7) of an 8-element chunk in the K order used by
 // the tensor-core operands: elements (0, 4, 1, 5, 2, 6, 3, 7) in that order.
 __host__ __device__ constexpr int kperm_pos(int e) { return (e & 3) * 2 + (e >> 2); }
 
-// Expands one 32-bit word of codes (elements 8w .. 8w+7, element i in bits
-// 4i..4i+3) into eight FP16 weights (q - z) * s in the operand K order.
-// zz = 1024 + round(z) and t = 1024 + q are exact, so t - zz = q - round(z)
-// exactly; the fused multiply-add adds (round(z) - z) * s (zero for an
-// integer zero point) and rounds once.
-__device__ __forceinline__ uint4 dq_word(uint32_t w, half2 zz, half2 s2, half2 c2) {
-  const uint32_t m = 0x000F000Fu, mg = 0x64006400u;
-  const uint32_t t0 = (w & m) | mg, t1 = ((w >> 4) & m) | mg, t2 = ((w >> 8) & m) | mg,
-                 t3 = ((w >> 12) & m) | mg;
-  uint4 o;
-  half2 h;
-  h = __hfma2(__hsub2(u32_as_h2(t0), zz), s2, c2);
-  o.x = *reinterpret_cast<uint32_t*>(&h);
-  h = __hfma2(__hsub2(u32_as_h2(t1), zz), s2, c2);
-  o.y = *reinterpret_cast<uint32_t*>(&h);
-  h = __hfma2(__hsub2(u32_as_h2(t2), zz), s2, c2);
-  o.z = *reinterpret_cast<uint32_t*>(&h);
-  h = __hfma2(__hsub2(u32_as_h2(t3), zz), s2, c2);
-  o.w = *reinterpret_cast<uint32_t*>(&h);
-  return o;
-}
+// The expanded operand holds 16 (q - z) s; the epilogue divides by 16 (exact).
+constexpr float kInvAScale = 0.0625f;
 
+// Constants of one (row, group) for dq_word, from its FP16 (s, z).
 struct DqConst {
-  half2 zz, s2, c2;
+  half2 zl, zh, sl, sh, cl, ch;
 };
-__device__ __forceinline__ DqConst dq_const(uint32_t sz) {  // sz: (s, z) FP16 bits
+__device__ __forceinline__ DqConst dq_const(uint32_t sz) {
   const float s = __half2float(__ushort_as_half((unsigned short)(sz & 0xFFFFu)));
   const float z = __half2float(__ushort_as_half((unsigned short)(sz >> 16)));
   const float zi = rintf(z);
+  const float zl = fminf(fmaxf(zi, -1000.0f), 1000.0f);  // 1024 + zl exact in FP16
+  const float zh = fabsf(zi) <= 63.0f ? zi : 0.0f;       // 1024 + 16 zh exact in FP16
   DqConst d;
-  d.zz = __float2half2_rn(1024.0f + zi);
-  d.s2 = __float2half2_rn(s);
-  d.c2 = __float2half2_rn((zi - z) * s);
+  d.zl = __float2half2_rn(1024.0f + zl);
+  d.zh = __float2half2_rn(1024.0f + 16.0f * zh);
+  d.sl = __float2half2_rn(16.0f * s);
+  d.sh = __float2half2_rn(s);
+  d.cl = __float2half2_rn(16.0f * (zl - z) * s);
+  d.ch = __float2half2_rn(16.0f * (zh - z) * s);
   return d;
 }
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  const uint32_t a = tc::smem_addr(p);
-  return p + ((1024u - (a & 1023u)) & 1023u);
-}
+__device__ __forceinline__ uint32_t h2_bits(half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-struct Ctrl {  // at the end of the stage area
-  uint64_t* tma_full;
-  uint64_t* a_full;
-  uint64_t* empty;
-  uint64_t* acc_full;
-  uint32_t* tmem_slot;
-  int* abort;
-};
-__device__ __forceinline__ Ctrl ctrl_at(uint8_t* p, int stages) {
-  Ctrl c;
-  c.tma_full = reinterpret_cast<uint64_t*>(p);
-  c.a_full = c.tma_full + stages;
-  c.empty = c.a_full + stages;
-  c.acc_full = c.empty + stages;
-  c.tmem_slot = reinterpret_cast<uint32_t*>(c.acc_full + 1);
-  c.abort = reinterpret_cast<int*>(c.tmem_slot + 1);
-  return c;
+// Eight codes of one word (element i in bits 4i..4i+3) to eight FP16 values
+// 16 (q - z) s in operand K order. Low nibbles OR-ed into 1024 give 1024 + q,
+// and minus (1024 + zl) the exact q - zl; high nibbles masked in place give
+// 1024 + 16 q, and minus (1024 + 16 zh) the exact 16 (q - zh). One fused
+// multiply-add each (by 16 s or s) adds the rest of the zero point, 16 (zl -
+// z) s or 16 (zh - z) s -- zero for an integer zero point -- and rounds once.
+__device__ __forceinline__ uint4 dq_word(uint32_t w, const DqConst& d) {
+  const uint32_t ml = 0x000F000Fu, mh = 0x00F000F0u, mg = 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  uint4 o;
+  o.x = h2_bits(__hfma2(__hsub2(u32_as_h2((w & ml) | mg), d.zl), d.sl, d.cl));   // elements 0, 4
+  o.y = h2_bits(__hfma2(__hsub2(u32_as_h2((w & mh) | mg), d.zh), d.sh, d.ch));   // 1, 5
+  o.z = h2_bits(__hfma2(__hsub2(u32_as_h2((w8 & ml) | mg), d.zl), d.sl, d.cl));  // 2, 6
+  o.w = h2_bits(__hfma2(__hsub2(u32_as_h2((w8 & mh) | mg), d.zh), d.sh, d.ch));  // 3, 7
+  return o;
 }
-
-__device__ __forceinline__ void set_abort(const Ctrl& c, int32_t* flags) {
-  atomicOr(flags, 4);
-  *reinterpret_cast<volatile int*>(c.abort) = 1;
-}
-__device__ __forceinline__ bool aborted(const Ctrl& c) { return *reinterpret_cast<volatile int*>(c.abort) != 0; }
 
 struct GemmParams {
   const int4* tiles;  // (slot, first sorted position, pairs, expert)
@@ -168,7 +167,8 @@ struct GemmParams {
   int rows;           // output rows of the weight matrix (I for gate/up, H for down)
   int K;              // reduction length (H for gate/up, I for down)
   int g;
-  uint32_t q0, q1, sz;  // byte offsets in a weight row: codes (gate, up) or codes (down), scale/zero
+  uint32_t g_magic;     // ceil(2^32 / g)
+  uint32_t q0, q1, sz;  // byte offsets in a weight row: codes (gate or down, up), scale/zero entries
   __half* h_sorted;     // gate/up output [P][I]
   float* pair_out;      // down output [T*k][H]
   const int32_t* pair_tok;
@@ -177,285 +177,259 @@ struct GemmParams {
   int32_t* flags;
 };
 
-// Common set-up: barriers, TMEM allocation. Returns the TMEM base address.
-__device__ __forceinline__ uint32_t gemm_setup(const Ctrl& c, int stages, uint32_t tmem_cols) {
-  const int warp = threadIdx.x >> 5;
+struct Bars {
+  uint64_t *c_full, *c_empty, *x_full, *x_empty, *a_full, *a_empty, *acc_full;
+  uint32_t* tmem_slot;
+  int* abort;
+};
+template <int NPROJ>
+__device__ __forceinline__ Bars bars_at(uint8_t* p) {
+  using G = Geo<NPROJ>;
+  Bars b;
+  uint64_t* q = reinterpret_cast<uint64_t*>(p);
+  b.c_full = q; q += G::SC;
+  b.c_empty = q; q += G::SC;
+  b.x_full = q; q += G::SX;
+  b.x_empty = q; q += G::SX;
+  b.a_full = q; q += G::SA;
+  b.a_empty = q; q += G::SA;
+  b.acc_full = q; q += 1;
+  b.tmem_slot = reinterpret_cast<uint32_t*>(q);
+  b.abort = reinterpret_cast<int*>(b.tmem_slot + 1);
+  return b;
+}
+// A bounded wait expired: report it (bit 2) and stop the block's other roles.
+__device__ __forceinline__ void abort_block(const Bars& b, int32_t* flags) {
+  atomicOr(flags, 4);
+  *reinterpret_cast<volatile int*>(b.abort) = 1;
+}
+__device__ __forceinline__ bool is_aborted(const Bars& b) { return *reinterpret_cast<volatile int*>(b.abort) != 0; }
+// Producer tail after an abort: wait (bounded) for its loads still in flight.
+__device__ __forceinline__ void drain(uint64_t* full, int stages, int issued) {
+  for (int kt = issued > stages ? issued - stages : 0; kt < issued; ++kt)
+    tc::bar_wait(&full[kt % stages], (kt / stages) & 1);
+}
+
+// One tile: 128 weight rows x up to 128 sorted pairs of one expert.
+//   NPROJ = 2: gate and up accumulators, epilogue h = silu(gate) * up (FP16).
+//   NPROJ = 1: down accumulator, epilogue pair_out[t*k + j] (FP32).
+template <int NPROJ>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
+                        const GemmParams a) {
+  using G = Geo<NPROJ>;
+  const int tile = blockIdx.y;
+  if (tile >= *a.n_tiles) return;
+  const int4 td = a.tiles[tile];
+  const int slot = td.x, pos0 = td.y, n = td.z;
+  const int row0 = blockIdx.x * BM;
+  const int nmma = (n + 15) & ~15;
+  const int KT = a.K / BK;
+  constexpr uint32_t kTmemCols = G::kTmemCols;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = tc::align1024(smraw);
+  const Bars b = bars_at<NPROJ>(sm + G::offCtrl);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      tc::bar_init(&c.tma_full[s], 1);
-      tc::bar_init(&c.a_full[s], kDqWarps);
-      tc::bar_init(&c.empty[s], 1);
+    tc::tma_prefetch_desc(&map_w);
+    tc::tma_prefetch_desc(&map_b);
+    for (int s = 0; s < G::SC; ++s) {
+      tc::bar_init(&b.c_full[s], 1);
+      tc::bar_init(&b.c_empty[s], 4);  // one expand warp per lane quarter takes each step
     }
-    tc::bar_init(c.acc_full, 1);
-    *c.abort = 0;
+    for (int s = 0; s < G::SX; ++s) {
+      tc::bar_init(&b.x_full[s], 1);
+      tc::bar_init(&b.x_empty[s], 2);  // one commit per issuing thread
+    }
+    for (int s = 0; s < G::SA; ++s) {
+      tc::bar_init(&b.a_full[s], 4);
+      tc::bar_init(&b.a_empty[s], 2);
+    }
+    tc::bar_init(b.acc_full, 2);
+    *b.abort = 0;
     tc::bar_init_fence();
   }
-  if (warp == 1) tc::tmem_alloc(c.tmem_slot, tmem_cols);
+  if (warp == 1) tc::tmem_alloc(b.tmem_slot, kTmemCols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  return *c.tmem_slot;
-}
+  const uint32_t tmem = *b.tmem_slot;
 
-__device__ __forceinline__ void gemm_teardown(uint32_t tmem, uint32_t tmem_cols) {
+  if (warp == 0) {
+    if (lane == 0) {  // codes and scale/zero entries of the tile's rows
+      int issued = 0;
+      for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % G::SC;
+        if (kt >= G::SC && !tc::bar_wait(&b.c_empty[s], ((kt / G::SC) - 1) & 1)) {
+          abort_block(b, a.flags);
+          break;
+        }
+        if (is_aborted(b)) break;
+        uint8_t* st = sm + G::offC + (size_t)s * G::kC;
+        const int k0 = kt * BK;
+        const int gb = (k0 / a.g) / G::kGAlign * G::kGAlign;
+        tc::bar_expect_tx(&b.c_full[s], G::kC);
+        tc::tma_load_3d(st, &map_w, (int)a.q0 + k0 / 2, row0, slot, &b.c_full[s]);
+        if (NPROJ == 2) tc::tma_load_3d(st + kCodeBytes, &map_w, (int)a.q1 + k0 / 2, row0, slot, &b.c_full[s]);
+        tc::tma_load_3d(st + NPROJ * kCodeBytes, &map_w, (int)(a.sz + G::kSzEntry * gb), row0, slot,
+                        &b.c_full[s]);
+        issued = kt + 1;
+      }
+      if (is_aborted(b)) drain(b.c_full, G::SC, issued);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {  // activation tile: 64 sorted pairs per load
+      const uint32_t bytes = (n > 64 ? 2u : 1u) * 64u * BK * 2u;
+      int issued = 0;
+      for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % G::SX;
+        if (kt >= G::SX && !tc::bar_wait(&b.x_empty[s], ((kt / G::SX) - 1) & 1)) {
+          abort_block(b, a.flags);
+          break;
+        }
+        if (is_aborted(b)) break;
+        uint8_t* st = sm + G::offX + (size_t)s * kXBytes;
+        tc::bar_expect_tx(&b.x_full[s], bytes);
+        tc::tma_load_2d(st, &map_b, kt * BK, pos0, &b.x_full[s]);
+        if (n > 64) tc::tma_load_2d(st + 64 * BK * 2, &map_b, kt * BK, pos0 + 64, &b.x_full[s]);
+        issued = kt + 1;
+      }
+      if (is_aborted(b)) drain(b.x_full, G::SX, issued);
+    }
+  } else if (warp == 1 || warp == 3) {
+    if (lane == 0) {
+      // Issuer p owns accumulator p: the gate (p = 0) or up (p = 1)
+      // projection, or for the down projection the K slices kk = p, p + 2.
+      const int p = warp == 1 ? 0 : 1;
+      const uint32_t idesc = tc::idesc_f16(BM, nmma);
+      for (int kt = 0; kt < KT; ++kt) {
+        const int sa = kt % G::SA, sx = kt % G::SX;
+        if (!tc::bar_wait(&b.a_full[sa], (kt / G::SA) & 1) || !tc::bar_wait(&b.x_full[sx], (kt / G::SX) & 1)) {
+          abort_block(b, a.flags);
+          break;
+        }
+        if (is_aborted(b)) break;
+        tc::tc_fence_after();
+        const uint32_t xbase = tc::smem_addr(sm + G::offX + (size_t)sx * kXBytes);
+        if (NPROJ == 2) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, p) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
+                           kt > 0 || kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = p; kk < BK / 16; kk += 2)
+            tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, 0) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
+                           kt > 0 || kk > p);
+        }
+        tc::mma_commit(&b.a_empty[sa]);
+        tc::mma_commit(&b.x_empty[sx]);
+      }
+      tc::mma_commit(b.acc_full);
+    }
+  } else if (warp >= 4) {
+    // Expand: warp w owns the TMEM lanes of its quarter (rows 32 (w % 4) ..
+    // +31) and every fourth step, kt = j (mod 4) with j = (w - 4) / 4, so
+    // four steps are expanded at once; lane t owns row 32 (w % 4) + t, all
+    // 64 codes of the step (at most two scale/zero groups: one per 32).
+    const int q4 = warp & 3, j4 = (warp - 4) >> 2;
+    const int r = 32 * q4 + lane;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
+    for (int kt = j4; kt < KT; kt += 4) {
+      const int sc = kt % G::SC, sa = kt % G::SA;
+      if (is_aborted(b)) break;
+      if (!tc::bar_wait(&b.c_full[sc], (kt / G::SC) & 1)) {
+        abort_block(b, a.flags);
+        break;
+      }
+      const uint8_t* cs = sm + G::offC + (size_t)sc * G::kC;
+      const uint32_t k0 = (uint32_t)kt * BK;
+      // floor(k / g) by multiply-high with the rounded-up reciprocal (exact
+      // for k, g <= 8192).
+      const int gi0 = (int)__umulhi(k0, a.g_magic), gi1 = (int)__umulhi(k0 + 32u, a.g_magic);
+      const int gb = gi0 / G::kGAlign * G::kGAlign;
+      uint4 cw[NPROJ][2];
+      DqConst d0[NPROJ], d1[NPROJ];
+#pragma unroll
+      for (int p = 0; p < NPROJ; ++p) {
+        const uint4* src = reinterpret_cast<const uint4*>(cs + p * kCodeBytes + r * 32);
+        cw[p][0] = src[0];
+        cw[p][1] = src[1];
+        const uint8_t* e = cs + NPROJ * kCodeBytes + r * 32 + 4 * p;
+        d0[p] = dq_const(*reinterpret_cast<const uint32_t*>(e + (gi0 - gb) * G::kSzEntry));
+        d1[p] = gi1 == gi0 ? d0[p] : dq_const(*reinterpret_cast<const uint32_t*>(e + (gi1 - gb) * G::kSzEntry));
+      }
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&b.c_empty[sc]);
+      if (kt >= G::SA && !tc::bar_wait(&b.a_empty[sa], ((kt / G::SA) - 1) & 1)) {
+        abort_block(b, a.flags);
+        break;
+      }
+      tc::tc_fence_after();
+#pragma unroll
+      for (int p = 0; p < NPROJ; ++p) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const DqConst& d = h ? d1[p] : d0[p];
+          const uint4 c = cw[p][h];
+          const uint4 o0 = dq_word(c.x, d), o1 = dq_word(c.y, d), o2 = dq_word(c.z, d), o3 = dq_word(c.w, d);
+          const uint32_t v[16] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w,
+                                  o2.x, o2.y, o2.z, o2.w, o3.x, o3.y, o3.z, o3.w};
+          tc::tmem_st16(tlane + G::colA(sa, p) + 16u * h, v);
+        }
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
+    }
+    // Epilogue: TMEM lanes of this warp's quarter, one quarter of the columns.
+    const bool ok = tc::bar_wait(b.acc_full, 0);
+    if (!ok) abort_block(b, a.flags);
+    tc::tc_fence_after();
+    const int row = row0 + r;
+    const bool live = ok && !is_aborted(b) && row < a.rows;
+    const uint32_t tl = tlane;
+    for (int c0 = j4 * (BN / 4); c0 < j4 * (BN / 4) + BN / 4 && c0 < nmma; c0 += 16) {
+      if (NPROJ == 2) {
+        float gv[16], uv[16];
+        tc::tmem_ld16(tl + (uint32_t)c0, gv);
+        tc::tmem_ld16(tl + (uint32_t)(BN + c0), uv);
+        tc::tmem_ld_wait();
+        if (live) {
+          const int prow = (row & ~7) | kperm_pos(row & 7);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < n)
+              a.h_sorted[(size_t)(pos0 + c0 + j) * a.rows + prow] =
+                  __float2half_rn(silu_f(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
+        }
+      } else {
+        float dv[16], ev[16];
+        tc::tmem_ld16(tl + (uint32_t)c0, dv);
+        tc::tmem_ld16(tl + (uint32_t)(BN + c0), ev);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dv[j] += ev[j];  // even + odd K slices, fixed order
+        if (live) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < n) {
+              const int pos = pos0 + c0 + j;
+              const size_t q = (size_t)a.pair_tok[pos] * a.k + a.pair_j[pos];
+              a.pair_out[q * a.rows + row] = dv[j] * kInvAScale;
+            }
+          }
+        }
+      }
+    }
+  }
   tc::tc_fence_before();
   __syncthreads();
-  if ((threadIdx.x >> 5) == 1) {
+  if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, tmem_cols);
+    tc::tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-// Producer tail after an abort: wait (bounded) for the loads still in flight.
-__device__ __forceinline__ void drain_loads(const Ctrl& c, int stages, int issued) {
-  for (int kt = max(0, issued - stages); kt < issued; ++kt) tc::bar_wait(&c.tma_full[kt % stages], (kt / stages) & 1);
-}
-
-// ---- gate/up GEMM + SwiGLU --------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gateup_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                          const GemmParams a) {
-  const int tile = blockIdx.y;
-  if (tile >= *a.n_tiles) return;
-  const int4 td = a.tiles[tile];
-  const int slot = td.x, pos0 = td.y, n = td.z;
-  const int row0 = blockIdx.x * BM;
-  const int nmma = (n + 15) & ~15;
-  const int KT = a.K / BK;
-  extern __shared__ uint8_t smraw[];
-  uint8_t* sm = align1024(smraw);
-  const Ctrl c = ctrl_at(sm + (size_t)kGuStages * kGuStage, kGuStages);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    tc::tma_prefetch_desc(&map_w);
-    tc::tma_prefetch_desc(&map_x);
-  }
-  const uint32_t tmem = gemm_setup(c, kGuStages, 2 * BN);
-
-  if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kGuStages;
-        if (kt >= kGuStages && !tc::bar_wait(&c.empty[s], ((kt / kGuStages) - 1) & 1)) {
-          set_abort(c, a.flags);
-          break;
-        }
-        if (aborted(c)) break;
-        uint8_t* st = sm + (size_t)s * kGuStage;
-        const int k0 = kt * BK;
-        const int gb = (k0 / a.g) & ~1;  // first of the four quads loaded
-        tc::bar_expect_tx(&c.tma_full[s], 3 * kCodeBytes + kTileBytes);
-        tc::tma_load_3d(st + kGuCg, &map_w, (int)a.q0 + k0 / 2, row0, slot, &c.tma_full[s]);
-        tc::tma_load_3d(st + kGuCu, &map_w, (int)a.q1 + k0 / 2, row0, slot, &c.tma_full[s]);
-        tc::tma_load_3d(st + kGuQ, &map_w, (int)a.sz + 8 * gb, row0, slot, &c.tma_full[s]);
-        tc::tma_load_2d(st + kGuB, &map_x, k0, pos0, &c.tma_full[s]);
-        issued = kt + 1;
-      }
-      if (aborted(c)) drain_loads(c, kGuStages, issued);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_f16(BM, nmma);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kGuStages;
-        if (!tc::bar_wait(&c.a_full[s], (kt / kGuStages) & 1)) {
-          set_abort(c, a.flags);
-          break;
-        }
-        if (aborted(c)) break;
-        tc::tc_fence_after();
-        const uint32_t base = tc::smem_addr(sm + (size_t)s * kGuStage);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t bdesc = tc::sw128_desc(base + kGuB + kk * 32);
-          const bool acc = kt > 0 || kk > 0;
-          tc::mma_f16(tmem, tc::sw128_desc(base + kGuAg + kk * 32), bdesc, idesc, acc);
-          tc::mma_f16(tmem + BN, tc::sw128_desc(base + kGuAu + kk * 32), bdesc, idesc, acc);
-        }
-        tc::mma_commit(&c.empty[s]);
-      }
-      tc::mma_commit(c.acc_full);
-    }
-  } else {
-    const int dt = threadIdx.x - 64;  // 0..255
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % kGuStages;
-      if (aborted(c)) break;
-      if (!tc::bar_wait(&c.tma_full[s], (kt / kGuStages) & 1)) {
-        set_abort(c, a.flags);
-        break;
-      }
-      uint8_t* st = sm + (size_t)s * kGuStage;
-      const int k0 = kt * BK;
-      const int gi0 = k0 / a.g, gb = gi0 & ~1, kb = (gi0 + 1) * a.g;
-#pragma unroll
-      for (int pj = 0; pj < 2; ++pj) {  // projection: 0 gate, 1 up
-        const int u = dt;
-        const int r = u >> 1, half = u & 1;
-        const uint4 cw = *reinterpret_cast<const uint4*>(st + (pj ? kGuCu : kGuCg) + r * 32 + half * 16);
-        const uint8_t* qrow = st + kGuQ + r * 32;
-        uint8_t* A = st + (pj ? kGuAu : kGuAg);
-        const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-        int gcur = -1;
-        DqConst d;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ch = half * 4 + j;
-          const int gi = (k0 + 8 * ch < kb) ? gi0 : gi0 + 1;
-          if (gi != gcur) {
-            d = dq_const(*reinterpret_cast<const uint32_t*>(qrow + (gi - gb) * 8 + pj * 4));
-            gcur = gi;
-          }
-          *reinterpret_cast<uint4*>(A + tc::sw128_offset(r, ch)) = dq_word(wv[j], d.zz, d.s2, d.c2);
-        }
-      }
-      tc::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::bar_arrive(&c.a_full[s]);
-    }
-    // Epilogue: TMEM lanes of this warp's quarter, half of the columns.
-    const bool ok = tc::bar_wait(c.acc_full, 0);
-    if (!ok) set_abort(c, a.flags);
-    tc::tc_fence_after();
-    const int q4 = warp & 3, chalf = (warp - 2) >> 2;
-    const int row = row0 + 32 * q4 + lane;
-    const int prow = (row & ~7) | kperm_pos(row & 7);
-    const bool live = ok && !aborted(c) && row < a.rows;
-    for (int c0 = chalf * (BN / 2); c0 < chalf * (BN / 2) + BN / 2 && c0 < nmma; c0 += 16) {
-      float gv[16], uv[16];
-      tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)c0, gv);
-      tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(BN + c0), uv);
-      tc::tmem_ld_wait();
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < n)
-            a.h_sorted[(size_t)(pos0 + c0 + j) * a.rows + prow] = __float2half_rn(silu_f(gv[j]) * uv[j]);
-      }
-    }
-  }
-  gemm_teardown(tmem, 2 * BN);
-}
-
-// ---- down GEMM ----------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_down_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
-                        const GemmParams a) {
-  const int tile = blockIdx.y;
-  if (tile >= *a.n_tiles) return;
-  const int4 td = a.tiles[tile];
-  const int slot = td.x, pos0 = td.y, n = td.z;
-  const int row0 = blockIdx.x * BM;
-  const int nmma = (n + 15) & ~15;
-  const int KT = a.K / BK;
-  extern __shared__ uint8_t smraw[];
-  uint8_t* sm = align1024(smraw);
-  const Ctrl c = ctrl_at(sm + (size_t)kDnStages * kDnStage, kDnStages);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    tc::tma_prefetch_desc(&map_w);
-    tc::tma_prefetch_desc(&map_h);
-  }
-  const uint32_t tmem = gemm_setup(c, kDnStages, BN);
-
-  if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kDnStages;
-        if (kt >= kDnStages && !tc::bar_wait(&c.empty[s], ((kt / kDnStages) - 1) & 1)) {
-          set_abort(c, a.flags);
-          break;
-        }
-        if (aborted(c)) break;
-        uint8_t* st = sm + (size_t)s * kDnStage;
-        const int k0 = kt * BK;
-        const int gb = (k0 / a.g) & ~3;  // first of the eight pairs loaded
-        tc::bar_expect_tx(&c.tma_full[s], 2 * kCodeBytes + kTileBytes);
-        tc::tma_load_3d(st + kDnC, &map_w, (int)a.q0 + k0 / 2, row0, slot, &c.tma_full[s]);
-        tc::tma_load_3d(st + kDnQ, &map_w, (int)a.sz + 4 * gb, row0, slot, &c.tma_full[s]);
-        tc::tma_load_2d(st + kDnB, &map_h, k0, pos0, &c.tma_full[s]);
-        issued = kt + 1;
-      }
-      if (aborted(c)) drain_loads(c, kDnStages, issued);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_f16(BM, nmma);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kDnStages;
-        if (!tc::bar_wait(&c.a_full[s], (kt / kDnStages) & 1)) {
-          set_abort(c, a.flags);
-          break;
-        }
-        if (aborted(c)) break;
-        tc::tc_fence_after();
-        const uint32_t base = tc::smem_addr(sm + (size_t)s * kDnStage);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          tc::mma_f16(tmem, tc::sw128_desc(base + kDnA + kk * 32), tc::sw128_desc(base + kDnB + kk * 32), idesc,
-                      kt > 0 || kk > 0);
-        tc::mma_commit(&c.empty[s]);
-      }
-      tc::mma_commit(c.acc_full);
-    }
-  } else {
-    const int dt = threadIdx.x - 64;
-    const int r = dt >> 1, half = dt & 1;
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % kDnStages;
-      if (aborted(c)) break;
-      if (!tc::bar_wait(&c.tma_full[s], (kt / kDnStages) & 1)) {
-        set_abort(c, a.flags);
-        break;
-      }
-      uint8_t* st = sm + (size_t)s * kDnStage;
-      const int k0 = kt * BK;
-      const int gi0 = k0 / a.g, gb = gi0 & ~3, kb = (gi0 + 1) * a.g;
-      const uint4 cw = *reinterpret_cast<const uint4*>(st + kDnC + r * 32 + half * 16);
-      const uint8_t* prow = st + kDnQ + r * 32;
-      uint8_t* A = st + kDnA;
-      const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-      int gcur = -1;
-      DqConst d;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch = half * 4 + j;
-        const int gi = (k0 + 8 * ch < kb) ? gi0 : gi0 + 1;
-        if (gi != gcur) {
-          d = dq_const(*reinterpret_cast<const uint32_t*>(prow + (gi - gb) * 4));
-          gcur = gi;
-        }
-        *reinterpret_cast<uint4*>(A + tc::sw128_offset(r, ch)) = dq_word(wv[j], d.zz, d.s2, d.c2);
-      }
-      tc::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::bar_arrive(&c.a_full[s]);
-    }
-    const bool ok = tc::bar_wait(c.acc_full, 0);
-    if (!ok) set_abort(c, a.flags);
-    tc::tc_fence_after();
-    const int q4 = warp & 3, chalf = (warp - 2) >> 2;
-    const int row = row0 + 32 * q4 + lane;
-    const bool live = ok && !aborted(c) && row < a.rows;
-    for (int c0 = chalf * (BN / 2); c0 < chalf * (BN / 2) + BN / 2 && c0 < nmma; c0 += 16) {
-      float dv[16];
-      tc::tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)c0, dv);
-      tc::tmem_ld_wait();
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c0 + j < n) {
-            const int pos = pos0 + c0 + j;
-            const size_t q = (size_t)a.pair_tok[pos] * a.k + a.pair_j[pos];
-            a.pair_out[q * a.rows + row] = dv[j];
-          }
-        }
-      }
-    }
-  }
-  gemm_teardown(tmem, BN);
 }
 
 // ---- small kernels -------------------------------------------------------------
@@ -635,7 +609,7 @@ int grouped_forward(const ForwardArgs& a) {
   {
     const uint64_t dims[2] = {(uint64_t)a.H, (uint64_t)P};
     const uint64_t str[1] = {(uint64_t)a.H * 2};
-    const uint32_t box[2] = {BK, BN};
+    const uint32_t box[2] = {BK, 64};
     if ((rc = encode_tensor_map(&m_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xs, dims, str, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B)) != MOE_OK)
       return rc;
@@ -643,20 +617,23 @@ int grouped_forward(const ForwardArgs& a) {
   {
     const uint64_t dims[2] = {(uint64_t)a.I, (uint64_t)P};
     const uint64_t str[1] = {(uint64_t)a.I * 2};
-    const uint32_t box[2] = {BK, BN};
+    const uint32_t box[2] = {BK, 64};
     if ((rc = encode_tensor_map(&m_h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hs, dims, str, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B)) != MOE_OK)
       return rc;
   }
   if (!g_attr_done) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGuSmem));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDnSmem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)Geo<2>::smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)Geo<1>::smem));
     g_attr_done = true;
   }
   GemmParams gp = {};
   gp.tiles = tiles;
   gp.n_tiles = n_tiles;
   gp.g = a.g;
+  gp.g_magic = (uint32_t)((0x100000000ull + (uint64_t)a.g - 1) / (uint64_t)a.g);
   gp.pair_tok = pair_tok;
   gp.pair_j = pair_j;
   gp.k = a.k;
@@ -668,7 +645,7 @@ int grouped_forward(const ForwardArgs& a) {
   gu.q1 = a.off.gu_q_up;
   gu.sz = a.off.gu_sz;
   gu.h_sorted = hs;
-  grouped_gateup_kernel<<<dim3((a.I + BM - 1) / BM, w.max_tiles), kThreads, kGuSmem, st>>>(m_gu, m_x, gu);
+  grouped_gemm_kernel<2><<<dim3((a.I + BM - 1) / BM, w.max_tiles), kThreads, Geo<2>::smem, st>>>(m_gu, m_x, gu);
   if ((rc = check_launch("grouped gate/up GEMM")) != MOE_OK) return rc;
   GemmParams dn = gp;
   dn.rows = a.H;
@@ -676,7 +653,7 @@ int grouped_forward(const ForwardArgs& a) {
   dn.q0 = a.off.d_q;
   dn.sz = a.off.d_sz;
   dn.pair_out = pair_out;
-  grouped_down_kernel<<<dim3((a.H + BM - 1) / BM, w.max_tiles), kThreads, kDnSmem, st>>>(m_dn, m_h, dn);
+  grouped_gemm_kernel<1><<<dim3((a.H + BM - 1) / BM, w.max_tiles), kThreads, Geo<1>::smem, st>>>(m_dn, m_h, dn);
   if ((rc = check_launch("grouped down GEMM")) != MOE_OK) return rc;
   grouped_combine_kernel<<<4 * 152, 256, 0, st>>>(pair_out, a.ids, a.weights, a.slot_of, a.n_slots, a.E, a.T,
                                                   a.k, a.H, a.y_shared, a.y);

@@ -105,6 +105,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 consecutive 32-bit columns from registers: thread t writes
+// lane (taddr.lane + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- tcgen05.mma, kind::f16 -------------------------------------------------
 // Shared-memory operand descriptor of a K-major tile in the 128-byte swizzle
@@ -135,6 +150,16 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
+// Same with the A operand in tensor memory: row m of A in lane m, two FP16
+// elements per 32-bit column in K order (a 16-element K slice = 8 columns).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -146,6 +171,78 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile.
 __host__ __device__ constexpr uint32_t sw128_offset(int r, int c) {
   return (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
+}
+
+// ---- pipeline scaffolding of the tile kernels -------------------------------
+// Roles: warp 0 issues TMA loads, warp 1 owns tensor memory and issues the
+// MMAs, the remaining warps expand operands (when any) and run the epilogue.
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_addr(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Control block after the stage area: per stage, "loads landed" (tma_full),
+// "operand expanded" (a_full) and "MMAs done with the stage" (empty); the
+// final accumulator barrier, the TMEM address and a block-local abort flag.
+struct Ctrl {
+  uint64_t* tma_full;
+  uint64_t* a_full;
+  uint64_t* empty;
+  uint64_t* acc_full;
+  uint32_t* tmem_slot;
+  int* abort;
+};
+__device__ __forceinline__ Ctrl ctrl_at(uint8_t* p, int stages) {
+  Ctrl c;
+  c.tma_full = reinterpret_cast<uint64_t*>(p);
+  c.a_full = c.tma_full + stages;
+  c.empty = c.a_full + stages;
+  c.acc_full = c.empty + stages;
+  c.tmem_slot = reinterpret_cast<uint32_t*>(c.acc_full + 1);
+  c.abort = reinterpret_cast<int*>(c.tmem_slot + 1);
+  return c;
+}
+
+// A bounded wait expired: report it (bit 2 of the error word) and make the
+// other roles of the block stop at their next check.
+__device__ __forceinline__ void set_abort(const Ctrl& c, int32_t* flags) {
+  atomicOr(flags, 4);
+  *reinterpret_cast<volatile int*>(c.abort) = 1;
+}
+__device__ __forceinline__ bool aborted(const Ctrl& c) { return *reinterpret_cast<volatile int*>(c.abort) != 0; }
+
+// Barrier initialisation and TMEM allocation; returns the TMEM base address.
+__device__ __forceinline__ uint32_t gemm_setup(const Ctrl& c, int stages, uint32_t tmem_cols, int a_full_count) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      bar_init(&c.tma_full[s], 1);
+      bar_init(&c.a_full[s], a_full_count);
+      bar_init(&c.empty[s], 1);
+    }
+    bar_init(c.acc_full, 1);
+    *c.abort = 0;
+    bar_init_fence();
+  }
+  if ((threadIdx.x >> 5) == 1) tmem_alloc(c.tmem_slot, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *c.tmem_slot;
+}
+
+__device__ __forceinline__ void gemm_teardown(uint32_t tmem, uint32_t tmem_cols) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// Producer tail after an abort: wait (bounded) for the loads still in flight.
+__device__ __forceinline__ void drain_loads(const Ctrl& c, int stages, int issued) {
+  for (int kt = issued > stages ? issued - stages : 0; kt < issued; ++kt)
+    bar_wait(&c.tma_full[kt % stages], (kt / stages) & 1);
 }
 
 }  // namespace tc
