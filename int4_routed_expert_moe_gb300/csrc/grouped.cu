@@ -86,17 +86,18 @@ constexpr uint32_t kCodeBytes = BM * 32;      // codes of 128 rows x 64 elements
 constexpr uint32_t kSzBytes = BM * 32;        // 32 bytes of scale/zero entries per row
 constexpr uint32_t kXBytes = BN * BK * 2;     // activation tile, up to 128 pairs
 
-// Ring geometry per kernel (NPROJ = 2: gate and up; 1: down). Three rings:
+// Ring geometry per kernel (NPROJ = 2: gate and up; 1: down). Two rings:
 // codes in shared memory (freed as soon as the expand warps hold them in
-// registers), activations in shared memory and the expanded FP16 weights in
-// tensor memory (both freed when the MMAs reading them complete). Keeping the
-// expanded operand out of shared memory leaves its bandwidth to the TMA
-// writes and the activation reads of the MMAs.
+// registers), and per step an activation tile in shared memory plus the
+// expanded FP16 weights in tensor memory (freed together, by one commit per
+// issuing thread, when the MMAs reading them complete). Keeping the expanded
+// operand out of shared memory leaves its bandwidth to the TMA writes and the
+// activation reads of the MMAs.
 template <int NPROJ>
 struct Geo {
   static constexpr int SC = 8;
-  static constexpr int SX = NPROJ == 2 ? 6 : 8;
   static constexpr int SA = 4;
+  static constexpr int SX = SA;
   static constexpr uint32_t kC = NPROJ * kCodeBytes + kSzBytes;
   static constexpr uint32_t offX = 0, offC = SX * kXBytes, offCtrl = offC + SC * kC;
   static constexpr size_t smem = (size_t)offCtrl + 1024 + 1024;
@@ -178,7 +179,7 @@ struct GemmParams {
 };
 
 struct Bars {
-  uint64_t *c_full, *c_empty, *x_full, *x_empty, *a_full, *a_empty, *acc_full;
+  uint64_t *c_full, *c_empty, *x_full, *a_full, *a_empty, *acc_full;
   uint32_t* tmem_slot;
   int* abort;
 };
@@ -190,7 +191,6 @@ __device__ __forceinline__ Bars bars_at(uint8_t* p) {
   b.c_full = q; q += G::SC;
   b.c_empty = q; q += G::SC;
   b.x_full = q; q += G::SX;
-  b.x_empty = q; q += G::SX;
   b.a_full = q; q += G::SA;
   b.a_empty = q; q += G::SA;
   b.acc_full = q; q += 1;
@@ -237,13 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::bar_init(&b.c_full[s], 1);
       tc::bar_init(&b.c_empty[s], 4);  // one expand warp per lane quarter takes each step
     }
-    for (int s = 0; s < G::SX; ++s) {
-      tc::bar_init(&b.x_full[s], 1);
-      tc::bar_init(&b.x_empty[s], 2);  // one commit per issuing thread
-    }
     for (int s = 0; s < G::SA; ++s) {
+      tc::bar_init(&b.x_full[s], 1);
       tc::bar_init(&b.a_full[s], 4);
-      tc::bar_init(&b.a_empty[s], 2);
+      tc::bar_init(&b.a_empty[s], 2);  // one commit per issuing thread
     }
     tc::bar_init(b.acc_full, 2);
     *b.abort = 0;
@@ -283,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % G::SX;
-        if (kt >= G::SX && !tc::bar_wait(&b.x_empty[s], ((kt / G::SX) - 1) & 1)) {
+        if (kt >= G::SX && !tc::bar_wait(&b.a_empty[s], ((kt / G::SX) - 1) & 1)) {
           abort_block(b, a.flags);
           break;
         }
@@ -323,7 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                            kt > 0 || kk > p);
         }
         tc::mma_commit(&b.a_empty[sa]);
-        tc::mma_commit(&b.x_empty[sx]);
       }
       tc::mma_commit(b.acc_full);
     }

@@ -38,9 +38,20 @@ __device__ __forceinline__ bool bar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(20000u) : "memory");
   return ok != 0;
 }
-// Bounded wait (about one second at most); false when it gave up.
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool bar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait (about one second at most); false when it gave up. A phase
+// that has already completed is taken without the suspending wait.
 constexpr unsigned kWaitTries = 50000;
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
+  if (bar_test(bar, parity)) return true;
   for (unsigned i = 0; i < kWaitTries; ++i)
     if (bar_try_wait(bar, parity)) return true;
   return false;
