@@ -777,8 +777,12 @@ def main():
     args = parse()
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
-        if rank == 0:
+        if rank == 0:  # the other ranks exit without work
             print(json.dumps(run_reference(args)), flush=True)
+        barrier(world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
