@@ -245,10 +245,17 @@ __device__ void route_block(const DecodeParams& a, const RouteSmem& r, const uin
     for (int i = tid; i < a.E * parts; i += nt) {
       const int e = i % a.E, part = i / a.E;
       const float v = r.lg[e];
-      if (part == 0) {
-        if (isnan(v) || v == INFINITY) atomicOr(&r.bad[0], 1);
-        else atomicMax(&r.bad[2], float_key(v));
-        if (v == -INFINITY) atomicAdd(&r.bad[1], 1);
+      if (i < a.E) {  // part 0 (whole warps while E is a multiple of 32): one atomic per warp
+        const unsigned mask = __activemask();
+        const int is_bad = isnan(v) || v == INFINITY;
+        const int32_t kmax = __reduce_max_sync(mask, is_bad ? float_key(-INFINITY) : float_key(v));
+        const int any_bad = __any_sync(mask, is_bad);
+        const int ninf = __popc(__ballot_sync(mask, v == -INFINITY));
+        if ((threadIdx.x & 31) == __ffs(mask) - 1) {
+          if (any_bad) atomicOr(&r.bad[0], 1);
+          atomicMax(&r.bad[2], kmax);
+          if (ninf) atomicAdd(&r.bad[1], ninf);
+        }
       }
       int cnt = 0;
       const int j1 = min(a.E, (part + 1) * span);
@@ -315,16 +322,24 @@ __device__ __forceinline__ void finish_weights(const DecodeParams& a, const Rout
 // return blk_of and ids are visible to the whole block; w is complete in
 // warp 0 (which forms it when the block routes itself) and becomes visible
 // to the other warps at their next barrier with warp 0.
-__device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, uint64_t* full,
-                                         uint64_t* empty, const uint8_t** blk_of, int empty_count,
-                                         bool writer) {
+// empty_count: arrivals that free a stage; for the gate/up kernel, the warps
+// of the sub-group that drains it (odd stages: odd_count).
+__device__ __forceinline__ void init_bars(const DecodeParams& a, uint64_t* full, uint64_t* empty,
+                                          int empty_count, int odd_count) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], empty_count);
+      mbar_init(&empty[s], (s & 1) ? odd_count : empty_count);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+}
+
+// Barriers (init_bars, by the caller, before any other thread uses them),
+// routing or the given ids, the expert block of every pair; ends with a
+// block barrier.
+__device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, const uint8_t** blk_of,
+                                         bool writer) {
   const RouteSmem r = route_smem(a, sm);
   const bool table = a.E <= kSlotTableMax;
   if (a.logits) {
@@ -455,8 +470,11 @@ __global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const De
   uint4* xs4 = reinterpret_cast<uint4*>(sm + a.part_off);                    // [H/32][4]
   float* xsum = reinterpret_cast<float*>(sm + a.part_off + (size_t)a.H * 2);  // [H/32]
   float* xback = xsum + a.H / 32;                                             // [H/32]
-  griddep_wait();  // logits / ids and x come from earlier kernels
-  prologue(a, sm, full, empty, blk_of, 1, c == 0);
+  // Independent of earlier kernels: before the wait. Every warp of the
+  // sub-group that drains a stage arrives on its empty barrier.
+  init_bars(a, full, empty, kSub0, kGateWarps - kSub0);
+  griddep_wait();                // logits / ids and x come from earlier kernels
+  prologue(a, sm, blk_of, c == 0);
   griddep_launch_dependents();  // the down kernel may start its prefetch
   if (warp == kGateWarps) {
     if (lane == 0) produce(a, sm, full, empty, blk_of, n0, n1, 0ull, a.off.gu_row);
@@ -502,9 +520,10 @@ __global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const De
         if (lane == 0) a.hbuf[(size_t)q * a.I + n0 + r] = __float2half_rn(blk ? silu_f(ag) * au : 0.0f);
       }
       // The sub-group has finished reading the stage: one arrival frees it.
-      if (sub == 0) asm volatile("bar.sync 2, %0;" ::"n"(kSub0 * 32) : "memory");
-      else asm volatile("bar.sync 3, %0;" ::"n"((kGateWarps - kSub0) * 32) : "memory");
-      if (wr == 0 && lane == 0) mbar_arrive(&empty[s]);
+      // This warp has finished reading the stage (no sub-group barrier: the
+      // stage is free once every warp of the sub-group has arrived).
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
     p += np;
   }
@@ -526,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_down_kernel(const DecodePa
   float* part = reinterpret_cast<float*>(sm + a.part_off);  // [P][rows]
   // Inputs the prefetch needs (logits or ids, slot_of, the pool) are final:
   // the gate/up kernel passed its own griddepcontrol.wait before signalling.
-  prologue(a, sm, full, empty, blk_of, 1, false);
+  init_bars(a, full, empty, 1, 1);
+  prologue(a, sm, blk_of, false);
   const RouteSmem rt = route_smem(a, sm);
   if (warp == kWarps) {
     if (lane == 0) produce(a, sm, full, empty, blk_of, m0, m1, a.off.d_offset, a.off.d_row);
