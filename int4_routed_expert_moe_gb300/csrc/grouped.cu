@@ -6,10 +6,10 @@
 // routed to them; the weights stay INT4 + FP16 scale/zero in memory and are
 // expanded only on chip, activations are FP16 and accumulation FP32.
 //
-// Steps (one stream, six launches):
-//   1. token sort: pairs p = t*k + j grouped by expert (stable);
-//   2. tile list: for every resident expert with pairs, tiles of up to 128
-//      consecutive sorted pairs; unusable ids are reported in the flags;
+// Steps (one stream, five launches):
+//   1-2. token sort: pairs p = t*k + j grouped by expert (stable), and in
+//      the same kernel the tile list (for every resident expert with pairs,
+//      tiles of up to 128 consecutive sorted pairs) and the unusable-id flags;
 //   3. gather: X_sorted[pos] = x[token of pos], K order permuted inside each
 //      8-element chunk (see dq_word);
 //   4. gate/up GEMM per (tile, 128 rows of I): TMA brings the INT4 codes and
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j)
             if (c0 + j < n)
               a.h_sorted[(size_t)(pos0 + c0 + j) * a.rows + prow] =
-                  __float2half_rn(silu_f(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
+                  __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
         }
       } else {
         float dv[16], ev[16];
@@ -429,46 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- small kernels -------------------------------------------------------------
-// Tile list (one block) and unusable-id reporting.
-__global__ void grouped_tiles_kernel(const int32_t* __restrict__ ids, int P, int E,
-                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ slot_of,
-                                     int n_slots, int4* __restrict__ tiles, int32_t* __restrict__ n_tiles,
-                                     int32_t* __restrict__ flags) {
-  const int tid = threadIdx.x;
-  for (int p = tid; p < P; p += blockDim.x) {
-    const int e = ids[p];
-    if (e != -1 && (e < 0 || e >= E)) {
-      atomicOr(flags, 2);
-    } else if (e >= 0) {
-      const int s = slot_of[e];
-      if (s < 0 || s >= n_slots) atomicOr(flags, 1);
-    }
-  }
-  if (tid < 32) {
-    int carry = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + tid;
-      int cnt = 0, s = -1, o0 = 0, ne = 0;
-      if (e < E) {
-        o0 = offsets[e];
-        ne = offsets[e + 1] - o0;
-        s = slot_of[e];
-        if (ne > 0 && s >= 0 && s < n_slots) cnt = (ne + BN - 1) / BN;
-      }
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tid >= o) incl += v;
-      }
-      for (int i = 0; i < cnt; ++i)
-        tiles[carry + incl - cnt + i] = make_int4(s, o0 + i * BN, min(BN, ne - i * BN), e);
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (tid == 0) *n_tiles = carry;
-  }
-}
-
 // X_sorted[pos] = x[pair_tok[pos]], each 8-element chunk in operand K order.
 __global__ void grouped_gather_kernel(const __half* __restrict__ x, int H, const int32_t* __restrict__ offsets,
                                       int E, const int32_t* __restrict__ pair_tok, __half* __restrict__ xs) {
@@ -576,10 +536,15 @@ int grouped_forward(const ForwardArgs& a) {
   float* pair_out = reinterpret_cast<float*>(ws + w.pair_out);
   cudaStream_t st = a.stream;
 
-  int rc = launch_token_sort(a.ids, P, a.k, a.E, offsets, pair_tok, pair_j, st);
+  SortTiles stl;
+  stl.slot_of = a.slot_of;
+  stl.n_slots = a.n_slots;
+  stl.tile_n = BN;
+  stl.tiles = tiles;
+  stl.n_tiles = n_tiles;
+  stl.flags = flags;
+  int rc = launch_token_sort(a.ids, P, a.k, a.E, offsets, pair_tok, pair_j, st, &stl);
   if (rc != MOE_OK) return rc;
-  grouped_tiles_kernel<<<1, 1024, 0, st>>>(a.ids, P, a.E, offsets, a.slot_of, a.n_slots, tiles, n_tiles, flags);
-  if ((rc = check_launch("grouped tiles")) != MOE_OK) return rc;
   grouped_gather_kernel<<<4 * 152, 256, 0, st>>>(a.x, a.H, offsets, a.E, pair_tok, xs);
   if ((rc = check_launch("grouped gather")) != MOE_OK) return rc;
 

@@ -54,9 +54,20 @@ struct ForwardArgs {
 size_t gemv_workspace_bytes(int H, int I, int T, int k);
 int gemv_forward(const ForwardArgs& a);
 
+// Optional outputs of the token sort for the grouped path: the tile list of
+// resident experts with pairs (tiles of up to tile_n sorted pairs) and the
+// unusable-id bits of the error word (0: no slot, 1: id outside [-1, E)).
+struct SortTiles {
+  const int32_t* slot_of;
+  int n_slots;
+  int tile_n;
+  int4* tiles;  // NULL: no tile list
+  int32_t* n_tiles;
+  int32_t* flags;
+};
 // Token sort of the (token, choice) pairs by expert (see moe_token_sort).
 int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
-                      int32_t* pair_tok, int32_t* pair_j, cudaStream_t st);
+                      int32_t* pair_tok, int32_t* pair_j, cudaStream_t st, const SortTiles* tiles);
 
 // Fused one-kernel decode path (persistent, one block per SM).
 size_t fused_workspace_bytes(int H, int I, int T, int k);

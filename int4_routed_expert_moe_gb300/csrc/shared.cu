@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (live) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (c0 + j < n) a.out[(size_t)(tok0 + c0 + j) * a.rows + row] = __float2half_rn(silu_f(gv[j]) * uv[j]);
+          if (c0 + j < n) a.out[(size_t)(tok0 + c0 + j) * a.rows + row] = __float2half_rn(silu_fast(gv[j]) * uv[j]);
       }
     }
   }

@@ -20,7 +20,7 @@ constexpr int kSortWarps = 32;
 
 __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
     const int32_t* __restrict__ ids, int P, int k, int E, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ pair_tok, int32_t* __restrict__ pair_j) {
+    int32_t* __restrict__ pair_tok, int32_t* __restrict__ pair_j, const SortTiles tl) {
   extern __shared__ __align__(16) int32_t sm[];
   int32_t* cnt = sm;                          // [kSortWarps][E]
   int32_t* total = sm + kSortWarps * E;       // [E + 1]
@@ -43,6 +43,19 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
     const unsigned active = __ballot_sync(0xffffffffu, p < p1);
     const unsigned peers = __match_any_sync(0xffffffffu, e) & active;
     if (p < p1 && e >= 0 && (peers & lt_mask) == 0) cnt[warp * E + e] += __popc(peers);
+    if (tl.tiles) {  // report unusable ids (error-word bits 0 and 1)
+      int bad_id = 0, no_slot = 0;
+      if (p < p1) {
+        const int raw = ids[p];
+        if (raw != -1 && (raw < 0 || raw >= E)) bad_id = 1;
+        else if (raw >= 0) {
+          const int sl = tl.slot_of[raw];
+          no_slot = sl < 0 || sl >= tl.n_slots;
+        }
+      }
+      const int any_bad = __any_sync(0xffffffffu, bad_id), any_noslot = __any_sync(0xffffffffu, no_slot);
+      if (lane == 0 && (any_bad || any_noslot)) atomicOr(tl.flags, (any_bad ? 2 : 0) | (any_noslot ? 1 : 0));
+    }
     __syncwarp();
   }
   __syncthreads();
@@ -73,6 +86,32 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) total[E] = carry;
+    // Tile list: every resident expert with pairs, tiles of up to tile_n
+    // consecutive sorted pairs (slot, first position, pairs, expert).
+    if (tl.tiles) {
+      __syncwarp();  // total[] of every lane visible to the warp
+      int tcarry = 0;
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int tc = 0, sl = -1, o0 = 0, ne = 0;
+        if (e < E) {
+          o0 = total[e];
+          ne = (e + 1 < E ? total[e + 1] : carry) - o0;
+          sl = tl.slot_of[e];
+          if (ne > 0 && sl >= 0 && sl < tl.n_slots) tc = (ne + tl.tile_n - 1) / tl.tile_n;
+        }
+        int incl = tc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        for (int i = 0; i < tc; ++i)
+          tl.tiles[tcarry + incl - tc + i] = make_int4(sl, o0 + i * tl.tile_n, min(tl.tile_n, ne - i * tl.tile_n), e);
+        tcarry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) *tl.n_tiles = tcarry;
+    }
   }
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) offsets[e] = total[e];
@@ -101,7 +140,7 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
 }  // namespace
 
 int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
-                      int32_t* pair_tok, int32_t* pair_j, cudaStream_t st) {
+                      int32_t* pair_tok, int32_t* pair_j, cudaStream_t st, const SortTiles* tiles) {
   const size_t smem = (size_t)(kSortWarps * E + E + 1) * sizeof(int32_t);
   cudaError_t e = cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort smem attr: %s", cudaGetErrorString(e));
@@ -115,7 +154,9 @@ int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, token_sort_kernel, ids, P, k, E, offsets, pair_tok, pair_j);
+  SortTiles tl = {};
+  if (tiles) tl = *tiles;
+  e = cudaLaunchKernelEx(&cfg, token_sort_kernel, ids, P, k, E, offsets, pair_tok, pair_j, tl);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort launch: %s", cudaGetErrorString(e));
   return MOE_OK;
 }
@@ -130,5 +171,5 @@ extern "C" int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* 
   if (!offsets || (T > 0 && (!ids || !pair_tok || !pair_j)))
     return moe::fail(MOE_ERR_ARG, "moe_token_sort: NULL pointer");
   return moe::launch_token_sort(ids, T * k, k, E, offsets, pair_tok, pair_j,
-                                static_cast<cudaStream_t>(stream));
+                                static_cast<cudaStream_t>(stream), nullptr);
 }
