@@ -179,7 +179,7 @@ struct GemmParams {
 };
 
 struct Bars {
-  uint64_t *c_full, *c_empty, *x_full, *a_full, *a_empty, *acc_full;
+  uint64_t *c_full, *c_empty, *x_full, *a_full, *a_empty, *acc_full, *acc_empty;
   uint32_t* tmem_slot;
   int* abort;
 };
@@ -194,6 +194,7 @@ __device__ __forceinline__ Bars bars_at(uint8_t* p) {
   b.a_full = q; q += G::SA;
   b.a_empty = q; q += G::SA;
   b.acc_full = q; q += 1;
+  b.acc_empty = q; q += 1;
   b.tmem_slot = reinterpret_cast<uint32_t*>(q);
   b.abort = reinterpret_cast<int*>(b.tmem_slot + 1);
   return b;
@@ -210,20 +211,37 @@ __device__ __forceinline__ void drain(uint64_t* full, int stages, int issued) {
     tc::bar_wait(&full[kt % stages], (kt / stages) & 1);
 }
 
-// One tile: 128 weight rows x up to 128 sorted pairs of one expert.
+// Work item: 128 weight rows (row block rb) x up to 128 sorted pairs of one
+// expert (tile). The grid is persistent: block c takes items c, c + G, ...;
+// the step counter of every ring runs on across items, so the TMA warps
+// prefetch the next item's codes and activations while the current item's
+// epilogue runs, and the accumulators are reused once the epilogue has read
+// them (acc_empty).
 //   NPROJ = 2: gate and up accumulators, epilogue h = silu(gate) * up (FP16).
-//   NPROJ = 1: down accumulator, epilogue pair_out[t*k + j] (FP32).
+//   NPROJ = 1: down accumulators (even and odd K slices), epilogue
+//              pair_out[t*k + j] (FP32).
+struct Item {
+  int slot, pos0, n, nmma, row0;
+};
+__device__ __forceinline__ Item item_of(const GemmParams& a, int w, int rblocks) {
+  const int4 td = a.tiles[w / rblocks];
+  Item it;
+  it.slot = td.x;
+  it.pos0 = td.y;
+  it.n = td.z;
+  it.nmma = (td.z + 15) & ~15;
+  it.row0 = (w % rblocks) * BM;
+  return it;
+}
+
 template <int NPROJ>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
                         const GemmParams a) {
   using G = Geo<NPROJ>;
-  const int tile = blockIdx.y;
-  if (tile >= *a.n_tiles) return;
-  const int4 td = a.tiles[tile];
-  const int slot = td.x, pos0 = td.y, n = td.z;
-  const int row0 = blockIdx.x * BM;
-  const int nmma = (n + 15) & ~15;
+  const int rblocks = (a.rows + BM - 1) / BM;
+  const int n_items = *a.n_tiles * rblocks;
+  if ((int)blockIdx.x >= n_items) return;
   const int KT = a.K / BK;
   constexpr uint32_t kTmemCols = G::kTmemCols;
   extern __shared__ uint8_t smraw[];
@@ -243,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::bar_init(&b.a_empty[s], 2);  // one commit per issuing thread
     }
     tc::bar_init(b.acc_full, 2);
+    tc::bar_init(b.acc_empty, kDqWarps);
     *b.abort = 0;
     tc::bar_init_fence();
   }
@@ -253,43 +272,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *b.tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {  // codes and scale/zero entries of the tile's rows
+    if (lane == 0) {  // codes and scale/zero entries of each item's rows
       int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % G::SC;
-        if (kt >= G::SC && !tc::bar_wait(&b.c_empty[s], ((kt / G::SC) - 1) & 1)) {
-          abort_block(b, a.flags);
-          break;
+      for (int w = blockIdx.x, li = 0; w < n_items && !is_aborted(b); w += gridDim.x, ++li) {
+        const Item it = item_of(a, w, rblocks);
+        for (int kt = 0; kt < KT; ++kt) {
+          const int g = li * KT + kt, s = g % G::SC;
+          if (g >= G::SC && !tc::bar_wait(&b.c_empty[s], ((g / G::SC) - 1) & 1)) {
+            abort_block(b, a.flags);
+            break;
+          }
+          if (is_aborted(b)) break;
+          uint8_t* st = sm + G::offC + (size_t)s * G::kC;
+          const int k0 = kt * BK;
+          const int gb = (k0 / a.g) / G::kGAlign * G::kGAlign;
+          tc::bar_expect_tx(&b.c_full[s], G::kC);
+          tc::tma_load_3d(st, &map_w, (int)a.q0 + k0 / 2, it.row0, it.slot, &b.c_full[s]);
+          if (NPROJ == 2) tc::tma_load_3d(st + kCodeBytes, &map_w, (int)a.q1 + k0 / 2, it.row0, it.slot, &b.c_full[s]);
+          tc::tma_load_3d(st + NPROJ * kCodeBytes, &map_w, (int)(a.sz + G::kSzEntry * gb), it.row0, it.slot,
+                          &b.c_full[s]);
+          issued = g + 1;
         }
-        if (is_aborted(b)) break;
-        uint8_t* st = sm + G::offC + (size_t)s * G::kC;
-        const int k0 = kt * BK;
-        const int gb = (k0 / a.g) / G::kGAlign * G::kGAlign;
-        tc::bar_expect_tx(&b.c_full[s], G::kC);
-        tc::tma_load_3d(st, &map_w, (int)a.q0 + k0 / 2, row0, slot, &b.c_full[s]);
-        if (NPROJ == 2) tc::tma_load_3d(st + kCodeBytes, &map_w, (int)a.q1 + k0 / 2, row0, slot, &b.c_full[s]);
-        tc::tma_load_3d(st + NPROJ * kCodeBytes, &map_w, (int)(a.sz + G::kSzEntry * gb), row0, slot,
-                        &b.c_full[s]);
-        issued = kt + 1;
       }
       if (is_aborted(b)) drain(b.c_full, G::SC, issued);
     }
   } else if (warp == 2) {
-    if (lane == 0) {  // activation tile: 64 sorted pairs per load
-      const uint32_t bytes = (n > 64 ? 2u : 1u) * 64u * BK * 2u;
+    if (lane == 0) {  // activation tile of each item: 64 sorted pairs per load
       int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % G::SX;
-        if (kt >= G::SX && !tc::bar_wait(&b.a_empty[s], ((kt / G::SX) - 1) & 1)) {
-          abort_block(b, a.flags);
-          break;
+      for (int w = blockIdx.x, li = 0; w < n_items && !is_aborted(b); w += gridDim.x, ++li) {
+        const Item it = item_of(a, w, rblocks);
+        const uint32_t bytes = (it.n > 64 ? 2u : 1u) * 64u * BK * 2u;
+        for (int kt = 0; kt < KT; ++kt) {
+          const int g = li * KT + kt, s = g % G::SX;
+          if (g >= G::SX && !tc::bar_wait(&b.a_empty[s], ((g / G::SX) - 1) & 1)) {
+            abort_block(b, a.flags);
+            break;
+          }
+          if (is_aborted(b)) break;
+          uint8_t* st = sm + G::offX + (size_t)s * kXBytes;
+          tc::bar_expect_tx(&b.x_full[s], bytes);
+          tc::tma_load_2d(st, &map_b, kt * BK, it.pos0, &b.x_full[s]);
+          if (it.n > 64) tc::tma_load_2d(st + 64 * BK * 2, &map_b, kt * BK, it.pos0 + 64, &b.x_full[s]);
+          issued = g + 1;
         }
-        if (is_aborted(b)) break;
-        uint8_t* st = sm + G::offX + (size_t)s * kXBytes;
-        tc::bar_expect_tx(&b.x_full[s], bytes);
-        tc::tma_load_2d(st, &map_b, kt * BK, pos0, &b.x_full[s]);
-        if (n > 64) tc::tma_load_2d(st + 64 * BK * 2, &map_b, kt * BK, pos0 + 64, &b.x_full[s]);
-        issued = kt + 1;
       }
       if (is_aborted(b)) drain(b.x_full, G::SX, issued);
     }
@@ -298,126 +323,147 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Issuer p owns accumulator p: the gate (p = 0) or up (p = 1)
       // projection, or for the down projection the K slices kk = p, p + 2.
       const int p = warp == 1 ? 0 : 1;
-      const uint32_t idesc = tc::idesc_f16(BM, nmma);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int sa = kt % G::SA, sx = kt % G::SX;
-        if (!tc::bar_wait(&b.a_full[sa], (kt / G::SA) & 1) || !tc::bar_wait(&b.x_full[sx], (kt / G::SX) & 1)) {
+      for (int w = blockIdx.x, li = 0; w < n_items && !is_aborted(b); w += gridDim.x, ++li) {
+        const Item it = item_of(a, w, rblocks);
+        const uint32_t idesc = tc::idesc_f16(BM, it.nmma);
+        // The previous item's epilogue has read the accumulators.
+        if (li > 0 && !tc::bar_wait(b.acc_empty, (li - 1) & 1)) {
           abort_block(b, a.flags);
           break;
         }
-        if (is_aborted(b)) break;
         tc::tc_fence_after();
-        const uint32_t xbase = tc::smem_addr(sm + G::offX + (size_t)sx * kXBytes);
-        if (NPROJ == 2) {
+        for (int kt = 0; kt < KT; ++kt) {
+          const int g = li * KT + kt, sa = g % G::SA;
+          if (!tc::bar_wait(&b.a_full[sa], (g / G::SA) & 1) || !tc::bar_wait(&b.x_full[sa], (g / G::SX) & 1)) {
+            abort_block(b, a.flags);
+            break;
+          }
+          if (is_aborted(b)) break;
+          tc::tc_fence_after();
+          const uint32_t xbase = tc::smem_addr(sm + G::offX + (size_t)sa * kXBytes);
+          if (NPROJ == 2) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, p) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
-                           kt > 0 || kk > 0);
-        } else {
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, p) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
+                             kt > 0 || kk > 0);
+          } else {
 #pragma unroll
-          for (int kk = p; kk < BK / 16; kk += 2)
-            tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, 0) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
-                           kt > 0 || kk > p);
+            for (int kk = p; kk < BK / 16; kk += 2)
+              tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, 0) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
+                             kt > 0 || kk > p);
+          }
+          tc::mma_commit(&b.a_empty[sa]);
         }
-        tc::mma_commit(&b.a_empty[sa]);
+        tc::mma_commit(b.acc_full);
       }
-      tc::mma_commit(b.acc_full);
     }
   } else if (warp >= 4) {
     // Expand: warp w owns the TMEM lanes of its quarter (rows 32 (w % 4) ..
-    // +31) and every fourth step, kt = j (mod 4) with j = (w - 4) / 4, so
-    // four steps are expanded at once; lane t owns row 32 (w % 4) + t, all
+    // +31) and every fourth step (global step g = j (mod 4), j = (w - 4) / 4),
+    // so four steps are expanded at once; lane t owns row 32 (w % 4) + t, all
     // 64 codes of the step (at most two scale/zero groups: one per 32).
     const int q4 = warp & 3, j4 = (warp - 4) >> 2;
     const int r = 32 * q4 + lane;
     const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
-    for (int kt = j4; kt < KT; kt += 4) {
-      const int sc = kt % G::SC, sa = kt % G::SA;
-      if (is_aborted(b)) break;
-      if (!tc::bar_wait(&b.c_full[sc], (kt / G::SC) & 1)) {
-        abort_block(b, a.flags);
-        break;
-      }
-      const uint8_t* cs = sm + G::offC + (size_t)sc * G::kC;
-      const uint32_t k0 = (uint32_t)kt * BK;
-      // floor(k / g) by multiply-high with the rounded-up reciprocal (exact
-      // for k, g <= 8192).
-      const int gi0 = (int)__umulhi(k0, a.g_magic), gi1 = (int)__umulhi(k0 + 32u, a.g_magic);
-      const int gb = gi0 / G::kGAlign * G::kGAlign;
-      uint4 cw[NPROJ][2];
-      DqConst d0[NPROJ], d1[NPROJ];
+    bool ok = true;
+    for (int w = blockIdx.x, li = 0; w < n_items && ok; w += gridDim.x, ++li) {
+      const Item it = item_of(a, w, rblocks);
+      const int g0 = li * KT;
+      for (int g = g0 + ((j4 - g0) % 4 + 4) % 4; g < g0 + KT; g += 4) {
+        const int kt = g - g0;
+        const int sc = g % G::SC, sa = g % G::SA;
+        if (is_aborted(b) || !tc::bar_wait(&b.c_full[sc], (g / G::SC) & 1)) {
+          abort_block(b, a.flags);
+          ok = false;
+          break;
+        }
+        const uint8_t* cs = sm + G::offC + (size_t)sc * G::kC;
+        const uint32_t k0 = (uint32_t)kt * BK;
+        // floor(k / g) by multiply-high with the rounded-up reciprocal (exact
+        // for k, g <= 8192).
+        const int gi0 = (int)__umulhi(k0, a.g_magic), gi1 = (int)__umulhi(k0 + 32u, a.g_magic);
+        const int gb = gi0 / G::kGAlign * G::kGAlign;
+        uint4 cw[NPROJ][2];
+        DqConst d0[NPROJ], d1[NPROJ];
 #pragma unroll
-      for (int p = 0; p < NPROJ; ++p) {
-        const uint4* src = reinterpret_cast<const uint4*>(cs + p * kCodeBytes + r * 32);
-        cw[p][0] = src[0];
-        cw[p][1] = src[1];
-        const uint8_t* e = cs + NPROJ * kCodeBytes + r * 32 + 4 * p;
-        d0[p] = dq_const(*reinterpret_cast<const uint32_t*>(e + (gi0 - gb) * G::kSzEntry));
-        d1[p] = gi1 == gi0 ? d0[p] : dq_const(*reinterpret_cast<const uint32_t*>(e + (gi1 - gb) * G::kSzEntry));
+        for (int p = 0; p < NPROJ; ++p) {
+          const uint4* src = reinterpret_cast<const uint4*>(cs + p * kCodeBytes + r * 32);
+          cw[p][0] = src[0];
+          cw[p][1] = src[1];
+          const uint8_t* e = cs + NPROJ * kCodeBytes + r * 32 + 4 * p;
+          d0[p] = dq_const(*reinterpret_cast<const uint32_t*>(e + (gi0 - gb) * G::kSzEntry));
+          d1[p] = gi1 == gi0 ? d0[p] : dq_const(*reinterpret_cast<const uint32_t*>(e + (gi1 - gb) * G::kSzEntry));
+        }
+        __syncwarp();
+        if (lane == 0) tc::bar_arrive(&b.c_empty[sc]);
+        if (g >= G::SA && !tc::bar_wait(&b.a_empty[sa], ((g / G::SA) - 1) & 1)) {
+          abort_block(b, a.flags);
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+#pragma unroll
+        for (int p = 0; p < NPROJ; ++p) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const DqConst& d = h ? d1[p] : d0[p];
+            const uint4 c = cw[p][h];
+            const uint4 o0 = dq_word(c.x, d), o1 = dq_word(c.y, d), o2 = dq_word(c.z, d), o3 = dq_word(c.w, d);
+            const uint32_t v[16] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w,
+                                    o2.x, o2.y, o2.z, o2.w, o3.x, o3.y, o3.z, o3.w};
+            tc::tmem_st16(tlane + G::colA(sa, p) + 16u * h, v);
+          }
+        }
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
       }
-      __syncwarp();
-      if (lane == 0) tc::bar_arrive(&b.c_empty[sc]);
-      if (kt >= G::SA && !tc::bar_wait(&b.a_empty[sa], ((kt / G::SA) - 1) & 1)) {
-        abort_block(b, a.flags);
-        break;
-      }
+      if (!ok) break;
+      // Epilogue of this item: TMEM lanes of this warp's quarter, one
+      // quarter of the columns; then release the accumulators.
+      const bool got = tc::bar_wait(b.acc_full, li & 1);
+      if (!got) abort_block(b, a.flags);
       tc::tc_fence_after();
+      const int row = it.row0 + r;
+      const bool live = got && !is_aborted(b) && row < a.rows;
+      for (int c0 = j4 * (BN / 4); c0 < j4 * (BN / 4) + BN / 4 && c0 < it.nmma; c0 += 16) {
+        if (NPROJ == 2) {
+          float gv[16], uv[16];
+          tc::tmem_ld16(tlane + (uint32_t)c0, gv);
+          tc::tmem_ld16(tlane + (uint32_t)(BN + c0), uv);
+          tc::tmem_ld_wait();
+          if (live) {
+            const int prow = (row & ~7) | kperm_pos(row & 7);
 #pragma unroll
-      for (int p = 0; p < NPROJ; ++p) {
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < it.n)
+                a.h_sorted[(size_t)(it.pos0 + c0 + j) * a.rows + prow] =
+                    __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
+          }
+        } else {
+          float dv[16], ev[16];
+          tc::tmem_ld16(tlane + (uint32_t)c0, dv);
+          tc::tmem_ld16(tlane + (uint32_t)(BN + c0), ev);
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const DqConst& d = h ? d1[p] : d0[p];
-          const uint4 c = cw[p][h];
-          const uint4 o0 = dq_word(c.x, d), o1 = dq_word(c.y, d), o2 = dq_word(c.z, d), o3 = dq_word(c.w, d);
-          const uint32_t v[16] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w,
-                                  o2.x, o2.y, o2.z, o2.w, o3.x, o3.y, o3.z, o3.w};
-          tc::tmem_st16(tlane + G::colA(sa, p) + 16u * h, v);
-        }
-      }
-      tc::tmem_st_wait();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
-    }
-    // Epilogue: TMEM lanes of this warp's quarter, one quarter of the columns.
-    const bool ok = tc::bar_wait(b.acc_full, 0);
-    if (!ok) abort_block(b, a.flags);
-    tc::tc_fence_after();
-    const int row = row0 + r;
-    const bool live = ok && !is_aborted(b) && row < a.rows;
-    const uint32_t tl = tlane;
-    for (int c0 = j4 * (BN / 4); c0 < j4 * (BN / 4) + BN / 4 && c0 < nmma; c0 += 16) {
-      if (NPROJ == 2) {
-        float gv[16], uv[16];
-        tc::tmem_ld16(tl + (uint32_t)c0, gv);
-        tc::tmem_ld16(tl + (uint32_t)(BN + c0), uv);
-        tc::tmem_ld_wait();
-        if (live) {
-          const int prow = (row & ~7) | kperm_pos(row & 7);
+          for (int j = 0; j < 16; ++j) dv[j] += ev[j];  // even + odd K slices, fixed order
+          if (live) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < n)
-              a.h_sorted[(size_t)(pos0 + c0 + j) * a.rows + prow] =
-                  __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
-        }
-      } else {
-        float dv[16], ev[16];
-        tc::tmem_ld16(tl + (uint32_t)c0, dv);
-        tc::tmem_ld16(tl + (uint32_t)(BN + c0), ev);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) dv[j] += ev[j];  // even + odd K slices, fixed order
-        if (live) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < n) {
-              const int pos = pos0 + c0 + j;
-              const size_t q = (size_t)a.pair_tok[pos] * a.k + a.pair_j[pos];
-              a.pair_out[q * a.rows + row] = dv[j] * kInvAScale;
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < it.n) {
+                const int pos = it.pos0 + c0 + j;
+                const size_t q = (size_t)a.pair_tok[pos] * a.k + a.pair_j[pos];
+                a.pair_out[q * a.rows + row] = dv[j] * kInvAScale;
+              }
             }
           }
         }
       }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(b.acc_empty);
+      if (!got) break;
     }
   }
   tc::tc_fence_before();
@@ -512,6 +558,16 @@ GroupedWs grouped_ws(int H, int I, int T, int k, int E) {
 }
 
 bool g_attr_done = false;
+int g_num_sms = 0;
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      g_num_sms = -1;
+  }
+  return g_num_sms;
+}
 
 }  // namespace
 
@@ -606,7 +662,10 @@ int grouped_forward(const ForwardArgs& a) {
   gu.q1 = a.off.gu_q_up;
   gu.sz = a.off.gu_sz;
   gu.h_sorted = hs;
-  grouped_gemm_kernel<2><<<dim3((a.I + BM - 1) / BM, w.max_tiles), kThreads, Geo<2>::smem, st>>>(m_gu, m_x, gu);
+  const int n_sm = num_sms();
+  if (n_sm <= 0) return fail(MOE_ERR_CUDA, "device query failed");
+  const int gu_items = ((a.I + BM - 1) / BM) * w.max_tiles, dn_items = ((a.H + BM - 1) / BM) * w.max_tiles;
+  grouped_gemm_kernel<2><<<std::min(n_sm, gu_items), kThreads, Geo<2>::smem, st>>>(m_gu, m_x, gu);
   if ((rc = check_launch("grouped gate/up GEMM")) != MOE_OK) return rc;
   GemmParams dn = gp;
   dn.rows = a.H;
@@ -614,7 +673,7 @@ int grouped_forward(const ForwardArgs& a) {
   dn.q0 = a.off.d_q;
   dn.sz = a.off.d_sz;
   dn.pair_out = pair_out;
-  grouped_gemm_kernel<1><<<dim3((a.H + BM - 1) / BM, w.max_tiles), kThreads, Geo<1>::smem, st>>>(m_dn, m_h, dn);
+  grouped_gemm_kernel<1><<<std::min(n_sm, dn_items), kThreads, Geo<1>::smem, st>>>(m_dn, m_h, dn);
   if ((rc = check_launch("grouped down GEMM")) != MOE_OK) return rc;
   grouped_combine_kernel<<<4 * 152, 256, 0, st>>>(pair_out, a.ids, a.weights, a.slot_of, a.n_slots, a.E, a.T,
                                                   a.k, a.H, a.y_shared, a.y);
