@@ -420,14 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
       }
       if (!ok) break;
-      // Epilogue of this item: TMEM lanes of this warp's quarter, one
-      // quarter of the columns; then release the accumulators.
+      // Epilogue of this item: TMEM lanes of this warp's quarter, the
+      // 16-column chunks ci = j4, j4 + 4, ... of the live columns; then
+      // release the accumulators.
       const bool got = tc::bar_wait(b.acc_full, li & 1);
       if (!got) abort_block(b, a.flags);
       tc::tc_fence_after();
       const int row = it.row0 + r;
       const bool live = got && !is_aborted(b) && row < a.rows;
-      for (int c0 = j4 * (BN / 4); c0 < j4 * (BN / 4) + BN / 4 && c0 < it.nmma; c0 += 16) {
+      for (int c0 = 16 * j4; c0 < it.nmma; c0 += 64) {
         if (NPROJ == 2) {
           float gv[16], uv[16];
           tc::tmem_ld16(tlane + (uint32_t)c0, gv);
@@ -442,21 +443,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
           }
         } else {
+          // Output pair index of column c0 + lane (lanes 0..15), shared by shuffles.
+          int qi = 0;
+          if (lane < 16 && c0 + lane < it.n) {
+            const int pos = it.pos0 + c0 + lane;
+            qi = a.pair_tok[pos] * a.k + a.pair_j[pos];
+          }
           float dv[16], ev[16];
           tc::tmem_ld16(tlane + (uint32_t)c0, dv);
           tc::tmem_ld16(tlane + (uint32_t)(BN + c0), ev);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) dv[j] += ev[j];  // even + odd K slices, fixed order
-          if (live) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c0 + j < it.n) {
-                const int pos = it.pos0 + c0 + j;
-                const size_t q = (size_t)a.pair_tok[pos] * a.k + a.pair_j[pos];
-                a.pair_out[q * a.rows + row] = dv[j] * kInvAScale;
-              }
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int q = __shfl_sync(0xffffffffu, qi, j);
+            if (live && c0 + j < it.n) a.pair_out[(size_t)q * a.rows + row] = dv[j] * kInvAScale;
           }
         }
       }
