@@ -38,6 +38,11 @@ from int4_routed_expert_moe_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer decode tokens/s (expert-weight HBM GB/s in roofline)"
 METRIC_PREFILL = "MoE-layer prefill tokens/s (tensor-core TFLOP/s in roofline)"
+# DRAM bytes per layer call from one ncu capture of the current kernels
+# (decode: gate/up 17.88 MB + down 9.00 MB read, nothing written; prefill:
+# gate/up GEMM 159.45 MB read + 5.10 MB written, down GEMM 79.77 + 8.18 MB).
+DECODE_LAYER_DRAM_BYTES = 26_875_904
+PREFILL_GEMM_DRAM_BYTES = 252_505_088
 
 
 def parse():
@@ -348,7 +353,9 @@ def run_ours(args, world, rank, local):
         "expert_hbm_frac_step": round(step_gbs / peak, 4),
         "roofline": {"bound": "hbm", "kernel": "moe_layer_forward GEMV path: decode_gateup_kernel (routing inside) + decode_down_kernel (overlapped via PDL), one layer",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": DECODE_LAYER_DRAM_BYTES,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the two kernels of "
+                                       "one layer call (profiles/decode_olmoe_streamed_kernels.md)",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": round(fwd_avg_s * 1e6, 3),
                      "peak_source": peak_src,
                      "timing": f"external event-record graph nodes around each call, "
@@ -638,7 +645,10 @@ def run_prefill(args, world, rank):
     out["roofline"] = {"bound": "tensor", "kernel": "moe_layer_forward grouped path, one layer (route, sort, "
                                                     "tiles, gather, tcgen05 gate/up GEMM, tcgen05 down GEMM, combine)",
                        "achieved": round(achieved, 1), "peak": peak_t, "unit": "TFLOP/s",
-                       "frac": round(achieved / peak_t, 4), "traffic": None,
+                       "frac": round(achieved / peak_t, 4), "traffic": PREFILL_GEMM_DRAM_BYTES,
+                       "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and "
+                                         "down GEMM kernels of one layer call (the small kernels not included; "
+                                         "profiles/prefill_olmoe_grouped_and_shared_kernels.md)",
                        "flops_per_launch": flops_layer, "avg_launch_us": round(layer_ms * 1e3, 2),
                        "peak_source": peak_t_src,
                        "weight_gbs": round(weight_gbs, 1), "weight_hbm_frac": round(weight_gbs / peak_h, 4),
