@@ -52,8 +52,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="olmoe_decode",
-                    choices=["olmoe_decode", "olmoe_partial", "olmoe_prefill", "large_fanout_b1",
-                             "large_fanout_b16", "large_fanout_b256"])
+                    choices=["olmoe_decode", "qwen_decode", "olmoe_partial", "olmoe_prefill",
+                             "large_fanout_b1", "large_fanout_b16", "large_fanout_b256"])
     ap.add_argument("--graph-window", type=int, default=128)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -218,10 +218,11 @@ def measured_tensor_peak(sustained):
 
 # --------------------------------------------------------------------------
 class DecodeWorkload:
-    """The OLMoE-shaped decode stack, resident on the device."""
+    """A decode stack (OLMoE-shaped by default), resident on the device."""
 
-    def __init__(self, moe, seed, steps_total, rank=0):
-        wl = synth.WORKLOADS["olmoe_decode"]
+    def __init__(self, moe, seed, steps_total, rank=0, name="olmoe_decode"):
+        wl = synth.WORKLOADS[name]
+        self.name = name
         self.moe = moe
         self.L, self.H, self.I, self.E = wl["L"], wl["H"], wl["I"], wl["E"]
         self.k, self.g, self.T, self.renorm = wl["k"], wl["g"], wl["T"], wl["renorm"]
@@ -263,12 +264,12 @@ class DecodeWorkload:
         return self.L * self.k * self.bb
 
 
-def run_ours(args, world, rank, local):
+def run_ours(args, world, rank, local, name="olmoe_decode"):
     from int4_routed_expert_moe_gb300 import moe
-    seed = synth.BASE_SEED + 1
+    seed = synth.BASE_SEED + (1 if name == "olmoe_decode" else 6)
     K = args.steps or 512
     W = args.warmup if args.warmup is not None else 128
-    wl = DecodeWorkload(moe, seed, K + W, rank)
+    wl = DecodeWorkload(moe, seed, K + W, rank, name)
     stream = torch.cuda.current_stream()
     win = max(1, args.graph_window)
 
@@ -342,18 +343,20 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded; random-init INT4 experts of the OLMoE shape)",
-        "config": {"workload": "olmoe_decode", "layers": wl.L, "hidden": wl.H, "experts": wl.E,
+        "data": "synthetic (seeded; random-init INT4 experts of the workload's shape)",
+        "config": {"workload": wl.name, "layers": wl.L, "hidden": wl.H, "experts": wl.E,
                    "top_k": wl.k, "inter": wl.I, "group": wl.g, "tokens_per_step": wl.T,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "arithmetic": "INT4 weights, FP16 products (<= 8 terms), FP32 accumulation",
-                   "l2": "inputs larger than L2: 427.8 MB of expert weights per step from a 3.42 GB pool",
+                   "l2": f"inputs larger than L2: {wl.expert_bytes_per_step() / 1e6:.1f} MB of expert weights "
+                         f"per step from a {wl.L * wl.E * wl.bb / 1e9:.2f} GB pool",
                    "launch": f"CUDA graphs of {win} steps, PDL between kernels"},
         "expert_hbm_gbs_step": round(step_gbs, 1),
         "expert_hbm_frac_step": round(step_gbs / peak, 4),
         "roofline": {"bound": "hbm", "kernel": "moe_layer_forward GEMV path: decode_gateup_kernel (routing inside) + decode_down_kernel (overlapped via PDL), one layer",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": DECODE_LAYER_DRAM_BYTES,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": DECODE_LAYER_DRAM_BYTES if wl.name == "olmoe_decode" else None,
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the two kernels of "
                                        "one layer call (profiles/decode_olmoe_streamed_kernels.md)",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": round(fwd_avg_s * 1e6, 3),
@@ -817,7 +820,7 @@ def main():
     elif args.workload.startswith("large_fanout_b"):
         out = run_fanout(args, world, rank, int(args.workload.split("_b")[1]))
     else:
-        out = run_ours(args, world, rank, local)
+        out = run_ours(args, world, rank, local, args.workload)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -36,6 +36,10 @@ WORKLOADS = {
                           T=512, logits="uniform", Ts=2048, Is=4096),
     "large_fanout": dict(L=48, H=2048, I=512, E=512, k=10, g=128, renorm=True,
                          T=(1, 16, 256), logits="zipf", alpha=1.1),
+    # Qwen-like routed stack: 60 experts, top-4 without renormalisation,
+    # expert intermediate 1408, 24 layers.
+    "qwen_decode": dict(L=24, H=2048, I=1408, E=60, k=4, g=128, renorm=False,
+                        T=1, steps=128, logits="normal"),
 }
 
 BASE_SEED = 20261202

@@ -36,10 +36,12 @@ def test_status_strings_and_version():
 
 
 @pytest.mark.parametrize("shape,want", [((256, 128, 64), 57344), ((2048, 1024, 128), 3342336),
-                                         ((2048, 512, 128), 1671168), ((192, 64, 64), 64 * 224 + 192 * 48)])
+                                         ((2048, 512, 128), 1671168), ((192, 64, 64), 64 * 224 + 192 * 48),
+                                         ((2048, 1408, 128), 1408 * 2176 + 2048 * 752)])
 def test_block_layout(shape, want):
     # Unpadded shapes hold exactly 3*H*I/2 + 3*(H*I/g)*4 bytes; rows whose
-    # contents are not a 16-byte multiple are padded (tiny: down rows 72 -> 80).
+    # contents are not a 16-byte multiple are padded (tiny: down rows 72 -> 80;
+    # Qwen-like inter 1408: down rows 748 -> 752).
     H, I, g = shape
     assert moe.moe_expert_block_bytes(shape) == want
     lay = moe.moe_expert_block_layout(shape)

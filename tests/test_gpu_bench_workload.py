@@ -1,7 +1,8 @@
-"""Parity at full size on the benchmark's own workload (needs a GB300).
+"""Parity at full size on the benchmark's own workloads (needs a GB300).
 
-The OLMoE-shaped decode stack that bench.py times: 16 layers x 64 experts of
-hidden 2048 / intermediate 1024, generated on the device. For sampled layers
+The decode stacks that bench.py times -- OLMoE-shaped (16 layers x 64 experts
+of hidden 2048 / intermediate 1024, top-8) and Qwen-like (24 layers x 60
+experts, intermediate 1408, top-4) -- generated on the device. For sampled layers
 the same moe_layer_forward call bench.py makes run on fresh
 N(0,1) activations, and the oracle recomputes the layer from the expert
 blocks read back from the pool (inputs, read before the kernels run)."""
@@ -17,12 +18,13 @@ from tests.gpu_util import tol_ok
 pytestmark = pytest.mark.gpu
 
 
-def test_bench_decode_workload_sampled_layers():
+@pytest.mark.parametrize("name,seed,layers", [("olmoe_decode", 1, (0, 7, 15)), ("qwen_decode", 6, (0, 11, 23))])
+def test_bench_decode_workload_sampled_layers(name, seed, layers):
     moe = binding()
     import bench
-    wl = bench.DecodeWorkload(moe, synth.BASE_SEED + 1, 4)
+    wl = bench.DecodeWorkload(moe, synth.BASE_SEED + seed, 4, name=name)
     dev = torch.device("cuda")
-    for l in (0, 7, 15):
+    for l in layers:
         pool = wl.layer_pool(l)
         lg = wl.logits[1, l]
         ids_ref, _ = moe_oracle.route(lg.cpu().numpy(), wl.k, wl.renorm)
