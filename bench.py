@@ -55,6 +55,8 @@ def parse():
                     choices=["olmoe_decode", "qwen_decode", "olmoe_partial", "olmoe_prefill",
                              "large_fanout_b1", "large_fanout_b16", "large_fanout_b256"])
     ap.add_argument("--graph-window", type=int, default=128)
+    ap.add_argument("--policy", default="decay", choices=["decay", "lru", "pinned"],
+                    help="residency victim policy (olmoe_partial)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -401,11 +403,16 @@ def run_partial(args, world, rank):
     pool = torch.zeros((L, C, bb), dtype=torch.uint8, device=dev)
     slot_of = torch.full((L, E), -1, dtype=torch.int32, device=dev)
     copy = torch.cuda.Stream()
-    h = moe.moe_residency_create(dict(layers=L, experts=E, slots=C, spares=0, max_ids_per_step=k,
-                                      block_bytes=bb, decay=wl["decay"]), src, pool, slot_of,
-                                 torch.cuda.current_stream(), copy)
     n = W + K
     ranks = np.stack([synth.zipf_ranks(seed, l, E) for l in range(L)])  # [L][E]
+    # Pinned policy: the profile is the popularity the stream is drawn from
+    # (a perfect measurement pass); C - k experts pinned, k slots follow LRU.
+    pinned = C - k if args.policy == "pinned" else 0
+    h = moe.moe_residency_create(dict(layers=L, experts=E, slots=C, spares=0, max_ids_per_step=k,
+                                      block_bytes=bb, decay=wl["decay"], policy=args.policy, pinned=pinned,
+                                      profile=(1.0 / ranks.astype(np.float64) ** wl["alpha"])
+                                      if args.policy == "pinned" else None),
+                                 src, pool, slot_of, torch.cuda.current_stream(), copy)
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
     gum = -torch.log(-torch.log(torch.rand((n, L, 1, E), generator=gen, device=dev).clamp_min(1e-20)))
@@ -453,6 +460,7 @@ def run_partial(args, world, rank):
     out = base_line(METRIC, K * world / (ms / 1e3), "tokens/s", world, K, W, ms,
                     {"workload": "olmoe_partial", "layers": L, "hidden": H, "experts": E, "top_k": k,
                      "inter": I, "group": g, "slots": C, "decay": wl["decay"], "zipf_alpha": wl["alpha"],
+                     "policy": args.policy, "pinned": pinned,
                      "tokens_per_step": 1,
                      "launch": "eager; per layer: route, D2H of ids, host decision, H2D misses, experts"})
     out["residency"] = {"hit_rate": round(hits / max(1, hits + misses), 4), "misses_per_token": round(misses / K, 3),

@@ -272,13 +272,12 @@ int moe_shared_forward(const void* x, int T, int H, int Is, const void* wg,
 
 /* ---- residency manager ----------------------------------------------------
  * Per-layer GPU slot pools fed from a complete, immutable host source
- * ("03 / Arquitetura", ADR 0009) with eviction by decayed access counts
- * (Strata page). One decode step of one layer:
+ * ("03 / Arquitetura", ADR 0009). One decode step of one layer:
  *   1. every count c of the layer becomes c*decay, then gains 1 per id given;
  *   2. N = distinct ids; |N| > slots is MOE_ERR_CAPACITY (nothing changes);
  *   3. misses N \ resident, in ascending id order; when the resident set is
- *      full the victim is argmin (count, id) over resident \ N; the miss
- *      takes the lowest free slot (a spare) else the victim's slot;
+ *      full a victim leaves it (policy below); the miss takes the lowest free
+ *      slot (a spare) else the victim's slot;
  *   4. each miss is copied host->device with cudaMemcpyAsync on the copy
  *      stream, after the copy stream waited for every reader of the slot
  *      enqueued so far on the compute stream;
@@ -286,7 +285,21 @@ int moe_shared_forward(const void* x, int T, int H, int Is, const void* wg,
  *      publishes the new slot table [E] of the layer (the new generation).
  * Initial state: expert e in slot e for e < slots ("canonical initial
  * placement"), counts 0, spare slots free.
+ * Victim policies (the candidates are resident \ N):
+ *   MOE_POLICY_DECAY   argmin (decayed count, id): an access counter whose
+ *                      old accesses lose weight (Strata page);
+ *   MOE_POLICY_LRU     argmin (step of last use, id), never-used = -1: the
+ *                      evolving LRU of the claims.json experiment contract;
+ *   MOE_POLICY_PINNED  the `pinned` experts of each layer with the highest
+ *                      `profile` value (ties: lower id) are resident from the
+ *                      start and never evicted; the other slots follow LRU
+ *                      (lucashiago.com.br "local" explainer, etapa 4: a
+ *                      profile fixes yesterday's popular set, LRU adapts).
+ *                      Initial resident set: the pinned experts plus the
+ *                      lowest other ids, in slots 0.. by ascending id.
+ *                      Requires pinned <= slots - min(max_ids_per_step, E).
  */
+enum { MOE_POLICY_DECAY = 0, MOE_POLICY_LRU = 1, MOE_POLICY_PINNED = 2 };
 typedef struct {
   int32_t layers;            /* L */
   int32_t experts;           /* E per layer */
@@ -296,6 +309,9 @@ typedef struct {
   int32_t dry_run;           /* 1: decide and trace only, no CUDA work */
   uint64_t block_bytes;      /* bytes of one expert block */
   double decay;              /* count decay per step, in (0, 1] */
+  int32_t policy;            /* MOE_POLICY_* (0: decayed counts) */
+  int32_t pinned;            /* MOE_POLICY_PINNED: experts pinned per layer */
+  const double* profile;     /* MOE_POLICY_PINNED: host [L][E] popularity, read by create */
 } moe_residency_cfg;
 
 typedef struct {

@@ -1,5 +1,6 @@
 // Residency manager: per-layer GPU slot pools fed from a complete, immutable
-// page-locked host source, evicting by decayed access counts.
+// page-locked host source, evicting by decayed access counts, by least recent
+// use, or by least recent use outside a profile-pinned set.
 //
 // "Horizon RunMap -- Prévia Técnica", "03 / Arquitetura" (contract
 // resident-qpacked-cache-v1, ADR 0009): the source in host RAM stays complete
@@ -10,7 +11,9 @@
 // of it; a failure before publish keeps the previous generation.
 // "Desenvolvedor do Strata cria mapa ao vivo de 24 576 especialistas MoE em
 // uma GTX 1070": eviction by an access counter whose old accesses lose weight.
-// Horizon RunMap claims.json, experiment contract: canonical initial placement.
+// Horizon RunMap claims.json, experiment contract: canonical initial
+// placement, evolving LRU. lucashiago.com.br "local" explainer, etapa 4: a
+// profile measured beforehand pins the popular set; LRU adapts by itself.
 //
 // Built with -ffp-contract=off: the count update c = c*decay; c = c + 1 is two
 // IEEE double operations, with no fused multiply-add.
@@ -30,6 +33,8 @@ struct moe_residency {
   cudaEvent_t readers_done = nullptr, copies_done = nullptr;
   struct Layer {
     std::vector<double> counts;
+    std::vector<int64_t> last_used;  // step of the last use, -1 never
+    std::vector<char> pinned;        // never evicted (MOE_POLICY_PINNED)
     std::vector<int32_t> slot_of;  // expert -> physical slot, -1 absent
     std::vector<int32_t> free;     // free physical slots
     moe_residency_stats st;
@@ -84,6 +89,15 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
                      "moe_residency_create: a step may need %d distinct experts but only %d slots",
                      std::min(c.max_ids_per_step, c.experts), c.slots);
   if (c.slots + c.spares > 4096) return moe::fail(MOE_ERR_CAPACITY, "too many physical slots");
+  if (c.policy < MOE_POLICY_DECAY || c.policy > MOE_POLICY_PINNED)
+    return moe::fail(MOE_ERR_ARG, "moe_residency_create: unknown policy %d", c.policy);
+  if (c.policy == MOE_POLICY_PINNED) {
+    if (!c.profile || c.pinned < 0) return moe::fail(MOE_ERR_ARG, "moe_residency_create: pinned policy needs a profile");
+    if (c.pinned > c.slots - std::min(c.max_ids_per_step, c.experts))
+      return moe::fail(MOE_ERR_CAPACITY,
+                       "moe_residency_create: %d pinned experts leave fewer than %d slots for a step's misses",
+                       c.pinned, std::min(c.max_ids_per_step, c.experts));
+  }
   if (!c.dry_run) {
     if (!host_src || !dev_pool || !dev_slot_of)
       return moe::fail(MOE_ERR_ARG, "moe_residency_create: NULL buffer");
@@ -102,21 +116,54 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
   r->copy = static_cast<cudaStream_t>(copy);
   r->physical = c.slots + c.spares;
   r->layers.resize(c.layers);
-  for (auto& L : r->layers) {
+  r->cfg.profile = nullptr;  // read here only
+  for (int l = 0; l < c.layers; ++l) {
+    auto& L = r->layers[l];
     L.counts.assign(c.experts, 0.0);
+    L.last_used.assign(c.experts, -1);
+    L.pinned.assign(c.experts, 0);
     L.slot_of.assign(c.experts, -1);
-    for (int e = 0; e < c.slots; ++e) L.slot_of[e] = e;
+    if (c.policy == MOE_POLICY_PINNED) {
+      // Top `pinned` experts by profile (ties: lower id), then the lowest
+      // other ids; slots in ascending expert order.
+      const double* prof = c.profile + (size_t)l * c.experts;
+      std::vector<int32_t> order(c.experts);
+      for (int e = 0; e < c.experts; ++e) order[e] = e;
+      std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return prof[x] > prof[y]; });
+      for (int i = 0; i < c.pinned; ++i) L.pinned[order[i]] = 1;
+      std::vector<char> res(c.experts, 0);
+      int n = 0;
+      for (int e = 0; e < c.experts; ++e)
+        if (L.pinned[e]) res[e] = 1, ++n;
+      for (int e = 0; e < c.experts && n < c.slots; ++e)
+        if (!res[e]) res[e] = 1, ++n;
+      int s = 0;
+      for (int e = 0; e < c.experts; ++e)
+        if (res[e]) L.slot_of[e] = s++;
+    } else {
+      for (int e = 0; e < c.slots; ++e) L.slot_of[e] = e;
+    }
     for (int s = c.slots; s < r->physical; ++s) L.free.push_back(s);
     std::memset(&L.st, 0, sizeof(L.st));
   }
   if (!c.dry_run) {
     cudaError_t e = cudaEventCreateWithFlags(&r->readers_done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->copies_done, cudaEventDisableTiming);
-    // Canonical initial placement: expert e of each layer in slot e, e < C.
+    // Initial placement: each resident expert's block into its slot
+    // (canonical: expert e in slot e, e < C, one copy per layer).
     for (int l = 0; e == cudaSuccess && l < c.layers; ++l) {
       const uint8_t* s = r->src + (size_t)l * c.experts * c.block_bytes;
       uint8_t* d = r->pool + (size_t)l * r->physical * c.block_bytes;
-      e = cudaMemcpy(d, s, (size_t)c.slots * c.block_bytes, cudaMemcpyHostToDevice);
+      if (c.policy != MOE_POLICY_PINNED) {
+        e = cudaMemcpy(d, s, (size_t)c.slots * c.block_bytes, cudaMemcpyHostToDevice);
+      } else {
+        for (int x = 0; e == cudaSuccess && x < c.experts; ++x) {
+          const int32_t sl = r->layers[l].slot_of[x];
+          if (sl >= 0)
+            e = cudaMemcpy(d + (size_t)sl * c.block_bytes, s + (size_t)x * c.block_bytes, c.block_bytes,
+                           cudaMemcpyHostToDevice);
+        }
+      }
     }
     if (e == cudaSuccess) {
       std::vector<int32_t> table((size_t)c.layers * c.experts);
@@ -171,8 +218,10 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
     int32_t victim = -1;
     if (n_resident == c.slots) {
       for (int v = 0; v < c.experts; ++v) {
-        if (slot_of[v] < 0 || needed[v]) continue;
-        if (victim < 0 || counts[v] < counts[victim]) victim = v;  // ties keep the lower id
+        if (slot_of[v] < 0 || needed[v] || L.pinned[v]) continue;
+        const bool better = c.policy == MOE_POLICY_DECAY ? counts[v] < counts[victim < 0 ? v : victim]
+                                                          : L.last_used[v] < L.last_used[victim < 0 ? v : victim];
+        if (victim < 0 || better) victim = v;  // ties keep the lower id
       }
       retiring.push_back(slot_of[victim]);
       slot_of[victim] = -1;
@@ -257,6 +306,7 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
   for (const Miss& m : misses)
     r->trace.push_back({L.steps, layer, m.expert, m.slot, m.victim});
   L.counts.swap(counts);
+  for (int32_t e : distinct) L.last_used[e] = L.steps;
   L.slot_of.swap(slot_of);
   L.free.swap(free_slots);
   L.st.steps += 1;

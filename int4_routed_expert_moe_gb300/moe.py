@@ -47,11 +47,16 @@ class moe_block_layout(ctypes.Structure):
         (n, ctypes.c_uint32) for n in ("gu_q_gate", "gu_q_up", "gu_sz", "d_q", "d_sz")]
 
 
+MOE_POLICY_DECAY, MOE_POLICY_LRU, MOE_POLICY_PINNED = 0, 1, 2
+
+
 class moe_residency_cfg(ctypes.Structure):
     _fields_ = [("layers", ctypes.c_int32), ("experts", ctypes.c_int32),
                 ("slots", ctypes.c_int32), ("spares", ctypes.c_int32),
                 ("max_ids_per_step", ctypes.c_int32), ("dry_run", ctypes.c_int32),
-                ("block_bytes", ctypes.c_uint64), ("decay", ctypes.c_double)]
+                ("block_bytes", ctypes.c_uint64), ("decay", ctypes.c_double),
+                ("policy", ctypes.c_int32), ("pinned", ctypes.c_int32),
+                ("profile", ctypes.c_void_p)]
 
 
 class moe_residency_stats(ctypes.Structure):
@@ -331,10 +336,20 @@ def moe_shared_forward(x: torch.Tensor, wg: torch.Tensor, wu: torch.Tensor, wd: 
 # ---- residency manager -----------------------------------------------------
 def moe_residency_create(cfg: dict, host_src: torch.Tensor | None, dev_pool: torch.Tensor | None,
                          dev_slot_of: torch.Tensor | None, compute=None, copy=None) -> int:
+    policy = cfg.get("policy", MOE_POLICY_DECAY)
+    if isinstance(policy, str):
+        policy = {"decay": MOE_POLICY_DECAY, "lru": MOE_POLICY_LRU, "pinned": MOE_POLICY_PINNED}[policy]
+    prof = cfg.get("profile")
+    prof_arr = None
+    if prof is not None:
+        prof_arr = np.ascontiguousarray(np.asarray(prof, dtype=np.float64).reshape(-1))
+        if prof_arr.size != int(cfg["layers"]) * int(cfg["experts"]):
+            raise ValueError("profile must hold layers x experts values")
     c = moe_residency_cfg(int(cfg["layers"]), int(cfg["experts"]), int(cfg["slots"]),
                           int(cfg.get("spares", 0)), int(cfg["max_ids_per_step"]),
                           int(cfg.get("dry_run", 0)), int(cfg["block_bytes"]),
-                          float(cfg["decay"]))
+                          float(cfg["decay"]), int(policy), int(cfg.get("pinned", 0)),
+                          prof_arr.ctypes.data if prof_arr is not None else None)
     dry = bool(c.dry_run)
     src = pool = slot = None
     cs = cp = None

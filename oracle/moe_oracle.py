@@ -239,20 +239,47 @@ class ResidencyLayer:
     One step with the ids needed by all tokens of this decode step:
       1. every count c becomes c * decay, then gains 1.0 per occurrence;
       2. N = the distinct needed ids; |N| > C is a capacity error;
-      3. misses N \\ R in ascending id order; for each, if |R| = C the victim
-         v = argmin over R \\ N of (count_v, v) leaves R; the miss takes the
-         lowest free slot, else the victim's slot;
+      3. misses N \\ R in ascending id order; for each, if |R| = C a victim
+         leaves R; the miss takes the lowest free slot, else the victim's slot;
       4. slots of victims that were not reused become free after the step.
+    Victims, over R \\ N:
+      "decay"  (Strata page: an access counter whose old accesses lose
+               weight): argmin of (count_v, v);
+      "lru"    (claims.json experiment contract: evolving LRU): argmin of
+               (last step v was needed, v), never needed = -1;
+      "pinned" (lucashiago.com.br "local", etapa 4: a measured profile pins
+               the popular set): the `pinned` experts with the largest
+               profile value (ties: lower id) are never victims and are
+               resident from the start together with the lowest other ids
+               (slots in ascending id order); the others follow "lru".
     """
 
-    def __init__(self, E: int, C: int, S: int, decay: float):
+    def __init__(self, E: int, C: int, S: int, decay: float, policy: str = "decay",
+                 profile=None, pinned: int = 0):
         if not (1 <= C <= E) or S < 0:
             raise CapacityError("bad capacity")
+        if policy not in ("decay", "lru", "pinned"):
+            raise ValueError("unknown policy")
         self.E, self.C, self.S, self.decay = E, C, S, float(decay)
+        self.policy = policy
         self.counts = [0.0] * E
+        self.last_used = [-1] * E
+        self.steps = 0
+        self.pinned = set()
         self.slot_of = [-1] * E
-        for e in range(C):
-            self.slot_of[e] = e
+        if policy == "pinned":
+            order = sorted(range(E), key=lambda e: (-float(profile[e]), e))
+            self.pinned = set(order[:pinned])
+            resident = set(self.pinned)
+            for e in range(E):
+                if len(resident) >= C:
+                    break
+                resident.add(e)
+            for slot, e in enumerate(sorted(resident)):
+                self.slot_of[e] = slot
+        else:
+            for e in range(C):
+                self.slot_of[e] = e
         self.free = list(range(C, C + S))
         self.hits = self.misses = self.evictions = 0
 
@@ -280,8 +307,11 @@ class ResidencyLayer:
         for e in misses:
             victim = -1
             if len(resident) == self.C:
-                candidates = [v for v in resident if v not in distinct]
-                victim = min(candidates, key=lambda v: (self.counts[v], v))
+                candidates = [v for v in resident if v not in distinct and v not in self.pinned]
+                if self.policy == "decay":
+                    victim = min(candidates, key=lambda v: (self.counts[v], v))
+                else:
+                    victim = min(candidates, key=lambda v: (self.last_used[v], v))
                 resident.remove(victim)
                 retiring.append(self.slot_of[victim])
                 self.slot_of[victim] = -1
@@ -295,12 +325,16 @@ class ResidencyLayer:
             resident.add(e)
             decisions.append((e, slot, victim))
         self.free.extend(retiring)
+        for e in distinct:
+            self.last_used[e] = self.steps
+        self.steps += 1
         return decisions
 
 
-def residency_sim(id_steps, E: int, C: int, S: int, decay: float) -> dict:
+def residency_sim(id_steps, E: int, C: int, S: int, decay: float, policy: str = "decay",
+                  profile=None, pinned: int = 0) -> dict:
     """Run the policy of one layer over a sequence of steps (lists of ids)."""
-    layer = ResidencyLayer(E, C, S, decay)
+    layer = ResidencyLayer(E, C, S, decay, policy, profile, pinned)
     trace = []
     for step, needed in enumerate(id_steps):
         for (e, slot, victim) in layer.step(needed):

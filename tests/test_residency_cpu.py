@@ -153,3 +153,112 @@ def test_injected_failure_in_place_marks_overwritten_victims_absent():
         assert t[8] >= 0 and t[9] >= 0 and t[10] >= 0
     finally:
         moe.moe_residency_destroy(h)
+
+
+# ---- victim policies: LRU and profile-pinned --------------------------------
+def dry_policy(E, C, S, decay, policy, pinned=0, profile=None, L=1, max_ids=8):
+    cfg = dict(layers=L, experts=E, slots=C, spares=S, max_ids_per_step=max_ids, dry_run=1,
+               block_bytes=4096, decay=decay, policy=policy, pinned=pinned, profile=profile)
+    return moe.moe_residency_create(cfg, None, None, None)
+
+
+def test_policy_hand_traces_match_golden():
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "residency_policy_traces.json")))
+    for c in g["cases"]:
+        prof = None if c["profile"] is None else np.asarray(c["profile"])
+        h = dry_policy(c["E"], c["C"], c["S"], c["decay"], c["policy"], c["pinned"], prof, max_ids=c["max_ids"])
+        try:
+            for ids in c["steps"]:
+                moe.moe_residency_prepare(h, 0, ids)
+            tr = [[s, e, sl, v] for (s, l, e, sl, v) in moe.moe_residency_trace(h)]
+            assert tr == c["trace"], c["name"]
+            assert moe.moe_residency_slot_table(h, 0, c["E"]).tolist() == c["slot_of_after"], c["name"]
+            st = moe.moe_residency_get_stats(h, 0)
+            assert (st["hits"], st["misses"], st["evictions"]) == (c["hits"], c["misses"], c["evictions"])
+        finally:
+            moe.moe_residency_destroy(h)
+        # The oracle's model gives the same trace by hand.
+        ref = moe_oracle.residency_sim(c["steps"], c["E"], c["C"], c["S"], c["decay"], c["policy"],
+                                       c["profile"], c["pinned"])
+        assert [list(t) for t in ref["trace"]] == c["trace"]
+        if "decay_trace" in c:
+            d = moe_oracle.residency_sim(c["steps"], c["E"], c["C"], c["S"], c["decay"], "decay")
+            assert [list(t) for t in d["trace"]] == c["decay_trace"]
+
+
+@pytest.mark.parametrize("policy,E,C,S,k,T,alpha,pinned", [
+    ("lru", 64, 30, 0, 8, 1, 1.0, 0),
+    ("lru", 64, 30, 2, 8, 1, 1.0, 0),
+    ("lru", 32, 12, 0, 4, 2, 0.5, 0),
+    ("pinned", 64, 30, 0, 8, 1, 1.0, 22),
+    ("pinned", 64, 40, 1, 8, 4, 1.0, 8),
+    ("pinned", 64, 16, 0, 8, 1, 0.0, 8),
+])
+def test_policy_variants_match_oracle(policy, E, C, S, k, T, alpha, pinned):
+    L, steps = 2, 300
+    prof = np.stack([1.0 / synth.zipf_ranks(9, l, E) ** max(alpha, 1e-9) for l in range(L)])
+    h = dry_policy(E, C, S, 0.9, policy, pinned, prof if policy == "pinned" else None, L=L, max_ids=T * k)
+    try:
+        per_layer = {l: [] for l in range(L)}
+        for step in range(steps):
+            for l in range(L):
+                lg = synth.logits_zipf(9, l, step, T, E, alpha)
+                ids, _ = moe_oracle.route(lg, k, False)
+                flat = ids.reshape(-1).tolist()
+                per_layer[l].append(flat)
+                moe.moe_residency_prepare(h, l, flat)
+        trace = moe.moe_residency_trace(h)
+        for l in range(L):
+            ref = moe_oracle.residency_sim(per_layer[l], E, C, S, 0.9, policy, prof[l], pinned)
+            got = [(s, e, sl, v) for (s, ll, e, sl, v) in trace if ll == l]
+            assert got == [tuple(t) for t in ref["trace"]]
+            st = moe.moe_residency_get_stats(h, l)
+            assert (st["hits"], st["misses"], st["evictions"]) == (ref["hits"], ref["misses"], ref["evictions"])
+            assert moe.moe_residency_slot_table(h, l, E).tolist() == ref["slot_of"]
+            if policy == "pinned":
+                top = np.argsort(-prof[l], kind="stable")[:pinned]
+                assert all(v not in set(top.tolist()) for (_, _, _, v) in got)
+                assert all(ref["slot_of"][e] >= 0 for e in top)
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+def test_pinned_capacity_and_arguments():
+    with pytest.raises(moe.MoeError):  # 25 pinned leave 5 < 8 slots for a step's misses
+        dry_policy(64, 30, 0, 0.9, "pinned", 25, np.ones((1, 64)))
+    with pytest.raises(moe.MoeError):  # the pinned policy needs a profile
+        dry_policy(64, 30, 0, 0.9, "pinned", 4, None)
+    with pytest.raises(moe.MoeError):  # unknown policy
+        dry_policy(64, 30, 0, 0.9, 7)
+
+
+@pytest.mark.parametrize("alpha", [1.0, 0.0])
+def test_policy_hit_rates_against_the_ceiling(alpha):
+    # Stationary popularity: over a long run no policy beats the best fixed
+    # set (the sum of the C largest inclusion frequencies, measured on the
+    # same stream); with the true profile, pinning is within a few points of
+    # it on Zipf popularity; with uniform popularity every policy sits at
+    # about C/E.
+    E, C, k, steps, pinned = 64, 30, 8, 3000, 22
+    stream = []
+    for s in range(steps):
+        ids, _ = moe_oracle.route(synth.logits_zipf(13, 0, s, 1, E, alpha), k, False)
+        stream.append(ids.reshape(-1).tolist())
+    freq = np.zeros(E)
+    for ids in stream:
+        freq[ids] += 1
+    p = freq / steps
+    ceiling = moe_oracle.hit_ceiling(p, C) / k  # hit fraction of the accesses
+    prof = 1.0 / synth.zipf_ranks(13, 0, E) ** max(alpha, 1e-9)
+    rates = {}
+    for policy in ("decay", "lru", "pinned"):
+        r = moe_oracle.residency_sim(stream, E, C, 0, 0.9, policy, prof, pinned)
+        rates[policy] = r["hits"] / (r["hits"] + r["misses"])
+    for policy, rate in rates.items():
+        assert rate <= ceiling + 0.01, (policy, rate, ceiling)
+    if alpha > 0:
+        assert rates["pinned"] >= ceiling - 0.08, (rates, ceiling)
+        assert rates["pinned"] >= rates["lru"] - 0.01, rates
+    else:
+        for rate in rates.values():
+            assert abs(rate - C / E) < 0.05, (rates, C / E)
