@@ -127,3 +127,25 @@ def test_grouped_workspace_reuse():
         ref = moe_oracle.moe_layer(x, lg, lp.arrays, k, False, 128)
         ok, err, bound = tol_ok(y.float().cpu().numpy(), ref["y"])
         assert ok, (rep, err, bound)
+
+
+@pytest.mark.parametrize("shape,E,k,T", [
+    ((8192, 128, 128), 2, 1, 48),   # largest hidden: 128 K steps of the gate/up GEMM
+    ((256, 8192, 64), 2, 1, 40),    # largest intermediate: 64 row blocks, 128 K steps of the down GEMM
+])
+def test_grouped_maximum_sizes(shape, E, k, T):
+    _case(shape, E, k, False, T, 49, zero="int")
+
+
+def test_grouped_empty_batch():
+    shape, E, k = (256, 128, 64), 8, 2
+    lp = LayerPool(moe, 50, 0, shape, E)
+    dev = torch.device("cuda")
+    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    x = torch.empty((0, 256), dtype=torch.float16, device=dev)
+    ids = torch.empty((0, k), dtype=torch.int32, device=dev)
+    w = torch.empty((0, k), dtype=torch.float32, device=dev)
+    y = torch.empty((0, 256), dtype=torch.float16, device=dev)
+    moe.moe_expert_forward(shape, x, ids, w, E, lp.pool, lp.slot_of, E, None, y, ws, GROUPED)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_flags(ws) == 0

@@ -133,11 +133,12 @@ def test_gemv_large_fanout_layer_b16(path):
 
 @pytest.mark.parametrize("path", GEMV_PATHS)
 @pytest.mark.parametrize("shape,E,k", [((512, 192, 64), 6, 3), ((1088, 320, 32), 5, 2),
-                                       ((8192, 64, 64), 3, 1), ((2048, 1024, 128), 64, 8)])
+                                       ((8192, 64, 64), 3, 1), ((256, 8192, 64), 3, 1),
+                                       ((2048, 1024, 128), 64, 8)])
 def test_gemv_ragged_shapes(shape, E, k, path):
     # H not a multiple of 1024 (partial lane loop), I and H not multiples of
     # the block count (ragged row slices), scale rows not 16-byte multiples,
-    # the largest H; and 16 tokens x 8 choices = 128 pairs (ring reuse).
+    # the largest H, the largest I; and 16 tokens x 8 choices = 128 pairs (ring reuse).
     T = 16 if shape == (2048, 1024, 128) else 2
     _layer_case(shape, E, k, False, T, 34, zero="int", path=path)
 

@@ -64,3 +64,22 @@ def test_shared_rejects_bad_shapes():
     ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
     with pytest.raises(moe.MoeError):
         moe.moe_shared_forward(x, wg, wg, wd, y, ws)
+
+
+def test_shared_largest_hidden():
+    # H = 8192: 128 K steps in the gate/up GEMM, 64 output row blocks in the down GEMM.
+    x, w, y = _run(40, 8192, 256, 54)
+    ref = moe_oracle.shared_ffn(x, w["wg"], w["wu"], w["wd"])
+    ok, err, bound = tol_ok(y, ref)
+    assert ok, (err, bound)
+
+
+def test_shared_empty_batch():
+    dev = torch.device("cuda")
+    x = torch.empty((0, 256), dtype=torch.float16, device=dev)
+    wg = torch.zeros((128, 256), dtype=torch.float16, device=dev)
+    wd = torch.zeros((256, 128), dtype=torch.float16, device=dev)
+    y = torch.empty((0, 256), dtype=torch.float16, device=dev)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    moe.moe_shared_forward(x, wg, wg, wd, y, ws)
+    torch.cuda.synchronize()
