@@ -56,7 +56,10 @@ def parse():
                              "large_fanout_b1", "large_fanout_b16", "large_fanout_b256"])
     ap.add_argument("--graph-window", type=int, default=128)
     ap.add_argument("--policy", default="decay", choices=["decay", "lru", "pinned"],
-                    help="residency victim policy (olmoe_partial)")
+                    help="residency victim policy (olmoe_partial, --mode copy)")
+    ap.add_argument("--mode", default="copy", choices=["copy", "zerocopy"],
+                    help="olmoe_partial: copy misses into slots, or read them in place over the CPU-GPU link")
+    ap.add_argument("--slots", type=int, default=None, help="olmoe_partial: experts resident per layer")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -382,61 +385,71 @@ def base_line(metric, value, unit, world, K, W, ms, config, hib=True):
             "data": "synthetic (seeded; random-init INT4 experts)", "config": config}
 
 
-def run_partial(args, world, rank):
-    """OLMoE shape with partial residency: 30 of 64 slots per layer, decayed
-    counts (0.9 per step), Zipf(1.0) popularity per layer; per layer and step
-    the router runs on the GPU, its ids reach the host, the residency manager
-    decides and streams misses from pinned host RAM on a side stream, then the
-    experts run from the managed pool. Timed: K decode steps after W."""
-    from int4_routed_expert_moe_gb300 import moe
-    wl = synth.WORKLOADS["olmoe_partial"]
-    L, H, I, E, k, g, C = wl["L"], wl["H"], wl["I"], wl["E"], wl["k"], wl["g"], wl["C"]
-    shape = (H, I, g)
-    K = args.steps or wl["seqs"] * wl["steps"]
-    W = args.warmup if args.warmup is not None else wl["warm_seqs"] * wl["steps"]
+class PartialStack:
+    """Inputs shared by the partial-residency runs of the OLMoE shape: the
+    complete pinned host source of all L x E expert blocks, each layer's
+    Zipf(alpha) popularity ranks, and per-step router logits and layer-0
+    inputs for n steps (all on the device)."""
+
+    def __init__(self, moe, rank, n):
+        wl = synth.WORKLOADS["olmoe_partial"]
+        self.wl = wl
+        self.L, self.H, self.I, self.E, self.k, self.g = (wl[key] for key in ("L", "H", "I", "E", "k", "g"))
+        self.shape = (self.H, self.I, self.g)
+        self.bb = moe.moe_expert_block_bytes(self.shape)
+        self.seed = synth.BASE_SEED + 3 + rank
+        dev = torch.device("cuda")
+        self.src = torch.empty((self.L, self.E, self.bb), dtype=torch.uint8).pin_memory()
+        for l in range(self.L):  # generated on the device, kept as the pinned host source
+            self.src[l].copy_(synth.device_pool(self.E, self.H, self.I, self.g, self.seed * 100 + l))
+        self.ranks = np.stack([synth.zipf_ranks(self.seed, l, self.E) for l in range(self.L)])  # [L][E]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(self.seed)
+        gum = -torch.log(-torch.log(torch.rand((n, self.L, 1, self.E), generator=gen, device=dev).clamp_min(1e-20)))
+        self.logits = (-wl["alpha"] * torch.log(torch.from_numpy(self.ranks).float().to(dev)))[None, :, None, :] + gum
+        self.x0 = torch.randn((n, 1, self.H), generator=gen, device=dev).half()
+        self.n = n
+
+    def profile(self):
+        return 1.0 / self.ranks.astype(np.float64) ** self.wl["alpha"]
+
+
+def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0):
+    """Residency by copies: per layer and step the router runs on the GPU, its
+    ids reach the host, the residency manager decides and streams misses from
+    pinned host RAM on a side stream into the layer's C slots, then the experts
+    run from the managed pool. Returns the device time of K steps after W."""
+    L, E, k, bb = ps.L, ps.E, ps.k, ps.bb
     dev = torch.device("cuda")
-    bb = moe.moe_expert_block_bytes(shape)
-    seed = synth.BASE_SEED + 3 + rank
-    src = torch.empty((L, E, bb), dtype=torch.uint8).pin_memory()
-    for l in range(L):  # generated on the device, kept as the pinned host source
-        src[l].copy_(synth.device_pool(E, H, I, g, seed * 100 + l))
     pool = torch.zeros((L, C, bb), dtype=torch.uint8, device=dev)
     slot_of = torch.full((L, E), -1, dtype=torch.int32, device=dev)
     copy = torch.cuda.Stream()
-    n = W + K
-    ranks = np.stack([synth.zipf_ranks(seed, l, E) for l in range(L)])  # [L][E]
     # Pinned policy: the profile is the popularity the stream is drawn from
     # (a perfect measurement pass); C - k experts pinned, k slots follow LRU.
-    pinned = C - k if args.policy == "pinned" else 0
+    pinned = C - k if policy == "pinned" else 0
     h = moe.moe_residency_create(dict(layers=L, experts=E, slots=C, spares=0, max_ids_per_step=k,
-                                      block_bytes=bb, decay=wl["decay"], policy=args.policy, pinned=pinned,
-                                      profile=(1.0 / ranks.astype(np.float64) ** wl["alpha"])
-                                      if args.policy == "pinned" else None),
-                                 src, pool, slot_of, torch.cuda.current_stream(), copy)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(seed)
-    gum = -torch.log(-torch.log(torch.rand((n, L, 1, E), generator=gen, device=dev).clamp_min(1e-20)))
-    logits = (-wl["alpha"] * torch.log(torch.from_numpy(ranks).float().to(dev)))[None, :, None, :] + gum
-    x0 = torch.randn((n, 1, H), generator=gen, device=dev).half()
+                                      block_bytes=bb, decay=ps.wl["decay"], policy=policy, pinned=pinned,
+                                      profile=ps.profile() if policy == "pinned" else None),
+                                 ps.src, pool, slot_of, torch.cuda.current_stream(), copy)
     ids = torch.empty((L, 1, k), dtype=torch.int32, device=dev)
     w = torch.empty((L, 1, k), dtype=torch.float32, device=dev)
-    y = torch.empty((L, 1, H), dtype=torch.float16, device=dev)
-    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, 1, k, E, moe.MOE_PATH_GEMV), dtype=torch.uint8,
+    y = torch.empty((L, 1, ps.H), dtype=torch.float16, device=dev)
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(ps.shape, 1, k, E, moe.MOE_PATH_GEMV), dtype=torch.uint8,
                      device=dev)
     ids_host = torch.empty((k,), dtype=torch.int32).pin_memory()
 
     def step(s):
         for l in range(L):
-            moe.moe_route(logits[s, l], k, wl["renorm"], ids[l], w[l])
+            moe.moe_route(ps.logits[s, l], k, ps.wl["renorm"], ids[l], w[l])
             ids_host.copy_(ids[l].view(-1), non_blocking=True)
             torch.cuda.current_stream().synchronize()  # the step's ids reach the host
             moe.moe_residency_prepare(h, l, ids_host.numpy())
-            x = x0[s] if l == 0 else y[l - 1]
-            moe.moe_expert_forward(shape, x, ids[l], w[l], E, pool[l], slot_of[l], C, None, y[l], ws,
+            x = ps.x0[s] if l == 0 else y[l - 1]
+            moe.moe_expert_forward(ps.shape, x, ids[l], w[l], E, pool[l], slot_of[l], C, None, y[l], ws,
                                    moe.MOE_PATH_GEMV)
 
     try:
-        for s in range(W):
+        for s in range(steps_from, steps_from + W):
             step(s)
         torch.cuda.synchronize()
         st0 = moe.moe_residency_get_stats(h)
@@ -445,7 +458,7 @@ def run_partial(args, world, rank):
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record()
         t0 = time.perf_counter()
-        for s in range(W, W + K):
+        for s in range(steps_from + W, steps_from + W + K):
             step(s)
         ev1.record()
         torch.cuda.synchronize()
@@ -456,16 +469,174 @@ def run_partial(args, world, rank):
     finally:
         moe.moe_residency_destroy(h)
     hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
-    h2d = st1["h2d_bytes"] - st0["h2d_bytes"]
-    out = base_line(METRIC, K * world / (ms / 1e3), "tokens/s", world, K, W, ms,
-                    {"workload": "olmoe_partial", "layers": L, "hidden": H, "experts": E, "top_k": k,
-                     "inter": I, "group": g, "slots": C, "decay": wl["decay"], "zipf_alpha": wl["alpha"],
-                     "policy": args.policy, "pinned": pinned,
-                     "tokens_per_step": 1,
-                     "launch": "eager; per layer: route, D2H of ids, host decision, H2D misses, experts"})
+    return {"ms": ms, "wall_s": wall, "hits": hits, "misses": misses, "pinned": pinned,
+            "bytes_out": st1["h2d_bytes"] - st0["h2d_bytes"], "launches_per_step": L * 7}
+
+
+def partial_zero_copy(moe, ps, C, K, W, world, graph=True, steps_from=0):
+    """Zero-copy residency: each layer keeps a fixed set of C experts in HBM
+    (the C most popular by the profile); the rest are read in place from the
+    pinned host source by the expert kernels over the CPU-GPU link. No host
+    round trip, so the 16 layers of a step are enqueued (and, with graph=True,
+    captured once into a CUDA graph and replayed per step)."""
+    L, E, k, bb = ps.L, ps.E, ps.k, ps.bb
+    dev = torch.device("cuda")
+    n_slots = max(1, C)
+    pool = torch.zeros((L, n_slots, bb), dtype=torch.uint8, device=dev)
+    slot_table = np.full((L, E), -1, dtype=np.int32)
+    for l in range(L):
+        resident = sorted(np.argsort(ps.ranks[l], kind="stable")[:C].tolist())
+        for s_i, e in enumerate(resident):
+            slot_table[l, e] = s_i
+            pool[l, s_i].copy_(ps.src[l, e])
+    slot_of = torch.from_numpy(slot_table).to(dev)
+    ids = torch.empty((L, 1, k), dtype=torch.int32, device=dev)
+    w = torch.empty((L, 1, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, 1, ps.H), dtype=torch.float16, device=dev)
+    lg_cur = torch.empty((L, 1, E), dtype=torch.float32, device=dev)
+    x_cur = torch.empty((1, ps.H), dtype=torch.float16, device=dev)
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(ps.shape, 1, k, E, moe.MOE_PATH_GEMV_UNFUSED),
+                     dtype=torch.uint8, device=dev)
+    hist = torch.empty((ps.n, L, k), dtype=torch.int32, device=dev)
+
+    def layers():
+        for l in range(L):
+            moe.moe_route(lg_cur[l], k, ps.wl["renorm"], ids[l], w[l])
+            x = x_cur if l == 0 else y[l - 1]
+            moe.moe_expert_forward_zero_copy(ps.shape, x, ids[l], w[l], E, pool[l], slot_of[l], n_slots,
+                                             ps.src[l], None, y[l], ws)
+
+    g = None
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            layers()  # warm the binding and the kernels before capture
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            layers()
+
+    def step(s):
+        lg_cur.copy_(ps.logits[s])
+        x_cur.copy_(ps.x0[s])
+        if g is not None:
+            g.replay()
+        else:
+            layers()
+        hist[s].copy_(ids.view(L, k))
+
+    for s in range(steps_from, steps_from + W):
+        step(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    t0 = time.perf_counter()
+    for s in range(steps_from + W, steps_from + W + K):
+        step(s)
+    ev1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    assert moe.moe_workspace_flags(ws) == 0
+    used = hist[steps_from + W:steps_from + W + K].cpu().numpy()  # [K][L][k]
+    resident = slot_table[np.arange(L)[None, :, None], used] >= 0
+    hits = int(resident.sum())
+    misses = int(resident.size - hits)
+    return {"ms": ms, "wall_s": wall, "hits": hits, "misses": misses, "bytes_out": misses * bb,
+            "launches_per_step": L * 3, "graph": graph}
+
+
+def copy_engine_gbs(ps, n=48):
+    """Host-to-device bandwidth of block-sized copies from the pinned source
+    (one cudaMemcpyAsync per block on a side stream), for context."""
+    dev = torch.device("cuda")
+    dst = torch.empty((n, ps.bb), dtype=torch.uint8, device=dev)
+    flat = ps.src.view(-1, ps.bb)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for i in range(8):
+            dst[i].copy_(flat[i], non_blocking=True)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(st)
+        for i in range(n):
+            dst[i].copy_(flat[(7 * i + 3) % flat.shape[0]], non_blocking=True)
+        ev1.record(st)
+    st.synchronize()
+    return n * ps.bb / (ev0.elapsed_time(ev1) / 1e3) / 1e9
+
+
+def run_partial(args, world, rank):
+    """OLMoE shape with partial residency: C of 64 experts per layer in HBM
+    (default 30), Zipf(1.0) popularity per layer, one token per step through
+    16 layers. --mode copy: misses are copied into slots chosen by the victim
+    policy (decayed counts 0.9 per step, LRU, or profile-pinned) before the
+    experts run. --mode zerocopy: a fixed profile set stays in HBM and misses
+    are read in place over the CPU-GPU link. The line adds the time model
+    t_token = t_calc + bytes_out / bandwidth fitted on the two extreme
+    residencies of the same mode and compared with the measured rate."""
+    from int4_routed_expert_moe_gb300 import moe
+    wl = synth.WORKLOADS["olmoe_partial"]
+    L, H, I, E, k, g = wl["L"], wl["H"], wl["I"], wl["E"], wl["k"], wl["g"]
+    C = args.slots if args.slots is not None else wl["C"]
+    if not (0 if args.mode == "zerocopy" else k) <= C <= E:
+        raise SystemExit(f"--slots must be in [{0 if args.mode == 'zerocopy' else k}, {E}] for --mode {args.mode}")
+    K = args.steps or wl["seqs"] * wl["steps"]
+    W = args.warmup if args.warmup is not None else wl["warm_seqs"] * wl["steps"]
+    Ktm, Wtm = min(K, 256), min(W, 32)
+    ps = PartialStack(moe, rank, max(W + K, 2 * (Wtm + Ktm)))
+    lo = 0 if args.mode == "zerocopy" else k
+
+    def run(c, steps, warm, graph=True):
+        r = (partial_zero_copy(moe, ps, c, steps, warm, world, graph=graph) if args.mode == "zerocopy"
+             else partial_copy(moe, ps, c, args.policy, steps, warm, world))
+        torch.cuda.empty_cache()
+        return r
+
+    main_run = run(C, K, W)
+    eager = run(C, Ktm, Wtm, graph=False) if args.mode == "zerocopy" else None
+    full = run(E, Ktm, Wtm)
+    low = run(lo, Ktm, Wtm)
+    # Fit on the two extremes: t = t_calc + bytes_out / bandwidth per token.
+    t_full, t_low = full["ms"] / 1e3 / Ktm, low["ms"] / 1e3 / Ktm
+    b_full, b_low = full["bytes_out"] / Ktm, low["bytes_out"] / Ktm
+    per_byte = (t_low - t_full) / max(1.0, b_low - b_full)
+    t_calc = t_full - b_full * per_byte
+    b_main = main_run["bytes_out"] / K
+    t_pred = t_calc + b_main * per_byte
+    ms = main_run["ms"]
+    value = K * world / (ms / 1e3)
+    cfg = {"workload": "olmoe_partial", "layers": L, "hidden": H, "experts": E, "top_k": k,
+           "inter": I, "group": g, "slots": C, "zipf_alpha": wl["alpha"], "mode": args.mode,
+           "tokens_per_step": 1}
+    if args.mode == "copy":
+        cfg.update({"policy": args.policy, "pinned": main_run["pinned"], "decay": wl["decay"],
+                    "launch": "eager; per layer: route, D2H of ids, host decision, H2D misses, experts"})
+    else:
+        cfg.update({"resident_set": "the C most popular experts of each layer (profile), fixed",
+                    "launch": "one CUDA graph per step: per layer route + two-kernel GEMV reading misses "
+                              "from pinned host memory"})
+    out = base_line(METRIC, value, "tokens/s", world, K, W, ms, cfg)
+    hits, misses = main_run["hits"], main_run["misses"]
     out["residency"] = {"hit_rate": round(hits / max(1, hits + misses), 4), "misses_per_token": round(misses / K, 3),
-                        "h2d_gb": round(h2d / 1e9, 3), "h2d_gbs": round(h2d / (ms / 1e3) / 1e9, 2),
-                        "wall_s": round(wall, 3)}
+                        "bytes_out_gb": round(main_run["bytes_out"] / 1e9, 3),
+                        "bytes_out_gbs": round(main_run["bytes_out"] / (ms / 1e3) / 1e9, 2),
+                        "wall_s": round(main_run["wall_s"], 3)}
+    if eager is not None:
+        out["residency"]["eager_value"] = round(Ktm * world / (eager["ms"] / 1e3), 2)
+    out["time_model"] = {
+        "form": "t_token = t_calc + bytes_out / bandwidth (lucashiago explainer, etapa 5)",
+        "fit": f"two runs of {Ktm} steps in the same mode: all {E} experts resident and {lo} resident",
+        "t_calc_us": round(t_calc * 1e6, 2), "bandwidth_gbs": round(1.0 / per_byte / 1e9, 2) if per_byte > 0 else None,
+        "bytes_out_per_token": int(b_main), "predicted_tok_s": round(1.0 / t_pred, 2),
+        "measured_tok_s": round(value / world, 2), "pred_over_meas": round((1.0 / t_pred) / (value / world), 4),
+        "endpoints_tok_s": {str(E): round(1.0 / t_full, 2), str(lo): round(1.0 / t_low, 2)}}
+    if args.mode == "copy":
+        out["time_model"]["copy_engine_gbs"] = round(copy_engine_gbs(ps), 2)
+    out["gpu_launches"] = main_run["launches_per_step"] * K
     return out
 
 

@@ -206,6 +206,27 @@ int moe_expert_forward(const moe_expert_shape* shape, const void* x, int T,
                        const void* pool, const int32_t* slot_of, int n_slots,
                        const void* y_shared, void* y, void* workspace,
                        size_t workspace_bytes, int path, void* stream);
+/* ---- routed expert FFN reading absent experts over the CPU-GPU link -------
+ * moe_expert_forward's result, computed by the two-kernel dequant-GEMV
+ * (MOE_PATH_GEMV_UNFUSED), where an expert whose slot_of entry is -1 is
+ * not skipped but read in place, by the kernels' own loads, from the layer's
+ * complete host source: a weight that is not in the right memory is read
+ * again at every use (lucashiago.com.br "local" explainer, etapa 5, whose
+ * time model t_token = t_calc + bytes_out / bandwidth prices it). No copy
+ * engine, slot change or host round trip is involved, so a whole decode step
+ * can be enqueued (or captured in a graph) without waiting for routing.
+ * host_src  host [E][block] of this layer, page-locked and mapped into the
+ *           device address space (cudaHostAlloc, or cudaHostRegister on a
+ *           unified-addressing system), 16-byte aligned; read only. Not
+ *           page-locked or not mapped: MOE_ERR_ARG.
+ * Entries of slot_of at or above n_slots still set bit 0 of the error word
+ * and contribute 0. Other arguments and limits as moe_expert_forward.
+ */
+int moe_expert_forward_zero_copy(const moe_expert_shape* shape, const void* x, int T,
+                                 const int32_t* ids, const float* weights, int k, int E,
+                                 const void* pool, const int32_t* slot_of, int n_slots,
+                                 const void* host_src, const void* y_shared, void* y,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 /* ---- routed layer: routing + expert FFN in one call ----------------------
  * The same result as moe_route(logits, ...) followed by
  * moe_expert_forward(...): the router picks each token's experts and their

@@ -23,20 +23,22 @@ namespace {
 constexpr int kWarps = 8;  // warps per block of both kernels
 
 // Resolve the block of expert e, or NULL (setting the flag word) if it is
-// not usable. e == -1 means "no expert" and is silent.
+// not usable. e == -1 means "no expert" and is silent. An expert without a
+// slot (slot_of[e] < 0) is read in place from `host` ([E][block], page-locked
+// host memory mapped into the device's address space) when that is given.
 __device__ __forceinline__ const uint8_t* expert_block(
     int e, int E, const int32_t* __restrict__ slot_of, int n_slots,
-    const uint8_t* __restrict__ pool, size_t block_bytes, int32_t* flags) {
+    const uint8_t* __restrict__ pool, size_t block_bytes, const uint8_t* __restrict__ host,
+    int32_t* flags) {
   if (e < 0 || e >= E) {
     if (e != -1 && flags) atomicOr(flags, 2);
     return nullptr;
   }
   const int s = slot_of[e];
-  if (s < 0 || s >= n_slots) {
-    if (flags) atomicOr(flags, 1);
-    return nullptr;
-  }
-  return pool + (size_t)s * block_bytes;
+  if (s >= 0 && s < n_slots) return pool + (size_t)s * block_bytes;
+  if (s < 0 && host) return host + (size_t)e * block_bytes;
+  if (flags) atomicOr(flags, 1);
+  return nullptr;
 }
 
 // Load activations [n] (fp16, global) into shared memory in the pair order
@@ -95,8 +97,8 @@ template <int NIT>
 __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
     const __half* __restrict__ x, const int32_t* __restrict__ ids, int k, int E,
     const uint8_t* __restrict__ pool, size_t block_bytes,
-    const int32_t* __restrict__ slot_of, int n_slots, int H, int I, int g,
-    BlockOffsets off, float* __restrict__ hbuf, int32_t* __restrict__ flags) {
+    const int32_t* __restrict__ slot_of, int n_slots, const uint8_t* __restrict__ host, int H, int I,
+    int g, BlockOffsets off, float* __restrict__ hbuf, int32_t* __restrict__ flags) {
   extern __shared__ __align__(16) uint8_t smem[];
   __half* xs = reinterpret_cast<__half*>(smem);
   float* xsum = reinterpret_cast<float*>(smem + (size_t)H * 2);
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * kWarps + warp;
   if (n >= I) return;
-  const uint8_t* blk = expert_block(e, E, slot_of, n_slots, pool, block_bytes,
+  const uint8_t* blk = expert_block(e, E, slot_of, n_slots, pool, block_bytes, host,
                                     (warp == 0 && lane == 0) ? flags : nullptr);
   if (!blk) {
     if (lane == 0) hbuf[(size_t)p * I + n] = 0.0f;
@@ -156,8 +158,9 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
 __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
     const float* __restrict__ hbuf, const int32_t* __restrict__ ids,
     const float* __restrict__ wts, int k, int E, const uint8_t* __restrict__ pool,
-    size_t block_bytes, const int32_t* __restrict__ slot_of, int n_slots, int H,
-    int I, int g, BlockOffsets off, const __half* __restrict__ y_shared,
+    size_t block_bytes, const int32_t* __restrict__ slot_of, int n_slots,
+    const uint8_t* __restrict__ host, int H, int I, int g, BlockOffsets off,
+    const __half* __restrict__ y_shared,
     __half* __restrict__ y, int32_t* __restrict__ flags) {
   extern __shared__ __align__(16) uint8_t smem[];
   __half* hs = reinterpret_cast<__half*>(smem);                       // [k][I]
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
   griddep_launch_dependents();
   if (threadIdx.x < k) {
     const int p = t * k + threadIdx.x;
-    blks[threadIdx.x] = expert_block(ids[p], E, slot_of, n_slots, pool, block_bytes,
+    blks[threadIdx.x] = expert_block(ids[p], E, slot_of, n_slots, pool, block_bytes, host,
                                      blockIdx.x == 0 ? flags : nullptr);
     wj[threadIdx.x] = wts[p];
   }
@@ -251,34 +254,38 @@ int gemv_forward(const ForwardArgs& a) {
   float* hbuf = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + ws_scratch_offset(T * k));
   int32_t* flags = static_cast<int32_t*>(a.ws);
   const size_t smem_a = (size_t)H * 2 + (size_t)(H / 32) * 4;
+  const size_t smem_b = (size_t)k * I * 2 + (size_t)k * (I / 32) * 4 + (size_t)k * sizeof(void*) + (size_t)k * 4;
+  if (smem_b > 200 * 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "GEMV path: k*I = %d too large for one block's shared memory", k * I);
   const dim3 grid_a((I + kWarps - 1) / kWarps, T * k);
   cudaError_t e;
   const int nit = (H / 32 + 31) / 32;
   if (nit <= 1)
     e = launch_pdl(gateup_gemv_kernel<1>, grid_a, dim3(kWarps * 32), smem_a, a.stream,
-                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, H, I, g, a.off, hbuf, flags);
+                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, a.host, H, I, g,
+                   a.off, hbuf, flags);
   else if (nit <= 2)
     e = launch_pdl(gateup_gemv_kernel<2>, grid_a, dim3(kWarps * 32), smem_a, a.stream,
-                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, H, I, g, a.off, hbuf, flags);
+                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, a.host, H, I, g,
+                   a.off, hbuf, flags);
   else if (nit <= 4)
     e = launch_pdl(gateup_gemv_kernel<4>, grid_a, dim3(kWarps * 32), smem_a, a.stream,
-                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, H, I, g, a.off, hbuf, flags);
+                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, a.host, H, I, g,
+                   a.off, hbuf, flags);
   else
     e = launch_pdl(gateup_gemv_kernel<8>, grid_a, dim3(kWarps * 32), smem_a, a.stream,
-                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, H, I, g, a.off, hbuf, flags);
+                   a.x, a.ids, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, a.host, H, I, g,
+                   a.off, hbuf, flags);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "gateup_gemv launch: %s", cudaGetErrorString(e));
 
-  const size_t smem_b = (size_t)k * I * 2 + (size_t)k * (I / 32) * 4 + (size_t)k * sizeof(void*) + (size_t)k * 4;
-  if (smem_b > 200 * 1024)
-    return fail(MOE_ERR_UNSUPPORTED, "GEMV path: k*I = %d too large for one block's shared memory", k * I);
   if (smem_b > 48 * 1024) {
     e = cudaFuncSetAttribute(down_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "down_gemv smem attr: %s", cudaGetErrorString(e));
   }
   const dim3 grid_b((H + kWarps - 1) / kWarps, T);
   e = launch_pdl(down_gemv_kernel, grid_b, dim3(kWarps * 32), smem_b, a.stream, (const float*)hbuf,
-                 a.ids, a.weights, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, H, I, g, a.off,
-                 a.y_shared, a.y, flags);
+                 a.ids, a.weights, k, a.E, a.pool, a.block_bytes, a.slot_of, a.n_slots, a.host, H, I, g,
+                 a.off, a.y_shared, a.y, flags);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "down_gemv launch: %s", cudaGetErrorString(e));
   return MOE_OK;
 }

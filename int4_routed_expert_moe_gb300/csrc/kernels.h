@@ -49,6 +49,9 @@ struct ForwardArgs {
   void* ws;
   size_t ws_bytes;
   cudaStream_t stream;
+  // Two-kernel GEMV only: device alias of the layer's page-locked host source
+  // [E][block]; experts without a slot are read from it in place. NULL: none.
+  const uint8_t* host = nullptr;
 };
 
 size_t gemv_workspace_bytes(int H, int I, int T, int k);

@@ -91,6 +91,7 @@ _SIGS = {
     "moe_token_sort": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_forward_workspace_bytes": (_SZ, [_SHAPE, _I, _I, _I, _I]),
     "moe_expert_forward": (_I, [_SHAPE, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
+    "moe_expert_forward_zero_copy": (_I, [_SHAPE, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_forward": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
     "moe_layer_forward_noalloc": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P]),
     "moe_workspace_clear_flags": (_I, [_P, _P]),
@@ -270,6 +271,29 @@ def moe_expert_forward(shape, x: torch.Tensor, ids: torch.Tensor, weights: torch
         _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True),
         _dev(y, torch.float16, "y", T * H), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), path, _stream(stream)), "moe_expert_forward")
+
+
+def moe_expert_forward_zero_copy(shape, x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, E: int,
+                                 pool: torch.Tensor, slot_of: torch.Tensor, n_slots: int,
+                                 host_src: torch.Tensor, y_shared: torch.Tensor | None, y: torch.Tensor,
+                                 workspace: torch.Tensor, stream=None) -> None:
+    """moe_expert_forward on the two-kernel GEMV path; experts with slot -1
+    are read in place from host_src (pinned CPU uint8 [E][block])."""
+    H, I, g = shape
+    T, k = ids.shape
+    s = _shape(shape)
+    bb = moe_expert_block_bytes(shape)
+    if not isinstance(host_src, torch.Tensor) or host_src.is_cuda or host_src.dtype != torch.uint8:
+        raise TypeError("host_src must be a CPU uint8 tensor")
+    if not host_src.is_contiguous() or host_src.numel() < E * bb:
+        raise ValueError(f"host_src must be contiguous with >= {E * bb} bytes")
+    _check(_lib.moe_expert_forward_zero_copy(
+        ctypes.byref(s), _dev(x, torch.float16, "x", T * H), T,
+        _dev(ids, torch.int32, "ids", T * k), _dev(weights, torch.float32, "weights", T * k), k, E,
+        _dev(pool, torch.uint8, "pool", n_slots * bb), _dev(slot_of, torch.int32, "slot_of", E), n_slots,
+        host_src.data_ptr(), _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True),
+        _dev(y, torch.float16, "y", T * H), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)), "moe_expert_forward_zero_copy")
 
 
 def moe_layer_forward(shape, x: torch.Tensor, logits: torch.Tensor, k: int, renorm: bool,

@@ -364,3 +364,35 @@ def expert_block_bytes(H: int, I: int, g: int) -> int:
 
 def silu_scalar(v: float) -> float:
     return v / (1.0 + math.exp(-v))
+
+
+# --------------------------------------------------------------------------
+# Cost of weights outside the fast memory (lucashiago explainer, etapa 5):
+# every weight not resident is read again at each use, and the declared
+# model prices a unit of work as t = t_calc + bytes_out / bandwidth, with no
+# overlap between the reads and the computation.
+# --------------------------------------------------------------------------
+def time_model(t_calc: float, bytes_out: float, bandwidth: float) -> float:
+    """Time of one unit of work whose non-resident weights total bytes_out.
+
+    The model is additive over tokens, so a unit may be one token or a whole
+    response (its summed compute time and summed traffic)."""
+    return t_calc + bytes_out / bandwidth
+
+
+def fit_time_model(bytes_out, times) -> tuple:
+    """(t_calc, bandwidth) of time_model by least squares over measured
+    (bytes_out, time) points: numpy lstsq on the columns [1, bytes_out]."""
+    b = np.asarray(bytes_out, dtype=np.float64)
+    t = np.asarray(times, dtype=np.float64)
+    A = np.stack([np.ones_like(b), b], axis=1)
+    (t_calc, per_byte), *_ = np.linalg.lstsq(A, t, rcond=None)
+    return float(t_calc), float(1.0 / per_byte)
+
+
+def expected_outside(E: int, C: int, k: int, n: int) -> float:
+    """Mean number of distinct non-resident experts that n tokens touch when
+    C of the E experts are resident and each token picks a uniform random
+    k-subset (etapa 3's per-expert miss probability (1-k/E)^n, applied to
+    each of the E - C experts outside)."""
+    return (E - C) * (1.0 - (1.0 - k / E) ** n)

@@ -304,11 +304,56 @@ def pin_hit_ceiling(orc):
     assert abs(rate - C / E) < 4 * math.sqrt((C / E) * (1 - C / E) / steps)
 
 
+# ---- cost of non-resident weights --------------------------------------------
+def pin_time_model_campaign(orc):
+    # The printed residency campaign (claims.json, experiment residency39):
+    # per configuration, response time and host-to-device traffic over 36
+    # measured responses. Fitted on the two extreme configurations of one
+    # model and executor, the model t = t_calc + bytes_out / bandwidth must
+    # predict the configurations between them to within 3 %, and a fit on all
+    # of them must leave no residual above 2 %.
+    d = _load("residency39_campaign.json")
+    n_resp = d["contract"]["measuredResponsesPerConfiguration"]
+    fams = {}
+    for r in d["results"]:
+        if r["measuredRequestH2dGiB"] > 0:  # the fully resident rows run another executor
+            fams.setdefault((r["model"], r["executor"]), []).append(r)
+    assert len(fams) == 3
+    for rows in fams.values():
+        b = [r["measuredRequestH2dGiB"] * 2.0 ** 30 / n_resp for r in rows]
+        t = [r["responseSeconds"] for r in rows]
+        lo, hi = b.index(min(b)), b.index(max(b))
+        tc, bw = orc.fit_time_model([b[lo], b[hi]], [t[lo], t[hi]])
+        assert 3.0 < tc < min(t) and 4e9 < bw < 1e10, (tc, bw)  # seconds, bytes/s
+        for bi, ti in zip(b, t):
+            assert abs(orc.time_model(tc, bi, bw) / ti - 1.0) < 0.03, (bi, ti)
+        tc, bw = orc.fit_time_model(b, t)
+        for bi, ti in zip(b, t):
+            assert abs(orc.time_model(tc, bi, bw) / ti - 1.0) < 0.02, (bi, ti)
+    # No traffic costs nothing beyond the computation.
+    assert orc.time_model(0.25, 0.0, 1e9) == 0.25
+
+
+def pin_expected_outside_bruteforce(orc):
+    # Exact mean over every routing of n tokens, each a k-subset of E experts
+    # (all equally likely), of the distinct touched experts outside the
+    # resident set {0..C-1}.
+    import itertools
+    for E, C, k, n in ((5, 2, 2, 2), (6, 3, 1, 3), (4, 1, 3, 2)):
+        subsets = list(itertools.combinations(range(E), k))
+        total = count = 0
+        for choice in itertools.product(subsets, repeat=n):
+            touched = set().union(*choice)
+            total += sum(1 for e in touched if e >= C)
+            count += 1
+        assert abs(orc.expected_outside(E, C, k, n) - total / count) < 1e-12, (E, C, k, n)
+
+
 ALL_PINS = [
     pin_nibble_order, pin_dequant_hand, pin_expert_ffn_hand,
     pin_expert_ffn_constant_codes, pin_group_axis, pin_block_bytes,
     pin_route_golden, pin_route_dense_softmax, pin_route_invariants,
     pin_coverage, pin_layer_dense_bruteforce, pin_shared_ffn_torch,
     pin_token_sort, pin_residency_hand, pin_residency_degenerate,
-    pin_hit_ceiling,
+    pin_hit_ceiling, pin_time_model_campaign, pin_expected_outside_bruteforce,
 ]

@@ -150,10 +150,27 @@ def m_coverage_formula(o):
     o.expected_touched = lambda E, k, n: E * (1.0 - (1.0 - k / E) ** (n + 1))
 
 
+def m_time_model_no_compute(o):
+    o.time_model = lambda t_calc, bytes_out, bandwidth: bytes_out / bandwidth
+
+
+def m_fit_slope_as_bandwidth(o):
+    orig = o.fit_time_model
+    def bad(b, t):
+        tc, bw = orig(b, t)
+        return tc, 1.0 / bw
+    o.fit_time_model = bad
+
+
+def m_outside_counts_resident(o):
+    o.expected_outside = lambda E, C, k, n: C * (1.0 - (1.0 - k / E) ** n)
+
+
 MUTATIONS = [m_nibble_swap, m_drop_zero, m_group_mod, m_tie_high, m_always_renorm,
              m_never_renorm, m_ascending, m_silu_sign, m_swap_gate_up,
              m_transposed_down, m_drop_weight, m_unstable_sort, m_victim_max,
-             m_decay_after_bump, m_coverage_formula]
+             m_decay_after_bump, m_coverage_formula, m_time_model_no_compute,
+             m_fit_slope_as_bandwidth, m_outside_counts_resident]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=lambda m: m.__name__)
