@@ -44,13 +44,15 @@ constexpr int kWarps = 8;                   // compute warps of the down kernel
 constexpr int kThreads = (kWarps + 1) * 32;   // + one producer warp
 constexpr int kGateWarps = 15;              // compute warps of the gate/up kernel
 constexpr int kGateThreads = (kGateWarps + 1) * 32;
-constexpr int kSub0 = 8;                    // gate/up: warps 0..7 take even pairs, 8..14 odd pairs
+constexpr int kSub0 = 8;                    // gate/up ring: warps 0..7 take even pairs, 8..14 odd pairs
 constexpr int kPairsPerIter = 2;
-// Stage ownership: a stage must always be drained by the same warp (down) or
-// sub-group (gate/up) so that no consumer waits on a phase two fills ahead
-// (an mbarrier parity test cannot tell those apart). With an even stage
-// count, stage q % S of pair q is drained by sub-group q & 1 (gate/up) and by
-// warp (q % S) % kWarps (down), each in increasing q.
+// Stage ownership when the ring wraps: a stage must always be drained by the
+// same warp (down) or sub-group (gate/up) so that no consumer waits on a
+// phase two fills ahead (an mbarrier parity test cannot tell those apart).
+// With an even stage count, stage q % S of pair q is drained by sub-group
+// q & 1 (gate/up) and by warp (q % S) % kWarps (down), each in increasing q.
+// When every pair has its own stage (P <= S, one decode token), each stage
+// is filled once and never released, and the gate/up warps share pairs.
 constexpr int kMaxStages = 8;
 constexpr unsigned kMbarTries = 50000;     // bounded mbarrier waits (~1 s)
 
@@ -322,8 +324,7 @@ __device__ __forceinline__ void finish_weights(const DecodeParams& a, const Rout
 // return blk_of and ids are visible to the whole block; w is complete in
 // warp 0 (which forms it when the block routes itself) and becomes visible
 // to the other warps at their next barrier with warp 0.
-// empty_count: arrivals that free a stage; for the gate/up kernel, the warps
-// of the sub-group that drains it (odd stages: odd_count).
+// empty_count: arrivals that free a stage (odd stages: odd_count).
 __device__ __forceinline__ void init_bars(const DecodeParams& a, uint64_t* full, uint64_t* empty,
                                           int empty_count, int odd_count) {
   if (threadIdx.x == 0) {
@@ -453,10 +454,53 @@ __device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffse
   }
 }
 
+// Two rows (same row index of two pairs of one token) at once.
+template <int NC>
+__device__ __forceinline__ void gate_up_row2(const uint8_t* ra, const uint8_t* rb, const BlockOffsets& off,
+                                             int nch, int lane, const int* gq, const int* xo, const uint4* xs4,
+                                             const float* xsum, const float* xback, float& aga, float& aua,
+                                             float& agb, float& aub) {
+  const uint2* sza = reinterpret_cast<const uint2*>(ra + off.gu_sz);
+  const uint2* szb = reinterpret_cast<const uint2*>(rb + off.gu_sz);
+#pragma unroll
+  for (int it = 0; it < NC; ++it) {
+    const int cc = lane + 32 * it;
+    if (cc < nch) {
+      const uint4 wga = *reinterpret_cast<const uint4*>(ra + off.gu_q_gate + 16 * cc);
+      const uint4 wua = *reinterpret_cast<const uint4*>(ra + off.gu_q_up + 16 * cc);
+      const uint4 wgb = *reinterpret_cast<const uint4*>(rb + off.gu_q_gate + 16 * cc);
+      const uint4 wub = *reinterpret_cast<const uint4*>(rb + off.gu_q_up + 16 * cc);
+      const uint2 qa = sza[gq[it]];
+      const uint2 qb = szb[gq[it]];
+      uint4 xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs4[xo[4 * it + i]];
+      const half2* xa = reinterpret_cast<const half2*>(&xv[0]);
+      const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
+      const float back = xback[cc];
+      const float xsm = xsum[cc];
+      const float dga = (dot16_scaled(wga.x, wga.y, xa) + dot16_scaled(wga.z, wga.w, xb)) * back;
+      const float dua = (dot16_scaled(wua.x, wua.y, xa) + dot16_scaled(wua.z, wua.w, xb)) * back;
+      const float dgb = (dot16_scaled(wgb.x, wgb.y, xa) + dot16_scaled(wgb.z, wgb.w, xb)) * back;
+      const float dub = (dot16_scaled(wub.x, wub.y, xa) + dot16_scaled(wub.z, wub.w, xb)) * back;
+      const float2 sga = __half22float2(u32_as_h2(qa.x)), sua = __half22float2(u32_as_h2(qa.y));
+      const float2 sgb = __half22float2(u32_as_h2(qb.x)), sub = __half22float2(u32_as_h2(qb.y));
+      aga += sga.x * (dga - sga.y * xsm);
+      aua += sua.x * (dua - sua.y * xsm);
+      agb += sgb.x * (dgb - sgb.y * xsm);
+      aub += sub.x * (dub - sub.y * xsm);
+    }
+  }
+}
+
 // ---- kernel 1: gate/up dequant-GEMV + SwiGLU -------------------------------
 // Stage: the block's gate/up rows [R][gu_row] (codes, scales and zeros of
-// both projections per row). Each iteration covers kPairsPerIter pairs of one
-// token: warp w takes row w % 8 (+8, ...) of pair p + w / 8.
+// both projections per row). With a stage per pair (P <= S), the work units
+// of a token are (couple, row): row r of pairs 2c and 2c + 1, computed
+// together by one warp (shared activation loads, two independent chains);
+// warp w takes units w, w + 15, ... Otherwise each iteration covers
+// kPairsPerIter pairs of one token: warp w takes row w % 8 (+8, ...) of pair
+// p + w / 8, and the sub-group releases the stage.
 template <int NC>
 __global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const DecodeParams a) {
   extern __shared__ __align__(128) uint8_t sm[];
@@ -489,6 +533,55 @@ __global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const De
 #pragma unroll
     for (int i = 0; i < 4; ++i) xo[4 * it + i] = xslot(cc, i);
   }
+  if (a.P <= a.stages) {
+    int cur_t = -1;
+    for (int p0 = 0; p0 < a.P; p0 += a.k) {
+      const int t = p0 / a.k;
+      if (t != cur_t) {
+        asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");  // previous x no longer read
+        stage_x(a.x + (size_t)t * a.H, a.H, xs4, xsum, xback, threadIdx.x, kGateWarps * 32);
+        asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");
+        cur_t = t;
+      }
+      const int couples = (a.k + 1) / 2;
+      for (int u = warp; u < couples * rows; u += kGateWarps) {
+        const int cpl = u / rows, r = u - cpl * rows;
+        const int qa = p0 + 2 * cpl, qb = qa + 1;
+        const bool two = 2 * cpl + 1 < a.k;
+        const int sa = qa % a.stages, sb = qb % a.stages;
+        if (!mbar_wait(&full[sa], (qa / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
+        if (two && !mbar_wait(&full[sb], (qb / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
+        const uint8_t* ba = blk_of[qa];
+        const uint8_t* bb = two ? blk_of[qb] : nullptr;
+        const uint8_t* ra = sm + (size_t)sa * a.st.bytes + (size_t)r * a.off.gu_row;
+        const uint8_t* rb = sm + (size_t)sb * a.st.bytes + (size_t)r * a.off.gu_row;
+        float aga = 0.0f, aua = 0.0f, agb = 0.0f, aub = 0.0f;
+        if (ba && bb) {
+          gate_up_row2<NC>(ra, rb, a.off, nch, lane, gq, xo, xs4, xsum, xback, aga, aua, agb, aub);
+        } else {
+          if (ba) gate_up_row<NC>(ra, a.off, nch, lane, gq, xo, xs4, xsum, xback, aga, aua);
+          if (bb) gate_up_row<NC>(rb, a.off, nch, lane, gq, xo, xs4, xsum, xback, agb, aub);
+        }
+        // Warp sums of the four values by a reduce-scatter butterfly (7
+        // shuffles instead of 20): after the exchanges at distance 16 and 8,
+        // lanes with bit 4 clear hold pair a's sums and set pair b's; bit 3
+        // clear the gate sum, set the up sum; the last three levels finish
+        // each sum within its group of eight lanes.
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
+        const float k0 = b4 ? agb : aga, k1 = b4 ? aub : aua;
+        const float w0 = k0 + __shfl_xor_sync(0xffffffffu, b4 ? aga : agb, 16);
+        const float w1 = k1 + __shfl_xor_sync(0xffffffffu, b4 ? aua : aub, 16);
+        float v = (b3 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b3 ? w0 : w1, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        const float up = __shfl_xor_sync(0xffffffffu, v, 8);  // lanes 0 and 16: the up sum
+        if (lane == 0) a.hbuf[(size_t)qa * a.I + n0 + r] = __float2half_rn(ba ? silu_f(v) * up : 0.0f);
+        if (lane == 16 && two) a.hbuf[(size_t)qb * a.I + n0 + r] = __float2half_rn(bb ? silu_f(v) * up : 0.0f);
+      }
+    }
+    return;
+  }
   const int sub = warp < kSub0 ? 0 : 1;                  // pair offset in the iteration
   const int wr = warp - sub * kSub0;                     // row lane within the sub-group
   const int nsub = sub ? kGateWarps - kSub0 : kSub0;     // warps of the sub-group
@@ -519,7 +612,6 @@ __global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const De
         }
         if (lane == 0) a.hbuf[(size_t)q * a.I + n0 + r] = __float2half_rn(blk ? silu_f(ag) * au : 0.0f);
       }
-      // The sub-group has finished reading the stage: one arrival frees it.
       // This warp has finished reading the stage (no sub-group barrier: the
       // stage is free once every warp of the sub-group has arrived).
       __syncwarp();
@@ -594,16 +686,27 @@ __global__ void __launch_bounds__(kThreads, 3) decode_down_kernel(const DecodePa
             }
           }
         }
+        // Warp sums of the 8 rows by a reduce-scatter butterfly (9 shuffles
+        // instead of 40): each exchange keeps half of the remaining rows, so
+        // after distances 16, 8 and 4 a lane holds one row (bits 4, 3, 2 of
+        // the lane pick it) and distances 2 and 1 finish its sum.
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+        float w4[4], w2[2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u], o);
+        for (int i = 0; i < 4; ++i) {
+          const float keep = b4 ? v[4 + i] : v[i], send = b4 ? v[i] : v[4 + i];
+          w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
         }
-        if (lane == 0) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (r0 + u < rows) part[q * rows + r0 + u] = v[u];
+        for (int i = 0; i < 2; ++i) {
+          const float keep = b3 ? w4[2 + i] : w4[i], send = b3 ? w4[i] : w4[2 + i];
+          w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
         }
+        float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+        w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+        w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+        const int u = 4 * b4 + 2 * b3 + b2;  // the row whose total this lane holds
+        if ((lane & 3) == 0 && r0 + u < rows) part[q * rows + r0 + u] = w1;
       }
     } else if (lane == 0) {
       for (int r = 0; r < rows; ++r) part[q * rows + r] = 0.0f;

@@ -256,3 +256,29 @@ def test_layer_forward_ties_and_bad_tokens():
     ids, y = _layer_forward_case((256, 128, 64), E, 3, False, 5, 44, logits=lg)
     assert ids[3].tolist() == [-1, -1, -1] and ids[4].tolist() == [-1, -1, -1]
     assert np.all(y[3] == 0) and np.all(y[4] == 0)
+
+
+_ONE_TOKEN_ROWS = [[1, 3, 3, 2, 3, 0, 0, 0], [0, 0, 0, 0, 0, 0, 0, 0],
+                   [-np.inf, 1, -np.inf, 0, -np.inf, -np.inf, -np.inf, -np.inf],
+                   [0, np.nan, 1, 2, 0, 0, 0, 0], [-np.inf] * 8, [np.inf, 0, 0, 0, 0, 0, 0, 0],
+                   [-0.0, 0.0, -0.0, 0.0, 1, 1, -1, -1]]
+
+
+@pytest.mark.parametrize("row", range(len(_ONE_TOKEN_ROWS)))
+def test_layer_forward_one_token_ties_and_bad(row):
+    # One token routed inside the kernels: ties by lower index, -inf last,
+    # a NaN/+inf or all -inf token chooses nobody and contributes 0.
+    lg = np.array([_ONE_TOKEN_ROWS[row]], dtype=np.float32)
+    ids, y = _layer_forward_case((256, 128, 64), 8, 3, False, 1, 45, logits=lg)
+    if row in (3, 4, 5):
+        assert ids[0].tolist() == [-1, -1, -1] and np.all(y == 0)
+
+
+@pytest.mark.parametrize("shape,E,k,renorm", [
+    ((512, 192, 64), 40, 8, True),      # E not a multiple of 32
+    ((2048, 1408, 128), 60, 4, False),  # Qwen-like expert count
+    ((1088, 320, 32), 5, 2, False),     # E below one warp
+    ((512, 256, 64), 64, 8, False),     # k = the ring's stage count
+])
+def test_layer_forward_one_token_shapes(shape, E, k, renorm):
+    _layer_forward_case(shape, E, k, renorm, 1, 46)
