@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--mode", default="copy", choices=["copy", "zerocopy"],
                     help="olmoe_partial: copy misses into slots, or read them in place over the CPU-GPU link")
     ap.add_argument("--slots", type=int, default=None, help="olmoe_partial: experts resident per layer")
+    ap.add_argument("--prefetch", type=int, default=0,
+                    help="olmoe_partial --mode copy: spare slots per layer filled with predicted misses")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -414,20 +416,24 @@ class PartialStack:
         return 1.0 / self.ranks.astype(np.float64) ** self.wl["alpha"]
 
 
-def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0):
+def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0, prefetch=0):
     """Residency by copies: per layer and step the router runs on the GPU, its
     ids reach the host, the residency manager decides and streams misses from
     pinned host RAM on a side stream into the layer's C slots, then the experts
-    run from the managed pool. Returns the device time of K steps after W."""
+    run from the managed pool. With prefetch = S > 0 the layer has S spare
+    slots and, once a layer's experts are enqueued, the next layer's S
+    non-resident experts with the highest decayed counts are copied into them
+    on the side stream, overlapping this layer. Returns the device time of K
+    steps after W."""
     L, E, k, bb = ps.L, ps.E, ps.k, ps.bb
     dev = torch.device("cuda")
-    pool = torch.zeros((L, C, bb), dtype=torch.uint8, device=dev)
+    pool = torch.zeros((L, C + prefetch, bb), dtype=torch.uint8, device=dev)
     slot_of = torch.full((L, E), -1, dtype=torch.int32, device=dev)
     copy = torch.cuda.Stream()
     # Pinned policy: the profile is the popularity the stream is drawn from
     # (a perfect measurement pass); C - k experts pinned, k slots follow LRU.
     pinned = C - k if policy == "pinned" else 0
-    h = moe.moe_residency_create(dict(layers=L, experts=E, slots=C, spares=0, max_ids_per_step=k,
+    h = moe.moe_residency_create(dict(layers=L, experts=E, slots=C, spares=prefetch, max_ids_per_step=k,
                                       block_bytes=bb, decay=ps.wl["decay"], policy=policy, pinned=pinned,
                                       profile=ps.profile() if policy == "pinned" else None),
                                  ps.src, pool, slot_of, torch.cuda.current_stream(), copy)
@@ -445,8 +451,14 @@ def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0):
             torch.cuda.current_stream().synchronize()  # the step's ids reach the host
             moe.moe_residency_prepare(h, l, ids_host.numpy())
             x = ps.x0[s] if l == 0 else y[l - 1]
-            moe.moe_expert_forward(ps.shape, x, ids[l], w[l], E, pool[l], slot_of[l], C, None, y[l], ws,
-                                   moe.MOE_PATH_GEMV)
+            moe.moe_expert_forward(ps.shape, x, ids[l], w[l], E, pool[l], slot_of[l], C + prefetch, None, y[l],
+                                   ws, moe.MOE_PATH_GEMV)
+            if prefetch:
+                nl = (l + 1) % L
+                counts = moe.moe_residency_counts(h, nl, E)
+                table = moe.moe_residency_slot_table(h, nl, E)
+                out = [e for e in np.lexsort((np.arange(E), -counts)) if table[e] < 0][:prefetch]
+                moe.moe_residency_prefetch(h, nl, out)
 
     try:
         for s in range(steps_from, steps_from + W):
@@ -470,7 +482,9 @@ def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0):
         moe.moe_residency_destroy(h)
     hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
     return {"ms": ms, "wall_s": wall, "hits": hits, "misses": misses, "pinned": pinned,
-            "bytes_out": st1["h2d_bytes"] - st0["h2d_bytes"], "launches_per_step": L * 7}
+            "bytes_out": st1["h2d_bytes"] - st0["h2d_bytes"], "launches_per_step": L * 7,
+            "prefetched": st1["prefetched"] - st0["prefetched"],
+            "prefetch_copies": st1["prefetch_copies"] - st0["prefetch_copies"]}
 
 
 def partial_zero_copy(moe, ps, C, K, W, world, graph=True, steps_from=0):
@@ -592,7 +606,7 @@ def run_partial(args, world, rank):
 
     def run(c, steps, warm, graph=True):
         r = (partial_zero_copy(moe, ps, c, steps, warm, world, graph=graph) if args.mode == "zerocopy"
-             else partial_copy(moe, ps, c, args.policy, steps, warm, world))
+             else partial_copy(moe, ps, c, args.policy, steps, warm, world, prefetch=args.prefetch))
         torch.cuda.empty_cache()
         return r
 
@@ -614,6 +628,7 @@ def run_partial(args, world, rank):
            "tokens_per_step": 1}
     if args.mode == "copy":
         cfg.update({"policy": args.policy, "pinned": main_run["pinned"], "decay": wl["decay"],
+                    "prefetch_spares": args.prefetch,
                     "launch": "eager; per layer: route, D2H of ids, host decision, H2D misses, experts"})
     else:
         cfg.update({"resident_set": "the C most popular experts of each layer (profile), fixed",
@@ -625,6 +640,9 @@ def run_partial(args, world, rank):
                         "bytes_out_gb": round(main_run["bytes_out"] / 1e9, 3),
                         "bytes_out_gbs": round(main_run["bytes_out"] / (ms / 1e3) / 1e9, 2),
                         "wall_s": round(main_run["wall_s"], 3)}
+    if args.mode == "copy" and args.prefetch:
+        out["residency"]["prefetched_per_token"] = round(main_run["prefetched"] / K, 3)
+        out["residency"]["prefetch_copies_per_token"] = round(main_run["prefetch_copies"] / K, 3)
     if eager is not None:
         out["residency"]["eager_value"] = round(Ktm * world / (eager["ms"] / 1e3), 2)
     out["time_model"] = {

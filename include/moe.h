@@ -337,6 +337,8 @@ typedef struct {
 
 typedef struct {
   uint64_t steps, hits, misses, evictions, copies, h2d_bytes;
+  uint64_t prefetched;       /* misses served by a prefetched copy (no copy in their step) */
+  uint64_t prefetch_copies;  /* copies made by moe_residency_prefetch */
 } moe_residency_stats;
 
 typedef struct {
@@ -363,6 +365,20 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
 /* host_ids: host int32 [n], the ids all tokens of this step need in `layer`
  * (entries outside [0, E) are rejected with MOE_ERR_ARG, state unchanged). */
 int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, int n);
+/* Prefetch of predicted misses into spare slots ("03 / Arquitetura", ADR
+ * 0009: a copy lands in a spare position while readers keep the current
+ * generation). For each id in order, skipping ids that are resident or
+ * already prefetched, while a free spare slot is left: the block is copied
+ * host->device on the copy stream into the lowest free slot. Nothing is
+ * published and no count changes. The copy waits only for the readers of
+ * the layer's slots retired so far (an event recorded by the layer's last
+ * prepare() that evicted), not for work enqueued since, so it overlaps the
+ * layers being computed. The layer's next prepare() takes a prefetched
+ * expert that its step needs as a miss in that slot, with no copy (counted
+ * in `prefetched`); prefetched experts that step does not need return to
+ * the free spares. Returns the number copied in *staged_out (nullable).
+ * Ids outside [0, E): MOE_ERR_ARG, nothing staged. */
+int moe_residency_prefetch(moe_residency* r, int layer, const int32_t* host_ids, int n, int* staged_out);
 /* layer = -1 sums over layers. */
 int moe_residency_get_stats(const moe_residency* r, int layer, moe_residency_stats* out);
 /* Copies up to `cap` events (all layers, in decision order); *n_out = total. */

@@ -14,6 +14,9 @@
 // Horizon RunMap claims.json, experiment contract: canonical initial
 // placement, evolving LRU. lucashiago.com.br "local" explainer, etapa 4: a
 // profile measured beforehand pins the popular set; LRU adapts by itself.
+// Prefetch (ADR 0009's spare positions): predicted misses are copied into
+// free spare slots ahead of the step that needs them, without publishing;
+// the step then takes them without a copy on its own path.
 //
 // Built with -ffp-contract=off: the count update c = c*decay; c = c + 1 is two
 // IEEE double operations, with no fused multiply-add.
@@ -37,6 +40,9 @@ struct moe_residency {
     std::vector<char> pinned;        // never evicted (MOE_POLICY_PINNED)
     std::vector<int32_t> slot_of;  // expert -> physical slot, -1 absent
     std::vector<int32_t> free;     // free physical slots
+    std::vector<int32_t> staged;   // expert -> spare slot holding a prefetched copy, -1 none
+    cudaEvent_t retired = nullptr;  // compute-stream point after every reader of a retired slot
+    bool retired_recorded = false;
     moe_residency_stats st;
     int64_t steps = 0;
   };
@@ -50,6 +56,7 @@ namespace {
 
 struct Miss {
   int32_t expert, slot, victim;
+  bool staged;  // its block was copied by a prefetch: no copy in this step
 };
 
 int publish(moe_residency* r, int layer, const std::vector<std::pair<int32_t, int32_t>>& upd) {
@@ -123,6 +130,7 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
     L.last_used.assign(c.experts, -1);
     L.pinned.assign(c.experts, 0);
     L.slot_of.assign(c.experts, -1);
+    L.staged.assign(c.experts, -1);
     if (c.policy == MOE_POLICY_PINNED) {
       // Top `pinned` experts by profile (ties: lower id), then the lowest
       // other ids; slots in ascending expert order.
@@ -149,6 +157,8 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
   if (!c.dry_run) {
     cudaError_t e = cudaEventCreateWithFlags(&r->readers_done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->copies_done, cudaEventDisableTiming);
+    for (int l = 0; e == cudaSuccess && l < c.layers; ++l)
+      e = cudaEventCreateWithFlags(&r->layers[l].retired, cudaEventDisableTiming);
     // Initial placement: each resident expert's block into its slot
     // (canonical: expert e in slot e, e < C, one copy per layer).
     for (int l = 0; e == cudaSuccess && l < c.layers; ++l) {
@@ -228,7 +238,10 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
       --n_resident;
     }
     int32_t slot;
-    if (!free_slots.empty()) {
+    const bool staged = L.staged[e] >= 0;
+    if (staged) {
+      slot = L.staged[e];  // prefetched: already in its spare slot
+    } else if (!free_slots.empty()) {
       auto it = std::min_element(free_slots.begin(), free_slots.end());
       slot = *it;
       free_slots.erase(it);
@@ -238,9 +251,14 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
     }
     slot_of[e] = slot;
     ++n_resident;
-    misses.push_back({e, slot, victim});
+    misses.push_back({e, slot, victim, staged});
   }
   for (int32_t s : retiring) free_slots.push_back(s);
+  // Prefetched copies this step did not need return to the free spares.
+  for (int e = 0; e < c.experts; ++e)
+    if (L.staged[e] >= 0 && !needed[e]) free_slots.push_back(L.staged[e]);
+  bool any_victim = false;
+  for (const Miss& m : misses) any_victim |= m.victim >= 0;
 
   // Enqueue copies: the copy stream first waits for every reader enqueued so
   // far on the compute stream (this retires the victims' readers).
@@ -249,9 +267,13 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
   if (!c.dry_run && !misses.empty()) {
     cudaError_t e = cudaEventRecord(r->readers_done, r->compute);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(r->copy, r->readers_done, 0);
+    // Every reader of this step's victims is enqueued before this point: a
+    // later prefetch into their slots waits for this event only.
+    if (e == cudaSuccess && any_victim) e = cudaEventRecord(L.retired, r->compute);
     if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "residency ordering: %s", cudaGetErrorString(e));
   }
   for (size_t i = 0; i < misses.size(); ++i) {
+    if (misses[i].staged) continue;
     if (r->inject_countdown == 0) {
       r->inject_countdown = -1;
       failed_at = (int)i;
@@ -303,8 +325,10 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
     if (prc != MOE_OK) return prc;
   }
   // Commit.
+  if (!c.dry_run && !misses.empty() && any_victim) L.retired_recorded = true;
   for (const Miss& m : misses)
     r->trace.push_back({L.steps, layer, m.expert, m.slot, m.victim});
+  for (int e = 0; e < c.experts; ++e) L.staged[e] = -1;
   L.counts.swap(counts);
   for (int32_t e : distinct) L.last_used[e] = L.steps;
   L.slot_of.swap(slot_of);
@@ -312,12 +336,61 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
   L.st.steps += 1;
   L.st.hits += hits;
   L.st.misses += misses.size();
-  for (const Miss& m : misses) L.st.evictions += m.victim >= 0;
-  if (!c.dry_run) {
-    L.st.copies += misses.size();
-    L.st.h2d_bytes += misses.size() * c.block_bytes;
+  for (const Miss& m : misses) {
+    L.st.evictions += m.victim >= 0;
+    L.st.prefetched += m.staged;
+    if (!c.dry_run && !m.staged) {
+      L.st.copies += 1;
+      L.st.h2d_bytes += c.block_bytes;
+    }
   }
   L.steps += 1;
+  return MOE_OK;
+}
+
+int moe_residency_prefetch(moe_residency* r, int layer, const int32_t* host_ids, int n, int* staged_out) {
+  moe::clear_error();
+  if (!r) return moe::fail(MOE_ERR_ARG, "moe_residency_prefetch: NULL handle");
+  const moe_residency_cfg& c = r->cfg;
+  if (layer < 0 || layer >= c.layers) return moe::fail(MOE_ERR_ARG, "layer %d out of range", layer);
+  if (n < 0 || (n > 0 && !host_ids)) return moe::fail(MOE_ERR_ARG, "moe_residency_prefetch: bad id list");
+  for (int i = 0; i < n; ++i)
+    if (host_ids[i] < 0 || host_ids[i] >= c.experts)
+      return moe::fail(MOE_ERR_ARG, "id %d out of range [0, %d)", host_ids[i], c.experts);
+  auto& L = r->layers[layer];
+  int staged = 0;
+  bool ordered = false;
+  for (int i = 0; i < n && !L.free.empty(); ++i) {
+    const int32_t e = host_ids[i];
+    if (L.slot_of[e] >= 0 || L.staged[e] >= 0) continue;
+    auto it = std::min_element(L.free.begin(), L.free.end());
+    const int32_t slot = *it;
+    if (r->inject_countdown == 0) {
+      r->inject_countdown = -1;
+      if (staged_out) *staged_out = staged;
+      return moe::fail(MOE_ERR_INJECTED, "injected failure at a prefetch copy of layer %d", layer);
+    }
+    if (r->inject_countdown > 0) --r->inject_countdown;
+    if (!c.dry_run) {
+      cudaError_t err = cudaSuccess;
+      if (!ordered && L.retired_recorded) err = cudaStreamWaitEvent(r->copy, L.retired, 0);
+      ordered = true;
+      const uint8_t* src = r->src + ((size_t)layer * c.experts + e) * c.block_bytes;
+      uint8_t* dst = r->pool + ((size_t)layer * r->physical + slot) * c.block_bytes;
+      if (err == cudaSuccess) err = cudaMemcpyAsync(dst, src, c.block_bytes, cudaMemcpyHostToDevice, r->copy);
+      if (err != cudaSuccess) {
+        if (staged_out) *staged_out = staged;
+        return moe::fail(MOE_ERR_CUDA, "prefetch copy of expert %d: %s", e, cudaGetErrorString(err));
+      }
+      L.st.copies += 1;
+      L.st.h2d_bytes += c.block_bytes;
+    }
+    L.free.erase(it);
+    L.staged[e] = slot;
+    L.st.prefetch_copies += 1;
+    ++staged;
+  }
+  if (staged_out) *staged_out = staged;
   return MOE_OK;
 }
 
@@ -335,6 +408,8 @@ int moe_residency_get_stats(const moe_residency* r, int layer, moe_residency_sta
     out->evictions += s.evictions;
     out->copies += s.copies;
     out->h2d_bytes += s.h2d_bytes;
+    out->prefetched += s.prefetched;
+    out->prefetch_copies += s.prefetch_copies;
   }
   return MOE_OK;
 }
@@ -375,6 +450,8 @@ void moe_residency_destroy(moe_residency* r) {
     if (r->copy) cudaStreamSynchronize(r->copy);
     if (r->readers_done) cudaEventDestroy(r->readers_done);
     if (r->copies_done) cudaEventDestroy(r->copies_done);
+    for (auto& L : r->layers)
+      if (L.retired) cudaEventDestroy(L.retired);
   }
   delete r;
 }

@@ -61,7 +61,8 @@ class moe_residency_cfg(ctypes.Structure):
 
 class moe_residency_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
-                ("steps", "hits", "misses", "evictions", "copies", "h2d_bytes")]
+                ("steps", "hits", "misses", "evictions", "copies", "h2d_bytes", "prefetched",
+                 "prefetch_copies")]
 
 
 class moe_residency_event(ctypes.Structure):
@@ -101,6 +102,7 @@ _SIGS = {
     "moe_residency_create": (_I, [ctypes.POINTER(moe_residency_cfg), _P, _P, _P, _P, _P,
                                   ctypes.POINTER(_P)]),
     "moe_residency_prepare": (_I, [_P, _I, _P, _I]),
+    "moe_residency_prefetch": (_I, [_P, _I, _P, _I, ctypes.POINTER(ctypes.c_int)]),
     "moe_residency_get_stats": (_I, [_P, _I, ctypes.POINTER(moe_residency_stats)]),
     "moe_residency_trace": (_I, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
     "moe_residency_slot_table": (_I, [_P, _I, _P]),
@@ -394,6 +396,15 @@ def moe_residency_prepare(handle: int, layer: int, host_ids) -> None:
     a = np.ascontiguousarray(np.asarray(host_ids, dtype=np.int32).reshape(-1))
     _check(_lib.moe_residency_prepare(handle, layer, a.ctypes.data if a.size else None, a.size),
            "moe_residency_prepare")
+
+
+def moe_residency_prefetch(handle: int, layer: int, host_ids) -> int:
+    """Copy predicted misses into free spare slots; returns how many were copied."""
+    a = np.ascontiguousarray(np.asarray(host_ids, dtype=np.int32).reshape(-1))
+    n = ctypes.c_int(0)
+    _check(_lib.moe_residency_prefetch(handle, layer, a.ctypes.data if a.size else None, a.size,
+                                       ctypes.byref(n)), "moe_residency_prefetch")
+    return int(n.value)
 
 
 def moe_residency_get_stats(handle: int, layer: int = -1) -> dict:

@@ -252,6 +252,13 @@ class ResidencyLayer:
                profile value (ties: lower id) are never victims and are
                resident from the start together with the lowest other ids
                (slots in ascending id order); the others follow "lru".
+    Prefetch ("03 / Arquitetura", ADR 0009: a copy lands in a spare
+    position before it is published): prefetch(ids) stages each listed
+    expert that is neither resident nor staged into the lowest free slot,
+    while one is free; the next step takes a staged expert it needs as a
+    miss in its staged slot (victim chosen as usual, the victim's slot then
+    goes free), and returns the staged experts it does not need to the free
+    slots.
     """
 
     def __init__(self, E: int, C: int, S: int, decay: float, policy: str = "decay",
@@ -281,7 +288,27 @@ class ResidencyLayer:
             for e in range(C):
                 self.slot_of[e] = e
         self.free = list(range(C, C + S))
+        self.staged = {}  # expert -> slot holding its prefetched copy
         self.hits = self.misses = self.evictions = 0
+        self.prefetched = self.prefetch_copies = 0
+
+    def prefetch(self, ids) -> list:
+        """Stage predicted misses; returns [(expert, slot)] in staging order."""
+        ids = [int(e) for e in ids]
+        if any(e < 0 or e >= self.E for e in ids):
+            raise ValueError("expert id out of range")
+        out = []
+        for e in ids:
+            if not self.free:
+                break
+            if self.slot_of[e] >= 0 or e in self.staged:
+                continue
+            slot = min(self.free)
+            self.free.remove(slot)
+            self.staged[e] = slot
+            out.append((e, slot))
+        self.prefetch_copies += len(out)
+        return out
 
     def resident(self):
         return [e for e in range(self.E) if self.slot_of[e] >= 0]
@@ -316,7 +343,10 @@ class ResidencyLayer:
                 retiring.append(self.slot_of[victim])
                 self.slot_of[victim] = -1
                 self.evictions += 1
-            if self.free:
+            if e in self.staged:
+                slot = self.staged[e]
+                self.prefetched += 1
+            elif self.free:
                 slot = min(self.free)
                 self.free.remove(slot)
             else:
@@ -325,6 +355,8 @@ class ResidencyLayer:
             resident.add(e)
             decisions.append((e, slot, victim))
         self.free.extend(retiring)
+        self.free.extend(slot for e, slot in self.staged.items() if e not in distinct)
+        self.staged = {}
         for e in distinct:
             self.last_used[e] = self.steps
         self.steps += 1

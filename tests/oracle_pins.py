@@ -349,6 +349,29 @@ def pin_expected_outside_bruteforce(orc):
         assert abs(orc.expected_outside(E, C, k, n) - total / count) < 1e-12, (E, C, k, n)
 
 
+def pin_residency_prefetch_hand(orc):
+    # Hand-derived trace (tests/golden/residency_prefetch_trace.json): a
+    # staged miss keeps its spare slot, unused staged copies go back to the
+    # free slots, prefetch stops when no slot is free.
+    c = _load("residency_prefetch_trace.json")
+    lay = orc.ResidencyLayer(c["E"], c["C"], c["S"], c["decay"], c["policy"])
+    trace, staged = [], []
+    step = 0
+    for op in c["ops"]:
+        if op["op"] == "prefetch":
+            staged.append(len(lay.prefetch(op["ids"])))
+        else:
+            for (e, slot, victim) in lay.step(op["ids"]):
+                trace.append([step, e, slot, victim])
+            step += 1
+    assert staged == [op["staged"] for op in c["ops"] if op["op"] == "prefetch"], staged
+    assert trace == c["trace"], trace
+    assert list(lay.slot_of) == c["slot_of_after"]
+    assert [float(v) for v in lay.counts] == c["counts_after"]
+    assert (lay.hits, lay.misses, lay.evictions, lay.prefetched, lay.prefetch_copies) == (
+        c["hits"], c["misses"], c["evictions"], c["prefetched"], c["prefetch_copies"])
+
+
 ALL_PINS = [
     pin_nibble_order, pin_dequant_hand, pin_expert_ffn_hand,
     pin_expert_ffn_constant_codes, pin_group_axis, pin_block_bytes,
@@ -356,4 +379,5 @@ ALL_PINS = [
     pin_coverage, pin_layer_dense_bruteforce, pin_shared_ffn_torch,
     pin_token_sort, pin_residency_hand, pin_residency_degenerate,
     pin_hit_ceiling, pin_time_model_campaign, pin_expected_outside_bruteforce,
+    pin_residency_prefetch_hand,
 ]

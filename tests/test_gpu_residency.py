@@ -116,3 +116,66 @@ def test_residency_rejects_pageable_source():
     with pytest.raises(ValueError):
         moe.moe_residency_create(cfg, torch.empty((1, E, bb), dtype=torch.uint8), torch.empty((1, 6, bb), dtype=torch.uint8, device=dev),
                                  torch.empty((1, E), dtype=torch.int32, device=dev))
+
+
+def test_residency_prefetch_copies_and_forward():
+    # After each layer's experts are enqueued, the next layer's predicted
+    # misses (the S non-resident experts with the highest decayed counts) are
+    # prefetched into spare slots on the copy stream; the next prepare() takes
+    # the needed ones without a copy. Outputs, slot contents, decisions and
+    # copy counts are checked against the oracle.
+    moe = binding()
+    H, I, g = SHAPE
+    C, S, T = 8, 3, 2
+    h, src, pool, slot_of, arrays, bb = _setup(moe, C, S, 73)
+    dev = torch.device("cuda")
+    ws = [torch.zeros(moe.moe_forward_workspace_bytes(SHAPE, T, K, E, moe.MOE_PATH_GEMV), dtype=torch.uint8,
+                      device=dev) for _ in range(L)]
+    orc = {l: moe_oracle.ResidencyLayer(E, C, S, 0.9) for l in range(L)}
+    pending = []
+
+    def predict_and_prefetch(l):
+        counts = moe.moe_residency_counts(h, l, E)
+        table = moe.moe_residency_slot_table(h, l, E)
+        cand = sorted((e for e in range(E) if table[e] < 0), key=lambda e: (-counts[e], e))[:S]
+        assert moe.moe_residency_prefetch(h, l, cand) == len(orc[l].prefetch(cand))
+
+    try:
+        for step in range(16):
+            for l in range(L):
+                lg = synth.logits_zipf(73, l, step, T, E, 1.2)
+                ids_d = torch.empty((T, K), dtype=torch.int32, device=dev)
+                w_d = torch.empty((T, K), dtype=torch.float32, device=dev)
+                moe.moe_route(torch.from_numpy(lg).to(dev), K, True, ids_d, w_d)
+                ids_h = ids_d.cpu().numpy()
+                moe.moe_residency_prepare(h, l, ids_h)
+                orc[l].step(ids_h.reshape(-1).tolist())
+                x16 = synth.activations(73, step * L + l, T, H)
+                y = torch.empty((T, H), dtype=torch.float16, device=dev)
+                moe.moe_expert_forward(SHAPE, torch.from_numpy(x16).to(dev), ids_d, w_d, E, pool[l],
+                                       slot_of[l], C + S, None, y, ws[l], moe.MOE_PATH_GEMV)
+                pending.append((y, moe_oracle.moe_layer(x16, lg, lambda e, l=l: arrays[(l, e)], K, True, g)["y"]))
+                predict_and_prefetch((l + 1) % L)  # overlaps this layer's experts
+        torch.cuda.synchronize()
+        for y, ref in pending:
+            ok, err, bound = tol_ok(y.float().cpu().numpy(), ref)
+            assert ok, (err, bound)
+        assert all(moe.moe_workspace_flags(w) == 0 for w in ws)
+        total_prefetched = 0
+        for l in range(L):
+            table = moe.moe_residency_slot_table(h, l, E)
+            assert np.array_equal(slot_of[l].cpu().numpy(), table)
+            assert table.tolist() == orc[l].slot_of
+            for e in range(E):
+                if table[e] >= 0:
+                    assert torch.equal(pool[l, table[e]].cpu(), src[l, e])
+            st = moe.moe_residency_get_stats(h, l)
+            o = orc[l]
+            assert (st["hits"], st["misses"], st["prefetched"], st["prefetch_copies"]) == (
+                o.hits, o.misses, o.prefetched, o.prefetch_copies)
+            assert st["copies"] == st["misses"] - st["prefetched"] + st["prefetch_copies"]
+            assert st["h2d_bytes"] == st["copies"] * bb
+            total_prefetched += st["prefetched"]
+        assert total_prefetched > 0
+    finally:
+        moe.moe_residency_destroy(h)

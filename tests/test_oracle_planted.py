@@ -166,11 +166,34 @@ def m_outside_counts_resident(o):
     o.expected_outside = lambda E, C, k, n: C * (1.0 - (1.0 - k / E) ** n)
 
 
+def m_prefetch_keeps_unused(o):
+    cls = o.ResidencyLayer
+    class Bad(cls):
+        def step(self, needed):
+            keep = {e: sl for e, sl in self.staged.items() if e not in set(int(x) for x in needed)}
+            out = cls.step(self, needed)
+            for e, sl in keep.items():  # unused staged copies are not freed
+                self.free.remove(sl)
+            return out
+    o.ResidencyLayer = Bad
+
+
+def m_prefetch_ignores_staged(o):
+    cls = o.ResidencyLayer
+    class Bad(cls):
+        def step(self, needed):
+            self.free.extend(self.staged.values())  # staged misses copied again into a free slot
+            self.staged = {}
+            return cls.step(self, needed)
+    o.ResidencyLayer = Bad
+
+
 MUTATIONS = [m_nibble_swap, m_drop_zero, m_group_mod, m_tie_high, m_always_renorm,
              m_never_renorm, m_ascending, m_silu_sign, m_swap_gate_up,
              m_transposed_down, m_drop_weight, m_unstable_sort, m_victim_max,
              m_decay_after_bump, m_coverage_formula, m_time_model_no_compute,
-             m_fit_slope_as_bandwidth, m_outside_counts_resident]
+             m_fit_slope_as_bandwidth, m_outside_counts_resident, m_prefetch_keeps_unused,
+             m_prefetch_ignores_staged]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=lambda m: m.__name__)

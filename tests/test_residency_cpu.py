@@ -262,3 +262,118 @@ def test_policy_hit_rates_against_the_ceiling(alpha):
     else:
         for rate in rates.values():
             assert abs(rate - C / E) < 0.05, (rates, C / E)
+
+
+# ---- prefetch of predicted misses into spare slots ---------------------------
+def _run_ops(ops, lib_h=None, orc=None):
+    out = []
+    for op in ops:
+        if op["op"] == "step":
+            if lib_h is not None:
+                moe.moe_residency_prepare(lib_h, 0, op["ids"])
+            if orc is not None:
+                orc.step(op["ids"])
+        else:
+            n_lib = moe.moe_residency_prefetch(lib_h, 0, op["ids"]) if lib_h is not None else None
+            n_orc = len(orc.prefetch(op["ids"])) if orc is not None else None
+            out.append((n_lib, n_orc))
+    return out
+
+
+def test_prefetch_hand_trace_matches_golden():
+    c = json.load(open(os.path.join(ROOT, "tests", "golden", "residency_prefetch_trace.json")))
+    h = dry_policy(c["E"], c["C"], c["S"], c["decay"], c["policy"], max_ids=2)
+    try:
+        staged = _run_ops(c["ops"], lib_h=h)
+        assert [n for n, _ in staged] == [op["staged"] for op in c["ops"] if op["op"] == "prefetch"]
+        tr = [[s, e, sl, v] for (s, l, e, sl, v) in moe.moe_residency_trace(h)]
+        assert tr == c["trace"]
+        assert moe.moe_residency_slot_table(h, 0, c["E"]).tolist() == c["slot_of_after"]
+        assert moe.moe_residency_counts(h, 0, c["E"]).tolist() == c["counts_after"]
+        st = moe.moe_residency_get_stats(h, 0)
+        assert (st["hits"], st["misses"], st["evictions"], st["prefetched"], st["prefetch_copies"]) == (
+            c["hits"], c["misses"], c["evictions"], c["prefetched"], c["prefetch_copies"])
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+@pytest.mark.parametrize("policy,E,C,S,k,alpha", [
+    ("decay", 64, 30, 4, 8, 1.0),
+    ("lru", 64, 30, 2, 8, 1.0),
+    ("pinned", 64, 30, 3, 8, 1.0),
+    ("decay", 32, 12, 6, 4, 0.0),
+])
+def test_prefetch_policies_match_oracle(policy, E, C, S, k, alpha):
+    # Each step is preceded by a prefetch of the S non-resident experts with
+    # the highest decayed counts (ties: lower id) -- a popularity predictor.
+    steps = 250
+    ranks = synth.zipf_ranks(5, 0, E)
+    profile = 1.0 / ranks.astype(np.float64) ** max(alpha, 1e-9)
+    pinned = C - k if policy == "pinned" else 0
+    h = dry_policy(E, C, S, 0.9, policy, pinned=pinned, profile=profile if policy == "pinned" else None,
+                   max_ids=k)
+    orc = moe_oracle.ResidencyLayer(E, C, S, 0.9, policy, profile, pinned)
+    try:
+        for step in range(steps):
+            counts = moe.moe_residency_counts(h, 0, E)
+            table = moe.moe_residency_slot_table(h, 0, E)
+            cand = sorted((e for e in range(E) if table[e] < 0), key=lambda e: (-counts[e], e))[:S]
+            n_lib = moe.moe_residency_prefetch(h, 0, cand)
+            assert n_lib == len(orc.prefetch(cand))
+            lg = synth.logits_zipf(5, 0, step, 1, E, alpha)
+            ids, _ = moe_oracle.route(lg, k, False)
+            moe.moe_residency_prepare(h, 0, ids.reshape(-1).tolist())
+            orc.step(ids.reshape(-1).tolist())
+        assert moe.moe_residency_slot_table(h, 0, E).tolist() == orc.slot_of
+        st = moe.moe_residency_get_stats(h, 0)
+        assert (st["hits"], st["misses"], st["evictions"], st["prefetched"], st["prefetch_copies"]) == (
+            orc.hits, orc.misses, orc.evictions, orc.prefetched, orc.prefetch_copies)
+        trace = [(s, e, sl, v) for (s, l, e, sl, v) in moe.moe_residency_trace(h)]
+        assert len(trace) == orc.misses
+        if alpha > 0:
+            assert orc.prefetched > 0  # the predictor serves some misses
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+def test_prefetch_arguments_and_limits():
+    h = dry_policy(8, 3, 0, 0.9, "decay", max_ids=2)  # no spare slots
+    try:
+        assert moe.moe_residency_prefetch(h, 0, [5, 6]) == 0
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prefetch(h, 0, [9])
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prefetch(h, 1, [5])
+    finally:
+        moe.moe_residency_destroy(h)
+    h = dry_policy(8, 3, 2, 0.9, "decay", max_ids=2)
+    try:
+        # Resident and repeated ids are skipped; out-of-range ids stage nothing.
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prefetch(h, 0, [5, 99])
+        assert moe.moe_residency_get_stats(h, 0)["prefetch_copies"] == 0
+        assert moe.moe_residency_prefetch(h, 0, [0, 5, 5, 6, 7]) == 2
+        # A rejected step (capacity) keeps the staged copies for the next one.
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prepare(h, 0, [1, 2, 3, 4])
+        moe.moe_residency_prepare(h, 0, [6])
+        st = moe.moe_residency_get_stats(h, 0)
+        assert (st["misses"], st["prefetched"]) == (1, 1)
+        # 5 was not needed: its spare slot is free again for the next prefetch.
+        assert moe.moe_residency_prefetch(h, 0, [5, 7]) == 2
+    finally:
+        moe.moe_residency_destroy(h)
+
+
+def test_prefetch_injected_failure_stages_nothing_more():
+    h = dry_policy(8, 3, 2, 0.9, "decay", max_ids=2)
+    try:
+        moe.moe_residency_inject_copy_failure(h, 1)  # the second copy from now fails
+        with pytest.raises(moe.MoeError):
+            moe.moe_residency_prefetch(h, 0, [5, 6])
+        # The first copy was staged, the second not; the next step uses the first.
+        moe.moe_residency_prepare(h, 0, [5, 6])
+        st = moe.moe_residency_get_stats(h, 0)
+        assert (st["prefetch_copies"], st["prefetched"], st["misses"]) == (1, 1, 2)
+    finally:
+        moe.moe_residency_destroy(h)
