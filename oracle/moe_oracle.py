@@ -21,7 +21,11 @@ Sources (web pages; cited by title and section):
   (eviction by an access counter whose old accesses lose weight).
 * lucashiago.com.br "local" explainer, etapa 1 (a scale and a zero point per
   block of weights), etapa 3 (experts touched by n tokens), etapa 4 (the hit
-  ceiling of any cache policy).
+  ceiling of any cache policy; profile against LRU), etapa 5 (the declared
+  time model t = t_calc + bytes_out / bandwidth).
+* "Horizon RunMap -- Prévia Técnica", "03 / Arquitetura", ADR 0009: copies
+  land in spare positions before a generation is published (prefetch into
+  spare slots).
 
 Readings where the pages are silent (listed with reasons in the design notes):
 groups run along each row's reduction axis; code element 2c is the low nibble
