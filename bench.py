@@ -863,11 +863,11 @@ def run_prefill(args, world, rank):
 
 def run_e2e(moe, wl, n, W):
     """Same metric through the public API with host buffers: per step the
-    token's activations and the 16 layers' router logits are copied from
-    pinned host memory, the 16 layers run, and the output is read back
-    (synchronising). The 16 moe_layer_forward calls are captured once into a
-    CUDA graph through the binding (as a latency-minded caller would) and
-    replayed per step; the eager per-call variant is reported beside it."""
+    token's activations and every layer's router logits are copied from
+    pinned host memory, the layers run, and the output is read back
+    (synchronising). The per-layer moe_layer_forward calls are captured once
+    into a CUDA graph through the binding (as a latency-minded caller would)
+    and replayed per step; the eager per-call variant is reported beside it."""
     x_h = wl.x0[W:W + n].cpu().pin_memory()
     lg_h = wl.logits[W:W + n].cpu().pin_memory()
     x_d = torch.empty_like(wl.x0[0])
@@ -901,8 +901,8 @@ def run_e2e(moe, wl, n, W):
             "h2d_bytes_per_step": int(x_h[0].numel() * 2 + lg_h[0].numel() * 4),
             "d2h_bytes_per_step": int(y_h.numel() * 2), "steps": n,
             "eager_value": round(eager, 2),
-            "how": "per step: pinned H2D of x and the 16 layers' logits, the 16 moe_layer_forward calls "
-                   "(captured once into a CUDA graph through the binding and replayed; eager_value: "
+            "how": f"per step: pinned H2D of x and the {wl.L} layers' logits, the {wl.L} moe_layer_forward "
+                   "calls (captured once into a CUDA graph through the binding and replayed; eager_value: "
                    "called one by one), D2H of the last layer's y, stream sync"}
 
 
