@@ -333,6 +333,7 @@ typedef struct {
   int32_t policy;            /* MOE_POLICY_* (0: decayed counts) */
   int32_t pinned;            /* MOE_POLICY_PINNED: experts pinned per layer */
   const double* profile;     /* MOE_POLICY_PINNED: host [L][E] popularity, read by create */
+  int32_t log_ops;           /* 1: keep a log of the stream operations (moe_residency_ops) */
 } moe_residency_cfg;
 
 typedef struct {
@@ -348,6 +349,20 @@ typedef struct {
   int32_t slot;    /* physical slot it was copied into */
   int32_t victim;  /* evicted expert, -1 if none */
 } moe_residency_event;
+
+/* One stream operation of the manager, in the order it was enqueued. Streams:
+ * 0 compute, 1 copy. Events: 0 "readers done" (compute), 1 "copies done"
+ * (copy). The log is the same in a dry run, which
+ * enqueues nothing, so the ordering can be checked without a GPU. */
+enum { MOE_OP_RECORD = 0, MOE_OP_WAIT = 1, MOE_OP_COPY = 2, MOE_OP_PUBLISH = 3 };
+typedef struct {
+  int32_t kind;    /* MOE_OP_*: RECORD event on stream, stream WAITs for event, COPY, PUBLISH */
+  int32_t stream;  /* 0 compute, 1 copy */
+  int32_t event;   /* RECORD / WAIT; else -1 */
+  int32_t layer;   /* COPY / PUBLISH; else -1 */
+  int32_t slot;    /* COPY: destination slot; else -1 */
+  int32_t expert;  /* COPY: the expert copied; else -1 */
+} moe_residency_op;
 
 typedef struct moe_residency moe_residency;
 
@@ -370,10 +385,10 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
  * generation). For each id in order, skipping ids that are resident or
  * already prefetched, while a free spare slot is left: the block is copied
  * host->device on the copy stream into the lowest free slot. Nothing is
- * published and no count changes. The copy waits only for the readers of
- * the layer's slots retired so far (an event recorded by the layer's last
- * prepare() that evicted), not for work enqueued since, so it overlaps the
- * layers being computed. The layer's next prepare() takes a prefetched
+ * published and no count changes. The copy adds no wait: a free slot was
+ * never read, or was freed by a prepare() whose copy-stream wait already
+ * follows every reader of its previous occupant (the copy stream runs in
+ * order), so it overlaps the layers being computed. The layer's next prepare() takes a prefetched
  * expert that its step needs as a miss in that slot, with no copy (counted
  * in `prefetched`); prefetched experts that step does not need return to
  * the free spares. Returns the number copied in *staged_out (nullable).
@@ -384,6 +399,8 @@ int moe_residency_get_stats(const moe_residency* r, int layer, moe_residency_sta
 /* Copies up to `cap` events (all layers, in decision order); *n_out = total. */
 int moe_residency_trace(const moe_residency* r, moe_residency_event* buf,
                         size_t cap, size_t* n_out);
+/* Copies up to `cap` logged stream operations (cfg.log_ops); *n_out = total. */
+int moe_residency_ops(const moe_residency* r, moe_residency_op* buf, size_t cap, size_t* n_out);
 /* Host copy of the layer's current slot table [E] (what was last published). */
 int moe_residency_slot_table(const moe_residency* r, int layer, int32_t* host_out);
 /* Host copy of the layer's decayed counts [E]. */

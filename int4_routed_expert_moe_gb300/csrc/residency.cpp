@@ -41,18 +41,47 @@ struct moe_residency {
     std::vector<int32_t> slot_of;  // expert -> physical slot, -1 absent
     std::vector<int32_t> free;     // free physical slots
     std::vector<int32_t> staged;   // expert -> spare slot holding a prefetched copy, -1 none
-    cudaEvent_t retired = nullptr;  // compute-stream point after every reader of a retired slot
-    bool retired_recorded = false;
     moe_residency_stats st;
     int64_t steps = 0;
   };
   std::vector<Layer> layers;
   std::vector<moe_residency_event> trace;
+  std::vector<moe_residency_op> ops;  // stream operations, when cfg.log_ops
   int64_t inject_countdown = -1;
   int physical = 0;
 };
 
 namespace {
+
+// Every stream operation of the manager goes through these helpers: logged
+// when the handle logs (cfg.log_ops), executed unless it is a dry run. The
+// ordering decisions are therefore the same with and without a GPU.
+enum { kCompute = 0, kCopy = 1 };
+enum { kReadersDone = 0, kCopiesDone = 1 };  // event ids
+
+void log_op(moe_residency* r, int kind, int stream, int event, int layer, int slot, int expert) {
+  if (r->cfg.log_ops) r->ops.push_back({kind, stream, event, layer, slot, expert});
+}
+cudaEvent_t event_of(moe_residency* r, int ev) { return ev == kReadersDone ? r->readers_done : r->copies_done; }
+cudaStream_t stream_of(moe_residency* r, int st) { return st == kCompute ? r->compute : r->copy; }
+
+cudaError_t op_record(moe_residency* r, int ev, int st) {
+  log_op(r, MOE_OP_RECORD, st, ev, -1, -1, -1);
+  return r->cfg.dry_run ? cudaSuccess : cudaEventRecord(event_of(r, ev), stream_of(r, st));
+}
+cudaError_t op_wait(moe_residency* r, int st, int ev) {
+  log_op(r, MOE_OP_WAIT, st, ev, -1, -1, -1);
+  return r->cfg.dry_run ? cudaSuccess : cudaStreamWaitEvent(stream_of(r, st), event_of(r, ev), 0);
+}
+// Host -> device copy of `expert`'s block of `layer` into `slot`, on the copy stream.
+cudaError_t op_copy(moe_residency* r, int layer, int slot, int expert) {
+  log_op(r, MOE_OP_COPY, kCopy, -1, layer, slot, expert);
+  if (r->cfg.dry_run) return cudaSuccess;
+  const moe_residency_cfg& c = r->cfg;
+  const uint8_t* src = r->src + ((size_t)layer * c.experts + expert) * c.block_bytes;
+  uint8_t* dst = r->pool + ((size_t)layer * r->physical + slot) * c.block_bytes;
+  return cudaMemcpyAsync(dst, src, c.block_bytes, cudaMemcpyHostToDevice, r->copy);
+}
 
 struct Miss {
   int32_t expert, slot, victim;
@@ -60,6 +89,8 @@ struct Miss {
 };
 
 int publish(moe_residency* r, int layer, const std::vector<std::pair<int32_t, int32_t>>& upd) {
+  log_op(r, MOE_OP_PUBLISH, kCompute, -1, layer, -1, -1);
+  if (r->cfg.dry_run) return MOE_OK;
   int32_t* table = r->slot_of_dev + (size_t)layer * r->cfg.experts;
   size_t i = 0;
   while (i < upd.size()) {
@@ -157,8 +188,6 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
   if (!c.dry_run) {
     cudaError_t e = cudaEventCreateWithFlags(&r->readers_done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->copies_done, cudaEventDisableTiming);
-    for (int l = 0; e == cudaSuccess && l < c.layers; ++l)
-      e = cudaEventCreateWithFlags(&r->layers[l].retired, cudaEventDisableTiming);
     // Initial placement: each resident expert's block into its slot
     // (canonical: expert e in slot e, e < C, one copy per layer).
     for (int l = 0; e == cudaSuccess && l < c.layers; ++l) {
@@ -257,19 +286,17 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
   // Prefetched copies this step did not need return to the free spares.
   for (int e = 0; e < c.experts; ++e)
     if (L.staged[e] >= 0 && !needed[e]) free_slots.push_back(L.staged[e]);
-  bool any_victim = false;
-  for (const Miss& m : misses) any_victim |= m.victim >= 0;
 
   // Enqueue copies: the copy stream first waits for every reader enqueued so
   // far on the compute stream (this retires the victims' readers).
   int failed_at = -1;
   int rc = MOE_OK;
-  if (!c.dry_run && !misses.empty()) {
-    cudaError_t e = cudaEventRecord(r->readers_done, r->compute);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(r->copy, r->readers_done, 0);
-    // Every reader of this step's victims is enqueued before this point: a
-    // later prefetch into their slots waits for this event only.
-    if (e == cudaSuccess && any_victim) e = cudaEventRecord(L.retired, r->compute);
+  if (!misses.empty()) {
+    // Every reader of this step's victims is enqueued before this point. The
+    // copy stream runs in order, so this wait also orders every later copy
+    // into a slot freed here (a prefetch's) after those readers.
+    cudaError_t e = op_record(r, kReadersDone, kCompute);
+    if (e == cudaSuccess) e = op_wait(r, kCopy, kReadersDone);
     if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "residency ordering: %s", cudaGetErrorString(e));
   }
   for (size_t i = 0; i < misses.size(); ++i) {
@@ -281,11 +308,8 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
       break;
     }
     if (r->inject_countdown > 0) --r->inject_countdown;
-    if (c.dry_run) continue;
     const Miss& m = misses[i];
-    const uint8_t* s = r->src + ((size_t)layer * c.experts + m.expert) * c.block_bytes;
-    uint8_t* d = r->pool + ((size_t)layer * r->physical + m.slot) * c.block_bytes;
-    cudaError_t e = cudaMemcpyAsync(d, s, c.block_bytes, cudaMemcpyHostToDevice, r->copy);
+    cudaError_t e = op_copy(r, layer, m.slot, m.expert);
     if (e != cudaSuccess) {
       failed_at = (int)i;
       rc = moe::fail(MOE_ERR_CUDA, "copy of expert %d: %s", m.expert, cudaGetErrorString(e));
@@ -307,25 +331,24 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
         }
       }
     }
-    if (!c.dry_run && !removal.empty()) {
-      cudaStreamWaitEvent(r->compute, r->readers_done, 0);
+    if (!removal.empty()) {
+      op_wait(r, kCompute, kReadersDone);
       publish(r, layer, removal);
     }
     return rc;
   }
-  if (!c.dry_run && !misses.empty()) {
+  if (!misses.empty()) {
     std::vector<std::pair<int32_t, int32_t>> upd;
     for (const Miss& m : misses)
       if (m.victim >= 0) upd.push_back({m.victim, -1});
     for (const Miss& m : misses) upd.push_back({m.expert, m.slot});
-    cudaError_t e = cudaEventRecord(r->copies_done, r->copy);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(r->compute, r->copies_done, 0);
+    cudaError_t e = op_record(r, kCopiesDone, kCopy);
+    if (e == cudaSuccess) e = op_wait(r, kCompute, kCopiesDone);
     if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "residency publish order: %s", cudaGetErrorString(e));
     const int prc = publish(r, layer, upd);
     if (prc != MOE_OK) return prc;
   }
   // Commit.
-  if (!c.dry_run && !misses.empty() && any_victim) L.retired_recorded = true;
   for (const Miss& m : misses)
     r->trace.push_back({L.steps, layer, m.expert, m.slot, m.victim});
   for (int e = 0; e < c.experts; ++e) L.staged[e] = -1;
@@ -359,7 +382,9 @@ int moe_residency_prefetch(moe_residency* r, int layer, const int32_t* host_ids,
       return moe::fail(MOE_ERR_ARG, "id %d out of range [0, %d)", host_ids[i], c.experts);
   auto& L = r->layers[layer];
   int staged = 0;
-  bool ordered = false;
+  // No wait: a free slot was either never read (a spare, or an unneeded
+  // prefetched copy) or freed by a prepare() whose copy-stream wait already
+  // follows every reader of its previous occupant.
   for (int i = 0; i < n && !L.free.empty(); ++i) {
     const int32_t e = host_ids[i];
     if (L.slot_of[e] >= 0 || L.staged[e] >= 0) continue;
@@ -371,17 +396,12 @@ int moe_residency_prefetch(moe_residency* r, int layer, const int32_t* host_ids,
       return moe::fail(MOE_ERR_INJECTED, "injected failure at a prefetch copy of layer %d", layer);
     }
     if (r->inject_countdown > 0) --r->inject_countdown;
+    const cudaError_t err = op_copy(r, layer, slot, e);
+    if (err != cudaSuccess) {
+      if (staged_out) *staged_out = staged;
+      return moe::fail(MOE_ERR_CUDA, "prefetch copy of expert %d: %s", e, cudaGetErrorString(err));
+    }
     if (!c.dry_run) {
-      cudaError_t err = cudaSuccess;
-      if (!ordered && L.retired_recorded) err = cudaStreamWaitEvent(r->copy, L.retired, 0);
-      ordered = true;
-      const uint8_t* src = r->src + ((size_t)layer * c.experts + e) * c.block_bytes;
-      uint8_t* dst = r->pool + ((size_t)layer * r->physical + slot) * c.block_bytes;
-      if (err == cudaSuccess) err = cudaMemcpyAsync(dst, src, c.block_bytes, cudaMemcpyHostToDevice, r->copy);
-      if (err != cudaSuccess) {
-        if (staged_out) *staged_out = staged;
-        return moe::fail(MOE_ERR_CUDA, "prefetch copy of expert %d: %s", e, cudaGetErrorString(err));
-      }
       L.st.copies += 1;
       L.st.h2d_bytes += c.block_bytes;
     }
@@ -423,6 +443,15 @@ int moe_residency_trace(const moe_residency* r, moe_residency_event* buf, size_t
   return MOE_OK;
 }
 
+int moe_residency_ops(const moe_residency* r, moe_residency_op* buf, size_t cap, size_t* n_out) {
+  moe::clear_error();
+  if (!r || !n_out || (cap && !buf)) return moe::fail(MOE_ERR_ARG, "NULL argument");
+  *n_out = r->ops.size();
+  const size_t n = std::min(cap, r->ops.size());
+  if (n) std::memcpy(buf, r->ops.data(), n * sizeof(moe_residency_op));
+  return MOE_OK;
+}
+
 int moe_residency_slot_table(const moe_residency* r, int layer, int32_t* host_out) {
   moe::clear_error();
   if (!r || !host_out || layer < 0 || layer >= r->cfg.layers) return moe::fail(MOE_ERR_ARG, "bad argument");
@@ -450,8 +479,6 @@ void moe_residency_destroy(moe_residency* r) {
     if (r->copy) cudaStreamSynchronize(r->copy);
     if (r->readers_done) cudaEventDestroy(r->readers_done);
     if (r->copies_done) cudaEventDestroy(r->copies_done);
-    for (auto& L : r->layers)
-      if (L.retired) cudaEventDestroy(L.retired);
   }
   delete r;
 }

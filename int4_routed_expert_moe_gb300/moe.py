@@ -56,7 +56,14 @@ class moe_residency_cfg(ctypes.Structure):
                 ("max_ids_per_step", ctypes.c_int32), ("dry_run", ctypes.c_int32),
                 ("block_bytes", ctypes.c_uint64), ("decay", ctypes.c_double),
                 ("policy", ctypes.c_int32), ("pinned", ctypes.c_int32),
-                ("profile", ctypes.c_void_p)]
+                ("profile", ctypes.c_void_p), ("log_ops", ctypes.c_int32)]
+
+
+class moe_residency_op(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("kind", "stream", "event", "layer", "slot", "expert")]
+
+
+MOE_OP_RECORD, MOE_OP_WAIT, MOE_OP_COPY, MOE_OP_PUBLISH = 0, 1, 2, 3
 
 
 class moe_residency_stats(ctypes.Structure):
@@ -105,6 +112,7 @@ _SIGS = {
     "moe_residency_prefetch": (_I, [_P, _I, _P, _I, ctypes.POINTER(ctypes.c_int)]),
     "moe_residency_get_stats": (_I, [_P, _I, ctypes.POINTER(moe_residency_stats)]),
     "moe_residency_trace": (_I, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    "moe_residency_ops": (_I, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
     "moe_residency_slot_table": (_I, [_P, _I, _P]),
     "moe_residency_counts": (_I, [_P, _I, _P]),
     "moe_residency_inject_copy_failure": (_I, [_P, ctypes.c_int64]),
@@ -375,7 +383,7 @@ def moe_residency_create(cfg: dict, host_src: torch.Tensor | None, dev_pool: tor
                           int(cfg.get("spares", 0)), int(cfg["max_ids_per_step"]),
                           int(cfg.get("dry_run", 0)), int(cfg["block_bytes"]),
                           float(cfg["decay"]), int(policy), int(cfg.get("pinned", 0)),
-                          prof_arr.ctypes.data if prof_arr is not None else None)
+                          prof_arr.ctypes.data if prof_arr is not None else None, int(cfg.get("log_ops", 0)))
     dry = bool(c.dry_run)
     src = pool = slot = None
     cs = cp = None
@@ -420,6 +428,15 @@ def moe_residency_trace(handle: int) -> list:
     _check(_lib.moe_residency_trace(handle, buf, n.value, ctypes.byref(n)), "moe_residency_trace")
     return [(int(b.step), int(b.layer), int(b.expert), int(b.slot), int(b.victim))
             for b in buf[:n.value]]
+
+
+def moe_residency_ops(handle: int) -> list:
+    """Logged stream operations: (kind, stream, event, layer, slot, expert) tuples."""
+    n = ctypes.c_size_t(0)
+    _check(_lib.moe_residency_ops(handle, None, 0, ctypes.byref(n)), "moe_residency_ops")
+    buf = (moe_residency_op * max(1, n.value))()
+    _check(_lib.moe_residency_ops(handle, buf, n.value, ctypes.byref(n)), "moe_residency_ops")
+    return [(o.kind, o.stream, o.event, o.layer, o.slot, o.expert) for o in buf[:n.value]]
 
 
 def moe_residency_slot_table(handle: int, layer: int, E: int) -> np.ndarray:
