@@ -69,7 +69,7 @@ def build(verbose: bool = False) -> str:
     if _stale(LIB, objs):
         lib64 = os.path.join(cuda, "lib64")
         cmd = [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-shared", "-cudart", "shared",
-               "-o", LIB + ".tmp", *objs, "-Xlinker", f"-rpath,{lib64}"]
+               "-o", LIB + ".tmp", *objs, "-ldl", "-Xlinker", f"-rpath,{lib64}"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

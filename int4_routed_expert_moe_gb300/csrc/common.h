@@ -8,9 +8,20 @@
 #include <cstdint>
 #include <cstdio>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe.h"
 
 namespace moe {
+
+// NVTX range over one ABI call (host side; a no-op unless a profiler is
+// attached), so timelines and `ncu --nvtx` filters see the library's calls.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Records a thread-local failure detail and returns `status`.
 int fail(int status, const char* fmt, ...);

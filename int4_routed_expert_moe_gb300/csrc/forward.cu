@@ -91,6 +91,7 @@ int moe_expert_forward(const moe_expert_shape* s, const void* x, int T,
                        const void* pool, const int32_t* slot_of, int n_slots,
                        const void* y_shared, void* y, void* workspace,
                        size_t workspace_bytes, int path, void* stream) {
+  moe::NvtxRange nvtx_range("moe_expert_forward");
   moe::clear_error();
   moe::ForwardArgs a;
   const int rc = expert_args("moe_expert_forward", s, x, T, ids, weights, k, E, pool, slot_of, n_slots, y_shared,
@@ -116,6 +117,7 @@ int moe_expert_forward_zero_copy(const moe_expert_shape* s, const void* x, int T
                                  const void* pool, const int32_t* slot_of, int n_slots,
                                  const void* host_src, const void* y_shared, void* y,
                                  void* workspace, size_t workspace_bytes, void* stream) {
+  moe::NvtxRange nvtx_range("moe_expert_forward_zero_copy");
   moe::clear_error();
   moe::ForwardArgs a;
   const int rc = expert_args("moe_expert_forward_zero_copy", s, x, T, ids, weights, k, E, pool, slot_of, n_slots,
@@ -146,6 +148,7 @@ int moe_layer_forward(const moe_expert_shape* s, const void* x, const float* log
                       int k, int renorm, int32_t* ids, float* weights, const void* pool,
                       const int32_t* slot_of, int n_slots, const void* y_shared, void* y,
                       void* workspace, size_t workspace_bytes, int path, void* stream) {
+  moe::NvtxRange nvtx_range("moe_layer_forward");
   moe::clear_error();
   if (!moe::valid_shape(s)) return moe::fail(MOE_ERR_SHAPE, "moe_layer_forward: invalid expert shape");
   if (T < 0 || E < 1 || E > 4096 || k < 1 || k > 32 || k > E || n_slots < 1)

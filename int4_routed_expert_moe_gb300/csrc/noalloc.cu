@@ -51,6 +51,7 @@ extern "C" int moe_layer_forward_noalloc(const moe_expert_shape* s, const void* 
                                          int32_t* ids, float* weights, const void* pool,
                                          const int32_t* slot_of, int n_slots,
                                          const void* y_shared, void* y, void* stream) {
+  moe::NvtxRange nvtx_range("moe_layer_forward_noalloc");
   moe::clear_error();
   if (!moe::valid_shape(s)) return moe::fail(MOE_ERR_SHAPE, "moe_layer_forward_noalloc: invalid expert shape");
   if (T < 0 || E < 1 || E > 4096 || k < 1 || k > 32 || k > E || n_slots < 1)

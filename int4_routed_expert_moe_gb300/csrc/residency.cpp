@@ -220,6 +220,7 @@ int moe_residency_create(const moe_residency_cfg* cfg, const void* host_src,
 }
 
 int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, int n) {
+  moe::NvtxRange nvtx_range("moe_residency_prepare");
   moe::clear_error();
   if (!r) return moe::fail(MOE_ERR_ARG, "moe_residency_prepare: NULL handle");
   const moe_residency_cfg& c = r->cfg;
@@ -372,6 +373,7 @@ int moe_residency_prepare(moe_residency* r, int layer, const int32_t* host_ids, 
 }
 
 int moe_residency_prefetch(moe_residency* r, int layer, const int32_t* host_ids, int n, int* staged_out) {
+  moe::NvtxRange nvtx_range("moe_residency_prefetch");
   moe::clear_error();
   if (!r) return moe::fail(MOE_ERR_ARG, "moe_residency_prefetch: NULL handle");
   const moe_residency_cfg& c = r->cfg;

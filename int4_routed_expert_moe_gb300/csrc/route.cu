@@ -129,6 +129,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm,
 extern "C" int moe_route(const float* logits, int T, int E, int k, int renorm,
                          int32_t* ids, float* weights, int32_t* bad_tokens,
                          void* stream) {
+  moe::NvtxRange nvtx_range("moe_route");
   moe::clear_error();
   if (T < 0 || E < 1 || E > 4096 || k < 1 || k > 32 || k > E)
     return moe::fail(MOE_ERR_ARG, "moe_route: need T >= 0, 1 <= k <= min(E, 32), E <= 4096 (T=%d E=%d k=%d)", T, E, k);

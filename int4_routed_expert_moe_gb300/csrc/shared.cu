@@ -238,6 +238,7 @@ extern "C" size_t moe_shared_workspace_bytes(int T, int H, int Is) {
 extern "C" int moe_shared_forward(const void* x, int T, int H, int Is, const void* wg,
                                   const void* wu, const void* wd, void* y, void* ws,
                                   size_t ws_bytes, void* stream) {
+  moe::NvtxRange nvtx_range("moe_shared_forward");
   moe::clear_error();
   if (T < 0 || H <= 0 || Is <= 0 || H % 64 || Is % 64 || H > 65536 || Is > 65536)
     return moe::fail(MOE_ERR_ARG, "moe_shared_forward: need H, Is positive multiples of 64 (H=%d Is=%d T=%d)", H,

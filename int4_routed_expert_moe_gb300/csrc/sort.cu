@@ -165,6 +165,7 @@ int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
 
 extern "C" int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* offsets,
                               int32_t* pair_tok, int32_t* pair_j, void* stream) {
+  moe::NvtxRange nvtx_range("moe_token_sort");
   moe::clear_error();
   if (T < 0 || k < 1 || E < 1 || E > 1024 || (long long)T * k > 65536)
     return moe::fail(MOE_ERR_ARG, "moe_token_sort: need E <= 1024, T*k <= 65536 (T=%d k=%d E=%d)", T, k, E);
