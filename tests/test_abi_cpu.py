@@ -126,3 +126,45 @@ def test_device_pool_generator_layout_matches_library(shape):
             assert v.min() >= 9e-4 and v.max() <= 1.01e-2
         for n in ("z_gate", "z_up", "z_down"):
             assert np.all(lib[n] == 8.0)
+
+
+def test_more_argument_checks_before_touching_the_gpu():
+    # Every case below fails in the host-side checks; fake non-NULL pointers
+    # (aligned addresses) are never dereferenced.
+    import ctypes
+    lib = moe._lib
+    s = moe.moe_expert_shape(256, 128, 64)
+    P = ctypes.c_void_p
+    A = P(1 << 20)  # an aligned fake address
+    fwd = lambda T, k, E, pool, ws, ws_bytes, path=1, x=A, ids=A: lib.moe_expert_forward(  # noqa: E731
+        ctypes.byref(s), x, T, ids, A, k, E, pool, A, 8, None, A, ws, ws_bytes, path, None)
+    assert fwd(1, 33, 64, A, A, 1 << 20) == moe.MOE_ERR_ARG          # k > 32
+    assert fwd(1, 2, 0, A, A, 1 << 20) == moe.MOE_ERR_ARG            # E = 0
+    assert fwd(1, 2, 8, None, A, 1 << 20) == moe.MOE_ERR_ARG         # NULL pool
+    assert fwd(1, 2, 8, P((1 << 20) + 16), A, 1 << 20) == moe.MOE_ERR_ARG  # pool not 256-aligned
+    assert fwd(1, 2, 8, A, P((1 << 20) + 8), 1 << 20) == moe.MOE_ERR_ARG   # workspace not 256-aligned
+    assert fwd(1, 2, 8, A, A, 1 << 20, x=P((1 << 20) + 2)) == moe.MOE_ERR_ARG  # x not 16-aligned
+    assert fwd(1, 2, 8, A, A, 16) == moe.MOE_ERR_CAPACITY            # workspace too small
+    assert fwd(-1, 2, 8, A, A, 1 << 20) == moe.MOE_ERR_ARG           # T < 0
+    # Zero-copy: the host source must be given, page-locked and mapped.
+    zc = lambda host: lib.moe_expert_forward_zero_copy(  # noqa: E731
+        ctypes.byref(s), A, 1, A, A, 2, 8, A, A, 8, host, None, A, A, 1 << 20, None)
+    assert zc(None) == moe.MOE_ERR_ARG
+    buf = (ctypes.c_uint8 * 4096)()
+    assert zc(ctypes.cast(buf, P)) == moe.MOE_ERR_ARG                # pageable memory
+    # Layer call: k > E, bad path.
+    assert lib.moe_layer_forward(ctypes.byref(s), A, A, 1, 4, 8, 0, A, A, A, A, 4, None, A, A,
+                                 1 << 20, 1, None) == moe.MOE_ERR_ARG
+    assert lib.moe_layer_forward(ctypes.byref(s), A, A, 1, 8, 2, 0, A, A, A, A, 8, None, A, A,
+                                 1 << 20, 9, None) == moe.MOE_ERR_ARG
+    # Shared FFN: sizes must be positive multiples of 64; T = 0 is a no-op.
+    assert lib.moe_shared_forward(A, 4, 100, 128, A, A, A, A, A, 1 << 20, None) == moe.MOE_ERR_ARG
+    assert lib.moe_shared_forward(A, 4, 256, 0, A, A, A, A, A, 1 << 20, None) == moe.MOE_ERR_ARG
+    assert lib.moe_shared_forward(None, 0, 256, 128, None, None, None, None, None, 0, None) == moe.MOE_OK
+    assert lib.moe_shared_forward(None, 4, 256, 128, A, A, A, A, A, 1 << 20, None) == moe.MOE_ERR_ARG
+    # Residency calls on a NULL handle.
+    n = ctypes.c_size_t(0)
+    assert lib.moe_residency_prepare(None, 0, None, 0) == moe.MOE_ERR_ARG
+    assert lib.moe_residency_prefetch(None, 0, None, 0, None) == moe.MOE_ERR_ARG
+    assert lib.moe_residency_ops(None, None, 0, ctypes.byref(n)) == moe.MOE_ERR_ARG
+    assert lib.moe_residency_trace(None, None, 0, ctypes.byref(n)) == moe.MOE_ERR_ARG
