@@ -940,6 +940,20 @@ def cpu_baseline(wl, budget_s=12.0):
             "cpu": cpu_model()}
 
 
+def device_info():
+    """Where the line was measured (best effort, never raises): GPU name, SM
+    count and memory, host core count and CPU model."""
+    info = {"host_cores": os.cpu_count(), "cpu": cpu_model()}
+    try:
+        if torch.cuda.is_available():
+            p = torch.cuda.get_device_properties(torch.cuda.current_device())
+            info.update({"gpu": p.name, "sms": int(p.multi_processor_count),
+                         "gpu_mem_gib": round(p.total_memory / 2 ** 30, 1)})
+    except Exception:  # metadata only
+        pass
+    return info
+
+
 def cpu_model():
     try:
         with open("/proc/cpuinfo") as f:
@@ -1002,7 +1016,9 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         if rank == 0:  # the other ranks exit without work
-            print(json.dumps(run_reference(args)), flush=True)
+            line = run_reference(args)
+            line["device"] = device_info()
+            print(json.dumps(line), flush=True)
         barrier(world)
         if world > 1:
             import torch.distributed as dist
@@ -1019,6 +1035,7 @@ def main():
     else:
         out = run_ours(args, world, rank, local, args.workload)
     if rank == 0:
+        out["device"] = device_info()
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
