@@ -387,6 +387,29 @@ def base_line(metric, value, unit, world, K, W, ms, config, hib=True):
             "data": "synthetic (seeded; random-init INT4 experts)", "config": config}
 
 
+def time_model_line(full, low, main, K, Ktm, E, lo):
+    """The declared time model t_token = t_calc + bytes_out / bandwidth
+    (lucashiago explainer, etapa 5) fitted on two runs of Ktm steps -- all E
+    experts resident (`full`) and `lo` resident (`low`) -- and the rate it
+    predicts for the main run of K steps, beside the measured one (one rank's
+    tokens). Each run: {"ms": device time, "bytes_out": bytes read or copied
+    from host memory}."""
+    t_full, t_low = full["ms"] / 1e3 / Ktm, low["ms"] / 1e3 / Ktm
+    b_full, b_low = full["bytes_out"] / Ktm, low["bytes_out"] / Ktm
+    per_byte = (t_low - t_full) / max(1.0, b_low - b_full)
+    t_calc = t_full - b_full * per_byte
+    b_main = main["bytes_out"] / K
+    t_pred = t_calc + b_main * per_byte
+    measured = K / (main["ms"] / 1e3)
+    return {"form": "t_token = t_calc + bytes_out / bandwidth (lucashiago explainer, etapa 5)",
+            "fit": f"two runs of {Ktm} steps in the same mode: all {E} experts resident and {lo} resident",
+            "t_calc_us": round(t_calc * 1e6, 2),
+            "bandwidth_gbs": round(1.0 / per_byte / 1e9, 2) if per_byte > 0 else None,
+            "bytes_out_per_token": int(b_main), "predicted_tok_s": round(1.0 / t_pred, 2),
+            "measured_tok_s": round(measured, 2), "pred_over_meas": round((1.0 / t_pred) / measured, 4),
+            "endpoints_tok_s": {str(E): round(1.0 / t_full, 2), str(lo): round(1.0 / t_low, 2)}}
+
+
 class PartialStack:
     """Inputs shared by the partial-residency runs of the OLMoE shape: the
     complete pinned host source of all L x E expert blocks, each layer's
@@ -614,13 +637,6 @@ def run_partial(args, world, rank):
     eager = run(C, Ktm, Wtm, graph=False) if args.mode == "zerocopy" else None
     full = run(E, Ktm, Wtm)
     low = run(lo, Ktm, Wtm)
-    # Fit on the two extremes: t = t_calc + bytes_out / bandwidth per token.
-    t_full, t_low = full["ms"] / 1e3 / Ktm, low["ms"] / 1e3 / Ktm
-    b_full, b_low = full["bytes_out"] / Ktm, low["bytes_out"] / Ktm
-    per_byte = (t_low - t_full) / max(1.0, b_low - b_full)
-    t_calc = t_full - b_full * per_byte
-    b_main = main_run["bytes_out"] / K
-    t_pred = t_calc + b_main * per_byte
     ms = main_run["ms"]
     value = K * world / (ms / 1e3)
     cfg = {"workload": "olmoe_partial", "layers": L, "hidden": H, "experts": E, "top_k": k,
@@ -645,13 +661,7 @@ def run_partial(args, world, rank):
         out["residency"]["prefetch_copies_per_token"] = round(main_run["prefetch_copies"] / K, 3)
     if eager is not None:
         out["residency"]["eager_value"] = round(Ktm * world / (eager["ms"] / 1e3), 2)
-    out["time_model"] = {
-        "form": "t_token = t_calc + bytes_out / bandwidth (lucashiago explainer, etapa 5)",
-        "fit": f"two runs of {Ktm} steps in the same mode: all {E} experts resident and {lo} resident",
-        "t_calc_us": round(t_calc * 1e6, 2), "bandwidth_gbs": round(1.0 / per_byte / 1e9, 2) if per_byte > 0 else None,
-        "bytes_out_per_token": int(b_main), "predicted_tok_s": round(1.0 / t_pred, 2),
-        "measured_tok_s": round(value / world, 2), "pred_over_meas": round((1.0 / t_pred) / (value / world), 4),
-        "endpoints_tok_s": {str(E): round(1.0 / t_full, 2), str(lo): round(1.0 / t_low, 2)}}
+    out["time_model"] = time_model_line(full, low, main_run, K, Ktm, E, lo)
     if args.mode == "copy":
         out["time_model"]["copy_engine_gbs"] = round(copy_engine_gbs(ps), 2)
     out["gpu_launches"] = main_run["launches_per_step"] * K
