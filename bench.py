@@ -38,10 +38,13 @@ from int4_routed_expert_moe_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer decode tokens/s (expert-weight HBM GB/s in roofline)"
 METRIC_PREFILL = "MoE-layer prefill tokens/s (tensor-core TFLOP/s in roofline)"
-# DRAM bytes per layer call from one ncu capture of the current kernels
-# (decode: gate/up 17.90 MB + down 9.00 MB read, nothing written; prefill:
-# gate/up GEMM 159.45 MB read + 5.10 MB written, down GEMM 79.77 + 8.18 MB).
-DECODE_LAYER_DRAM_BYTES = 26_891_776
+# DRAM bytes (read + written) of one launch of the decode kernel per
+# workload, from an ncu capture of the current kernel build; a workload
+# without an entry reports null.
+DECODE_DRAM_BYTES = {}
+# Prefill: DRAM bytes of the gate/up and down grouped GEMMs of one layer call
+# from an ncu capture (gate/up 159.45 MB read + 5.10 MB written, down 79.77 +
+# 8.18 MB).
 PREFILL_GEMM_DRAM_BYTES = 252_505_088
 
 
@@ -155,47 +158,6 @@ class ClockSampler:
                 "samples": len(used), "samples_in_timed_region": len(inside)}
 
 
-class ExtEvents:
-    """CUDA events recorded as graph nodes (cudaEventRecordExternal), through
-    the CUDA runtime torch already loaded; used only for timing."""
-
-    def __init__(self, n):
-        import ctypes
-        self.ct = ctypes
-        self.rt = None
-        for name in ("libcudart.so.13", "libcudart.so"):
-            try:
-                self.rt = ctypes.CDLL(name)
-                break
-            except OSError:
-                continue
-        if self.rt is None:
-            raise RuntimeError("libcudart not found")
-        self.ev = []
-        for _ in range(n):
-            e = ctypes.c_void_p()
-            rc = self.rt.cudaEventCreate(ctypes.byref(e))
-            if rc != 0:
-                raise RuntimeError(f"cudaEventCreate: {rc}")
-            self.ev.append(e)
-
-    def record(self, i, stream_handle):
-        rc = self.rt.cudaEventRecordWithFlags(self.ev[i], self.ct.c_void_p(stream_handle), 1)
-        if rc != 0:
-            raise RuntimeError(f"cudaEventRecordWithFlags: {rc}")
-
-    def elapsed(self, i, j):
-        f = self.ct.c_float()
-        rc = self.rt.cudaEventElapsedTime(self.ct.byref(f), self.ev[i], self.ev[j])
-        if rc != 0:
-            raise RuntimeError(f"cudaEventElapsedTime: {rc}")
-        return f.value
-
-    def destroy(self):
-        for e in self.ev:
-            self.rt.cudaEventDestroy(e)
-
-
 def smi_index():
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     first = vis.split(",")[0].strip() if vis else ""
@@ -264,23 +226,56 @@ class DecodeWorkload:
                                   moe.MOE_PATH_GEMV)
 
     def launches_per_step(self):
-        return self.L * 2  # decode gate/up kernel (routing inside), decode down kernel
+        return self.L  # one decode kernel per layer (routing inside)
 
     def expert_bytes_per_step(self):
         # T = 1: the k chosen experts of every layer are read once each.
         return self.L * self.k * self.bb
 
 
+def timed_blocks(graph_blocks, warm_graphs, world, stream):
+    """Replays the warm-up graphs, then each block of graphs bracketed by
+    CUDA events on the launching stream (barrier + synchronize around the
+    whole timed region). Returns (total ms, [ms per block], host t0, t1)."""
+    for g in warm_graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(graph_blocks) + 1)]
+    t_host0 = time.time()
+    evs[0].record(stream)
+    for i, blk in enumerate(graph_blocks):
+        for g in blk:
+            g.replay()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(world)
+    block_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(graph_blocks))]
+    return sum(block_ms), block_ms, t_host0, t_host1
+
+
+def split_blocks(K, n_blocks=3):
+    """[(first step, steps)] of n_blocks nearly equal blocks of K steps."""
+    sizes = [K // n_blocks + (1 if i < K % n_blocks else 0) for i in range(n_blocks)]
+    out, s0 = [], 0
+    for n in sizes:
+        if n:
+            out.append((s0, n))
+        s0 += n
+    return out
+
+
 def run_ours(args, world, rank, local, name="olmoe_decode"):
     from int4_routed_expert_moe_gb300 import moe
     seed = synth.BASE_SEED + (1 if name == "olmoe_decode" else 6)
     K = args.steps or 512
-    W = args.warmup if args.warmup is not None else 128
+    W = max(3, args.warmup if args.warmup is not None else 128)
     wl = DecodeWorkload(moe, seed, K + W, rank, name)
     stream = torch.cuda.current_stream()
     win = max(1, args.graph_window)
 
-    # Capture windows of `win` steps into CUDA graphs (warm-up windows first).
     wl.step(0)  # eager pass: sets up kernel attributes before capture
     torch.cuda.synchronize()
 
@@ -291,61 +286,25 @@ def run_ours(args, world, rank, local, name="olmoe_decode"):
                 wl.step(s)
         return g
 
+    # Warm-up, then the timed steps as 3 blocks (the pages pool their decode
+    # rate over blocks and report the spread between them), each block one or
+    # more CUDA graphs of at most `win` steps.
     warm_graphs = [capture(s, min(W, s + win)) for s in range(0, W, win)]
-    timed_graphs = [capture(s, min(W + K, s + win)) for s in range(W, W + K, win)]
+    graph_blocks = [[capture(W + b0 + s, W + b0 + min(n, s + win)) for s in range(0, n, win)]
+                    for b0, n in split_blocks(K)]
     torch.cuda.synchronize()
 
     sampler = ClockSampler(smi_index())
     time.sleep(0.2)
-    for g in warm_graphs:
-        g.replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host0 = time.time()
-    ev0.record(stream)
-    for g in timed_graphs:
-        g.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    t_host1 = time.time()
-    barrier(world)
-    ms = ev0.elapsed_time(ev1)
-    ms_max = max_over_ranks(ms, world)
-
-    # Dominant unit: one moe_layer_forward call of the GEMV path (the gate/up
-    # and down streaming kernels, which overlap through PDL). A separate graph of n_kt steps brackets each
-    # call with external event-record nodes on the launching stream; the
-    # average of those durations is the per-launch time of the roofline.
-    n_kt = min(K, 32)
-    ev = ExtEvents(2 * n_kt * wl.L)
-    g_kt = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_kt):
-        st = torch.cuda.current_stream().cuda_stream
-        for i, s in enumerate(range(W, W + n_kt)):
-            for l in range(wl.L):
-                x = wl.x0[s] if l == 0 else wl.y[l - 1]
-                ev.record(2 * (i * wl.L + l), st)
-                moe.moe_layer_forward(wl.shape, x, wl.logits[s, l], wl.k, wl.renorm, wl.ids[l], wl.w[l],
-                                      wl.layer_pool(l), wl.slot_of, wl.E, None, wl.y[l], wl.ws,
-                                      moe.MOE_PATH_GEMV)
-                ev.record(2 * (i * wl.L + l) + 1, st)
-    g_kt.replay()
-    torch.cuda.synchronize()
-    fwd_ms = [ev.elapsed(2 * j, 2 * j + 1) for j in range(n_kt * wl.L)]
-    ev.destroy()
-    fwd_avg_s = statistics.mean(fwd_ms) / 1e3
+    ms, block_ms, t_host0, t_host1 = timed_blocks(graph_blocks, warm_graphs, world, stream)
     rows = sampler.stop()
     clocks = ClockSampler.summarize(rows, t_host0, t_host1)
+    assert moe.moe_workspace_flags(wl.ws) == 0
+    ms_max = max_over_ranks(ms, world)
 
     tokens = K * wl.T * world
     value = tokens / (ms_max / 1e3)
-    bytes_per_launch = wl.k * wl.bb
     peak, peak_src = measured_peaks()
-    achieved = bytes_per_launch / fwd_avg_s / 1e9
-    step_gbs = wl.expert_bytes_per_step() * K / (ms / 1e3) / 1e9
-
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
@@ -357,19 +316,9 @@ def run_ours(args, world, rank, local, name="olmoe_decode"):
                    "arithmetic": "INT4 weights, FP16 products (<= 8 terms), FP32 accumulation",
                    "l2": f"inputs larger than L2: {wl.expert_bytes_per_step() / 1e6:.1f} MB of expert weights "
                          f"per step from a {wl.L * wl.E * wl.bb / 1e9:.2f} GB pool",
-                   "launch": f"CUDA graphs of {win} steps, PDL between kernels"},
-        "expert_hbm_gbs_step": round(step_gbs, 1),
-        "expert_hbm_frac_step": round(step_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "moe_layer_forward GEMV path: decode_gateup_kernel (routing inside) + decode_down_kernel (overlapped via PDL), one layer",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": DECODE_LAYER_DRAM_BYTES if wl.name == "olmoe_decode" else None,
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the two kernels of "
-                                       "one layer call (profiles/decode_olmoe_streamed_kernels.md)",
-                     "bytes_per_launch": bytes_per_launch, "avg_launch_us": round(fwd_avg_s * 1e6, 3),
-                     "peak_source": peak_src,
-                     "timing": f"external event-record graph nodes around each call, "
-                               f"{n_kt} steps x {wl.L} layers, graph replay"},
+                   "launch": f"CUDA graphs of <= {win} steps, one kernel per layer, PDL between layers"},
+        "blocks": block_stats(block_ms, [n for _, n in split_blocks(K)], wl.T),
+        "roofline": decode_roofline(wl, ms / K, peak, peak_src),
         "gpu_launches": wl.launches_per_step() * K,
         "clocks": clocks,
     }
@@ -378,6 +327,36 @@ def run_ours(args, world, rank, local, name="olmoe_decode"):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
+
+
+def block_stats(block_ms, block_steps, T):
+    """Rate of each timed block and the spread between blocks ((max - min) /
+    pooled rate), as the pages report their decode blocks."""
+    rates = [n * T / (ms / 1e3) for ms, n in zip(block_ms, block_steps)]
+    pooled = sum(block_steps) * T / (sum(block_ms) / 1e3)
+    return {"n": len(rates), "tokens_per_s": [round(r, 2) for r in rates],
+            "spread": round((max(rates) - min(rates)) / pooled, 5) if rates else None,
+            "pooled_tokens_per_s": round(pooled, 2)}
+
+
+def decode_roofline(wl, step_ms, peak, peak_src):
+    """Roofline of the decode kernel (one launch = one layer): the expert
+    bytes a launch reads (k blocks at one token) over the launch's average
+    duration in the timed region, i.e. the step time over the layers (the
+    launches run back to back on one stream, so L x launch time = step time)."""
+    bytes_per_launch = wl.expert_bytes_per_step() / wl.L
+    launch_s = step_ms / 1e3 / wl.L
+    assert wl.L * launch_s * 1e3 <= step_ms * (1 + 1e-9)
+    achieved = bytes_per_launch / launch_s / 1e9
+    traffic = DECODE_DRAM_BYTES.get(wl.name)
+    return {"bound": "hbm", "kernel": "decode_stream_kernel (routing, gate/up + SwiGLU, down + combine; one layer)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the current "
+                              "kernel on this workload" if traffic else "not captured for this kernel build",
+            "bytes_per_launch": int(bytes_per_launch), "avg_launch_us": round(launch_s * 1e6, 3),
+            "peak_source": peak_src,
+            "timing": "CUDA events over the timed region on the launching stream; launch time = step time / layers"}
 
 
 def base_line(metric, value, unit, world, K, W, ms, config, hib=True):
@@ -671,13 +650,17 @@ def run_partial(args, world, rank):
 def run_fanout(args, world, rank, T):
     """Large fan-out stack: 48 layers x 512 experts (hidden 2048, inter 512,
     top-10 renormalised, Zipf(1.1) popularity), ~41 GB of INT4 experts all
-    resident; T tokens per step through all 48 layers."""
+    resident; T tokens per step through all 48 layers on the path
+    MOE_PATH_AUTO picks (the streamed decode kernel up to 16 tokens, the
+    grouped tensor-core path above). The roofline bytes of a step are the
+    distinct experts each layer reads, counted from the routing of every
+    timed step."""
     from int4_routed_expert_moe_gb300 import moe
     wl = synth.WORKLOADS["large_fanout"]
     L, H, I, E, k, g = wl["L"], wl["H"], wl["I"], wl["E"], wl["k"], wl["g"]
     shape = (H, I, g)
-    K = args.steps or 64
-    W = args.warmup if args.warmup is not None else 8
+    K = args.steps or (24 if T >= 256 else 96)
+    W = max(3, args.warmup if args.warmup is not None else 8)
     dev = torch.device("cuda")
     bb = moe.moe_expert_block_bytes(shape)
     seed = synth.BASE_SEED + 5 + rank
@@ -689,50 +672,72 @@ def run_fanout(args, world, rank, T):
     gen.manual_seed(seed)
     base = (-wl["alpha"] * torch.log(torch.from_numpy(ranks).float().to(dev)))[:, None, :]
     x0 = torch.randn((n, T, H), generator=gen, device=dev).half()
-    ids = torch.empty((L, T, k), dtype=torch.int32, device=dev)
+    ids = torch.empty((n, L, T, k), dtype=torch.int32, device=dev)  # every step's routing is kept
     w = torch.empty((L, T, k), dtype=torch.float32, device=dev)
     y = torch.empty((L, T, H), dtype=torch.float16, device=dev)
-    path = moe.MOE_PATH_GEMV
+    path = moe.MOE_PATH_AUTO
     ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, T, k, E, path), dtype=torch.uint8, device=dev)
-    n_lg = n + 4
-    logits = torch.empty((n_lg, L, T, E), device=dev)  # drawn before the timed region
-    for s in range(n_lg):
+    logits = torch.empty((n, L, T, E), device=dev)  # drawn before the timed region
+    for s in range(n):
         u = torch.rand((L, T, E), generator=gen, device=dev).clamp_min(1e-20)
         logits[s] = base - torch.log(-torch.log(u))
-    uniq = []
 
-    def step(s, count=False):
+    def step(s):
         for l in range(L):
-            x = x0[s % n] if l == 0 else y[l - 1]
-            moe.moe_layer_forward(shape, x, logits[s, l], k, wl["renorm"], ids[l], w[l],
+            x = x0[s] if l == 0 else y[l - 1]
+            moe.moe_layer_forward(shape, x, logits[s, l], k, wl["renorm"], ids[s, l], w[l],
                                   pool[l * E:(l + 1) * E], slot_of, E, None, y[l], ws, path)
-        if count:
-            uniq.append(sum(len(torch.unique(ids[l])) for l in range(L)))
 
-    for s in range(W):
-        step(s)
+    step(0)
     torch.cuda.synchronize()
-    barrier(world)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for s in range(W, W + K):
-        step(s)
-    ev1.record()
+    stream = torch.cuda.current_stream()
+
+    def capture(steps):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for s in steps:
+                step(s)
+        return gr
+
+    warm = [capture(range(W))]
+    blocks = [[capture(range(W + b0, W + b0 + nb))] for b0, nb in split_blocks(K)]
     torch.cuda.synchronize()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    for s in range(4):  # distinct experts per step, counted outside the timed region
-        step(W + s, count=True)
-    u_mean = float(np.mean(uniq))
+    sampler = ClockSampler(smi_index())
+    time.sleep(0.2)
+    ms, block_ms, t_host0, t_host1 = timed_blocks(blocks, warm, world, stream)
+    rows = sampler.stop()
+    clocks = ClockSampler.summarize(rows, t_host0, t_host1)
+    assert moe.moe_workspace_flags(ws) == 0
+    ms_max = max_over_ranks(ms, world)
+    # Distinct experts read per layer, from the timed steps' routing.
+    idc = ids[W:].reshape(K, L, T * k).cpu().numpy()
+    uniq = np.array([[len(np.unique(idc[s, l][idc[s, l] >= 0])) for l in range(L)] for s in range(K)])
+    bytes_step = float(uniq.sum(axis=1).mean()) * bb
     peak, peak_src = measured_peaks()
-    gbs = u_mean * bb * K / (ms / 1e3) / 1e9
-    out = base_line(METRIC, K * T * world / (ms / 1e3), "tokens/s", world, K, W, ms,
+    step_s = ms / 1e3 / K
+    achieved = bytes_step / step_s / 1e9
+    streamed = T <= 16
+    launch_s = step_s / L
+    out = base_line(METRIC, K * T * world / (ms_max / 1e3), "tokens/s", world, K, W, ms_max,
                     {"workload": f"large_fanout_b{T}", "layers": L, "hidden": H, "experts": E, "top_k": k,
                      "inter": I, "group": g, "tokens_per_step": T, "zipf_alpha": wl["alpha"],
-                     "launch": "eager moe_layer_forward per layer",
-                     "l2": "inputs larger than L2: 41 GB pool"})
-    out["expert_hbm_gbs_step"] = round(gbs, 1)
-    out["expert_hbm_frac_step"] = round(gbs / peak, 4)
-    out["unique_experts_per_step"] = round(u_mean, 1)
+                     "path": "streamed decode kernel" if streamed else "grouped tensor-core path",
+                     "launch": f"CUDA graphs (one per block of steps), {L} moe_layer_forward calls per step",
+                     "l2": f"inputs larger than L2: {L * E * bb / 1e9:.1f} GB pool"})
+    out["blocks"] = block_stats(block_ms, [nb for _, nb in split_blocks(K)], T)
+    out["unique_experts_per_layer"] = round(float(uniq.mean()), 2)
+    out["roofline"] = {"bound": "hbm",
+                       "kernel": ("decode_stream_kernel, one layer" if streamed else
+                                  "moe_layer_forward grouped path (route, sort, gather, 2 GEMMs, combine), one layer"),
+                       "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                       "frac": round(achieved / peak, 4), "traffic": None,
+                       "traffic_source": "not captured for this kernel build",
+                       "bytes_per_launch": int(bytes_step / L), "avg_launch_us": round(launch_s * 1e6, 3),
+                       "bytes_rule": "distinct experts of each layer x expert block bytes, from the timed steps' ids",
+                       "peak_source": peak_src,
+                       "timing": "CUDA events over the timed region; layer time = step time / layers"}
+    out["gpu_launches"] = L * K * (1 if streamed else 7)
+    out["clocks"] = clocks
     return out
 
 
@@ -799,21 +804,11 @@ def run_prefill(args, world, rank):
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     assert moe.moe_workspace_flags(ws) == 0
 
-    # Per-layer call durations (external event nodes around each call).
-    n_kt = min(K, 4)
-    ev = ExtEvents(2 * n_kt * L)
-    g_kt = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_kt):
-        st = torch.cuda.current_stream().cuda_stream
-        for i in range(n_kt):
-            for l in range(L):
-                ev.record(2 * (i * L + l), st)
-                layer(W + i, l)
-                ev.record(2 * (i * L + l) + 1, st)
-    g_kt.replay()
-    torch.cuda.synchronize()
-    layer_ms = statistics.mean(ev.elapsed(2 * j, 2 * j + 1) for j in range(n_kt * L))
-    ev.destroy()
+    # One layer call = the routing kernel and the six grouped-path kernels,
+    # back to back on one stream: its average duration is the step time over
+    # the layers (an upper bound of the dominant GEMM kernel's own time, so
+    # the fraction below is a lower bound for that kernel).
+    layer_ms = ms / K / L
 
     # Shared FFN leg.
     sw = {kk: torch.from_numpy(v).to(dev) for kk, v in synth.shared_weights(seed, H, Is).items()}
@@ -857,12 +852,11 @@ def run_prefill(args, world, rank):
                        "achieved": round(achieved, 1), "peak": peak_t, "unit": "TFLOP/s",
                        "frac": round(achieved / peak_t, 4), "traffic": PREFILL_GEMM_DRAM_BYTES,
                        "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and "
-                                         "down GEMM kernels of one layer call (the small kernels not included; "
-                                         "profiles/prefill_olmoe_grouped_and_shared_kernels.md)",
+                                         "down GEMM kernels of one layer call (the small kernels not included)",
                        "flops_per_launch": flops_layer, "avg_launch_us": round(layer_ms * 1e3, 2),
                        "peak_source": peak_t_src,
                        "weight_gbs": round(weight_gbs, 1), "weight_hbm_frac": round(weight_gbs / peak_h, 4),
-                       "timing": f"external event-record graph nodes around each call, {n_kt} steps x {L} layers"}
+                       "timing": "CUDA events over the timed region; layer time = step time / layers"}
     out["shared_ffn"] = {"tokens": Ts, "hidden": H, "inter": Is, "us_per_call": round(sh_s * 1e6, 2),
                          "tflops": round(sh_flops / sh_s / 1e12, 1),
                          "frac_of_tensor_peak": round(sh_flops / sh_s / 1e12 / peak_t, 4)}
@@ -922,32 +916,87 @@ def oracle_layer_sample(wl, s, l, x16, experts_from_device):
     return moe_oracle.moe_layer(x16, lg, experts_from_device, wl.k, wl.renorm, wl.g)
 
 
-def cpu_baseline(wl, budget_s=12.0):
-    """The oracle as it stands, on host cores, on a bounded sample: one decode
-    token through as many of the 16 layers as fit in ~budget_s (at least one),
-    fresh N(0,1) activations per layer. Expert arrays are read from the
-    device pool before the clock starts."""
+def physical_cores():
+    """Physical cores available to this process: distinct SMT sibling sets of
+    the allowed CPUs (each CPU its own core where the kernel gives no
+    topology)."""
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+    except AttributeError:
+        cpus = list(range(os.cpu_count() or 1))
+    cores = set()
+    for c in cpus:
+        try:
+            with open(f"/sys/devices/system/cpu/cpu{c}/topology/thread_siblings_list") as f:
+                cores.add(f.read().strip())
+        except OSError:
+            cores.add(str(c))
+    return max(1, len(cores))
+
+
+def _oracle_expert_task(args):
+    """One routed expert of one token through the oracle (dequantise the
+    block's arrays in FP64, SwiGLU FFN, weighted by the routing weight):
+    the unit of the parallel CPU-baseline leg, run in worker processes."""
+    from oracle import moe_oracle
+    arrs, group, x, w = args
+    return w * moe_oracle.expert_ffn(x, *moe_oracle.dequantize_expert(arrs, group))
+
+
+def cpu_baseline(wl, budget_s=10.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    decode workload, at 1 thread and at the physical core count:
+    * 1 thread: one decode token through as many of the layers as fit in
+      ~budget_s (at least one): routing, FP64 dequantisation of each chosen
+      expert, SwiGLU FFN, weighted sum;
+    * all physical cores: the same per-expert work of as many (token, layer)
+      pairs as fit in ~budget_s, one expert per task on a pool of worker
+      processes (spawned; the oracle is unchanged, only its per-expert calls
+      run side by side).
+    Expert arrays are read out of the device pool before the clock starts."""
+    import multiprocessing as mp
     from oracle import moe_oracle
     t_total, layers = 0.0, 0
     s = 0
+    samples = []
     for l in range(wl.L):
         lg = wl.logits[s, l].cpu().numpy()
-        ids, _ = moe_oracle.route(lg, wl.k, wl.renorm)
+        ids, wts = moe_oracle.route(lg, wl.k, wl.renorm)
         pool = wl.layer_pool(l)
-        experts = {int(e): synth.arrays_from_block(pool[int(e)].cpu().numpy(), *wl.shape)
-                   for e in ids.reshape(-1)}
+        blocks = {int(e): pool[int(e)].cpu().numpy() for e in ids.reshape(-1)}
+        experts = {e: synth.arrays_from_block(b, *wl.shape) for e, b in blocks.items()}
         x16 = synth.activations(7, l, wl.T, wl.H)
+        samples.append((x16, ids, wts, experts))
         t0 = time.perf_counter()
         moe_oracle.moe_layer(x16, lg, experts, wl.k, wl.renorm, wl.g)
         t_total += time.perf_counter() - t0
         layers += 1
         if t_total >= budget_s:
             break
-    tokens = wl.T * layers / wl.L
-    return {"value": round(tokens / t_total, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    one = wl.T * layers / wl.L / t_total
+    ncores = physical_cores()
+    tasks = []
+    for x16, ids, wts, experts in samples:
+        for j in range(wl.k):
+            e = int(ids[0, j])
+            tasks.append((experts[e], wl.g, x16[0].astype(np.float64), float(wts[0, j])))
+    per_task = t_total / max(1, len(tasks))
+    n_tasks = min(len(tasks) * 8, max(ncores, int(budget_s * ncores / max(per_task, 1e-6))))
+    work = [tasks[i % len(tasks)] for i in range(n_tasks)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(ncores) as pool_p:
+        pool_p.map(_oracle_expert_task, work[:ncores])  # start-up outside the clock
+        t0 = time.perf_counter()
+        pool_p.map(_oracle_expert_task, work, chunksize=1)
+        t_par = time.perf_counter() - t0
+    many = n_tasks / (wl.L * wl.k) / t_par
+    return {"value": round(one, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"1 decode token through {layers} of {wl.L} layers ({layers * wl.k} experts "
                       f"dequantised in FP64), {t_total:.1f} s single-threaded",
-            "cpu": cpu_model()}
+            "all_cores": {"value": round(many, 5), "unit": "tokens/s", "cores": ncores,
+                          "sample": f"{n_tasks} routed experts (= {n_tasks / (wl.L * wl.k):.2f} decode tokens) "
+                                    f"on {ncores} worker processes, {t_par:.1f} s"},
+            "nproc": os.cpu_count(), "cpu": cpu_model()}
 
 
 def device_info():

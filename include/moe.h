@@ -167,22 +167,28 @@ int moe_token_sort(const int32_t* ids, int T, int k, int E, int32_t* offsets,
  * y         device fp16 [T][H] out (round to nearest even)
  * workspace device, >= moe_forward_workspace_bytes(...) bytes, 256-aligned,
  *           zero-filled before its first use (calls leave it reusable: the
- *           synchronisation counters inside are reset by the call itself).
- *           Calls sharing a workspace must be ordered (same stream).
+ *           synchronisation counters inside are reset by the call itself;
+ *           after a call that set bit 2, zero it again). Calls sharing a
+ *           workspace must be ordered (same stream). The GEMV path's blocks
+ *           wait on each other (bounded) and so must all be resident at
+ *           once: one block per SM, as the library launches them.
  *           Its first 4 bytes are a sticky error word: bit 0 = an id mapped
  *           to a slot outside [0, n_slots) (that pair contributed 0); bit 1 =
  *           an id outside [-1, E); bit 2 = a bounded device wait expired (the
  *           result is not valid). Read it with moe_workspace_flags.
- * path      MOE_PATH_AUTO: GEMV up to 256 (token, choice) pairs, else grouped.
- *           MOE_PATH_GEMV: decode dequant-GEMV. Two streaming kernels (one
- *             block per SM each) chained with programmatic dependent launch:
- *             the first streams each block's rows of the chosen experts'
- *             gate/up sections through shared memory with bulk async copies
- *             and writes h = silu(gate) * up per pair; the second, started
- *             while the first runs, prefetches the down rows, then computes
- *             the down projection and the top-k combine. Falls back to the
- *             unfused kernels when its shared memory does not fit (H > 4096
- *             or I > 2048).
+ * path      MOE_PATH_AUTO: GEMV up to 16 tokens and 256 (token, choice) pairs,
+ *             else grouped.
+ *           MOE_PATH_GEMV: decode dequant-GEMV. One streaming kernel, one
+ *             block per SM: the (token, choice) pairs are grouped by expert
+ *             so every distinct expert is read once per call; each block
+ *             streams its rows of every chosen expert's gate/up and down
+ *             sections through shared memory with bulk async copies (both
+ *             requested up front), writes h = silu(gate) * up for its rows,
+ *             exchanges h with the other blocks through the workspace, and
+ *             forms its output rows of the down projection and the top-k
+ *             combine. Falls back to the unfused kernels beyond its limits
+ *             (H > 4096, I > 2048, more than 16 tokens or 256 pairs,
+ *             E > 1024, or shared memory).
  *           MOE_PATH_GROUPED: token-sorted tensor-core grouped GEMM: pairs
  *             sorted by expert, tiles of up to 128 pairs; tcgen05 MMAs with
  *             the expert rows as the 128-row operand (expanded from INT4 to
@@ -245,29 +251,41 @@ int moe_layer_forward(const moe_expert_shape* shape, const void* x, const float*
                       void* workspace, size_t workspace_bytes, int path, void* stream);
 /* ---- routed layer without any device allocation --------------------------
  * The pages have no counterpart to this call; it exists for callers that
- * cannot allocate device memory: code running inside another component's
- * CUDA stream capture (cudaMalloc is not permitted during capture), plugins
- * and serving runtimes whose host framework owns every device allocation,
- * and deployments with a fixed, pre-planned memory budget.
+ * cannot allocate device memory: plugins and serving runtimes whose host
+ * framework owns every device allocation and forbids extra ones, deployments
+ * with a fixed, pre-planned memory budget, and code running inside another
+ * component's CUDA stream capture, where cudaMalloc is not permitted.
  * Same arguments and result as moe_layer_forward on the MOE_PATH_GEMV path,
- * minus the workspace: the scratch it needs (an error word and the FP16
- * SwiGLU intermediate of every (token, choice) pair) lives in a 1 MiB array
- * compiled into the library, held by every GPU that loads the library until
- * the process exits. The call allocates nothing (no cudaMalloc/cudaFree).
- * Limits: T*k*inter*2 bytes plus a header of at most 1.3 KiB <= 1 MiB, else
- * MOE_ERR_CAPACITY; H <= 4096 and inter <= 2048 (the streamed decode
- * kernels), else MOE_ERR_UNSUPPORTED.
+ * minus the workspace: the scratch it needs (a header with the error word and
+ * the kernel's counters, then the FP16 SwiGLU intermediate of every
+ * (token, choice) pair) lives in a 1 MiB array compiled into the library,
+ * held by every GPU that loads the library until the process exits. The call
+ * allocates nothing (no cudaMalloc/cudaFree); it clears the header with one
+ * cudaMemsetAsync on `stream` before the kernel.
+ * Limits: 256 + ceil(4*T*k / 256)*256 + T*k*inter*2 bytes <= 1 MiB, else
+ * MOE_ERR_CAPACITY (at inter 1024 about 500 pairs; the kernel's own limits
+ * below come first); H <= 4096, inter <= 2048, T <= 16, T*k <= 256 and
+ * E <= 1024 (the streamed decode kernel), else MOE_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture. Every call shares the one array: calls that overlap on
- * the GPU (different streams, or other threads) race and corrupt each
- * other's results; order them on one stream. Device-side error bits are not
- * reported (unusable ids contribute nothing, as in moe_expert_forward).
+ * stream capture. The cached address belongs to the device's current
+ * context: after cudaDeviceReset the library must be reloaded (or the process
+ * restarted) before this call is used again on that device.
+ * Every call shares the one array: calls that overlap on the GPU (different
+ * streams, or other threads) race and corrupt each other's results; order
+ * them on one stream. Each call keeps its error word (bit 0: an id without a
+ * slot, bit 1: an id outside [-1, E), bit 2: a bounded device wait expired and
+ * y is not valid) until the next call clears it: read it with
+ * moe_layer_forward_noalloc_flags.
  */
 int moe_layer_forward_noalloc(const moe_expert_shape* shape, const void* x, const float* logits,
                               int T, int E, int k, int renorm, int32_t* ids, float* weights,
                               const void* pool, const int32_t* slot_of, int n_slots,
                               const void* y_shared, void* y, void* stream);
+/* The error word of the last moe_layer_forward_noalloc call on the current
+ * device (bits as above) into *flags_out (host): one cudaMemcpyAsync on
+ * `stream`, then a synchronisation of `stream`. No allocation. */
+int moe_layer_forward_noalloc_flags(int32_t* flags_out, void* stream);
 /* Clear (zero) the workspace error word: enqueued on `stream`. */
 int moe_workspace_clear_flags(void* workspace, void* stream);
 /* Read the workspace error word into *flags_out: synchronises `stream`. */

@@ -12,7 +12,10 @@
 //
 // Zero points: sum_c (q_c - z) s x_c = s * (sum_c q_c x_c - z * sum_c x_c)
 // per 32-element chunk (a chunk never straddles a group since g % 32 == 0),
-// with the chunk sums of x precomputed once per block.
+// with the chunk sums of x precomputed once per block. The products q_c x_c
+// are FP16 (sums of at most 8 per lane) on the activations scaled per chunk
+// by a power of two (dot16_scaled), so no product leaves the FP16 range
+// whatever the activations' magnitude.
 #include "common.h"
 #include "device.cuh"
 #include "kernels.h"
@@ -41,54 +44,76 @@ __device__ __forceinline__ const uint8_t* expert_block(
   return nullptr;
 }
 
-// Load activations [n] (fp16, global) into shared memory in the pair order
-// of dot8_codes, and their 32-element chunk sums (FP32) into xsum. Each
-// thread takes 8 elements (one 16-byte load); the 4 threads of a chunk are
-// adjacent lanes and combine their sums with two shuffles. All threads run
-// the same number of iterations so the shuffles see full warps.
-__device__ __forceinline__ void stage_activations(const __half* __restrict__ src, int n,
-                                                  __half* xs, float* xsum) {
-  const int nb = n / 8;
-  for (int base = 0; base < nb; base += blockDim.x) {
-    const int b = base + threadIdx.x;
-    float s = 0.0f;
-    if (b < nb) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * b);
-      __half a[8];
-      *reinterpret_cast<uint4*>(a) = v;
-      store_perm8(xs + 8 * b, a);
+// Activations of one 8-element piece as the scaled pairs of dot16_scaled:
+// the 4 threads of a 32-element chunk are adjacent lanes; they combine the
+// chunk's largest magnitude and sum with shuffles, scale the chunk by the
+// power of two 2^s that keeps every product an FP16 normal (chunk_shift),
+// and the chunk keeps its FP32 sum (xsum) and the factor back 2^(24-s)
+// (xback). All threads run the same number of iterations so the shuffles
+// see full warps.
+__device__ __forceinline__ void stage_piece(const float (&v)[8], bool valid, int b, __half* xs, float* xsum,
+                                            float* xback) {
+  float s = 0.0f, amax = 0.0f;
+  if (valid) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += __half2float(a[i]);
+    for (int i = 0; i < 8; ++i) {
+      s += v[i];
+      amax = fmaxf(amax, fabsf(v[i]));
     }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    if (b < nb && (b & 3) == 0) xsum[b >> 2] = s;
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  if (valid) {
+    const int sh = chunk_shift(amax);
+    scaled_perm8(v, sh, reinterpret_cast<half2*>(xs + 8 * b));
+    if ((b & 3) == 0) {
+      xsum[b >> 2] = s;
+      xback[b >> 2] = pow2f(24 - sh);
+    }
   }
 }
 
-// Same for FP32 intermediate values: round to FP16 (the explicit rounding
-// point before the down projection), stage in pair order, and sum the
-// rounded values per 32-element chunk.
-__device__ __forceinline__ void stage_rounded(const float* __restrict__ src, int n,
-                                              __half* xs, float* xsum) {
+// Load FP16 activations [n] into shared memory as scaled pairs.
+__device__ __forceinline__ void stage_activations(const __half* __restrict__ src, int n, __half* xs,
+                                                  float* xsum, float* xback) {
   const int nb = n / 8;
   for (int base = 0; base < nb; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    float s = 0.0f;
+    float v[8];
+    if (b < nb) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(src + 8 * b);
+      const __half* a = reinterpret_cast<const __half*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __half2float(a[i]);
+    }
+    stage_piece(v, b < nb, b, xs, xsum, xback);
+  }
+}
+
+// Same for FP32 intermediate values: round to FP16 first (the explicit
+// rounding point before the down projection).
+__device__ __forceinline__ void stage_rounded(const float* __restrict__ src, int n, __half* xs, float* xsum,
+                                              float* xback) {
+  const int nb = n / 8;
+  for (int base = 0; base < nb; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    float v[8];
     if (b < nb) {
       const float4 v0 = *reinterpret_cast<const float4*>(src + 8 * b);
       const float4 v1 = *reinterpret_cast<const float4*>(src + 8 * b + 4);
-      __half a[8] = {__float2half_rn(v0.x), __float2half_rn(v0.y), __float2half_rn(v0.z),
-                     __float2half_rn(v0.w), __float2half_rn(v1.x), __float2half_rn(v1.y),
-                     __float2half_rn(v1.z), __float2half_rn(v1.w)};
-      store_perm8(xs + 8 * b, a);
+      const float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += __half2float(a[i]);
+      for (int i = 0; i < 8; ++i) v[i] = __half2float(__float2half_rn(f[i]));
     }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    if (b < nb && (b & 3) == 0) xsum[b >> 2] = s;
+    stage_piece(v, b < nb, b, xs, xsum, xback);
   }
+}
+
+// Dot of the 32 codes of a 16-byte chunk with the chunk's scaled pairs.
+__device__ __forceinline__ float dot32_scaled(const uint4& w, const half2* xp, float back) {
+  return (dot16_scaled(w.x, w.y, xp) + dot16_scaled(w.z, w.w, xp + 8)) * back;
 }
 
 // grid (ceil(I / kWarps), P); one warp per row n, gate and up rows together.
@@ -102,12 +127,13 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
   extern __shared__ __align__(16) uint8_t smem[];
   __half* xs = reinterpret_cast<__half*>(smem);
   float* xsum = reinterpret_cast<float*>(smem + (size_t)H * 2);
+  float* xback = xsum + H / 32;
   griddep_wait();
   griddep_launch_dependents();
   const int p = blockIdx.y;
   const int t = p / k;
   const int e = ids[p];
-  stage_activations(x + (size_t)t * H, H, xs, xsum);
+  stage_activations(x + (size_t)t * H, H, xs, xsum, xback);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * kWarps + warp;
@@ -139,8 +165,8 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_gemv_kernel(
     const int c = lane + 32 * it;
     if (c < nch) {
       const half2* xp = reinterpret_cast<const half2*>(xs + 32 * c);
-      const float dg = dot32_codes(wg[it], xp);
-      const float du = dot32_codes(wu[it], xp);
+      const float dg = dot32_scaled(wg[it], xp, xback[c]);
+      const float du = dot32_scaled(wu[it], xp, xback[c]);
       const int gi = (32 * c) / g;
       const float xsm = xsum[c];
       ag += __half2float(sz[4 * gi + 0]) * (dg - __half2float(sz[4 * gi + 1]) * xsm);
@@ -165,7 +191,8 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
   extern __shared__ __align__(16) uint8_t smem[];
   __half* hs = reinterpret_cast<__half*>(smem);                       // [k][I]
   float* hsum = reinterpret_cast<float*>(smem + (size_t)k * I * 2);   // [k][I/32]
-  const uint8_t** blks = reinterpret_cast<const uint8_t**>(hsum + (size_t)k * (I / 32));  // [k]
+  float* hback = hsum + (size_t)k * (I / 32);                         // [k][I/32]
+  const uint8_t** blks = reinterpret_cast<const uint8_t**>(hback + (size_t)k * (I / 32));  // [k]
   float* wj = reinterpret_cast<float*>(blks + k);                     // [k]
   const int t = blockIdx.y;
   griddep_wait();
@@ -177,7 +204,7 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
     wj[threadIdx.x] = wts[p];
   }
   // h of the k pairs of token t: [k][I] floats, contiguous.
-  stage_rounded(hbuf + (size_t)t * k * I, k * I, hs, hsum);
+  stage_rounded(hbuf + (size_t)t * k * I, k * I, hs, hsum, hback);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * kWarps + warp;
@@ -213,7 +240,7 @@ __global__ void __launch_bounds__(kWarps * 32) down_gemv_kernel(
         const float s = __half2float(dsz[2 * gi]);
         const float z = __half2float(dsz[2 * gi + 1]);
         const half2* hp = reinterpret_cast<const half2*>(hs + (size_t)j * I + 32 * c);
-        const float d = dot32_codes(w[u], hp);
+        const float d = dot32_scaled(w[u], hp, hback[j * nch + c]);
         acc += wj[j] * (s * (d - z * hsum[j * nch + c]));
       }
     }
@@ -253,8 +280,8 @@ int gemv_forward(const ForwardArgs& a) {
   const int H = a.H, I = a.I, g = a.g, T = a.T, k = a.k;
   float* hbuf = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + ws_scratch_offset(T * k));
   int32_t* flags = static_cast<int32_t*>(a.ws);
-  const size_t smem_a = (size_t)H * 2 + (size_t)(H / 32) * 4;
-  const size_t smem_b = (size_t)k * I * 2 + (size_t)k * (I / 32) * 4 + (size_t)k * sizeof(void*) + (size_t)k * 4;
+  const size_t smem_a = (size_t)H * 2 + (size_t)(H / 32) * 8;
+  const size_t smem_b = (size_t)k * I * 2 + (size_t)k * (I / 32) * 8 + (size_t)k * sizeof(void*) + (size_t)k * 4;
   if (smem_b > 200 * 1024)
     return fail(MOE_ERR_UNSUPPORTED, "GEMV path: k*I = %d too large for one block's shared memory", k * I);
   const dim3 grid_a((I + kWarps - 1) / kWarps, T * k);

@@ -1,35 +1,41 @@
-// Decode path: two streaming kernels per routed layer, chained with
-// programmatic dependent launch.
+// Decode path: one streaming kernel per routed layer.
 //
 // "Horizon RunMap -- Prévia Técnica", "03 / Arquitetura" and
 // "08 / Comportamento do modelo": the expert kernel reads compact INT4 codes
 // and FP16 scales, converts them inside the kernel (no expanded expert is
 // kept) and works with FP16 activations and FP32 accumulation.
 //
-// Both kernels run one block per SM (G blocks). Block c owns gate/up rows
-// n in [c*I/G, (c+1)*I/G) of every (token, choice) pair p and output rows
-// m in [c*H/G, (c+1)*H/G) of y. In each kernel a producer warp streams the
-// block's slice of expert ids[p]'s block into a ring of shared-memory stages
-// with bulk async copies (cp.async.bulk, completion counted on mbarriers);
-// for one decode token the ring holds every pair, so the whole slice is
-// requested at once and HBM sees one deep stream.
-//   * Routing (optional, moe_layer_forward): each block ranks the router
-//     logits itself -- expert e is chosen at position r when exactly r
-//     experts precede it in (logit desc, index asc) order -- and computes the
-//     softmax weights with fixed-order reductions, so every block of both
-//     kernels derives identical ids and weights without waiting for another.
-//   * decode_gateup_kernel: h[p][n] = silu(W_g x_t)[n] * (W_u x_t)[n],
-//     rounded to FP16 (the explicit rounding point) into the workspace.
-//   * decode_down_kernel: launched while the first kernel runs; before
-//     waiting on it (griddepcontrol.wait) it already requests its down-row
-//     slices (the ids are final), so the down weights stream concurrently
-//     with the gate/up weights. After the wait it reads h and computes
-//     y[t][m] = sum_j w[t][j] * (W_d h[t*k+j])[m] (+ y_shared), combining the
-//     k pairs of a token in j order (deterministic).
-// The kernel boundary is the only synchronisation: nothing spins on flags
-// written by other blocks. mbarrier waits are bounded; on expiry bit 2 of the
-// workspace error word is set.
+// One block per SM (G blocks). Block c owns gate/up rows n in
+// [c*I/G, (c+1)*I/G) and output rows m in [c*H/G, (c+1)*H/G) of every expert
+// the step uses. Per call:
+//   1. Routing (moe_layer_forward) inside every block: one warp per token
+//      picks the top-k by (logit desc, index asc) and forms the softmax
+//      weights with the same fixed-order reductions as moe_route, so all
+//      blocks hold identical ids and weights. The token activations are
+//      staged in shared memory meanwhile.
+//   2. The (token, choice) pairs are grouped by expert (ascending expert id,
+//      pairs in ascending order inside an expert): a "unit" is one distinct
+//      expert, read once per call however many tokens chose it.
+//   3. A producer lane streams the block's rows of every unit into two rings
+//      of shared-memory stages with bulk async copies (cp.async.bulk,
+//      completion counted on mbarriers): the gate/up rows first, the down
+//      rows as soon as the first gate/up copies are out, so the down weights
+//      stream while the gate/up rows are computed.
+//   4. Compute warps form h = silu(W_g x) * (W_u x) for their rows of every
+//      pair of a unit, round it to FP16 (the explicit rounding point) into
+//      the workspace, and count the unit as done on a per-unit counter in
+//      global memory (release).
+//   5. A down item of unit u waits (acquire, bounded) until every block has
+//      counted u, reads the complete h of each pair of u through L2 and
+//      forms the block's output rows of W_d h per pair.
+//   6. y[t][m] = sum_j w[t][j] * (W_d h[t*k+j])[m] (+ y_shared), the k pairs
+//      of a token combined in j order (deterministic).
+// The last block to finish resets the counters, so the workspace is reusable
+// by the next call on the same stream. All waits are bounded; on expiry bit 2
+// of the workspace error word is set and the block stops waiting.
 #include <algorithm>
+#include <climits>
+#include <mutex>
 
 #include "common.h"
 #include "device.cuh"
@@ -38,23 +44,18 @@
 namespace moe {
 namespace {
 
-// Warp counts: registers are granted to a block in units of four warps, so
-// 16 + 12 warps of the two kernels fit one SM together (64K registers).
-constexpr int kWarps = 8;                   // compute warps of the down kernel
+constexpr int kWarps = 16;                    // compute warps
 constexpr int kThreads = (kWarps + 1) * 32;   // + one producer warp
-constexpr int kGateWarps = 15;              // compute warps of the gate/up kernel
-constexpr int kGateThreads = (kGateWarps + 1) * 32;
-constexpr int kSub0 = 8;                    // gate/up ring: warps 0..7 take even pairs, 8..14 odd pairs
-constexpr int kPairsPerIter = 2;
-// Stage ownership when the ring wraps: a stage must always be drained by the
-// same warp (down) or sub-group (gate/up) so that no consumer waits on a
-// phase two fills ahead (an mbarrier parity test cannot tell those apart).
-// With an even stage count, stage q % S of pair q is drained by sub-group
-// q & 1 (gate/up) and by warp (q % S) % kWarps (down), each in increasing q.
-// When every pair has its own stage (P <= S, one decode token), each stage
-// is filled once and never released, and the gate/up warps share pairs.
-constexpr int kMaxStages = 8;
-constexpr unsigned kMbarTries = 50000;     // bounded mbarrier waits (~1 s)
+constexpr int kProducer = kWarps;
+constexpr int kMaxT = 16;                     // tokens per call
+constexpr int kMaxP = 256;                    // (token, choice) pairs per call
+constexpr int kMaxE = 1024;                   // experts (in-block tables)
+constexpr int kMaxRing = 16;                  // stages per ring
+constexpr int kDownRows = 8;                  // rows per down work item
+constexpr unsigned kMbarTries = 50000;        // ~1 s (20 us suspend hint per try)
+constexpr unsigned kIdleTries = 16000000;     // ~1 s of idle producer loop iterations
+constexpr unsigned kSpinTries = 2000000;      // ~1 s of counter polls (one L2 round trip each)
+constexpr int kCntBase = 64;                  // workspace word of unit counter 0
 
 // ---- PTX wrappers: mbarrier, bulk copies, acquire/release -----------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -71,7 +72,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // try_wait with a suspend-time hint: the thread sleeps until the phase
-// completes or about 20 us pass, instead of spinning on issue slots.
+// completes or about 20 us pass.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -80,41 +81,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(20000u) : "memory");
   return ok != 0;
 }
-// Bounded wait on an mbarrier phase; returns false on expiry (~1 s at most).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (unsigned i = 0; i < kMbarTries; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-  }
-  return false;
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-
-// ---- shared-memory stages -------------------------------------------------
-__host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
-
-// One stage = the block's rows of one pair's expert (rmax rows at most).
-struct Stage {
-  uint32_t bytes;
-};
-__host__ __device__ inline Stage stage_of(int rmax, uint32_t row_bytes) {
-  Stage st;
-  st.bytes = align16((uint32_t)rmax * row_bytes);
-  return st;
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// 32 FP16 values (64 bytes, read through L2) as the scaled pairs of
-// dot16_scaled; returns their sum, and 2^(24-s) in back.
+__host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
+
+// 32 FP16 values (64 bytes, read through L2, or from shared memory when
+// SMEM) as the scaled pairs of dot16_scaled; returns their sum, and
+// 2^(24-s) in back.
+template <bool SMEM>
 __device__ __forceinline__ float load_scaled_chunk(const __half* src, half2 (&xp)[16], float& back) {
   float v[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(src + 8 * q) : "memory");
+    if constexpr (SMEM) {
+      r = *reinterpret_cast<const uint4*>(src + 8 * q);
+    } else {
+      asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(src + 8 * q) : "memory");
+    }
     const __half* e = reinterpret_cast<const __half*>(&r);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[8 * q + i] = __half2float(e[i]);
@@ -132,13 +138,13 @@ __device__ __forceinline__ float load_scaled_chunk(const __half* src, half2 (&xp
   return sum;
 }
 
-struct DecodeParams {
+struct StreamParams {
   const __half* x;
-  const float* logits;  // [T][E] when the kernels route themselves, else NULL
+  const float* logits;  // [T][E] when the kernel routes itself, else NULL
   int renorm;
   const int32_t* ids;   // [T][k] given ids (logits == NULL)
   const float* wts;     // [T][k] given weights (logits == NULL)
-  int32_t* ids_out;     // routed ids / weights written by block 0 (nullable)
+  int32_t* ids_out;     // routing written by block 0 (nullable)
   float* wts_out;
   const uint8_t* pool;
   unsigned long long block_bytes;
@@ -146,604 +152,946 @@ struct DecodeParams {
   const int32_t* slot_of;
   const __half* y_shared;
   __half* y;
-  int32_t* flags;  // workspace error word
-  __half* hbuf;    // workspace: h [P][I]
-  int H, I, g, T, k, E, n_slots, P, G, stages;
-  Stage st;
-  uint32_t part_off, route_off, bar_off, blk_off;  // shared-memory carve-up after the stages
+  int32_t* ws;          // workspace words: [0] error, [1] done, [kCntBase + u] unit counters
+  __half* hbuf;         // workspace: h [P][I]
+  int H, I, g, T, k, E, n_slots, P, G;
+  int Sg, Sd;           // stages of the gate/up and down rings
+  uint32_t sg, sd;      // bytes of one stage
+  int rgu, rdn;         // largest row counts of a block
+  int fast1;            // one token routed in the block, every unit with its own stages
+  // shared-memory carve-up (byte offsets)
+  uint32_t o_ring_d, o_x, o_part, o_hst, o_hsm, o_small, o_bar, smem;
 };
 
-// Per-block routing state in shared memory.
-struct RouteSmem {
-  int32_t* ids;    // [P]
-  float* w;        // [P]
-  float* exsel;    // [P]   exp(logit - max) of each chosen expert
-  float* sall;     // [T]   softmax denominator per token
-  float* red;      // [ceil(E/32)] sums of exp over 32-expert slices
-  int32_t* bad;    // [4]:  any NaN/+inf, count of -inf, max key
-  float* lg;       // [E]   logits of the token being routed
-  int32_t* rank;   // [E]
-  int32_t* slot;   // [E]   copy of slot_of (when slot_tab)
+// Small per-block tables (in shared memory at o_small).
+struct Tables {
+  const uint8_t** blk;  // [P] expert block of each unit
+  int32_t* ids;         // [P]
+  float* w;             // [P]
+  int32_t* punit;       // [P] unit of each pair, -1 if it contributes nothing
+  int32_t* uexp;        // [P] expert of each unit
+  int32_t* uoff;        // [P+1] first sorted pair of each unit
+  int32_t* upairs;      // [P] pairs sorted by unit
+  int32_t* udone;       // [P] gate/up items finished per unit (this block)
+  int32_t* ecnt;        // [E] pairs per expert, then first sorted position
+  int32_t* eunit;       // [E] unit of each expert
+  int32_t* eslot;       // [E] copy of slot_of
+  float* lg;            // [E] logits of the token routed by the producer warp
+  int32_t* misc;        // [0] units, [1] abort, [3] token without a routing, [4] -inf logits,
+                        // [5] one token: bit u set when unit u's h copy was issued
 };
 
-// Experts up to this count get a shared-memory copy of slot_of.
-constexpr int kSlotTableMax = 1024;
-
-__host__ __device__ inline size_t route_smem_bytes(int P, int T, int E, bool routing) {
-  return (size_t)P * 12 + (size_t)T * 4 + (size_t)(4 + (E + 31) / 32) * 4 + (routing ? (size_t)E * 8 : 0) +
-         (E <= kSlotTableMax ? (size_t)E * 4 : 0);
+__host__ __device__ inline size_t tables_bytes(int P, int E) {
+  return (size_t)P * 8 + (size_t)P * 4 * 7 + 4 + (size_t)E * 4 * 4 + 32;
 }
 
-__device__ __forceinline__ RouteSmem route_smem(const DecodeParams& a, uint8_t* sm) {
-  RouteSmem r;
-  uint8_t* b = sm + a.route_off;
-  r.ids = reinterpret_cast<int32_t*>(b);
-  r.w = reinterpret_cast<float*>(r.ids + a.P);
-  r.exsel = r.w + a.P;
-  r.sall = r.exsel + a.P;
-  r.red = r.sall + a.T;
-  r.bad = reinterpret_cast<int32_t*>(r.red + (a.E + 31) / 32);
-  r.lg = reinterpret_cast<float*>(r.bad + 4);
-  r.rank = reinterpret_cast<int32_t*>(r.lg + (a.logits ? a.E : 0));
-  r.slot = r.rank + (a.logits ? a.E : 0);
-  return r;
+__device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) {
+  Tables t;
+  uint8_t* b = sm + a.o_small;
+  t.blk = reinterpret_cast<const uint8_t**>(b);
+  t.ids = reinterpret_cast<int32_t*>(b + (size_t)a.P * 8);
+  t.w = reinterpret_cast<float*>(t.ids + a.P);
+  t.punit = reinterpret_cast<int32_t*>(t.w + a.P);
+  t.uexp = t.punit + a.P;
+  t.uoff = t.uexp + a.P;
+  t.upairs = t.uoff + a.P + 1;
+  t.udone = t.upairs + a.P;
+  t.ecnt = t.udone + a.P;
+  t.eunit = t.ecnt + a.E;
+  t.eslot = t.eunit + a.E;
+  t.lg = reinterpret_cast<float*>(t.eslot + a.E);
+  t.misc = reinterpret_cast<int32_t*>(t.lg + a.E);
+  return t;
 }
 
-// Order-preserving int key of a float that is not NaN (for atomicMax).
-__device__ __forceinline__ int32_t float_key(float v) {
-  const int32_t b = __float_as_int(v);
-  return b >= 0 ? b : b ^ 0x7fffffff;
-}
-__device__ __forceinline__ float key_float(int32_t k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
-
-__device__ __forceinline__ const uint8_t* resolve_slot(const DecodeParams& a, int e, int s) {
-  if (e < 0 || e >= a.E || s < 0 || s >= a.n_slots) return nullptr;
-  return a.pool + (size_t)s * a.block_bytes;
-}
-
-// Expert block of expert e, with unusable-id reporting by the writer block.
-__device__ __forceinline__ const uint8_t* resolve_report(const DecodeParams& a, const RouteSmem& r, int e,
-                                                         bool table, bool writer) {
-  const int s = (e < 0 || e >= a.E) ? -1 : (table ? r.slot[e] : a.slot_of[e]);
-  const uint8_t* b = resolve_slot(a, e, s);
-  if (writer && !b) {
-    if (e != -1 && (e < 0 || e >= a.E)) atomicOr(a.flags, 2);
-    else if (e >= 0) atomicOr(a.flags, 1);
+// Bounded wait on an mbarrier phase; gives up at once when the block has
+// already aborted. Returns false (and marks the abort) on expiry.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
+                                           int32_t* err) {
+  #pragma unroll 1
+  for (unsigned i = 0; i < kMbarTries; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
   }
-  return b;
+  *abort_flag = 1;
+  atomicOr(err, 4);
+  return false;
 }
 
 // "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
-// experts of each token. Same definition as moe_route: top-k by (logit desc,
-// index asc), softmax over all E, optionally renormalised over the k; a
-// token with NaN/+inf logits or all -inf gets ids -1 and weights 0.
-// Per token: (A) logits to shared memory; (B) rank counts split over threads
-// (thread (e, part) counts the experts of one slice of j that precede e;
-// integer sums, so the order is free) and the maximum logit; (C) the chosen
-// experts, their blocks and exp(logit - max), and the sum of exp over each
-// slice of 32 experts (one warp, fixed tree); the slice sums are then added
-// in slice order, so the denominator does not depend on the block size.
-// Three block barriers per token. The weights are formed afterwards by warp
-// 0 (finish_weights).
-__device__ void route_block(const DecodeParams& a, const RouteSmem& r, const uint8_t** blk_of, bool table,
-                            bool writer) {
-  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-  const int nslices = (a.E + 31) / 32;
-  const int parts = max(1, nt / a.E);
-  const int span = (a.E + parts - 1) / parts;
-  for (int t = 0; t < a.T; ++t) {
-    // (A)
-    if (tid == 0) {
-      r.bad[0] = r.bad[1] = 0;
-      r.bad[2] = float_key(-INFINITY);
+// experts of each token. One warp, one token, logits lg[E] in shared memory.
+// Same definition and the same arithmetic as moe_route: top-k by (logit
+// desc, index asc); softmax over all E (per-lane sums in index order, then a
+// butterfly), renormalised over the k when asked. A token with NaN/+inf
+// logits or all -inf gets ids -1 and weights 0.
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Lane l owns elements l, l + 32, ...; it keeps its best element not yet
+// taken. Each round the warp's best candidate is the next pick (lane r keeps
+// pick r), and only the lane that owned it rescans its elements for the best
+// one ranking after it. Returns false for a token without a routing.
+__device__ __forceinline__ bool topk_warp(const float* lg, int E, int k, int lane, float& my_v, int& my_i) {
+  const unsigned full = 0xffffffffu;
+  bool bad = false;
+  int ninf = 0;
+  float cv = -INFINITY;
+  int ci = INT_MAX;
+#pragma unroll 4
+  for (int e = lane; e < E; e += 32) {
+    const float v = lg[e];
+    bad |= isnan(v) || v == INFINITY;
+    ninf += v == -INFINITY;
+    if (ranks_before(v, e, cv, ci)) {
+      cv = v;
+      ci = e;
     }
-    for (int e = tid; e < a.E; e += nt) {
-      r.lg[e] = a.logits[(size_t)t * a.E + e];
-      r.rank[e] = 0;
-      if (t == 0 && table) r.slot[e] = a.slot_of[e];
+  }
+  bad = __any_sync(full, bad);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ninf += __shfl_xor_sync(full, ninf, o);
+  if (bad || ninf == E) return false;
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    float bv = cv;
+    int bi = ci;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(full, bv, o);
+      const int oi = __shfl_xor_sync(full, bi, o);
+      if (ranks_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
     }
-    __syncthreads();
-    // (B)
-    for (int i = tid; i < a.E * parts; i += nt) {
-      const int e = i % a.E, part = i / a.E;
-      const float v = r.lg[e];
-      if (i < a.E) {  // part 0 (whole warps while E is a multiple of 32): one atomic per warp
-        const unsigned mask = __activemask();
-        const int is_bad = isnan(v) || v == INFINITY;
-        const int32_t kmax = __reduce_max_sync(mask, is_bad ? float_key(-INFINITY) : float_key(v));
-        const int any_bad = __any_sync(mask, is_bad);
-        const int ninf = __popc(__ballot_sync(mask, v == -INFINITY));
-        if ((threadIdx.x & 31) == __ffs(mask) - 1) {
-          if (any_bad) atomicOr(&r.bad[0], 1);
-          atomicMax(&r.bad[2], kmax);
-          if (ninf) atomicAdd(&r.bad[1], ninf);
+    if (lane == r) {
+      my_v = bv;
+      my_i = bi;
+    }
+    if ((bi & 31) == lane) {  // this lane's candidate was taken
+      cv = -INFINITY;
+      ci = INT_MAX;
+#pragma unroll 4
+      for (int e = lane; e < E; e += 32) {
+        const float v = lg[e];
+        if (ranks_before(bv, bi, v, e) && ranks_before(v, e, cv, ci)) {
+          cv = v;
+          ci = e;
         }
       }
-      int cnt = 0;
-      const int j1 = min(a.E, (part + 1) * span);
-      for (int j = part * span; j < j1; ++j) {
-        const float u = r.lg[j];
-        cnt += (u > v) || (u == v && j < e);
-      }
-      if (cnt) atomicAdd(&r.rank[e], cnt);
     }
-    __syncthreads();
-    // (C)
-    const bool token_bad = r.bad[0] != 0 || r.bad[1] == a.E;
-    const float m = key_float(r.bad[2]);
-    for (int base = warp * 32; base < a.E; base += nt) {  // warp-uniform: one slice
-      const int e = base + lane;
-      float ex = 0.0f;
-      if (e < a.E) {
-        ex = token_bad ? 0.0f : expf(r.lg[e] - m);
-        const int rk = r.rank[e];
-        if (rk < a.k) {
-          const int q = t * a.k + rk;
-          const int id = token_bad ? -1 : e;
-          r.ids[q] = id;
-          r.exsel[q] = ex;
-          blk_of[q] = resolve_report(a, r, id, table, writer);
-          if (writer && a.ids_out) a.ids_out[q] = id;
-        }
-      }
-      ex = warp_sum(ex);
-      if (lane == 0) r.red[base / 32] = ex;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float s_all = 0.0f;
-      for (int i = 0; i < nslices; ++i) s_all += r.red[i];
-      r.sall[t] = s_all;
-    }
+  }
+  return true;
+}
+
+// Softmax weight of lane's pick (lane < k): exp(l - max) over the sum over
+// all E (or over the k picks when renormalised).
+__device__ __forceinline__ float pick_weight(const float* lg, int E, int k, int renorm, int lane, float my_v) {
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  float s_all = 0.0f;
+#pragma unroll 4
+  for (int e = lane; e < E; e += 32) s_all += expf(lg[e] - m);
+  s_all = warp_sum(s_all);
+  const float mine = lane < k ? expf(my_v - m) : 0.0f;
+  const float s_sel = warp_sum(mine);
+  return mine / (renorm ? s_sel : s_all);
+}
+
+__device__ void route_warp(const float* lg, int E, int k, int renorm, int lane, int32_t* ids_out,
+                           float* w_out) {
+  float my_v = 0.0f;
+  int my_i = -1;
+  const bool ok = topk_warp(lg, E, k, lane, my_v, my_i);
+  const float wq = ok ? pick_weight(lg, E, k, renorm, lane, my_v) : 0.0f;
+  if (lane < k) {
+    ids_out[lane] = ok ? my_i : -1;
+    w_out[lane] = wq;
   }
 }
 
-// Warp 0 after route_block: w[q] = exp(l - max) / (sum over all E, or over
-// the k chosen, in choice order); 0 for a token without a routing.
-__device__ __forceinline__ void finish_weights(const DecodeParams& a, const RouteSmem& r, bool writer) {
-  __syncwarp();
-  for (int q = threadIdx.x; q < a.P; q += 32) {
-    const int t = q / a.k;
-    float wq = 0.0f;
-    if (r.ids[q] >= 0) {
-      float den = r.sall[t];
-      if (a.renorm) {
-        den = 0.0f;
-        for (int j = 0; j < a.k; ++j) den += r.exsel[t * a.k + j];
-      }
-      wq = r.exsel[q] / den;
-    }
-    r.w[q] = wq;
-    if (writer && a.wts_out) a.wts_out[q] = wq;
-  }
-  __syncwarp();
-}
-
-// Shared prologue: barriers, routing (or the given ids), the expert block of
-// every pair (resolved once), unusable-id reporting and routed outputs. On
-// return blk_of and ids are visible to the whole block; w is complete in
-// warp 0 (which forms it when the block routes itself) and becomes visible
-// to the other warps at their next barrier with warp 0.
-// empty_count: arrivals that free a stage (odd stages: odd_count).
-__device__ __forceinline__ void init_bars(const DecodeParams& a, uint64_t* full, uint64_t* empty,
-                                          int empty_count, int odd_count) {
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < a.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], (s & 1) ? odd_count : empty_count);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-}
-
-// Barriers (init_bars, by the caller, before any other thread uses them),
-// routing or the given ids, the expert block of every pair; ends with a
-// block barrier.
-__device__ __forceinline__ void prologue(const DecodeParams& a, uint8_t* sm, const uint8_t** blk_of,
-                                         bool writer) {
-  const RouteSmem r = route_smem(a, sm);
-  const bool table = a.E <= kSlotTableMax;
-  if (a.logits) {
-    route_block(a, r, blk_of, table, writer);
-    if (threadIdx.x < 32) finish_weights(a, r, writer);
-  } else {
-    for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
-      r.ids[p] = a.ids[p];
-      r.w[p] = a.wts[p];
-    }
-    if (table)
-      for (int e = threadIdx.x; e < a.E; e += blockDim.x) r.slot[e] = a.slot_of[e];
-    __syncthreads();
-    for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
-      blk_of[p] = resolve_report(a, r, r.ids[p], table, writer);
-      if (writer) {
-        if (a.ids_out) a.ids_out[p] = r.ids[p];
-        if (a.wts_out) a.wts_out[p] = r.w[p];
-      }
-    }
-    __syncthreads();
-  }
-}
-
-// Producer loop of one kernel: for each pair, wait for the stage to be free,
-// then request the block's rows [r0, r1) of the expert's section starting at
-// `section` (row stride row_bytes) -- one contiguous bulk copy.
-__device__ __forceinline__ void produce(const DecodeParams& a, uint8_t* sm, uint64_t* full,
-                                        uint64_t* empty, const uint8_t* const* blk_of, int r0,
-                                        int r1, unsigned long long section, uint32_t row_bytes) {
-  const uint32_t bytes = (uint32_t)(r1 - r0) * row_bytes;
-  for (int p = 0; p < a.P; ++p) {
-    const int s = p % a.stages;
-    if (p >= a.stages && !mbar_wait(&empty[s], ((p / a.stages) - 1) & 1)) atomicOr(a.flags, 4);
-    const uint8_t* blk = blk_of[p];
-    if (!blk || bytes == 0) {
-      mbar_arrive_expect_tx(&full[s], 0);
-      continue;
-    }
-    mbar_arrive_expect_tx(&full[s], bytes);
-    bulk_g2s(sm + (size_t)s * a.st.bytes, blk + section + (size_t)r0 * row_bytes, bytes, &full[s]);
-  }
-}
-
-// The activations of the current token in shared memory as the scaled pairs
-// of dot16_scaled, 64 bytes per 32-element chunk; piece i (16 bytes) of chunk
+// The activations of a token in shared memory as the scaled pairs of
+// dot16_scaled, 64 bytes per 32-element chunk; piece i (16 bytes) of chunk
 // cc sits at slot (i + cc/2) % 4 so that the 8 lanes of a quarter-warp, which
 // read chunks cc..cc+7, hit 8 different bank groups. Per chunk: xsum = sum of
 // the (unscaled) FP16 values, xback = 2^(24-s).
 __device__ __forceinline__ int xslot(int cc, int i) { return cc * 4 + ((i + (cc >> 1)) & 3); }
 
-__device__ __forceinline__ void stage_x(const __half* __restrict__ src, int H, uint4* xs4, float* xsum,
-                                        float* xback, int tid, int nthreads) {
-  for (int cc = tid; cc < H / 32; cc += nthreads) {
-    float v[32];
+__device__ __forceinline__ void stage_x_chunk(const __half* __restrict__ src, uint4* xs4, float* xsum,
+                                              float* xback, int cc) {
+  float v[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(src + 32 * cc + 8 * i);
-      const __half* e = reinterpret_cast<const __half*>(&raw);
+  for (int i = 0; i < 4; ++i) {
+    const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(src + 32 * cc + 8 * i));
+    const __half* e = reinterpret_cast<const __half*>(&raw);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[8 * i + j] = __half2float(e[j]);
-    }
-    float sum = 0.0f, amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      sum += v[j];
-      amax = fmaxf(amax, fabsf(v[j]));
-    }
-    const int sh = chunk_shift(amax);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 o;
-      scaled_perm8(v + 8 * i, sh, reinterpret_cast<half2*>(&o));
-      xs4[xslot(cc, i)] = o;
-    }
-    xsum[cc] = sum;
-    xback[cc] = pow2f(24 - sh);
+    for (int j = 0; j < 8; ++j) v[8 * i + j] = __half2float(e[j]);
   }
+  float sum = 0.0f, amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    sum += v[j];
+    amax = fmaxf(amax, fabsf(v[j]));
+  }
+  const int sh = chunk_shift(amax);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 o;
+    scaled_perm8(v + 8 * i, sh, reinterpret_cast<half2*>(&o));
+    xs4[xslot(cc, i)] = o;
+  }
+  xsum[cc] = sum;
+  xback[cc] = pow2f(24 - sh);
 }
 
-// Gate and up sums of one row for one lane (before the warp sum):
-// s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks cc = lane + 32 it.
-// gq / xo: the lane's group index and activation slots per chunk, computed
-// once per kernel.
+// Gate and up sums of up to two rows (same pair) for one lane, before the
+// warp sum: s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks
+// cc = lane + 32 it. The activation chunk is loaded once for both rows.
 template <int NC>
-__device__ __forceinline__ void gate_up_row(const uint8_t* row, const BlockOffsets& off, int nch,
-                                            int lane, const int* gq, const int* xo, const uint4* xs4,
-                                            const float* xsum, const float* xback, float& ag, float& au) {
-  const uint2* sz = reinterpret_cast<const uint2*>(row + off.gu_sz);  // quads per group
+__device__ __forceinline__ void gate_up_rows(const uint8_t* r0, const uint8_t* r1, bool two,
+                                             const BlockOffsets& off, int nch, int lane, const int* gq,
+                                             const uint4* xs4, const float* xsum, const float* xback,
+                                             float (&acc)[4]) {
 #pragma unroll
   for (int it = 0; it < NC; ++it) {
     const int cc = lane + 32 * it;
     if (cc < nch) {
-      const uint4 wg = *reinterpret_cast<const uint4*>(row + off.gu_q_gate + 16 * cc);
-      const uint4 wu = *reinterpret_cast<const uint4*>(row + off.gu_q_up + 16 * cc);
-      const uint2 q = sz[gq[it]];
       uint4 xv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) xv[i] = xs4[xo[4 * it + i]];
+      for (int i = 0; i < 4; ++i) xv[i] = xs4[xslot(cc, i)];
       const half2* xa = reinterpret_cast<const half2*>(&xv[0]);  // pieces 0, 1 are contiguous
       const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
-      const float back = xback[cc];
-      const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
-      const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
-      const float2 sgz = __half22float2(u32_as_h2(q.x));  // (s_gate, z_gate)
-      const float2 suz = __half22float2(u32_as_h2(q.y));  // (s_up, z_up)
-      const float xsm = xsum[cc];
-      ag += sgz.x * (dg - sgz.y * xsm);
-      au += suz.x * (du - suz.y * xsm);
+      const float back = xback[cc], xsm = xsum[cc];
+      {
+        const uint4 wg = *reinterpret_cast<const uint4*>(r0 + off.gu_q_gate + 16 * cc);
+        const uint4 wu = *reinterpret_cast<const uint4*>(r0 + off.gu_q_up + 16 * cc);
+        const uint2 q = reinterpret_cast<const uint2*>(r0 + off.gu_sz)[gq[it]];
+        const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
+        const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
+        const float2 sgz = __half22float2(u32_as_h2(q.x)), suz = __half22float2(u32_as_h2(q.y));
+        acc[0] += sgz.x * (dg - sgz.y * xsm);
+        acc[1] += suz.x * (du - suz.y * xsm);
+      }
+      if (two) {
+        const uint4 wg = *reinterpret_cast<const uint4*>(r1 + off.gu_q_gate + 16 * cc);
+        const uint4 wu = *reinterpret_cast<const uint4*>(r1 + off.gu_q_up + 16 * cc);
+        const uint2 q = reinterpret_cast<const uint2*>(r1 + off.gu_sz)[gq[it]];
+        const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
+        const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
+        const float2 sgz = __half22float2(u32_as_h2(q.x)), suz = __half22float2(u32_as_h2(q.y));
+        acc[2] += sgz.x * (dg - sgz.y * xsm);
+        acc[3] += suz.x * (du - suz.y * xsm);
+      }
     }
   }
 }
 
-// Two rows (same row index of two pairs of one token) at once.
-template <int NC>
-__device__ __forceinline__ void gate_up_row2(const uint8_t* ra, const uint8_t* rb, const BlockOffsets& off,
-                                             int nch, int lane, const int* gq, const int* xo, const uint4* xs4,
-                                             const float* xsum, const float* xback, float& aga, float& aua,
-                                             float& agb, float& aub) {
-  const uint2* sza = reinterpret_cast<const uint2*>(ra + off.gu_sz);
-  const uint2* szb = reinterpret_cast<const uint2*>(rb + off.gu_sz);
-#pragma unroll
-  for (int it = 0; it < NC; ++it) {
-    const int cc = lane + 32 * it;
-    if (cc < nch) {
-      const uint4 wga = *reinterpret_cast<const uint4*>(ra + off.gu_q_gate + 16 * cc);
-      const uint4 wua = *reinterpret_cast<const uint4*>(ra + off.gu_q_up + 16 * cc);
-      const uint4 wgb = *reinterpret_cast<const uint4*>(rb + off.gu_q_gate + 16 * cc);
-      const uint4 wub = *reinterpret_cast<const uint4*>(rb + off.gu_q_up + 16 * cc);
-      const uint2 qa = sza[gq[it]];
-      const uint2 qb = szb[gq[it]];
-      uint4 xv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) xv[i] = xs4[xo[4 * it + i]];
-      const half2* xa = reinterpret_cast<const half2*>(&xv[0]);
-      const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
-      const float back = xback[cc];
-      const float xsm = xsum[cc];
-      const float dga = (dot16_scaled(wga.x, wga.y, xa) + dot16_scaled(wga.z, wga.w, xb)) * back;
-      const float dua = (dot16_scaled(wua.x, wua.y, xa) + dot16_scaled(wua.z, wua.w, xb)) * back;
-      const float dgb = (dot16_scaled(wgb.x, wgb.y, xa) + dot16_scaled(wgb.z, wgb.w, xb)) * back;
-      const float dub = (dot16_scaled(wub.x, wub.y, xa) + dot16_scaled(wub.z, wub.w, xb)) * back;
-      const float2 sga = __half22float2(u32_as_h2(qa.x)), sua = __half22float2(u32_as_h2(qa.y));
-      const float2 sgb = __half22float2(u32_as_h2(qb.x)), sub = __half22float2(u32_as_h2(qb.y));
-      aga += sga.x * (dga - sga.y * xsm);
-      aua += sua.x * (dua - sua.y * xsm);
-      agb += sgb.x * (dgb - sgb.y * xsm);
-      aub += sub.x * (dub - sub.y * xsm);
-    }
-  }
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
+__device__ __forceinline__ void bar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
-// ---- kernel 1: gate/up dequant-GEMV + SwiGLU -------------------------------
-// Stage: the block's gate/up rows [R][gu_row] (codes, scales and zeros of
-// both projections per row). With a stage per pair (P <= S), the work units
-// of a token are (couple, row): row r of pairs 2c and 2c + 1, computed
-// together by one warp (shared activation loads, two independent chains);
-// warp w takes units w, w + 15, ... Otherwise each iteration covers
-// kPairsPerIter pairs of one token: warp w takes row w % 8 (+8, ...) of pair
-// p + w / 8, and the sub-group releases the stage.
-template <int NC>
-__global__ void __launch_bounds__(kGateThreads, 2) decode_gateup_kernel(const DecodeParams a) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
-  const int n0 = (int)(((long long)c * a.I) / a.G), n1 = (int)(((long long)(c + 1) * a.I) / a.G);
-  const int rows = n1 - n0;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + a.bar_off);
-  uint64_t* empty = full + kMaxStages;
-  const uint8_t** blk_of = reinterpret_cast<const uint8_t**>(sm + a.blk_off);
-  uint4* xs4 = reinterpret_cast<uint4*>(sm + a.part_off);                    // [H/32][4]
-  float* xsum = reinterpret_cast<float*>(sm + a.part_off + (size_t)a.H * 2);  // [H/32]
-  float* xback = xsum + a.H / 32;                                             // [H/32]
-  // Independent of earlier kernels: before the wait. Every warp of the
-  // sub-group that drains a stage arrives on its empty barrier.
-  init_bars(a, full, empty, kSub0, kGateWarps - kSub0);
-  griddep_wait();                // logits / ids and x come from earlier kernels
-  prologue(a, sm, blk_of, c == 0);
-  griddep_launch_dependents();  // the down kernel may start its prefetch
-  if (warp == kGateWarps) {
-    if (lane == 0) produce(a, sm, full, empty, blk_of, n0, n1, 0ull, a.off.gu_row);
+// Named barriers (0 is __syncthreads).
+constexpr int kBarCompute = 1;  // compute warps wait, producer arrives (weights and tables final)
+constexpr int kBarTables = 2;   // producer arrives with the routing tables, compute warps wait
+constexpr int kBarPolled = 3;   // compute warps arrive after their last counter poll, producer waits
+
+// "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
+// experts of the token. The whole block routes one token in two stages, the
+// same selection as moe_route (top-k by (logit desc, index asc)):
+//   1. warp w ranks the experts of 32-expert segment w (w + 17, ...) among
+//      themselves; each segment's best min(k, 32) are candidates (every pick
+//      is among its own segment's best k);
+//   2. each candidate counts the candidates that rank before it: its count
+//      is its rank among all E experts when it is below k.
+// Three block barriers; the logits and the slot table go to shared memory
+// on the way. On return tb.ids[0..k) and pv[0..k) hold the picks and their
+// logits (tb.misc[3] set: the token has NaN/+inf logits, or all -inf).
+__device__ void route_one_token(const StreamParams& a, const Tables& tb, float* cv, int32_t* ci, float* pv,
+                                uint4* xs4, float* xsum, float* xback) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, k = a.k, kk = min(k, 32), nseg = (E + 31) / 32, C = nseg * kk;
+  const int nchx = a.H / 32;
+  bool bad = false;
+  int ninf = 0;
+#pragma unroll 1
+  for (int e = tid; e < E; e += kThreads) {
+    const float v = __ldcg(a.logits + e);
+    tb.lg[e] = v;
+    tb.eslot[e] = __ldcg(a.slot_of + e);
+    bad |= isnan(v) || v == INFINITY;
+    ninf += v == -INFINITY;
+  }
+#pragma unroll 1
+  for (int c = tid; c < C; c += kThreads) {
+    cv[c] = -INFINITY;
+    ci[c] = INT_MAX;
+  }
+#pragma unroll 1
+  for (int cc = tid; cc < nchx; cc += kThreads) stage_x_chunk(a.x, xs4, xsum, xback, cc);
+  bad = __any_sync(0xffffffffu, bad);
+  ninf = __reduce_add_sync(0xffffffffu, ninf);
+  if (lane == 0) {
+    if (bad) atomicOr(&tb.misc[3], 1);
+    if (ninf) atomicAdd(&tb.misc[4], ninf);
+  }
+  __syncthreads();
+  if (tb.misc[3] || tb.misc[4] == E) {
+    if (tid == 0) tb.misc[3] = 1;
+    __syncthreads();
+    __syncthreads();
     return;
   }
-  const int nch = a.H / 32;
-  int gq[NC], xo[4 * NC];
-#pragma unroll
-  for (int it = 0; it < NC; ++it) {
-    const int cc = lane + 32 * it;
-    gq[it] = (32 * cc) / a.g;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) xo[4 * it + i] = xslot(cc, i);
-  }
-  if (a.P <= a.stages) {
-    int cur_t = -1;
-    for (int p0 = 0; p0 < a.P; p0 += a.k) {
-      const int t = p0 / a.k;
-      if (t != cur_t) {
-        asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");  // previous x no longer read
-        stage_x(a.x + (size_t)t * a.H, a.H, xs4, xsum, xback, threadIdx.x, kGateWarps * 32);
-        asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");
-        cur_t = t;
+#pragma unroll 1
+  for (int seg = warp; seg < nseg; seg += kThreads / 32) {
+    const int e = 32 * seg + lane;
+    if (e < E) {
+      const float v = tb.lg[e];
+      int lrank = 0;
+      const int e1 = min(E, 32 * seg + 32);
+#pragma unroll 4
+      for (int j = 32 * seg; j < e1; ++j) lrank += ranks_before(tb.lg[j], j, v, e);
+      if (lrank < kk) {
+        cv[seg * kk + lrank] = v;
+        ci[seg * kk + lrank] = e;
       }
-      const int couples = (a.k + 1) / 2;
-      for (int u = warp; u < couples * rows; u += kGateWarps) {
-        const int cpl = u / rows, r = u - cpl * rows;
-        const int qa = p0 + 2 * cpl, qb = qa + 1;
-        const bool two = 2 * cpl + 1 < a.k;
-        const int sa = qa % a.stages, sb = qb % a.stages;
-        if (!mbar_wait(&full[sa], (qa / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
-        if (two && !mbar_wait(&full[sb], (qb / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
-        const uint8_t* ba = blk_of[qa];
-        const uint8_t* bb = two ? blk_of[qb] : nullptr;
-        const uint8_t* ra = sm + (size_t)sa * a.st.bytes + (size_t)r * a.off.gu_row;
-        const uint8_t* rb = sm + (size_t)sb * a.st.bytes + (size_t)r * a.off.gu_row;
-        float aga = 0.0f, aua = 0.0f, agb = 0.0f, aub = 0.0f;
-        if (ba && bb) {
-          gate_up_row2<NC>(ra, rb, a.off, nch, lane, gq, xo, xs4, xsum, xback, aga, aua, agb, aub);
-        } else {
-          if (ba) gate_up_row<NC>(ra, a.off, nch, lane, gq, xo, xs4, xsum, xback, aga, aua);
-          if (bb) gate_up_row<NC>(rb, a.off, nch, lane, gq, xo, xs4, xsum, xback, agb, aub);
+    }
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int c = tid; c < C; c += kThreads) {
+    const float v = cv[c];
+    const int i = ci[c];
+    if (i == INT_MAX) continue;
+    int rank = 0;
+#pragma unroll 4
+    for (int j = 0; j < C; ++j) rank += ranks_before(cv[j], ci[j], v, i);
+    if (rank < k) {
+      tb.ids[rank] = i;
+      pv[rank] = v;
+    }
+  }
+  __syncthreads();
+}
+
+// Producer warp after route_one_token: lane j < k resolves pick j's expert
+// block, the warp writes the tables the compute warps read (units are the
+// picks in choice order; every unit has its own stage in both rings) and
+// releases them; lane 0 then issues the copies. The softmax weights follow, with the
+// arithmetic of moe_route (sum over all E per lane in index order, then a
+// butterfly), and are released to the combine.
+__device__ void producer_one_token(const StreamParams& a, const Tables& tb, const float* pv, uint64_t* full_g,
+                                   uint64_t* full_d, uint8_t* ring_g, uint8_t* ring_d, int n0, int rg_rows,
+                                   int m0, int rd_rows, bool writer) {
+  const int lane = threadIdx.x & 31;
+  const int E = a.E, k = a.k;
+  const uint32_t gbytes = (uint32_t)rg_rows * a.off.gu_row, dbytes = (uint32_t)rd_rows * a.off.d_row;
+  const bool ok = tb.misc[3] == 0;
+  // The picks' logits live in the ring, which the copies below overwrite.
+  const float m = ok ? pv[0] : 0.0f;
+  const float my_v = (ok && lane < k) ? pv[lane] : 0.0f;
+  const uint8_t* blk = nullptr;
+  int id = -1;
+  if (lane < k) {
+    if (ok) {
+      id = tb.ids[lane];
+      const int sl = tb.eslot[id];
+      blk = (sl >= 0 && sl < a.n_slots) ? a.pool + (size_t)sl * a.block_bytes : nullptr;
+      if (!blk && writer) atomicOr(a.ws, 1);
+    }
+    tb.blk[lane] = blk;
+    tb.ids[lane] = id;
+    tb.punit[lane] = blk ? lane : -1;
+    tb.uoff[lane] = lane;
+    tb.upairs[lane] = lane;
+    tb.udone[lane] = 0;
+    if (writer && a.ids_out) a.ids_out[lane] = id;
+  }
+  if (lane == 0) {
+    tb.misc[0] = ok ? k : 0;
+    tb.uoff[k] = k;
+  }
+  __syncwarp();
+  bar_arrive(kBarTables, kThreads);  // releases the tables to the compute warps
+  // One lane issues the gate/up copies in choice order, so the stages
+  // complete in the order the compute warps drain them (copies issued side by
+  // side complete together).
+  if (lane == 0) {
+#pragma unroll 1
+    for (int j = 0; j < k && gbytes; ++j) {
+      const uint8_t* b = tb.blk[j];
+      if (!b) continue;
+      mbar_arrive_expect_tx(&full_g[j], gbytes);
+      bulk_g2s(ring_g + (size_t)j * a.sg, b + (size_t)n0 * a.off.gu_row, gbytes, &full_g[j]);
+    }
+  }
+  __syncwarp();
+  // The down rows are needed only after the exchange: lane j issues pick j's.
+  if (blk && dbytes) {
+    mbar_arrive_expect_tx(&full_d[lane], dbytes);
+    bulk_g2s(ring_d + (size_t)lane * a.sd, blk + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes, &full_d[lane]);
+  }
+  float wq = 0.0f;
+  if (ok) {
+    float s_all = 0.0f;
+#pragma unroll 4
+    for (int e = lane; e < E; e += 32) s_all += expf(tb.lg[e] - m);
+    s_all = warp_sum(s_all);
+    const float mine = lane < k ? expf(my_v - m) : 0.0f;
+    const float s_sel = warp_sum(mine);
+    wq = mine / (a.renorm ? s_sel : s_all);
+  }
+  if (lane < k) {
+    tb.w[lane] = wq;
+    if (writer && a.wts_out) a.wts_out[lane] = wq;
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// prefetch_one_token (producer warp, one decode token): lane u watches unit
+// u (the k <= 32 units are polled together, one load per round); once every
+// block has released it (acquire), the lane copies the unit's complete h into
+// shared memory with a bulk copy, after a proxy fence (the h rows were written
+// by ordinary stores of other SMs); the copy completes on hfull[u]. Bit u of
+// tb.misc[5] is set when unit u's copy was issued.
+__device__ void prefetch_one_token(const StreamParams& a, const Tables& tb, __half* hsm, uint64_t* hfull, int U,
+                                   int cnt_target, volatile int32_t* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  int32_t* cnt = a.ws + kCntBase;
+  bool pending = lane < U && tb.blk[lane] != nullptr;
+  unsigned tries = 0;
+#pragma unroll 1
+  while (pending) {
+    if (ld_acquire_gpu(&cnt[lane]) >= cnt_target) {
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(&hfull[lane], (uint32_t)a.I * 2);
+      bulk_g2s(hsm + (size_t)lane * a.I, a.hbuf + (size_t)lane * a.I, (uint32_t)a.I * 2, &hfull[lane]);
+      atomicOr(&tb.misc[5], 1 << lane);
+      pending = false;
+    } else if (*abort_flag) {
+      pending = false;
+    } else if (++tries > kSpinTries) {
+      *abort_flag = 1;
+      atomicOr(a.ws, 4);
+      pending = false;
+    }
+  }
+}
+
+template <int NCX, int NCH, bool FAST>
+__global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const StreamParams a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int c = blockIdx.x;
+  const int n0 = (int)(((long long)c * a.I) / a.G), n1 = (int)(((long long)(c + 1) * a.I) / a.G);
+  const int m0 = (int)(((long long)c * a.H) / a.G), m1 = (int)(((long long)(c + 1) * a.H) / a.G);
+  const int rg_rows = n1 - n0, rd_rows = m1 - m0;
+  constexpr int grow = 2;                                  // gate/up rows per item
+  const int ng = (rg_rows + grow - 1) / grow;              // gate/up items per unit
+  const int nd = (rd_rows + kDownRows - 1) / kDownRows;   // down items per unit
+  uint8_t* ring_g = sm;
+  uint8_t* ring_d = sm + a.o_ring_d;
+  const int nchx = a.H / 32;
+  uint4* xs4 = reinterpret_cast<uint4*>(sm + a.o_x);                                // [T][H/32][4]
+  float* xsum = reinterpret_cast<float*>(sm + a.o_x + (size_t)a.T * a.H * 2);       // [T][H/32]
+  float* xback = xsum + (size_t)a.T * nchx;                                          // [T][H/32]
+  float* part = reinterpret_cast<float*>(sm + a.o_part);                            // [P][rdn]
+  __half* hst = reinterpret_cast<__half*>(sm + a.o_hst);                            // [P][rgu]
+  __half* hsm = reinterpret_cast<__half*>(sm + a.o_hsm);                            // one token: [U][I]
+  uint64_t* full_g = reinterpret_cast<uint64_t*>(sm + a.o_bar);
+  uint64_t* empty_g = full_g + kMaxRing;
+  uint64_t* full_d = empty_g + kMaxRing;
+  uint64_t* empty_d = full_d + kMaxRing;
+  uint64_t* hfull = empty_d + kMaxRing;  // one token: h of unit u landed in hsm
+  const Tables tb = tables_of(a, sm);
+  volatile int32_t* abort_flag = tb.misc + 1;
+  const bool writer = c == 0;
+  int32_t* cnt = a.ws + kCntBase;
+  const int cnt_target = min(a.I, a.G);  // blocks that own gate/up rows
+
+  if (tid == 0) {
+    #pragma unroll 1
+    for (int s = 0; s < a.Sg; ++s) {
+      mbar_init(&full_g[s], 1);
+      mbar_init(&empty_g[s], ng > 0 ? ng : 1);
+    }
+    #pragma unroll 1
+    for (int s = 0; s < a.Sd; ++s) {
+      mbar_init(&full_d[s], 1);
+      mbar_init(&empty_d[s], nd > 0 ? nd : 1);
+      mbar_init(&hfull[s], 1);
+    }
+    tb.misc[1] = 0;
+    tb.misc[3] = 0;
+    tb.misc[4] = 0;
+    tb.misc[5] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  griddep_wait();  // x, logits / ids and slot_of come from earlier work
+
+  if constexpr (FAST) {
+    // ---- one token routed in the block: see route_one_token ----------------
+    // Routing scratch in the rings (no copy is issued before the picks).
+    const int C = ((a.E + 31) / 32) * min(a.k, 32);
+    float* cv = reinterpret_cast<float*>(sm);
+    int32_t* ci = reinterpret_cast<int32_t*>(cv + C);
+    float* pv = reinterpret_cast<float*>(ci + C);
+    route_one_token(a, tb, cv, ci, pv, xs4, xsum, xback);
+    if (warp == kProducer) {
+      producer_one_token(a, tb, pv, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
+      bar_arrive(kBarCompute, kThreads);  // weights ready for the combine
+    } else {
+      bar_sync(kBarTables, kThreads);
+    }
+    griddep_launch_dependents();
+  } else {
+    // ---- routing (one warp per token) or the given ids; activations ---------
+    #pragma unroll 1
+    for (int e = tid; e < a.E; e += kThreads) {
+      tb.ecnt[e] = 0;
+      tb.eslot[e] = __ldcg(a.slot_of + e);
+    }
+    #pragma unroll 1
+    for (int p = tid; p < a.P; p += kThreads) tb.udone[p] = 0;
+    if (a.logits) {
+      if (warp < a.T) {
+        float* lg = reinterpret_cast<float*>(sm) + (size_t)warp * a.E;  // scratch in the rings
+        #pragma unroll 1
+        for (int e = lane; e < a.E; e += 32) lg[e] = __ldcg(a.logits + (size_t)warp * a.E + e);
+        __syncwarp();
+        route_warp(lg, a.E, a.k, a.renorm, lane, tb.ids + warp * a.k, tb.w + warp * a.k);
+        __syncwarp();
+        if (writer && lane < a.k) {
+          if (a.ids_out) a.ids_out[warp * a.k + lane] = tb.ids[warp * a.k + lane];
+          if (a.wts_out) a.wts_out[warp * a.k + lane] = tb.w[warp * a.k + lane];
         }
-        // Warp sums of the four values by a reduce-scatter butterfly (7
-        // shuffles instead of 20): after the exchanges at distance 16 and 8,
-        // lanes with bit 4 clear hold pair a's sums and set pair b's; bit 3
-        // clear the gate sum, set the up sum; the last three levels finish
-        // each sum within its group of eight lanes.
+      }
+    } else {
+      #pragma unroll 1
+      for (int p = tid; p < a.P; p += kThreads) {
+        tb.ids[p] = __ldcg(a.ids + p);
+        tb.w[p] = __ldcg(a.wts + p);
+        if (writer) {
+          if (a.ids_out) a.ids_out[p] = tb.ids[p];
+          if (a.wts_out) a.wts_out[p] = tb.w[p];
+        }
+      }
+    }
+    #pragma unroll 1
+    for (int i = tid; i < a.T * nchx; i += kThreads) {
+      const int t = i / nchx, cc = i - t * nchx;
+      stage_x_chunk(a.x + (size_t)t * a.H, xs4 + (size_t)t * nchx * 4, xsum + (size_t)t * nchx,
+                    xback + (size_t)t * nchx, cc);
+    }
+    __syncthreads();
+    // Usable pairs, counted per expert.
+    #pragma unroll 1
+    for (int p = tid; p < a.P; p += kThreads) {
+      const int e = tb.ids[p];
+      int u = -1;
+      if (e >= 0 && e < a.E) {
+        const int s = tb.eslot[e];
+        if (s >= 0 && s < a.n_slots) {
+          atomicAdd(&tb.ecnt[e], 1);
+          u = 0;
+        } else if (writer) {
+          atomicOr(a.ws, 1);
+        }
+      } else if (e != -1 && writer) {
+        atomicOr(a.ws, 2);
+      }
+      tb.punit[p] = u;
+    }
+    __syncthreads();
+    // Units: experts with pairs, in ascending id (one warp, exclusive scans).
+    if (warp == 0) {
+      const int per = (a.E + 31) / 32;
+      const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
+      int nu = 0, np = 0;
+      #pragma unroll 1
+      for (int e = e0; e < e1; ++e) {
+        nu += tb.ecnt[e] > 0;
+        np += tb.ecnt[e];
+      }
+      int su = nu, sp = np;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vu = __shfl_up_sync(0xffffffffu, su, o), vp = __shfl_up_sync(0xffffffffu, sp, o);
+        if (lane >= o) {
+          su += vu;
+          sp += vp;
+        }
+      }
+      int u = su - nu, pos = sp - np;
+      #pragma unroll 1
+      for (int e = e0; e < e1; ++e) {
+        const int n = tb.ecnt[e];
+        tb.eunit[e] = n > 0 ? u : -1;
+        if (n > 0) {
+          tb.uexp[u] = e;
+          tb.uoff[u] = pos;
+          tb.blk[u] = a.pool + (size_t)tb.eslot[e] * a.block_bytes;
+          tb.ecnt[e] = pos;
+          ++u;
+          pos += n;
+        }
+      }
+      if (lane == 31) {
+        tb.misc[0] = su;
+        tb.uoff[su] = sp;
+      }
+    }
+    __syncthreads();
+    #pragma unroll 1
+    for (int p = tid; p < a.P; p += kThreads) {
+      if (tb.punit[p] < 0) continue;
+      const int e = tb.ids[p];
+      int rank = 0;
+      #pragma unroll 1
+      for (int q = 0; q < p; ++q) rank += tb.punit[q] >= 0 && tb.ids[q] == e;
+      tb.upairs[tb.ecnt[e] + rank] = p | ((p / a.k) << 16);  // pair, and its token above bit 16
+      tb.punit[p] = tb.eunit[e];
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    // ---- producer: both rings, gate/up first ------------------------------
+    if (warp == kProducer && lane == 0) {
+      const int U = tb.misc[0];
+      const uint32_t gbytes = (uint32_t)rg_rows * a.off.gu_row, dbytes = (uint32_t)rd_rows * a.off.d_row;
+      int qg = ng > 0 ? 0 : U, qd = nd > 0 ? 0 : U;
+      const int first_g = min(U, a.Sg);
+      unsigned idle = 0;
+      while ((qg < U || qd < U) && !*abort_flag) {
+        bool issued = false;
+        if (qg < U) {
+          const int s = qg % a.Sg;
+          if (qg < a.Sg || mbar_test(&empty_g[s], ((qg / a.Sg) - 1) & 1)) {
+            mbar_arrive_expect_tx(&full_g[s], gbytes);
+            bulk_g2s(ring_g + (size_t)s * a.sg, tb.blk[qg] + (size_t)n0 * a.off.gu_row, gbytes, &full_g[s]);
+            ++qg;
+            issued = true;
+          }
+        }
+        if (!issued && qd < U && (qg >= first_g || ng == 0)) {
+          const int s = qd % a.Sd;
+          if (qd < a.Sd || mbar_test(&empty_d[s], ((qd / a.Sd) - 1) & 1)) {
+            mbar_arrive_expect_tx(&full_d[s], dbytes);
+            bulk_g2s(ring_d + (size_t)s * a.sd, tb.blk[qd] + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes,
+                     &full_d[s]);
+            ++qd;
+            issued = true;
+          }
+        }
+        if (issued) {
+          idle = 0;
+        } else {
+          if (++idle > kIdleTries) {
+            *abort_flag = 1;
+            atomicOr(a.ws, 4);
+            break;
+          }
+        }
+      }
+      // Before the block may exit, every copy it issued has landed (bounded):
+      // a slot is refilled only after its consumers drained the previous
+      // fill, so the last fill's parity is unambiguous.
+      if (ng > 0 && (qg < U || *abort_flag)) {
+        #pragma unroll 1
+        for (int s = 0; s < a.Sg && s < qg; ++s) {
+          const int last = s + a.Sg * ((qg - 1 - s) / a.Sg);
+          #pragma unroll 1
+          for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_g[s], (last / a.Sg) & 1); ++i) {
+          }
+        }
+      }
+      if (nd > 0 && (qd < U || *abort_flag)) {
+        #pragma unroll 1
+        for (int s = 0; s < a.Sd && s < qd; ++s) {
+          const int last = s + a.Sd * ((qd - 1 - s) / a.Sd);
+          #pragma unroll 1
+          for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_d[s], (last / a.Sd) & 1); ++i) {
+          }
+        }
+      }
+    }
+  }
+  const int U = tb.misc[0];
+
+  if (warp == kProducer) {
+    __syncwarp();
+    if constexpr (FAST) {
+      // One token: the producer warp polls the other blocks and copies the
+      // complete h of each unit into shared memory for the down items.
+      prefetch_one_token(a, tb, hsm, hfull, U, cnt_target, abort_flag);
+      __syncwarp();
+    } else {
+      bar_arrive(kBarCompute, kThreads);
+      // After every compute warp's last counter poll.
+      bar_sync(kBarPolled, kThreads);
+    }
+    // Count the block out; the last block out resets the unit counters for
+    // the next call (every block has passed all of its waits on them).
+    if (lane == 0) {
+      if (FAST && *abort_flag) {  // copies of an aborted block land before it exits
+        #pragma unroll 1
+        for (int u = 0; u < U; ++u) {
+          if (!tb.blk[u]) continue;
+          #pragma unroll 1
+          for (unsigned i = 0; ng > 0 && i < kMbarTries && !mbar_try_wait(&full_g[u], 0); ++i) {
+          }
+          #pragma unroll 1
+          for (unsigned i = 0; nd > 0 && i < kMbarTries && !mbar_try_wait(&full_d[u], 0); ++i) {
+          }
+          #pragma unroll 1
+          for (unsigned i = 0; ((tb.misc[5] >> u) & 1) && i < kMbarTries && !mbar_try_wait(&hfull[u], 0); ++i) {
+          }
+        }
+      }
+      if (atom_add_acq_rel_gpu(&a.ws[1], 1) == a.G - 1) {
+        #pragma unroll 1
+        for (int u = 0; u < U; ++u) a.ws[kCntBase + u] = 0;
+        a.ws[1] = 0;
+      }
+    }
+    return;
+  }
+
+  // ---- compute warps: gate/up items, then down items -------------------------
+  // Item (u, r) of a ring stage s = u % S belongs to warp (s * n + r) % kWarps,
+  // so every fill of a stage is drained by the same warps in increasing u
+  // (no warp waits on a fill two phases ahead of one it has not drained).
+  // Each warp walks the units once, keeping the stage and its fill count,
+  // and visits only its own items of each unit.
+  int gq[NCX];
+#pragma unroll
+  for (int it = 0; it < NCX; ++it) gq[it] = (32 * (lane + 32 * it)) / a.g;
+  #pragma unroll 1
+  for (int u = 0, s = 0, fill = 0; u < U && ng > 0; ++u, s = (s + 1 == a.Sg) ? 0 : s + 1, fill += s == 0) {
+    if (!tb.blk[u]) continue;
+    #pragma unroll 1
+    for (int r = (warp - s * ng) & (kWarps - 1); r < ng; r += kWarps) {
+      const bool ok = __all_sync(0xffffffffu, wait_phase(&full_g[s], fill & 1, abort_flag, a.ws));
+      const int ra = r * grow;
+      const bool two = grow == 2 && ra + 1 < rg_rows;
+      const uint8_t* rowa = ring_g + (size_t)s * a.sg + (size_t)ra * a.off.gu_row;
+      const uint8_t* rowb = rowa + a.off.gu_row;
+      #pragma unroll 1
+      for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
+        const int p = tb.upairs[i] & 0xffff, t = tb.upairs[i] >> 16;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        gate_up_rows<NCX>(rowa, rowb, two, a.off, nchx, lane, gq, xs4 + (size_t)t * nchx * 4,
+                          xsum + (size_t)t * nchx, xback + (size_t)t * nchx, acc);
+        // Reduce-scatter butterfly of the four sums (7 shuffles): lanes with
+        // bit 4 clear end with row a's sums, set row b's; bit 3 clear the
+        // gate sum, set the up sum; lanes 0 / 16 then take the up sum of
+        // their row from lane 8 / 24.
         const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
-        const float k0 = b4 ? agb : aga, k1 = b4 ? aub : aua;
-        const float w0 = k0 + __shfl_xor_sync(0xffffffffu, b4 ? aga : agb, 16);
-        const float w1 = k1 + __shfl_xor_sync(0xffffffffu, b4 ? aua : aub, 16);
+        const float k0 = b4 ? acc[2] : acc[0], k1 = b4 ? acc[3] : acc[1];
+        const float w0 = k0 + __shfl_xor_sync(0xffffffffu, b4 ? acc[0] : acc[2], 16);
+        const float w1 = k1 + __shfl_xor_sync(0xffffffffu, b4 ? acc[1] : acc[3], 16);
         float v = (b3 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b3 ? w0 : w1, 8);
         v += __shfl_xor_sync(0xffffffffu, v, 4);
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         v += __shfl_xor_sync(0xffffffffu, v, 1);
-        const float up = __shfl_xor_sync(0xffffffffu, v, 8);  // lanes 0 and 16: the up sum
-        if (lane == 0) a.hbuf[(size_t)qa * a.I + n0 + r] = __float2half_rn(ba ? silu_f(v) * up : 0.0f);
-        if (lane == 16 && two) a.hbuf[(size_t)qb * a.I + n0 + r] = __float2half_rn(bb ? silu_f(v) * up : 0.0f);
+        const float up = __shfl_xor_sync(0xffffffffu, v, 8);
+        __half* hp = hst + (size_t)p * a.rgu + ra;
+        if (lane == 0) hp[0] = __float2half_rn(silu_f(v) * up);
+        if (lane == 16 && two) hp[1] = __float2half_rn(silu_f(v) * up);
       }
-    }
-    return;
-  }
-  const int sub = warp < kSub0 ? 0 : 1;                  // pair offset in the iteration
-  const int wr = warp - sub * kSub0;                     // row lane within the sub-group
-  const int nsub = sub ? kGateWarps - kSub0 : kSub0;     // warps of the sub-group
-  int cur_t = -1;
-  for (int p = 0; p < a.P;) {
-    const int t = p / a.k;
-    int np = 1;  // pairs of token t in this iteration
-    while (np < kPairsPerIter && p + np < a.P && (p + np) / a.k == t) ++np;
-    if (t != cur_t) {
-      asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");  // previous x no longer read
-      stage_x(a.x + (size_t)t * a.H, a.H, xs4, xsum, xback, threadIdx.x, kGateWarps * 32);
-      asm volatile("bar.sync 1, %0;" ::"n"(kGateWarps * 32) : "memory");
-      cur_t = t;
-    }
-    const int q = (p & 1) == sub ? p : p + 1;  // this sub-group's pair, if any
-    if (q < p + np) {
-      const int s = q % a.stages;
-      if (!mbar_wait(&full[s], (q / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
-      const uint8_t* blk = blk_of[q];
-      const uint8_t* stg = sm + (size_t)s * a.st.bytes;
-      for (int r = wr; r < rows; r += nsub) {
-        float ag = 0.0f, au = 0.0f;
-        if (blk) gate_up_row<NC>(stg + (size_t)r * a.off.gu_row, a.off, nch, lane, gq, xo, xs4, xsum, xback, ag, au);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          ag += __shfl_xor_sync(0xffffffffu, ag, o);
-          au += __shfl_xor_sync(0xffffffffu, au, o);
-        }
-        if (lane == 0) a.hbuf[(size_t)q * a.I + n0 + r] = __float2half_rn(blk ? silu_f(ag) * au : 0.0f);
-      }
-      // This warp has finished reading the stage (no sub-group barrier: the
-      // stage is free once every warp of the sub-group has arrived).
+      // The warp that completes the unit in this block publishes the block's
+      // h rows of every pair of the unit and releases the unit (one release
+      // per unit and block).
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    p += np;
-  }
-}
-
-// ---- kernel 2: down dequant-GEMV + top-k weighted combine -------------------
-// Stage: the block's down rows [R][d_row] (codes, then scale/zero pairs).
-// Warp w computes the block's rows for pairs w, w+8, ...
-template <int kMaxHChunks>
-__global__ void __launch_bounds__(kThreads, 3) decode_down_kernel(const DecodeParams a) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
-  const int m0 = (int)(((long long)c * a.H) / a.G), m1 = (int)(((long long)(c + 1) * a.H) / a.G);
-  const int rows = m1 - m0;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + a.bar_off);
-  uint64_t* empty = full + kMaxStages;
-  const uint8_t** blk_of = reinterpret_cast<const uint8_t**>(sm + a.blk_off);
-  float* part = reinterpret_cast<float*>(sm + a.part_off);  // [P][rows]
-  // Inputs the prefetch needs (logits or ids, slot_of, the pool) are final:
-  // the gate/up kernel passed its own griddepcontrol.wait before signalling.
-  init_bars(a, full, empty, 1, 1);
-  prologue(a, sm, blk_of, false);
-  const RouteSmem rt = route_smem(a, sm);
-  if (warp == kWarps) {
-    if (lane == 0) produce(a, sm, full, empty, blk_of, m0, m1, a.off.d_offset, a.off.d_row);
-    griddep_launch_dependents();
-    return;
-  }
-  griddep_wait();  // h of every pair is complete and visible
-  griddep_launch_dependents();
-  const int nch = a.I / 32;
-  int gix[kMaxHChunks];
-#pragma unroll
-  for (int it = 0; it < kMaxHChunks; ++it) gix[it] = (32 * (lane + 32 * it)) / a.g;
-  for (int q = 0; q < a.P; ++q) {
-    const int s = q % a.stages;
-    if (s % kWarps != warp) continue;
-    const uint8_t* blk = blk_of[q];
-    if (!mbar_wait(&full[s], (q / a.stages) & 1) && lane == 0) atomicOr(a.flags, 4);
-    if (blk && rows > 0) {
-      half2 hr[kMaxHChunks][16];
-      float hsum[kMaxHChunks], hback[kMaxHChunks];
-#pragma unroll
-      for (int it = 0; it < kMaxHChunks; ++it) {
-        const int cc = lane + 32 * it;
-        if (cc < nch) hsum[it] = load_scaled_chunk(a.hbuf + (size_t)q * a.I + 32 * cc, hr[it], hback[it]);
+      int last = 0;
+      if (lane == 0 && ok) {
+        mbar_arrive(&empty_g[s]);
+        __threadfence_block();
+        last = atomicAdd(&tb.udone[u], 1) == ng - 1;
       }
-      const uint8_t* stg = sm + (size_t)s * a.st.bytes;
-      for (int r0 = 0; r0 < rows; r0 += 8) {
-        float v[8];
+      if (last && lane == 0) {
+        // Lane 0 stores the block's h rows of every pair of the unit itself,
+        // so the release orders exactly its own stores before the count.
+        __threadfence_block();  // the other warps' staged h (counted above)
+        #pragma unroll 1
+        for (int i = tb.uoff[u]; i < tb.uoff[u + 1]; ++i) {
+          const int p = tb.upairs[i] & 0xffff;
+          #pragma unroll 1
+          for (int q = 0; q < rg_rows; ++q) a.hbuf[(size_t)p * a.I + n0 + q] = hst[(size_t)p * a.rgu + q];
+        }
+        red_release_gpu_add(&cnt[u], 1);
+      }
+      __syncwarp();
+    }
+  }
+  // The last down item of this warp (its last counter poll).
+  int last_u = -1, last_r = -1;
+  #pragma unroll 1
+  for (int u = 0, s = 0; u < U && nd > 0; ++u, s = (s + 1 == a.Sd) ? 0 : s + 1) {
+    if (!tb.blk[u]) continue;
+    #pragma unroll 1
+    for (int r = (warp - s * nd) & (kWarps - 1); r < nd; r += kWarps) {
+      last_u = u;
+      last_r = r;
+    }
+  }
+  if (!FAST && last_u < 0) bar_arrive(kBarPolled, kThreads);
+  int gd[NCH];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          v[u] = 0.0f;
-          const int r = r0 + u;
-          if (r < rows) {
-            const uint8_t* row = stg + (size_t)r * a.off.d_row;
+  for (int it = 0; it < NCH; ++it) gd[it] = (32 * (lane + 32 * it)) / a.g;
+  const int nchh = a.I / 32;
+  #pragma unroll 1
+  for (int u = 0, s = 0, fill = 0; u < U && nd > 0; ++u, s = (s + 1 == a.Sd) ? 0 : s + 1, fill += s == 0) {
+    if (!tb.blk[u]) continue;
+    #pragma unroll 1
+    for (int r = (warp - s * nd) & (kWarps - 1); r < nd; r += kWarps) {
+      // h of unit u complete in every block (bounded acquire poll; one
+      // token: the producer copied it into shared memory).
+      bool ok = true;
+      if (FAST) {
+        ok = __all_sync(0xffffffffu, wait_phase(&hfull[s], 0, abort_flag, a.ws));
+      } else if (lane == 0) {
+        unsigned tries = 0;
+        while (ld_acquire_gpu(&cnt[u]) < cnt_target) {
+          if (*abort_flag || ++tries > kSpinTries) {
+            if (!*abort_flag) {
+              *abort_flag = 1;
+              atomicOr(a.ws, 4);
+            }
+            ok = false;
+            break;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!FAST && u == last_u && r == last_r) bar_arrive(kBarPolled, kThreads);
+      const bool landed = __all_sync(0xffffffffu, wait_phase(&full_d[s], fill & 1, abort_flag, a.ws));
+      ok = ok && landed;
+      const int r0 = r * kDownRows;
+      const uint8_t* stg = ring_d + (size_t)s * a.sd + (size_t)r0 * a.off.d_row;
+      #pragma unroll 1
+      for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
+        const int p = tb.upairs[i] & 0xffff;
+        half2 hr[NCH][16];
+        float hsum[NCH], hback[NCH];
+#pragma unroll
+        for (int it = 0; it < NCH; ++it) {
+          const int cc = lane + 32 * it;
+          if (cc < nchh) {
+            if (FAST) hsum[it] = load_scaled_chunk<true>(hsm + (size_t)u * a.I + 32 * cc, hr[it], hback[it]);
+            else hsum[it] = load_scaled_chunk<false>(a.hbuf + (size_t)p * a.I + 32 * cc, hr[it], hback[it]);
+          }
+        }
+        float v[kDownRows];
+#pragma unroll
+        for (int q = 0; q < kDownRows; ++q) {
+          v[q] = 0.0f;
+          if (r0 + q < rd_rows) {
+            const uint8_t* row = stg + (size_t)q * a.off.d_row;
             const uint32_t* sz = reinterpret_cast<const uint32_t*>(row + a.off.d_sz);  // pairs per group
 #pragma unroll
-            for (int it = 0; it < kMaxHChunks; ++it) {
+            for (int it = 0; it < NCH; ++it) {
               const int cc = lane + 32 * it;
-              if (cc < nch) {
+              if (cc < nchh) {
                 const uint4 w = *reinterpret_cast<const uint4*>(row + a.off.d_q + 16 * cc);
-                const float2 s2 = __half22float2(u32_as_h2(sz[gix[it]]));  // (s, z)
+                const float2 s2 = __half22float2(u32_as_h2(sz[gd[it]]));  // (s, z)
                 const float d = (dot16_scaled(w.x, w.y, hr[it]) + dot16_scaled(w.z, w.w, hr[it] + 8)) * hback[it];
-                v[u] += s2.x * (d - s2.y * hsum[it]);
+                v[q] += s2.x * (d - s2.y * hsum[it]);
               }
             }
           }
         }
-        // Warp sums of the 8 rows by a reduce-scatter butterfly (9 shuffles
-        // instead of 40): each exchange keeps half of the remaining rows, so
-        // after distances 16, 8 and 4 a lane holds one row (bits 4, 3, 2 of
-        // the lane pick it) and distances 2 and 1 finish its sum.
+        // Warp sums of the 8 rows by a reduce-scatter butterfly (9 shuffles):
+        // each exchange keeps half of the remaining rows, so after distances
+        // 16, 8 and 4 a lane holds one row (lane bits 4, 3, 2 pick it) and
+        // distances 2 and 1 finish its sum.
         const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
         float w4[4], w2[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float keep = b4 ? v[4 + i] : v[i], send = b4 ? v[i] : v[4 + i];
-          w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        for (int q = 0; q < 4; ++q) {
+          const float keep = b4 ? v[4 + q] : v[q], send = b4 ? v[q] : v[4 + q];
+          w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float keep = b3 ? w4[2 + i] : w4[i], send = b3 ? w4[i] : w4[2 + i];
-          w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        for (int q = 0; q < 2; ++q) {
+          const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
+          w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
         }
         float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
         w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
         w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
-        const int u = 4 * b4 + 2 * b3 + b2;  // the row whose total this lane holds
-        if ((lane & 3) == 0 && r0 + u < rows) part[q * rows + r0 + u] = w1;
+        const int q = 4 * b4 + 2 * b3 + b2;  // the row whose total this lane holds
+        if ((lane & 3) == 0 && r0 + q < rd_rows) part[(size_t)p * a.rdn + r0 + q] = w1;
       }
-    } else if (lane == 0) {
-      for (int r = 0; r < rows; ++r) part[q * rows + r] = 0.0f;
+      __syncwarp();
+      if (lane == 0 && landed) mbar_arrive(&empty_d[s]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // compute warps only
+  bar_sync(kBarCompute, kThreads);
   // y[t][m0 + r] = sum_j w[t][j] * part[t*k + j][r] (+ y_shared), in j order.
-  for (int i = threadIdx.x; i < a.T * rows; i += kWarps * 32) {
-    const int t = i / rows, r = i - t * rows;
+  #pragma unroll 1
+  for (int i = tid; i < a.T * rd_rows; i += kWarps * 32) {
+    const int t = i / rd_rows, r = i - t * rd_rows;
     float v = 0.0f;
+    #pragma unroll 1
     for (int j = 0; j < a.k; ++j) {
-      const int q = t * a.k + j;
-      v += rt.w[q] * part[q * rows + r];
+      const int p = t * a.k + j;
+      if (tb.punit[p] >= 0) v += tb.w[p] * part[(size_t)p * a.rdn + r];
     }
     if (a.y_shared) v += __half2float(a.y_shared[(size_t)t * a.H + m0 + r]);
     a.y[(size_t)t * a.H + m0 + r] = __float2half_rn(v);
   }
 }
 
-int g_num_sms = 0;
+// ---- host side ----------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_num_sms[kMaxDevices] = {0};
+// Per device: the largest dynamic shared memory already granted to each kernel
+// instantiation (cudaFuncSetAttribute is called only when a launch needs more).
+int g_smem_set[kMaxDevices][3][2][2] = {};
 
-template <typename K>
-cudaError_t launch(K kern, const DecodeParams& a, size_t smem, int threads, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  // Ask for the full shared-memory carveout so that a block of the other
-  // decode kernel fits on the same SM (the down kernel prefetches while the
-  // gate/up kernel runs).
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
+int device_sms(int* dev_out, int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    g_num_sms[dev] = n;
+  }
+  *dev_out = dev;
+  *sms_out = g_num_sms[dev];
+  return MOE_OK;
+}
+
+template <int NCX, int NCH, bool FAST>
+cudaError_t launch_stream(int dev, const StreamParams& a, cudaStream_t st) {
+  auto kern = decode_stream_kernel<NCX, NCH, FAST>;
+  const int xi = NCX == 1 ? 0 : (NCX == 2 ? 1 : 2), hi = NCH - 1;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_smem_set[dev][xi][hi][FAST] < (int)a.smem) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
+      if (e != cudaSuccess) return e;
+      g_smem_set[dev][xi][hi][FAST] = (int)a.smem;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.G);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = a.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -753,23 +1101,62 @@ cudaError_t launch(K kern, const DecodeParams& a, size_t smem, int threads, cuda
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Carve-up: stages | part | route | barriers | block table. Returns total bytes.
-size_t carve(DecodeParams& a, size_t part, size_t budget) {
-  const size_t route = route_smem_bytes(a.P, a.T, a.E, a.logits != nullptr);
-  const size_t tail = ((part + 15) & ~(size_t)15) + ((route + 15) & ~(size_t)15) + 2 * kMaxStages * 8 +
-                      (size_t)a.P * 8 + 64;
-  if (tail + 2 * (size_t)a.st.bytes > budget) return 0;
-  a.stages = (int)std::min<size_t>(kMaxStages, (budget - tail) / a.st.bytes) & ~1;  // even
-  size_t o = (size_t)a.stages * a.st.bytes;
-  a.part_off = (uint32_t)o;
-  o = (o + part + 15) & ~(size_t)15;
-  a.route_off = (uint32_t)o;
-  o = (o + route + 15) & ~(size_t)15;
-  a.bar_off = (uint32_t)o;
-  o += 2 * kMaxStages * 8;
-  a.blk_off = (uint32_t)o;
-  o += (size_t)a.P * 8;
-  return o;
+template <int NCX, int NCH>
+cudaError_t launch_stream2(int dev, const StreamParams& a, cudaStream_t st) {
+  return a.fast1 ? launch_stream<NCX, NCH, true>(dev, a, st) : launch_stream<NCX, NCH, false>(dev, a, st);
+}
+
+constexpr size_t kSmemBudget = 227 * 1024;
+
+// Shared-memory carve-up: [ring_g | ring_d] (also the routing scratch) | x |
+// part | tables | barriers. Returns false when the shape does not fit.
+bool carve(StreamParams& a) {
+  const int Umax = std::min(a.P, a.E);
+  const size_t xbytes = (size_t)a.T * a.H * 2 + (size_t)a.T * (a.H / 32) * 8;
+  const size_t partb = (size_t)a.P * a.rdn * 4;
+  const size_t hstb = (size_t)a.P * a.rgu * 2;
+  const size_t tabb = tables_bytes(a.P, a.E);
+  // One routed token: the complete h of each pick is copied into shared
+  // memory for the down projection.
+  const bool want_fast = a.T == 1 && a.logits != nullptr && a.k <= kMaxRing;
+  const size_t hsmb = want_fast ? (size_t)a.k * a.I * 2 : 0;
+  auto r16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
+  const size_t fixed = r16(xbytes) + r16(partb) + r16(hstb) + r16(hsmb) + r16(tabb) + 5 * kMaxRing * 8;
+  if (fixed + a.sg + a.sd > kSmemBudget) return false;
+  const size_t ring = kSmemBudget - fixed;
+  int Sg = std::min(Umax, kMaxRing), Sd = std::min(Umax, kMaxRing);
+  if ((size_t)Sg * a.sg + (size_t)Sd * a.sd > ring) {
+    // Split the ring budget: about two thirds of the bytes to the gate/up ring.
+    Sg = (int)std::min<size_t>(Sg, std::max<size_t>(1, (ring * 2 / 3) / a.sg));
+    Sd = (int)std::min<size_t>(Sd, std::max<size_t>(1, (ring - (size_t)Sg * a.sg) / a.sd));
+    if ((size_t)Sg * a.sg + (size_t)Sd * a.sd > ring) return false;
+  }
+  a.Sg = Sg;
+  a.Sd = Sd;
+  // One routed token whose k picks all have their own stages: the producer
+  // warp routes and streams; gate/up items of one row spread the last
+  // expert's rows over more warps.
+  a.fast1 = (want_fast && a.k <= Sg && a.k <= Sd) ? 1 : 0;
+  size_t ringb = (size_t)Sg * a.sg + (size_t)Sd * a.sd;
+  if (a.fast1) ringb = std::max(ringb, (size_t)((a.E + 31) / 32) * std::min(a.k, 32) * 8 + (size_t)a.k * 4);
+  else ringb = std::max(ringb, (size_t)a.T * a.E * 4);  // routing scratch
+  size_t o = r16(ringb);
+  a.o_ring_d = (uint32_t)((size_t)Sg * a.sg);
+  a.o_x = (uint32_t)o;
+  o += r16(xbytes);
+  a.o_part = (uint32_t)o;
+  o += r16(partb);
+  a.o_hst = (uint32_t)o;
+  o += r16(hstb);
+  a.o_hsm = (uint32_t)o;
+  o += r16(hsmb);
+  a.o_small = (uint32_t)o;
+  o += r16(tabb);
+  a.o_bar = (uint32_t)o;
+  o += 5 * kMaxRing * 8;
+  if (o > kSmemBudget) return false;
+  a.smem = (uint32_t)o;
+  return true;
 }
 
 }  // namespace
@@ -779,47 +1166,36 @@ size_t fused_workspace_bytes(int H, int I, int T, int k) {
   return ws_scratch_offset(T * k) + (size_t)T * k * I * 2;
 }
 
-// Shared-memory budgets keep one block of each kernel resident on an SM at
-// the same time (the down kernel prefetches while the gate/up kernel runs).
-constexpr size_t kGateupBudget = 140 * 1024;
-constexpr size_t kDownBudget = 80 * 1024;
-
 int fused_forward_routed(const ForwardArgs& fa, const float* logits, int renorm, int32_t* ids_out,
                          float* wts_out) {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-  }
+  int dev = 0, sms = 0;
+  int rc = device_sms(&dev, &sms);
+  if (rc != MOE_OK) return rc;
   const int xc = (fa.H + 1023) / 1024, hc = (fa.I + 1023) / 1024;
   if (xc > 4 || hc > 2) return fail(MOE_ERR_UNSUPPORTED, "streamed decode: H <= 4096 and I <= 2048 only");
-  DecodeParams a;
+  if (fa.T > kMaxT || fa.T * fa.k > kMaxP || fa.E > kMaxE)
+    return fail(MOE_ERR_UNSUPPORTED, "streamed decode: T <= %d, T*k <= %d and E <= %d only", kMaxT, kMaxP, kMaxE);
+  StreamParams a;
   a.H = fa.H; a.I = fa.I; a.g = fa.g; a.T = fa.T; a.k = fa.k; a.E = fa.E; a.n_slots = fa.n_slots;
   a.P = fa.T * fa.k;
-  a.G = g_num_sms;
+  a.G = sms;
   a.x = fa.x; a.ids = fa.ids; a.wts = fa.weights; a.pool = fa.pool; a.block_bytes = fa.block_bytes;
   a.logits = logits; a.renorm = renorm; a.ids_out = ids_out; a.wts_out = wts_out;
   a.off = fa.off; a.slot_of = fa.slot_of; a.y_shared = fa.y_shared; a.y = fa.y;
   uint8_t* ws = static_cast<uint8_t*>(fa.ws);
-  a.flags = reinterpret_cast<int32_t*>(ws);
+  a.ws = reinterpret_cast<int32_t*>(ws);
   a.hbuf = reinterpret_cast<__half*>(ws + ws_scratch_offset(a.P));
-  const int rgu = (a.I + a.G - 1) / a.G, rdn = (a.H + a.G - 1) / a.G;
-
-  DecodeParams ag = a;
-  ag.st = stage_of(rgu, a.off.gu_row);
-  const size_t smem_g = carve(ag, (size_t)a.H * 2 + (size_t)(a.H / 32) * 8, kGateupBudget);
-  DecodeParams ad = a;
-  ad.st = stage_of(rdn, a.off.d_row);
-  const size_t smem_d = carve(ad, (size_t)a.P * rdn * 4, kDownBudget);
-  if (!smem_g || !smem_d) return fail(MOE_ERR_UNSUPPORTED, "streamed decode: shapes exceed shared memory");
+  a.rgu = (a.I + a.G - 1) / a.G;
+  a.rdn = (a.H + a.G - 1) / a.G;
+  a.sg = align16((uint32_t)a.rgu * fa.off.gu_row);
+  a.sd = align16((uint32_t)a.rdn * fa.off.d_row);
+  if (!carve(a)) return fail(MOE_ERR_UNSUPPORTED, "streamed decode: shapes exceed shared memory");
   cudaError_t e;
-  if (xc <= 2) e = launch(decode_gateup_kernel<2>, ag, smem_g, kGateThreads, fa.stream);
-  else e = launch(decode_gateup_kernel<4>, ag, smem_g, kGateThreads, fa.stream);
-  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode gate/up launch: %s", cudaGetErrorString(e));
-  if (hc <= 1) e = launch(decode_down_kernel<1>, ad, smem_d, kThreads, fa.stream);
-  else e = launch(decode_down_kernel<2>, ad, smem_d, kThreads, fa.stream);
-  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode down launch: %s", cudaGetErrorString(e));
+  cudaStream_t st = fa.stream;
+  if (xc == 1) e = hc == 1 ? launch_stream2<1, 1>(dev, a, st) : launch_stream2<1, 2>(dev, a, st);
+  else if (xc == 2) e = hc == 1 ? launch_stream2<2, 1>(dev, a, st) : launch_stream2<2, 2>(dev, a, st);
+  else e = hc == 1 ? launch_stream2<4, 1>(dev, a, st) : launch_stream2<4, 2>(dev, a, st);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "decode stream launch: %s", cudaGetErrorString(e));
   return MOE_OK;
 }
 

@@ -9,11 +9,14 @@
 namespace moe {
 namespace {
 
-// Pairs at or below this count take the GEMV path under MOE_PATH_AUTO.
+// Batches the streamed decode kernel takes under MOE_PATH_AUTO: up to 16
+// tokens and 256 (token, choice) pairs; larger batches take the grouped path.
+constexpr int kAutoGemvMaxTokens = 16;
 constexpr int kAutoGemvMaxPairs = 256;
 
 int pick_path(int path, int T, int k) {
-  if (path == MOE_PATH_AUTO) return (T * k <= kAutoGemvMaxPairs) ? MOE_PATH_GEMV : MOE_PATH_GROUPED;
+  if (path == MOE_PATH_AUTO)
+    return (T <= kAutoGemvMaxTokens && T * k <= kAutoGemvMaxPairs) ? MOE_PATH_GEMV : MOE_PATH_GROUPED;
   return path;
 }
 
@@ -160,7 +163,7 @@ int moe_layer_forward(const moe_expert_shape* s, const void* x, const float* log
   if (!x || !logits || !ids || !weights || !pool || !slot_of || !y || !workspace)
     return moe::fail(MOE_ERR_ARG, "moe_layer_forward: NULL pointer");
   const int p = moe::pick_path(path, T, k);
-  if (p == MOE_PATH_GEMV && (long long)T * E * E <= 262144) {
+  if (p == MOE_PATH_GEMV) {
     if (reinterpret_cast<uintptr_t>(workspace) % 256 || reinterpret_cast<uintptr_t>(pool) % 256 ||
         reinterpret_cast<uintptr_t>(x) % 16)
       return moe::fail(MOE_ERR_ARG, "moe_layer_forward: workspace/pool must be 256-byte and x 16-byte aligned");

@@ -71,9 +71,10 @@ extern "C" int moe_layer_forward_noalloc(const moe_expert_shape* s, const void* 
   int rc = moe::scratch_address(&ws);
   if (rc != MOE_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The error word must start at zero for this call.
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
-  if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "clearing the scratch error word: %s", cudaGetErrorString(e));
+  // The header (error word, the kernel's counters) must start at zero for
+  // this call, whatever an earlier call left in it.
+  cudaError_t e = cudaMemsetAsync(ws, 0, moe::ws_scratch_offset(T * k), st);
+  if (e != cudaSuccess) return moe::fail(MOE_ERR_CUDA, "clearing the scratch header: %s", cudaGetErrorString(e));
   const moe::BlockLayout bl = moe::block_layout(s->hidden, s->inter, s->group);
   moe::ForwardArgs a;
   a.H = s->hidden; a.I = s->inter; a.g = s->group; a.T = T; a.k = k; a.E = E; a.n_slots = n_slots;
@@ -88,15 +89,24 @@ extern "C" int moe_layer_forward_noalloc(const moe_expert_shape* s, const void* 
   a.ws = ws;
   a.ws_bytes = moe::kNoAllocScratchBytes;
   a.stream = st;
-  if ((long long)T * E * E <= 262144) {
-    rc = moe::fused_forward_routed(a, logits, renorm, ids, weights);
-  } else {
-    rc = moe_route(logits, T, E, k, renorm, ids, weights, nullptr, stream);
-    if (rc == MOE_OK) rc = moe::fused_forward(a);
-  }
+  rc = moe::fused_forward_routed(a, logits, renorm, ids, weights);
   if (rc == MOE_ERR_UNSUPPORTED)
     return moe::fail(MOE_ERR_UNSUPPORTED,
-                     "moe_layer_forward_noalloc: shape outside the streamed decode kernels (H <= 4096, "
-                     "I <= 2048, shared-memory fit)");
+                     "moe_layer_forward_noalloc: request outside the streamed decode kernel (H <= 4096, "
+                     "I <= 2048, T <= 16, T*k <= 256, E <= 1024, shared-memory fit)");
   return rc;
+}
+
+extern "C" int moe_layer_forward_noalloc_flags(int32_t* flags_out, void* stream) {
+  moe::clear_error();
+  if (!flags_out) return moe::fail(MOE_ERR_ARG, "moe_layer_forward_noalloc_flags: NULL flags_out");
+  void* ws = nullptr;
+  int rc = moe::scratch_address(&ws);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(flags_out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess)
+    return moe::fail(MOE_ERR_CUDA, "moe_layer_forward_noalloc_flags: %s", cudaGetErrorString(e));
+  return MOE_OK;
 }

@@ -102,6 +102,7 @@ _SIGS = {
     "moe_expert_forward_zero_copy": (_I, [_SHAPE, _P, _I, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_forward": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _I, _P]),
     "moe_layer_forward_noalloc": (_I, [_SHAPE, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P]),
+    "moe_layer_forward_noalloc_flags": (_I, [ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_workspace_clear_flags": (_I, [_P, _P]),
     "moe_workspace_flags": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_shared_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -338,6 +339,13 @@ def moe_layer_forward_noalloc(shape, x: torch.Tensor, logits: torch.Tensor, k: i
         _dev(pool, torch.uint8, "pool", n_slots * bb), _dev(slot_of, torch.int32, "slot_of", E), n_slots,
         _dev(y_shared, torch.float16, "y_shared", T * H, nullable=True), _dev(y, torch.float16, "y", T * H),
         _stream(stream)), "moe_layer_forward_noalloc")
+
+
+def moe_layer_forward_noalloc_flags(stream=None) -> int:
+    """Error word of the last moe_layer_forward_noalloc call on the current device (synchronises)."""
+    v = ctypes.c_int32(0)
+    _check(_lib.moe_layer_forward_noalloc_flags(ctypes.byref(v), _stream(stream)), "moe_layer_forward_noalloc_flags")
+    return v.value
 
 
 def moe_workspace_clear_flags(workspace: torch.Tensor, stream=None) -> None:

@@ -36,8 +36,6 @@ shared path's output; the decayed-count policy steps below.
 """
 from __future__ import annotations
 
-import math
-
 import numpy as np
 
 
@@ -396,10 +394,6 @@ def hit_ceiling(p, C: int) -> float:
 def expert_block_bytes(H: int, I: int, g: int) -> int:
     """Bytes of one expert: 3*H*I/2 code bytes + FP16 scale and zero per group."""
     return 3 * H * I // 2 + 3 * (H * I // g) * 2 * 2
-
-
-def silu_scalar(v: float) -> float:
-    return v / (1.0 + math.exp(-v))
 
 
 # --------------------------------------------------------------------------

@@ -110,7 +110,7 @@ def _layer_case(shape, E, k, renorm, T, seed, zero="eight", path=1, shared=False
     return y
 
 
-GEMV_PATHS = [1, 3]  # fused one-kernel decode, unfused two-kernel decode
+GEMV_PATHS = [1, 3]  # streamed decode kernels, unfused two-kernel GEMV
 
 
 @pytest.mark.parametrize("path", GEMV_PATHS)

@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("shape,E,k,renorm,T", [((2048, 1024, 128), 64, 8, False, 1),
-                                                ((256, 128, 64), 8, 2, True, 4)])
+                                                ((256, 128, 64), 8, 2, True, 4),
+                                                ((2048, 512, 128), 512, 10, True, 2)])
 def test_noalloc_matches_workspace_entry_point_twice(shape, E, k, renorm, T):
     moe = binding()
     H = shape[0]
@@ -39,7 +40,8 @@ def test_noalloc_matches_workspace_entry_point_twice(shape, E, k, renorm, T):
         w_b = torch.empty((T, k), dtype=torch.float32, device=dev)
         y_b = torch.empty((T, H), dtype=torch.float16, device=dev)
         moe.moe_layer_forward_noalloc(shape, x, lg, k, renorm, ids_b, w_b, lp.pool, lp.slot_of, E, None, y_b)
-        torch.cuda.synchronize()
+        assert moe.moe_layer_forward_noalloc_flags() == 0, call
+        assert moe.moe_workspace_flags(ws) == 0, call
         assert np.array_equal(ids_a.cpu().numpy(), ids_b.cpu().numpy()), call
         assert np.allclose(w_a.cpu().numpy(), w_b.cpu().numpy(), rtol=1e-6, atol=0), call
         ok, err, bound = tol_ok(y_b.float().cpu().numpy(), y_a.float().cpu().numpy())
