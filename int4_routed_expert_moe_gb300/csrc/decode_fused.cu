@@ -344,14 +344,15 @@ __device__ __forceinline__ void stage_x_chunk(const __half* __restrict__ src, ui
   xback[cc] = pow2f(24 - sh);
 }
 
-// Gate and up sums of up to two rows (same pair) for one lane, before the
-// warp sum: s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks
-// cc = lane + 32 it. The activation chunk is loaded once for both rows.
+// Gate and up sums of up to kGateRows rows (same pair) for one lane, before
+// the warp sum: s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks
+// cc = lane + 32 it. The activation chunk is loaded once for all rows; the
+// rows' dot products are independent chains. acc = (g0, u0, g1, u1, ...).
+constexpr int kGateRows = 4;  // rows per gate/up work item
 template <int NC>
-__device__ __forceinline__ void gate_up_rows(const uint8_t* r0, const uint8_t* r1, bool two,
-                                             const BlockOffsets& off, int nch, int lane, const int* gq,
-                                             const uint4* xs4, const float* xsum, const float* xback,
-                                             float (&acc)[4]) {
+__device__ __forceinline__ void gate_up_rows(const uint8_t* row0, int nrows, const BlockOffsets& off, int nch,
+                                             int lane, const int* gq, const uint4* xs4, const float* xsum,
+                                             const float* xback, float (&acc)[2 * kGateRows]) {
 #pragma unroll
   for (int it = 0; it < NC; ++it) {
     const int cc = lane + 32 * it;
@@ -362,25 +363,19 @@ __device__ __forceinline__ void gate_up_rows(const uint8_t* r0, const uint8_t* r
       const half2* xa = reinterpret_cast<const half2*>(&xv[0]);  // pieces 0, 1 are contiguous
       const half2* xb = reinterpret_cast<const half2*>(&xv[2]);
       const float back = xback[cc], xsm = xsum[cc];
-      {
-        const uint4 wg = *reinterpret_cast<const uint4*>(r0 + off.gu_q_gate + 16 * cc);
-        const uint4 wu = *reinterpret_cast<const uint4*>(r0 + off.gu_q_up + 16 * cc);
-        const uint2 q = reinterpret_cast<const uint2*>(r0 + off.gu_sz)[gq[it]];
-        const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
-        const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
-        const float2 sgz = __half22float2(u32_as_h2(q.x)), suz = __half22float2(u32_as_h2(q.y));
-        acc[0] += sgz.x * (dg - sgz.y * xsm);
-        acc[1] += suz.x * (du - suz.y * xsm);
-      }
-      if (two) {
-        const uint4 wg = *reinterpret_cast<const uint4*>(r1 + off.gu_q_gate + 16 * cc);
-        const uint4 wu = *reinterpret_cast<const uint4*>(r1 + off.gu_q_up + 16 * cc);
-        const uint2 q = reinterpret_cast<const uint2*>(r1 + off.gu_sz)[gq[it]];
-        const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
-        const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
-        const float2 sgz = __half22float2(u32_as_h2(q.x)), suz = __half22float2(u32_as_h2(q.y));
-        acc[2] += sgz.x * (dg - sgz.y * xsm);
-        acc[3] += suz.x * (du - suz.y * xsm);
+#pragma unroll
+      for (int rr = 0; rr < kGateRows; ++rr) {
+        if (rr < nrows) {
+          const uint8_t* r = row0 + (size_t)rr * off.gu_row;
+          const uint4 wg = *reinterpret_cast<const uint4*>(r + off.gu_q_gate + 16 * cc);
+          const uint4 wu = *reinterpret_cast<const uint4*>(r + off.gu_q_up + 16 * cc);
+          const uint2 q = reinterpret_cast<const uint2*>(r + off.gu_sz)[gq[it]];
+          const float dg = (dot16_scaled(wg.x, wg.y, xa) + dot16_scaled(wg.z, wg.w, xb)) * back;
+          const float du = (dot16_scaled(wu.x, wu.y, xa) + dot16_scaled(wu.z, wu.w, xb)) * back;
+          const float2 sgz = __half22float2(u32_as_h2(q.x)), suz = __half22float2(u32_as_h2(q.y));
+          acc[2 * rr] += sgz.x * (dg - sgz.y * xsm);
+          acc[2 * rr + 1] += suz.x * (du - suz.y * xsm);
+        }
       }
     }
   }
@@ -407,13 +402,19 @@ constexpr int kBarPolled = 3;   // compute warps arrive after their last counter
 //      is among its own segment's best k);
 //   2. each candidate counts the candidates that rank before it: its count
 //      is its rank among all E experts when it is below k.
-// Three block barriers; the logits and the slot table go to shared memory
+// Four block barriers; the logits and the slot table go to shared memory
 // on the way. On return tb.ids[0..k) and pv[0..k) hold the picks and their
 // logits (tb.misc[3] set: the token has NaN/+inf logits, or all -inf).
-__device__ void route_one_token(const StreamParams& a, const Tables& tb, float* cv, int32_t* ci, float* pv,
+__host__ __device__ inline int route_candidates(int E, int k) { return (((E + 31) / 32) * k + 3) & ~3; }
+
+__device__ void route_one_token(const StreamParams& a, const Tables& tb, uint8_t* scratch, float* pv,
                                 uint4* xs4, float* xsum, float* xback) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, kk = min(k, 32), nseg = (E + 31) / 32, C = nseg * kk;
+  const int C4 = route_candidates(E, kk);  // candidates padded to whole 16-byte groups
+  float* cv = reinterpret_cast<float*>(scratch);
+  int32_t* ci = reinterpret_cast<int32_t*>(cv + C4);
+  int32_t* crank = ci + C4;
   const int nchx = a.H / 32;
   bool bad = false;
   int ninf = 0;
@@ -426,9 +427,10 @@ __device__ void route_one_token(const StreamParams& a, const Tables& tb, float* 
     ninf += v == -INFINITY;
   }
 #pragma unroll 1
-  for (int c = tid; c < C; c += kThreads) {
+  for (int c = tid; c < C4; c += kThreads) {
     cv[c] = -INFINITY;
     ci[c] = INT_MAX;
+    crank[c] = 0;
   }
 #pragma unroll 1
   for (int cc = tid; cc < nchx; cc += kThreads) stage_x_chunk(a.x, xs4, xsum, xback, cc);
@@ -441,6 +443,7 @@ __device__ void route_one_token(const StreamParams& a, const Tables& tb, float* 
   __syncthreads();
   if (tb.misc[3] || tb.misc[4] == E) {
     if (tid == 0) tb.misc[3] = 1;
+    __syncthreads();
     __syncthreads();
     __syncthreads();
     return;
@@ -461,17 +464,34 @@ __device__ void route_one_token(const StreamParams& a, const Tables& tb, float* 
     }
   }
   __syncthreads();
+  // Candidate c's comparisons are split over `parts` threads (c, part), each
+  // reading 4 candidates per 16-byte load; the partial counts are added.
+  const int parts = max(1, min(8, kThreads / C));
+  const int span = ((C4 / 4 + parts - 1) / parts) * 4;
 #pragma unroll 1
-  for (int c = tid; c < C; c += kThreads) {
+  for (int t = tid; t < C * parts; t += kThreads) {
+    const int part = t / C, c = t - part * C;
     const float v = cv[c];
     const int i = ci[c];
     if (i == INT_MAX) continue;
-    int rank = 0;
-#pragma unroll 4
-    for (int j = 0; j < C; ++j) rank += ranks_before(cv[j], ci[j], v, i);
-    if (rank < k) {
-      tb.ids[rank] = i;
-      pv[rank] = v;
+    int cnt = 0;
+    const int j1 = min(C4, (part + 1) * span);
+#pragma unroll 2
+    for (int j = part * span; j < j1; j += 4) {
+      const float4 v4 = *reinterpret_cast<const float4*>(cv + j);
+      const int4 i4 = *reinterpret_cast<const int4*>(ci + j);
+      cnt += ranks_before(v4.x, i4.x, v, i) + ranks_before(v4.y, i4.y, v, i) + ranks_before(v4.z, i4.z, v, i) +
+             ranks_before(v4.w, i4.w, v, i);
+    }
+    if (cnt) atomicAdd(&crank[c], cnt);
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int c = tid; c < C; c += kThreads) {
+    const int rank = crank[c];
+    if (ci[c] != INT_MAX && rank < k) {
+      tb.ids[rank] = ci[c];
+      pv[rank] = cv[c];
     }
   }
   __syncthreads();
@@ -585,6 +605,62 @@ __device__ void prefetch_one_token(const StreamParams& a, const Tables& tb, __ha
   }
 }
 
+// Down rows [r0, r0 + nrows) (nrows <= kDownRows) of one pair, from the
+// stage row `stg` (row r0): part_row[q] = (W_d h)[m0 + r0 + q], the block's
+// output rows. h (the pair's FP16 intermediate, I values) is read from shared
+// memory (SMEM) or through L2, as the scaled pairs of dot16_scaled.
+template <int NCH, bool SMEM>
+__device__ __forceinline__ void down_rows(const uint8_t* stg, int nrows, const BlockOffsets& off, const __half* h,
+                                          int nchh, int lane, const int* gd, float* part_row) {
+  half2 hr[NCH][16];
+  float hsum[NCH], hback[NCH];
+#pragma unroll
+  for (int it = 0; it < NCH; ++it) {
+    const int cc = lane + 32 * it;
+    if (cc < nchh) hsum[it] = load_scaled_chunk<SMEM>(h + 32 * cc, hr[it], hback[it]);
+  }
+  float v[kDownRows];
+#pragma unroll
+  for (int q = 0; q < kDownRows; ++q) {
+    v[q] = 0.0f;
+    if (q < nrows) {
+      const uint8_t* row = stg + (size_t)q * off.d_row;
+      const uint32_t* sz = reinterpret_cast<const uint32_t*>(row + off.d_sz);  // pairs per group
+#pragma unroll
+      for (int it = 0; it < NCH; ++it) {
+        const int cc = lane + 32 * it;
+        if (cc < nchh) {
+          const uint4 w = *reinterpret_cast<const uint4*>(row + off.d_q + 16 * cc);
+          const float2 s2 = __half22float2(u32_as_h2(sz[gd[it]]));  // (s, z)
+          const float d = (dot16_scaled(w.x, w.y, hr[it]) + dot16_scaled(w.z, w.w, hr[it] + 8)) * hback[it];
+          v[q] += s2.x * (d - s2.y * hsum[it]);
+        }
+      }
+    }
+  }
+  // Warp sums of the 8 rows by a reduce-scatter butterfly (9 shuffles): each
+  // exchange keeps half of the remaining rows, so after distances 16, 8 and 4
+  // a lane holds one row (lane bits 4, 3, 2 pick it) and distances 2 and 1
+  // finish its sum.
+  const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+  float w4[4], w2[2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float keep = b4 ? v[4 + q] : v[q], send = b4 ? v[q] : v[4 + q];
+    w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
+    w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+  w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+  w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+  const int q = 4 * b4 + 2 * b3 + b2;  // the row whose total this lane holds
+  if ((lane & 3) == 0 && q < nrows) part_row[q] = w1;
+}
+
 template <int NCX, int NCH, bool FAST>
 __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const StreamParams a) {
   extern __shared__ __align__(128) uint8_t sm[];
@@ -593,8 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
   const int n0 = (int)(((long long)c * a.I) / a.G), n1 = (int)(((long long)(c + 1) * a.I) / a.G);
   const int m0 = (int)(((long long)c * a.H) / a.G), m1 = (int)(((long long)(c + 1) * a.H) / a.G);
   const int rg_rows = n1 - n0, rd_rows = m1 - m0;
-  constexpr int grow = 2;                                  // gate/up rows per item
-  const int ng = (rg_rows + grow - 1) / grow;              // gate/up items per unit
+  const int ng = (rg_rows + kGateRows - 1) / kGateRows;   // gate/up items per unit
   const int nd = (rd_rows + kDownRows - 1) / kDownRows;   // down items per unit
   uint8_t* ring_g = sm;
   uint8_t* ring_d = sm + a.o_ring_d;
@@ -640,11 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
   if constexpr (FAST) {
     // ---- one token routed in the block: see route_one_token ----------------
     // Routing scratch in the rings (no copy is issued before the picks).
-    const int C = ((a.E + 31) / 32) * min(a.k, 32);
-    float* cv = reinterpret_cast<float*>(sm);
-    int32_t* ci = reinterpret_cast<int32_t*>(cv + C);
-    float* pv = reinterpret_cast<float*>(ci + C);
-    route_one_token(a, tb, cv, ci, pv, xs4, xsum, xback);
+    float* pv = reinterpret_cast<float*>(sm) + 3 * route_candidates(a.E, min(a.k, 32));
+    route_one_token(a, tb, sm, pv, xs4, xsum, xback);
     if (warp == kProducer) {
       producer_one_token(a, tb, pv, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
       bar_arrive(kBarCompute, kThreads);  // weights ready for the combine
@@ -880,32 +952,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     #pragma unroll 1
     for (int r = (warp - s * ng) & (kWarps - 1); r < ng; r += kWarps) {
       const bool ok = __all_sync(0xffffffffu, wait_phase(&full_g[s], fill & 1, abort_flag, a.ws));
-      const int ra = r * grow;
-      const bool two = grow == 2 && ra + 1 < rg_rows;
+      const int ra = r * kGateRows;
+      const int nrows = min(kGateRows, rg_rows - ra);
       const uint8_t* rowa = ring_g + (size_t)s * a.sg + (size_t)ra * a.off.gu_row;
-      const uint8_t* rowb = rowa + a.off.gu_row;
       #pragma unroll 1
       for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
         const int p = tb.upairs[i] & 0xffff, t = tb.upairs[i] >> 16;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        gate_up_rows<NCX>(rowa, rowb, two, a.off, nchx, lane, gq, xs4 + (size_t)t * nchx * 4,
-                          xsum + (size_t)t * nchx, xback + (size_t)t * nchx, acc);
-        // Reduce-scatter butterfly of the four sums (7 shuffles): lanes with
-        // bit 4 clear end with row a's sums, set row b's; bit 3 clear the
-        // gate sum, set the up sum; lanes 0 / 16 then take the up sum of
-        // their row from lane 8 / 24.
-        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1;
-        const float k0 = b4 ? acc[2] : acc[0], k1 = b4 ? acc[3] : acc[1];
-        const float w0 = k0 + __shfl_xor_sync(0xffffffffu, b4 ? acc[0] : acc[2], 16);
-        const float w1 = k1 + __shfl_xor_sync(0xffffffffu, b4 ? acc[1] : acc[3], 16);
-        float v = (b3 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b3 ? w0 : w1, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        float acc[2 * kGateRows];
+#pragma unroll
+        for (int q = 0; q < 2 * kGateRows; ++q) acc[q] = 0.0f;
+        gate_up_rows<NCX>(rowa, nrows, a.off, nchx, lane, gq, xs4 + (size_t)t * nchx * 4, xsum + (size_t)t * nchx,
+                          xback + (size_t)t * nchx, acc);
+        // Warp sums of the 8 values (gate, up of 4 rows) by a reduce-scatter
+        // butterfly (9 shuffles): after distances 16, 8 and 4 a lane holds
+        // value 4*b4 + 2*b3 + b2 (lane bits), distances 2 and 1 finish it;
+        // lanes with b2 clear hold a gate sum and take the row's up sum from
+        // the lane 4 above.
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+        float w4[4], w2[2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float keep = b4 ? acc[4 + q] : acc[q], send = b4 ? acc[q] : acc[4 + q];
+          w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
+          w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        float v = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         v += __shfl_xor_sync(0xffffffffu, v, 1);
-        const float up = __shfl_xor_sync(0xffffffffu, v, 8);
-        __half* hp = hst + (size_t)p * a.rgu + ra;
-        if (lane == 0) hp[0] = __float2half_rn(silu_f(v) * up);
-        if (lane == 16 && two) hp[1] = __float2half_rn(silu_f(v) * up);
+        const float up = __shfl_xor_sync(0xffffffffu, v, 4);
+        const int rr = 2 * b4 + b3;  // the row whose gate sum this lane holds (b2 clear)
+        if ((lane & 7) == 0 && rr < nrows)
+          hst[(size_t)p * a.rgu + ra + rr] = __float2half_rn(silu_f(v) * up);
       }
       // The warp that completes the unit in this block publishes the block's
       // h rows of every pair of the unit and releases the unit (one release
@@ -954,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     #pragma unroll 1
     for (int r = (warp - s * nd) & (kWarps - 1); r < nd; r += kWarps) {
       // h of unit u complete in every block (bounded acquire poll; one
-      // token: the producer copied it into shared memory).
+      // token: the producer warp copied it into shared memory).
       bool ok = true;
       if (FAST) {
         ok = __all_sync(0xffffffffu, wait_phase(&hfull[s], 0, abort_flag, a.ws));
@@ -980,56 +1061,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       #pragma unroll 1
       for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
         const int p = tb.upairs[i] & 0xffff;
-        half2 hr[NCH][16];
-        float hsum[NCH], hback[NCH];
-#pragma unroll
-        for (int it = 0; it < NCH; ++it) {
-          const int cc = lane + 32 * it;
-          if (cc < nchh) {
-            if (FAST) hsum[it] = load_scaled_chunk<true>(hsm + (size_t)u * a.I + 32 * cc, hr[it], hback[it]);
-            else hsum[it] = load_scaled_chunk<false>(a.hbuf + (size_t)p * a.I + 32 * cc, hr[it], hback[it]);
-          }
-        }
-        float v[kDownRows];
-#pragma unroll
-        for (int q = 0; q < kDownRows; ++q) {
-          v[q] = 0.0f;
-          if (r0 + q < rd_rows) {
-            const uint8_t* row = stg + (size_t)q * a.off.d_row;
-            const uint32_t* sz = reinterpret_cast<const uint32_t*>(row + a.off.d_sz);  // pairs per group
-#pragma unroll
-            for (int it = 0; it < NCH; ++it) {
-              const int cc = lane + 32 * it;
-              if (cc < nchh) {
-                const uint4 w = *reinterpret_cast<const uint4*>(row + a.off.d_q + 16 * cc);
-                const float2 s2 = __half22float2(u32_as_h2(sz[gd[it]]));  // (s, z)
-                const float d = (dot16_scaled(w.x, w.y, hr[it]) + dot16_scaled(w.z, w.w, hr[it] + 8)) * hback[it];
-                v[q] += s2.x * (d - s2.y * hsum[it]);
-              }
-            }
-          }
-        }
-        // Warp sums of the 8 rows by a reduce-scatter butterfly (9 shuffles):
-        // each exchange keeps half of the remaining rows, so after distances
-        // 16, 8 and 4 a lane holds one row (lane bits 4, 3, 2 pick it) and
-        // distances 2 and 1 finish its sum.
-        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
-        float w4[4], w2[2];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float keep = b4 ? v[4 + q] : v[q], send = b4 ? v[q] : v[4 + q];
-          w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
-          w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-        float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
-        w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
-        w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
-        const int q = 4 * b4 + 2 * b3 + b2;  // the row whose total this lane holds
-        if ((lane & 3) == 0 && r0 + q < rd_rows) part[(size_t)p * a.rdn + r0 + q] = w1;
+        const int nr = min(kDownRows, rd_rows - r0);
+        if (FAST)
+          down_rows<NCH, true>(stg, nr, a.off, hsm + (size_t)u * a.I, nchh, lane, gd, part + (size_t)p * a.rdn + r0);
+        else
+          down_rows<NCH, false>(stg, nr, a.off, a.hbuf + (size_t)p * a.I, nchh, lane, gd, part + (size_t)p * a.rdn + r0);
       }
       __syncwarp();
       if (lane == 0 && landed) mbar_arrive(&empty_d[s]);
@@ -1120,6 +1156,7 @@ bool carve(StreamParams& a) {
   // memory for the down projection.
   const bool want_fast = a.T == 1 && a.logits != nullptr && a.k <= kMaxRing;
   const size_t hsmb = want_fast ? (size_t)a.k * a.I * 2 : 0;
+
   auto r16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
   const size_t fixed = r16(xbytes) + r16(partb) + r16(hstb) + r16(hsmb) + r16(tabb) + 5 * kMaxRing * 8;
   if (fixed + a.sg + a.sd > kSmemBudget) return false;
@@ -1138,7 +1175,7 @@ bool carve(StreamParams& a) {
   // expert's rows over more warps.
   a.fast1 = (want_fast && a.k <= Sg && a.k <= Sd) ? 1 : 0;
   size_t ringb = (size_t)Sg * a.sg + (size_t)Sd * a.sd;
-  if (a.fast1) ringb = std::max(ringb, (size_t)((a.E + 31) / 32) * std::min(a.k, 32) * 8 + (size_t)a.k * 4);
+  if (a.fast1) ringb = std::max(ringb, (size_t)route_candidates(a.E, std::min(a.k, 32)) * 12 + (size_t)a.k * 4);
   else ringb = std::max(ringb, (size_t)a.T * a.E * 4);  // routing scratch
   size_t o = r16(ringb);
   a.o_ring_d = (uint32_t)((size_t)Sg * a.sg);
@@ -1150,6 +1187,7 @@ bool carve(StreamParams& a) {
   o += r16(hstb);
   a.o_hsm = (uint32_t)o;
   o += r16(hsmb);
+
   a.o_small = (uint32_t)o;
   o += r16(tabb);
   a.o_bar = (uint32_t)o;

@@ -48,11 +48,11 @@ __device__ __forceinline__ half2 dot8_scaled(uint32_t w, const half2* xp, half2 
   return acc;
 }
 
-// 16 codes (two words); each FP16 lane sums 8 products, then FP32.
+// 16 codes (two words); each FP16 lane sums 8 products -- the two words'
+// 4-product chains side by side, then added -- and is widened to FP32.
 __device__ __forceinline__ float dot16_scaled(uint32_t w0, uint32_t w1, const half2* xp) {
-  half2 acc = __float2half2_rn(0.0f);
-  acc = dot8_scaled(w0, xp, acc);
-  acc = dot8_scaled(w1, xp + 4, acc);
+  const half2 zero = __float2half2_rn(0.0f);
+  const half2 acc = __hadd2(dot8_scaled(w0, xp, zero), dot8_scaled(w1, xp + 4, zero));
   return __low2float(acc) + __high2float(acc);
 }
 
