@@ -7,29 +7,29 @@
 //
 // One block per SM (G blocks). Block c owns gate/up rows n in
 // [c*I/G, (c+1)*I/G) and output rows m in [c*H/G, (c+1)*H/G) of every expert
-// the step uses. Per call:
-//   1. Routing (moe_layer_forward) inside every block: one warp per token
-//      picks the top-k by (logit desc, index asc) and forms the softmax
-//      weights with the same fixed-order reductions as moe_route, so all
-//      blocks hold identical ids and weights. The token activations are
+// the step uses; a "unit" is one distinct expert of the call, read once
+// however many tokens chose it. Per call:
+//   1. Routing (moe_layer_forward) inside every block with moe_route's
+//      selection (top-k by (logit desc, index asc)) and softmax arithmetic,
+//      so all blocks hold identical ids and weights; the activations are
 //      staged in shared memory meanwhile.
-//   2. The (token, choice) pairs are grouped by expert (ascending expert id,
-//      pairs in ascending order inside an expert): a "unit" is one distinct
-//      expert, read once per call however many tokens chose it.
-//   3. A producer lane streams the block's rows of every unit into two rings
-//      of shared-memory stages with bulk async copies (cp.async.bulk,
-//      completion counted on mbarriers): the gate/up rows first, the down
-//      rows as soon as the first gate/up copies are out, so the down weights
-//      stream while the gate/up rows are computed.
-//   4. Compute warps form h = silu(W_g x) * (W_u x) for their rows of every
-//      pair of a unit, round it to FP16 (the explicit rounding point) into
-//      the workspace, and count the unit as done on a per-unit counter in
-//      global memory (release).
-//   5. A down item of unit u waits (acquire, bounded) until every block has
-//      counted u, reads the complete h of each pair of u through L2 and
-//      forms the block's output rows of W_d h per pair.
-//   6. y[t][m] = sum_j w[t][j] * (W_d h[t*k+j])[m] (+ y_shared), the k pairs
+//   2. A producer lane streams the block's rows of every unit into shared-
+//      memory stages with bulk async copies (cp.async.bulk, completion
+//      counted on mbarriers).
+//   3. Compute warps form h = silu(W_g x) * (W_u x) for their rows of every
+//      pair of a unit and round it to FP16 (the explicit rounding point)
+//      into the workspace.
+//   4. Once every block's h rows of a unit are out, the down rows of the
+//      unit form the block's output rows of W_d h per pair.
+//   5. y[t][m] = sum_j w[t][j] * (W_d h[t*k+j])[m] (+ y_shared), the k pairs
 //      of a token combined in j order (deterministic).
+// One routed token (the decode step proper): the whole block routes the
+// token, every pick has its own stages, each unit is released on its own
+// global counter and an exchange warp copies each unit's complete h into
+// shared memory as soon as every block has released it. Several tokens: one
+// ring of stages filled in order (every unit's gate/up rows, then the down
+// rows of groups of units), work items dealt round-robin to the compute
+// warps, and one grid barrier between the gate/up and the down items.
 // The last block to finish resets the counters, so the workspace is reusable
 // by the next call on the same stream. All waits are bounded; on expiry bit 2
 // of the workspace error word is set and the block stops waiting.
@@ -45,13 +45,16 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 16;                    // compute warps
-constexpr int kThreads = (kWarps + 1) * 32;   // + one producer warp
+constexpr int kThreads = (kWarps + 2) * 32;   // + producer warp + exchange warp
 constexpr int kProducer = kWarps;
+constexpr int kExchange = kWarps + 1;
 constexpr int kMaxT = 16;                     // tokens per call
 constexpr int kMaxP = 256;                    // (token, choice) pairs per call
 constexpr int kMaxE = 1024;                   // experts (in-block tables)
-constexpr int kMaxRing = 16;                  // stages per ring
+constexpr int kMaxRing = 32;                  // stages per ring
+constexpr int kMaxFastK = 16;                 // one routed token: picks that each get their own stages
 constexpr int kDownRows = 8;                  // rows per down work item
+constexpr int kPairsDown = 2;                 // batched: pairs per down work item
 constexpr unsigned kMbarTries = 50000;        // ~1 s (20 us suspend hint per try)
 constexpr unsigned kIdleTries = 16000000;     // ~1 s of idle producer loop iterations
 constexpr unsigned kSpinTries = 2000000;      // ~1 s of counter polls (one L2 round trip each)
@@ -79,15 +82,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(20000u) : "memory");
-  return ok != 0;
-}
-// Non-blocking test of a phase.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -155,8 +149,9 @@ struct StreamParams {
   int32_t* ws;          // workspace words: [0] error, [1] done, [kCntBase + u] unit counters
   __half* hbuf;         // workspace: h [P][I]
   int H, I, g, T, k, E, n_slots, P, G;
-  int Sg, Sd;           // stages of the gate/up and down rings
-  uint32_t sg, sd;      // bytes of one stage
+  int Sg, Sd;           // one token: stages of the gate/up and down rings; batched: Sg stages, Sd = 0
+  uint32_t sg, sd;      // one token: bytes of a stage of each ring; batched: stage bytes, one unit's down rows
+  int dpack;            // batched: units whose down rows share a stage
   int rgu, rdn;         // largest row counts of a block
   int fast1;            // one token routed in the block, every unit with its own stages
   // shared-memory carve-up (byte offsets)
@@ -172,7 +167,10 @@ struct Tables {
   int32_t* uexp;        // [P] expert of each unit
   int32_t* uoff;        // [P+1] first sorted pair of each unit
   int32_t* upairs;      // [P] pairs sorted by unit
-  int32_t* udone;       // [P] gate/up items finished per unit (this block)
+  int32_t* udone;       // [P] one token: gate/up items finished per unit (this block)
+  int32_t* gio;         // [P+1] batched: first gate/up item of each unit
+  int32_t* dio;         // [P+1] batched: first down item of each unit
+  int32_t* fdone;       // [2P] batched: items finished per ring fill
   int32_t* ecnt;        // [E] pairs per expert, then first sorted position
   int32_t* eunit;       // [E] unit of each expert
   int32_t* eslot;       // [E] copy of slot_of
@@ -182,7 +180,7 @@ struct Tables {
 };
 
 __host__ __device__ inline size_t tables_bytes(int P, int E) {
-  return (size_t)P * 8 + (size_t)P * 4 * 7 + 4 + (size_t)E * 4 * 4 + 32;
+  return (size_t)P * 8 + ((size_t)P * 11 + 3 + (size_t)E * 4 + 8) * 4;
 }
 
 __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) {
@@ -196,7 +194,10 @@ __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) 
   t.uoff = t.uexp + a.P;
   t.upairs = t.uoff + a.P + 1;
   t.udone = t.upairs + a.P;
-  t.ecnt = t.udone + a.P;
+  t.gio = t.udone + a.P;
+  t.dio = t.gio + a.P + 1;
+  t.fdone = t.dio + a.P + 1;
+  t.ecnt = t.fdone + 2 * a.P;
   t.eunit = t.ecnt + a.E;
   t.eslot = t.eunit + a.E;
   t.lg = reinterpret_cast<float*>(t.eslot + a.E);
@@ -219,95 +220,12 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 }
 
 // "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
-// experts of each token. One warp, one token, logits lg[E] in shared memory.
-// Same definition and the same arithmetic as moe_route: top-k by (logit
-// desc, index asc); softmax over all E (per-lane sums in index order, then a
-// butterfly), renormalised over the k when asked. A token with NaN/+inf
-// logits or all -inf gets ids -1 and weights 0.
+// experts of each token: top-k by (logit desc, index asc), softmax over all
+// E, renormalised over the k when asked -- moe_route's definition. A token
+// with NaN/+inf logits or all -inf gets ids -1 and weights 0. a ranks before
+// b in (value desc, index asc); -0 == +0 by IEEE compare.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
-}
-
-// Lane l owns elements l, l + 32, ...; it keeps its best element not yet
-// taken. Each round the warp's best candidate is the next pick (lane r keeps
-// pick r), and only the lane that owned it rescans its elements for the best
-// one ranking after it. Returns false for a token without a routing.
-__device__ __forceinline__ bool topk_warp(const float* lg, int E, int k, int lane, float& my_v, int& my_i) {
-  const unsigned full = 0xffffffffu;
-  bool bad = false;
-  int ninf = 0;
-  float cv = -INFINITY;
-  int ci = INT_MAX;
-#pragma unroll 4
-  for (int e = lane; e < E; e += 32) {
-    const float v = lg[e];
-    bad |= isnan(v) || v == INFINITY;
-    ninf += v == -INFINITY;
-    if (ranks_before(v, e, cv, ci)) {
-      cv = v;
-      ci = e;
-    }
-  }
-  bad = __any_sync(full, bad);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ninf += __shfl_xor_sync(full, ninf, o);
-  if (bad || ninf == E) return false;
-#pragma unroll 1
-  for (int r = 0; r < k; ++r) {
-    float bv = cv;
-    int bi = ci;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(full, bv, o);
-      const int oi = __shfl_xor_sync(full, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == r) {
-      my_v = bv;
-      my_i = bi;
-    }
-    if ((bi & 31) == lane) {  // this lane's candidate was taken
-      cv = -INFINITY;
-      ci = INT_MAX;
-#pragma unroll 4
-      for (int e = lane; e < E; e += 32) {
-        const float v = lg[e];
-        if (ranks_before(bv, bi, v, e) && ranks_before(v, e, cv, ci)) {
-          cv = v;
-          ci = e;
-        }
-      }
-    }
-  }
-  return true;
-}
-
-// Softmax weight of lane's pick (lane < k): exp(l - max) over the sum over
-// all E (or over the k picks when renormalised).
-__device__ __forceinline__ float pick_weight(const float* lg, int E, int k, int renorm, int lane, float my_v) {
-  const float m = __shfl_sync(0xffffffffu, my_v, 0);
-  float s_all = 0.0f;
-#pragma unroll 4
-  for (int e = lane; e < E; e += 32) s_all += expf(lg[e] - m);
-  s_all = warp_sum(s_all);
-  const float mine = lane < k ? expf(my_v - m) : 0.0f;
-  const float s_sel = warp_sum(mine);
-  return mine / (renorm ? s_sel : s_all);
-}
-
-__device__ void route_warp(const float* lg, int E, int k, int renorm, int lane, int32_t* ids_out,
-                           float* w_out) {
-  float my_v = 0.0f;
-  int my_i = -1;
-  const bool ok = topk_warp(lg, E, k, lane, my_v, my_i);
-  const float wq = ok ? pick_weight(lg, E, k, renorm, lane, my_v) : 0.0f;
-  if (lane < k) {
-    ids_out[lane] = ok ? my_i : -1;
-    w_out[lane] = wq;
-  }
 }
 
 // The activations of a token in shared memory as the scaled pairs of
@@ -381,6 +299,31 @@ __device__ __forceinline__ void gate_up_rows(const uint8_t* row0, int nrows, con
   }
 }
 
+// Warp sums of the 8 values (gate, up of 4 rows) by a reduce-scatter
+// butterfly (9 shuffles): after distances 16, 8 and 4 a lane holds value
+// 4*b4 + 2*b3 + b2 (lane bits), distances 2 and 1 finish it; lanes with b2
+// clear hold a gate sum and take the row's up sum from the lane 4 above.
+// Lanes with (lane & 7) == 0 return silu(gate) * up of row 2*b4 + b3.
+__device__ __forceinline__ float swiglu_lanes(const float (&acc)[2 * kGateRows], int lane) {
+  const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+  float w4[4], w2[2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float keep = b4 ? acc[4 + q] : acc[q], send = b4 ? acc[q] : acc[4 + q];
+    w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
+    w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float v = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  const float up = __shfl_xor_sync(0xffffffffu, v, 4);
+  return silu_f(v) * up;
+}
+
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -390,9 +333,10 @@ __device__ __forceinline__ void bar_arrive(int id, int n) { asm volatile("bar.ar
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // Named barriers (0 is __syncthreads).
-constexpr int kBarCompute = 1;  // compute warps wait, producer arrives (weights and tables final)
+constexpr int kBarCompute = 1;  // before the combine: compute warps (and, batched, the producer) wait
 constexpr int kBarTables = 2;   // producer arrives with the routing tables, compute warps wait
-constexpr int kBarPolled = 3;   // compute warps arrive after their last counter poll, producer waits
+constexpr int kBarGate = 3;     // batched: the compute warps around the grid barrier
+constexpr int kBarPolled = 4;   // exchange warp arrives after its last counter poll, producer waits (64)
 
 // "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
 // experts of the token. The whole block routes one token in two stages, the
@@ -497,6 +441,75 @@ __device__ void route_one_token(const StreamParams& a, const Tables& tb, uint8_t
   __syncthreads();
 }
 
+// Batched routing: warp t routes token t from its logits in shared memory
+// (lane l looks at experts l, l + 32, ...). Round r picks the best expert
+// that ranks after round r-1's pick, so no taken mask is needed; the
+// selection and the softmax arithmetic are moe_route's (sum over all E per
+// lane in index order, then a butterfly). A token with NaN/+inf logits, or
+// with every logit -inf, gets ids -1 and weights 0.
+__device__ void route_token_warp(const StreamParams& a, const Tables& tb, const float* lg, int t) {
+  const int lane = threadIdx.x & 31, E = a.E, k = a.k;
+  const unsigned full = 0xffffffffu;
+  bool bad = false;
+  int ninf = 0;
+#pragma unroll 4
+  for (int e = lane; e < E; e += 32) {
+    const float v = lg[e];
+    bad |= isnan(v) || v == INFINITY;
+    ninf += v == -INFINITY;
+  }
+  bad = __any_sync(full, bad);
+  ninf = __reduce_add_sync(full, ninf);
+  if (bad || ninf == E) {
+    if (lane < k) {
+      tb.ids[t * k + lane] = -1;
+      tb.w[t * k + lane] = 0.0f;
+    }
+    return;
+  }
+  float prev_v = INFINITY, my_v = 0.0f;
+  int prev_i = -1, my_i = -1;
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll 4
+    for (int e = lane; e < E; e += 32) {
+      const float v = lg[e];
+      if (ranks_before(prev_v, prev_i, v, e) && ranks_before(v, e, bv, bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(full, bv, o);
+      const int oi = __shfl_xor_sync(full, bi, o);
+      if (ranks_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == r) {
+      my_v = bv;
+      my_i = bi;
+    }
+    prev_v = bv;
+    prev_i = bi;
+  }
+  const float m = __shfl_sync(full, my_v, 0);
+  float s_all = 0.0f;
+#pragma unroll 4
+  for (int e = lane; e < E; e += 32) s_all += expf(lg[e] - m);
+  s_all = warp_sum(s_all);
+  const float mine = lane < k ? expf(my_v - m) : 0.0f;
+  const float s_sel = warp_sum(mine);
+  if (lane < k) {
+    tb.ids[t * k + lane] = my_i;
+    tb.w[t * k + lane] = mine / (a.renorm ? s_sel : s_all);
+  }
+}
+
 // Producer warp after route_one_token: lane j < k resolves pick j's expert
 // block, the warp writes the tables the compute warps read (units are the
 // picks in choice order; every unit has its own stage in both rings) and
@@ -575,7 +588,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// prefetch_one_token (producer warp, one decode token): lane u watches unit
+// prefetch_one_token (exchange warp, one decode token): lane u watches unit
 // u (the k <= 32 units are polled together, one load per round); once every
 // block has released it (acquire), the lane copies the unit's complete h into
 // shared memory with a bulk copy, after a proxy fence (the h rows were written
@@ -661,6 +674,23 @@ __device__ __forceinline__ void down_rows(const uint8_t* stg, int nrows, const B
   if ((lane & 3) == 0 && q < nrows) part_row[q] = w1;
 }
 
+// Batched path: wait (bounded) until the producer has issued fill `lap` of
+// stage s, so that the stage's mbarrier is at that fill's phase.
+__device__ __forceinline__ bool wait_fill(const int32_t* fillno, int s, int lap, volatile int32_t* abort_flag,
+                                          int32_t* err) {
+  unsigned tries = 0;
+  #pragma unroll 1
+  while (*(const volatile int32_t*)&fillno[s] <= lap) {
+    if (*abort_flag) return false;
+    if (++tries > kIdleTries) {
+      *abort_flag = 1;
+      atomicOr(err, 4);
+      return false;
+    }
+  }
+  return true;
+}
+
 template <int NCX, int NCH, bool FAST>
 __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const StreamParams a) {
   extern __shared__ __align__(128) uint8_t sm[];
@@ -685,6 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
   uint64_t* full_d = empty_g + kMaxRing;
   uint64_t* empty_d = full_d + kMaxRing;
   uint64_t* hfull = empty_d + kMaxRing;  // one token: h of unit u landed in hsm
+  // Batched path: fills issued per stage (the producer raises it after each
+  // fill), so a consumer of fill n waits on the right phase from any warp.
+  int32_t* fillno = reinterpret_cast<int32_t*>(hfull + kMaxRing);
   const Tables tb = tables_of(a, sm);
   volatile int32_t* abort_flag = tb.misc + 1;
   const bool writer = c == 0;
@@ -695,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     #pragma unroll 1
     for (int s = 0; s < a.Sg; ++s) {
       mbar_init(&full_g[s], 1);
-      mbar_init(&empty_g[s], ng > 0 ? ng : 1);
+      mbar_init(&empty_g[s], (FAST && ng > 0) ? ng : 1);  // batched: the fill's last item arrives
     }
     #pragma unroll 1
     for (int s = 0; s < a.Sd; ++s) {
@@ -703,6 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       mbar_init(&empty_d[s], nd > 0 ? nd : 1);
       mbar_init(&hfull[s], 1);
     }
+    for (int s = 0; s < kMaxRing; ++s) fillno[s] = 0;
     tb.misc[1] = 0;
     tb.misc[3] = 0;
     tb.misc[4] = 0;
@@ -725,38 +759,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     }
     griddep_launch_dependents();
   } else {
-    // ---- routing (one warp per token) or the given ids; activations ---------
+    // ---- batched: logits (or the given ids), slot table, activations -------
+    float* lgT = reinterpret_cast<float*>(sm);  // [T][E], routing scratch in the ring (no copy issued yet)
+    if (a.logits) {
+      const int n = a.T * a.E;
+      if ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0 && (n & 3) == 0) {
+        const float4* src = reinterpret_cast<const float4*>(a.logits);
+        float4* dst = reinterpret_cast<float4*>(lgT);
+        #pragma unroll 4
+        for (int i = tid; i < n / 4; i += kThreads) dst[i] = __ldcg(src + i);
+      } else {
+        #pragma unroll 4
+        for (int i = tid; i < n; i += kThreads) lgT[i] = __ldcg(a.logits + i);
+      }
+    }
     #pragma unroll 1
     for (int e = tid; e < a.E; e += kThreads) {
       tb.ecnt[e] = 0;
       tb.eslot[e] = __ldcg(a.slot_of + e);
     }
     #pragma unroll 1
-    for (int p = tid; p < a.P; p += kThreads) tb.udone[p] = 0;
-    if (a.logits) {
-      if (warp < a.T) {
-        float* lg = reinterpret_cast<float*>(sm) + (size_t)warp * a.E;  // scratch in the rings
-        #pragma unroll 1
-        for (int e = lane; e < a.E; e += 32) lg[e] = __ldcg(a.logits + (size_t)warp * a.E + e);
-        __syncwarp();
-        route_warp(lg, a.E, a.k, a.renorm, lane, tb.ids + warp * a.k, tb.w + warp * a.k);
-        __syncwarp();
-        if (writer && lane < a.k) {
-          if (a.ids_out) a.ids_out[warp * a.k + lane] = tb.ids[warp * a.k + lane];
-          if (a.wts_out) a.wts_out[warp * a.k + lane] = tb.w[warp * a.k + lane];
-        }
-      }
-    } else {
-      #pragma unroll 1
-      for (int p = tid; p < a.P; p += kThreads) {
-        tb.ids[p] = __ldcg(a.ids + p);
-        tb.w[p] = __ldcg(a.wts + p);
-        if (writer) {
-          if (a.ids_out) a.ids_out[p] = tb.ids[p];
-          if (a.wts_out) a.wts_out[p] = tb.w[p];
-        }
-      }
-    }
+    for (int q = tid; q < 2 * a.P; q += kThreads) tb.fdone[q] = 0;
     #pragma unroll 1
     for (int i = tid; i < a.T * nchx; i += kThreads) {
       const int t = i / nchx, cc = i - t * nchx;
@@ -764,10 +787,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
                     xback + (size_t)t * nchx, cc);
     }
     __syncthreads();
-    // Usable pairs, counted per expert.
+    if (a.logits) {
+      #pragma unroll 1
+      for (int t = warp; t < a.T; t += kThreads / 32) route_token_warp(a, tb, lgT + (size_t)t * a.E, t);
+    } else {
+      #pragma unroll 1
+      for (int p = tid; p < a.P; p += kThreads) {
+        tb.ids[p] = __ldcg(a.ids + p);
+        tb.w[p] = __ldcg(a.wts + p);
+      }
+    }
+    __syncthreads();
+    // Usable pairs, counted per expert; block 0 writes the routing out.
     #pragma unroll 1
     for (int p = tid; p < a.P; p += kThreads) {
       const int e = tb.ids[p];
+      if (writer) {
+        if (a.ids_out) a.ids_out[p] = e;
+        if (a.wts_out) a.wts_out[p] = tb.w[p];
+      }
       int u = -1;
       if (e >= 0 && e < a.E) {
         const int s = tb.eslot[e];
@@ -783,7 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       tb.punit[p] = u;
     }
     __syncthreads();
-    // Units: experts with pairs, in ascending id (one warp, exclusive scans).
+    // Units (experts with pairs, ascending id) and their work items, by one
+    // warp with exclusive scans: per unit, a gate/up item for every (pair,
+    // row group) and a down item for every (group of kPairsDown pairs,
+    // 8-row group).
     if (warp == 0) {
       const int per = (a.E + 31) / 32;
       const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
@@ -811,107 +852,125 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
           tb.uexp[u] = e;
           tb.uoff[u] = pos;
           tb.blk[u] = a.pool + (size_t)tb.eslot[e] * a.block_bytes;
-          tb.ecnt[e] = pos;
+          tb.ecnt[e] = pos;  // placement cursor
           ++u;
           pos += n;
         }
       }
+      const int U = __shfl_sync(0xffffffffu, su, 31);
       if (lane == 31) {
-        tb.misc[0] = su;
-        tb.uoff[su] = sp;
+        tb.misc[0] = U;
+        tb.uoff[U] = sp;
+      }
+      __syncwarp();
+      const int per2 = (U + 31) / 32;
+      const int u0 = min(U, lane * per2), u1 = min(U, u0 + per2);
+      int gi = 0, di = 0;
+      #pragma unroll 1
+      for (int v = u0; v < u1; ++v) {
+        const int n = tb.uoff[v + 1] - tb.uoff[v];
+        gi += n * ng;
+        di += nd * ((n + kPairsDown - 1) / kPairsDown);
+      }
+      int sg = gi, sd = di;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vg = __shfl_up_sync(0xffffffffu, sg, o), vd = __shfl_up_sync(0xffffffffu, sd, o);
+        if (lane >= o) {
+          sg += vg;
+          sd += vd;
+        }
+      }
+      int g = sg - gi, d = sd - di;
+      #pragma unroll 1
+      for (int v = u0; v < u1; ++v) {
+        const int n = tb.uoff[v + 1] - tb.uoff[v];
+        tb.gio[v] = g;
+        tb.dio[v] = d;
+        g += n * ng;
+        d += nd * ((n + kPairsDown - 1) / kPairsDown);
+      }
+      if (lane == 31) {
+        tb.gio[U] = sg;
+        tb.dio[U] = sd;
       }
     }
     __syncthreads();
+    // Pairs under their unit. Atomic cursors: the order of a unit's pairs
+    // changes no result (every pair has its own h and its own down rows).
     #pragma unroll 1
     for (int p = tid; p < a.P; p += kThreads) {
       if (tb.punit[p] < 0) continue;
       const int e = tb.ids[p];
-      int rank = 0;
-      #pragma unroll 1
-      for (int q = 0; q < p; ++q) rank += tb.punit[q] >= 0 && tb.ids[q] == e;
-      tb.upairs[tb.ecnt[e] + rank] = p | ((p / a.k) << 16);  // pair, and its token above bit 16
+      tb.upairs[atomicAdd(&tb.ecnt[e], 1)] = p | ((p / a.k) << 16);  // pair, and its token above bit 16
       tb.punit[p] = tb.eunit[e];
     }
     __syncthreads();
     griddep_launch_dependents();
 
-    // ---- producer: both rings, gate/up first ------------------------------
+    // ---- producer: one ring, fills in order --------------------------------
+    // Fill q < Ug is unit q's gate/up rows; fill Ug + j holds the down rows
+    // of units j*dpack .. j*dpack + dpack - 1 (their slices side by side).
+    // Fill q goes to stage q % S once the stage's previous fill is consumed;
+    // the down fills need nothing but a free stage, so they stream while the
+    // last gate/up rows are computed and while the blocks meet.
     if (warp == kProducer && lane == 0) {
       const int U = tb.misc[0];
+      const int Ug = ng > 0 ? U : 0, Q = Ug + (nd > 0 ? (U + a.dpack - 1) / a.dpack : 0);
       const uint32_t gbytes = (uint32_t)rg_rows * a.off.gu_row, dbytes = (uint32_t)rd_rows * a.off.d_row;
-      int qg = ng > 0 ? 0 : U, qd = nd > 0 ? 0 : U;
-      const int first_g = min(U, a.Sg);
-      unsigned idle = 0;
-      while ((qg < U || qd < U) && !*abort_flag) {
-        bool issued = false;
-        if (qg < U) {
-          const int s = qg % a.Sg;
-          if (qg < a.Sg || mbar_test(&empty_g[s], ((qg / a.Sg) - 1) & 1)) {
-            mbar_arrive_expect_tx(&full_g[s], gbytes);
-            bulk_g2s(ring_g + (size_t)s * a.sg, tb.blk[qg] + (size_t)n0 * a.off.gu_row, gbytes, &full_g[s]);
-            ++qg;
-            issued = true;
-          }
-        }
-        if (!issued && qd < U && (qg >= first_g || ng == 0)) {
-          const int s = qd % a.Sd;
-          if (qd < a.Sd || mbar_test(&empty_d[s], ((qd / a.Sd) - 1) & 1)) {
-            mbar_arrive_expect_tx(&full_d[s], dbytes);
-            bulk_g2s(ring_d + (size_t)s * a.sd, tb.blk[qd] + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes,
-                     &full_d[s]);
-            ++qd;
-            issued = true;
-          }
-        }
-        if (issued) {
-          idle = 0;
+      int q = 0;
+      #pragma unroll 1
+      for (int s = 0, lap = 0; q < Q; ++q) {
+        if (lap > 0 && !wait_phase(&empty_g[s], (lap - 1) & 1, abort_flag, a.ws)) break;
+        uint8_t* dst = ring_g + (size_t)s * a.sg;
+        if (q < Ug) {
+          mbar_arrive_expect_tx(&full_g[s], gbytes);
+          bulk_g2s(dst, tb.blk[q] + (size_t)n0 * a.off.gu_row, gbytes, &full_g[s]);
         } else {
-          if (++idle > kIdleTries) {
-            *abort_flag = 1;
-            atomicOr(a.ws, 4);
-            break;
-          }
+          const int u0 = (q - Ug) * a.dpack, u1 = min(U, u0 + a.dpack);
+          mbar_arrive_expect_tx(&full_g[s], (uint32_t)(u1 - u0) * dbytes);
+          #pragma unroll 1
+          for (int u = u0; u < u1; ++u)
+            bulk_g2s(dst + (size_t)(u - u0) * a.sd, tb.blk[u] + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes,
+                     &full_g[s]);
+        }
+        *(volatile int32_t*)&fillno[s] = lap + 1;
+        if (++s == a.Sg) {
+          s = 0;
+          ++lap;
         }
       }
       // Before the block may exit, every copy it issued has landed (bounded):
-      // a slot is refilled only after its consumers drained the previous
-      // fill, so the last fill's parity is unambiguous.
-      if (ng > 0 && (qg < U || *abort_flag)) {
+      // no fill follows the last one of each stage, so its parity is final.
+      #pragma unroll 1
+      for (int s = 0; s < a.Sg && s < q; ++s) {
+        const int last = s + a.Sg * ((q - 1 - s) / a.Sg);
         #pragma unroll 1
-        for (int s = 0; s < a.Sg && s < qg; ++s) {
-          const int last = s + a.Sg * ((qg - 1 - s) / a.Sg);
-          #pragma unroll 1
-          for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_g[s], (last / a.Sg) & 1); ++i) {
-          }
-        }
-      }
-      if (nd > 0 && (qd < U || *abort_flag)) {
-        #pragma unroll 1
-        for (int s = 0; s < a.Sd && s < qd; ++s) {
-          const int last = s + a.Sd * ((qd - 1 - s) / a.Sd);
-          #pragma unroll 1
-          for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_d[s], (last / a.Sd) & 1); ++i) {
-          }
+        for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_g[s], (last / a.Sg) & 1); ++i) {
         }
       }
     }
   }
   const int U = tb.misc[0];
 
-  if (warp == kProducer) {
-    __syncwarp();
+  if (warp == kExchange) {
+    // One token: the exchange warp polls the other blocks and copies each
+    // unit's complete h into shared memory (the batched path meets the
+    // other blocks once, in the compute warps).
+    bar_arrive(kBarCompute, kThreads);
     if constexpr (FAST) {
-      // One token: the producer warp polls the other blocks and copies the
-      // complete h of each unit into shared memory for the down items.
       prefetch_one_token(a, tb, hsm, hfull, U, cnt_target, abort_flag);
       __syncwarp();
-    } else {
-      bar_arrive(kBarCompute, kThreads);
-      // After every compute warp's last counter poll.
-      bar_sync(kBarPolled, kThreads);
+      bar_arrive(kBarPolled, 64);
     }
-    // Count the block out; the last block out resets the unit counters for
-    // the next call (every block has passed all of its waits on them).
+    return;
+  }
+  if (warp == kProducer) {
+    __syncwarp();
+    if constexpr (FAST) bar_sync(kBarPolled, 64);  // the exchange warp's last poll is done
+    else bar_sync(kBarCompute, kThreads);          // the compute warps passed the grid barrier
+    // Count the block out; the last block out resets the counters for the
+    // next call (every block has passed all of its waits on them).
     if (lane == 0) {
       if (FAST && *abort_flag) {  // copies of an aborted block land before it exits
         #pragma unroll 1
@@ -929,146 +988,188 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
         }
       }
       if (atom_add_acq_rel_gpu(&a.ws[1], 1) == a.G - 1) {
-        #pragma unroll 1
-        for (int u = 0; u < U; ++u) a.ws[kCntBase + u] = 0;
+        if constexpr (FAST) {
+          #pragma unroll 1
+          for (int u = 0; u < U; ++u) a.ws[kCntBase + u] = 0;
+        } else {
+          a.ws[kCntBase] = 0;
+        }
         a.ws[1] = 0;
       }
     }
     return;
   }
 
-  // ---- compute warps: gate/up items, then down items -------------------------
-  // Item (u, r) of a ring stage s = u % S belongs to warp (s * n + r) % kWarps,
-  // so every fill of a stage is drained by the same warps in increasing u
-  // (no warp waits on a fill two phases ahead of one it has not drained).
-  // Each warp walks the units once, keeping the stage and its fill count,
-  // and visits only its own items of each unit.
-  int gq[NCX];
-#pragma unroll
-  for (int it = 0; it < NCX; ++it) gq[it] = (32 * (lane + 32 * it)) / a.g;
-  #pragma unroll 1
-  for (int u = 0, s = 0, fill = 0; u < U && ng > 0; ++u, s = (s + 1 == a.Sg) ? 0 : s + 1, fill += s == 0) {
-    if (!tb.blk[u]) continue;
+  if constexpr (FAST) {
+    // ---- compute warps ---------------------------------------------------------
+    // One token: every unit has its own stages (filled once). Item (u, r)
+    // belongs to warp (u * n + r) % kWarps; gate/up items first, then down.
+    int gq[NCX];
+  #pragma unroll
+    for (int it = 0; it < NCX; ++it) gq[it] = (32 * (lane + 32 * it)) / a.g;
     #pragma unroll 1
-    for (int r = (warp - s * ng) & (kWarps - 1); r < ng; r += kWarps) {
-      const bool ok = __all_sync(0xffffffffu, wait_phase(&full_g[s], fill & 1, abort_flag, a.ws));
+    for (int u = 0, s = 0, fill = 0; u < U && ng > 0; ++u, s = (s + 1 == a.Sg) ? 0 : s + 1, fill += s == 0) {
+      if (!tb.blk[u]) continue;
+      #pragma unroll 1
+      for (int r = (warp - s * ng) & (kWarps - 1); r < ng; r += kWarps) {
+        const bool ok = __all_sync(0xffffffffu, wait_phase(&full_g[s], fill & 1, abort_flag, a.ws));
+        const int ra = r * kGateRows;
+        const int nrows = min(kGateRows, rg_rows - ra);
+        const uint8_t* rowa = ring_g + (size_t)s * a.sg + (size_t)ra * a.off.gu_row;
+        #pragma unroll 1
+        for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
+          const int p = tb.upairs[i] & 0xffff, t = tb.upairs[i] >> 16;
+          float acc[2 * kGateRows];
+  #pragma unroll
+          for (int q = 0; q < 2 * kGateRows; ++q) acc[q] = 0.0f;
+          gate_up_rows<NCX>(rowa, nrows, a.off, nchx, lane, gq, xs4 + (size_t)t * nchx * 4, xsum + (size_t)t * nchx,
+                            xback + (size_t)t * nchx, acc);
+          const float hv = swiglu_lanes(acc, lane);
+          const int rr = 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);  // the lane's row (lanes 0, 8, 16, 24)
+          if ((lane & 7) == 0 && rr < nrows) hst[(size_t)p * a.rgu + ra + rr] = __float2half_rn(hv);
+        }
+        // The warp that completes the unit in this block publishes the block's
+        // h rows of every pair of the unit and releases the unit (one release
+        // per unit and block).
+        __syncwarp();
+        int last = 0;
+        if (lane == 0 && ok) {
+          mbar_arrive(&empty_g[s]);
+          __threadfence_block();
+          last = atomicAdd(&tb.udone[u], 1) == ng - 1;
+        }
+        if (last && lane == 0) {
+          // Lane 0 stores the block's h rows of every pair of the unit itself,
+          // so the release orders exactly its own stores before the count.
+          __threadfence_block();  // the other warps' staged h (counted above)
+          #pragma unroll 1
+          for (int i = tb.uoff[u]; i < tb.uoff[u + 1]; ++i) {
+            const int p = tb.upairs[i] & 0xffff;
+            #pragma unroll 1
+            for (int q = 0; q < rg_rows; ++q) a.hbuf[(size_t)p * a.I + n0 + q] = hst[(size_t)p * a.rgu + q];
+          }
+          red_release_gpu_add(&cnt[u], 1);
+        }
+        __syncwarp();
+      }
+    }
+    int gd[NCH];
+  #pragma unroll
+    for (int it = 0; it < NCH; ++it) gd[it] = (32 * (lane + 32 * it)) / a.g;
+    const int nchh = a.I / 32;
+    #pragma unroll 1
+    for (int u = 0, s = 0, fill = 0; u < U && nd > 0; ++u, s = (s + 1 == a.Sd) ? 0 : s + 1, fill += s == 0) {
+      if (!tb.blk[u]) continue;
+      #pragma unroll 1
+      for (int r = (warp - s * nd) & (kWarps - 1); r < nd; r += kWarps) {
+        // h of unit u complete in every block: the exchange warp copied it
+        // into shared memory.
+        bool ok = __all_sync(0xffffffffu, wait_phase(&hfull[s], 0, abort_flag, a.ws));
+        const bool landed = __all_sync(0xffffffffu, wait_phase(&full_d[s], fill & 1, abort_flag, a.ws));
+        ok = ok && landed;
+        const int r0 = r * kDownRows;
+        const uint8_t* stg = ring_d + (size_t)s * a.sd + (size_t)r0 * a.off.d_row;
+        #pragma unroll 1
+        for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
+          const int p = tb.upairs[i] & 0xffff;
+          const int nr = min(kDownRows, rd_rows - r0);
+          down_rows<NCH, true>(stg, nr, a.off, hsm + (size_t)u * a.I, nchh, lane, gd, part + (size_t)p * a.rdn + r0);
+        }
+        __syncwarp();
+        if (lane == 0 && landed) mbar_arrive(&empty_d[s]);
+      }
+    }
+  } else {
+    // Batched: the work items are dealt round-robin to the compute warps
+    // (item j to warp j % kWarps), gate/up items first. A consumer of fill q
+    // first waits until the producer has issued it (the stage's fill
+    // number), so the stage's mbarrier is at that very phase; the warp that
+    // finishes the last item of a fill frees its stage.
+    const unsigned full = 0xffffffffu;
+    const int Ug = ng > 0 ? U : 0;
+    int gq[NCX];
+#pragma unroll
+    for (int it = 0; it < NCX; ++it) gq[it] = (32 * (lane + 32 * it)) / a.g;
+    int gd[NCH];
+#pragma unroll
+    for (int it = 0; it < NCH; ++it) gd[it] = (32 * (lane + 32 * it)) / a.g;
+    const int nchh = a.I / 32;
+    bool ok = true;
+    // ---- gate/up: item i of unit u is (pair i / ng, row group i % ng) -------
+    const int NG = ng > 0 ? tb.gio[U] : 0;
+    int u = 0;
+    #pragma unroll 1
+    for (int j = warp; j < NG; j += kWarps) {
+      while (tb.gio[u + 1] <= j) ++u;
+      const int i = j - tb.gio[u], c = i / ng, r = i - c * ng;
+      const int s = u % a.Sg, lap = u / a.Sg;
+      ok = __all_sync(full, wait_fill(fillno, s, lap, abort_flag, a.ws) &&
+                                wait_phase(&full_g[s], lap & 1, abort_flag, a.ws));
+      if (!ok) break;
+      const int pr = tb.upairs[tb.uoff[u] + c], p = pr & 0xffff, t = pr >> 16;
       const int ra = r * kGateRows;
       const int nrows = min(kGateRows, rg_rows - ra);
-      const uint8_t* rowa = ring_g + (size_t)s * a.sg + (size_t)ra * a.off.gu_row;
-      #pragma unroll 1
-      for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
-        const int p = tb.upairs[i] & 0xffff, t = tb.upairs[i] >> 16;
-        float acc[2 * kGateRows];
+      float acc[2 * kGateRows];
 #pragma unroll
-        for (int q = 0; q < 2 * kGateRows; ++q) acc[q] = 0.0f;
-        gate_up_rows<NCX>(rowa, nrows, a.off, nchx, lane, gq, xs4 + (size_t)t * nchx * 4, xsum + (size_t)t * nchx,
-                          xback + (size_t)t * nchx, acc);
-        // Warp sums of the 8 values (gate, up of 4 rows) by a reduce-scatter
-        // butterfly (9 shuffles): after distances 16, 8 and 4 a lane holds
-        // value 4*b4 + 2*b3 + b2 (lane bits), distances 2 and 1 finish it;
-        // lanes with b2 clear hold a gate sum and take the row's up sum from
-        // the lane 4 above.
-        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
-        float w4[4], w2[2];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float keep = b4 ? acc[4 + q] : acc[q], send = b4 ? acc[q] : acc[4 + q];
-          w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
-          w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-        float v = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        const float up = __shfl_xor_sync(0xffffffffu, v, 4);
-        const int rr = 2 * b4 + b3;  // the row whose gate sum this lane holds (b2 clear)
-        if ((lane & 7) == 0 && rr < nrows)
-          hst[(size_t)p * a.rgu + ra + rr] = __float2half_rn(silu_f(v) * up);
-      }
-      // The warp that completes the unit in this block publishes the block's
-      // h rows of every pair of the unit and releases the unit (one release
-      // per unit and block).
+      for (int q = 0; q < 2 * kGateRows; ++q) acc[q] = 0.0f;
+      gate_up_rows<NCX>(ring_g + (size_t)s * a.sg + (size_t)ra * a.off.gu_row, nrows, a.off, nchx, lane, gq,
+                        xs4 + (size_t)t * nchx * 4, xsum + (size_t)t * nchx, xback + (size_t)t * nchx, acc);
+      const float hv = swiglu_lanes(acc, lane);
+      const int rr = 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);  // the lane's row (lanes 0, 8, 16, 24)
+      if ((lane & 7) == 0 && rr < nrows) a.hbuf[(size_t)p * a.I + n0 + ra + rr] = __float2half_rn(hv);
       __syncwarp();
-      int last = 0;
-      if (lane == 0 && ok) {
-        mbar_arrive(&empty_g[s]);
+      if (lane == 0) {
         __threadfence_block();
-        last = atomicAdd(&tb.udone[u], 1) == ng - 1;
+        if (atomicAdd(&tb.fdone[u], 1) == (tb.uoff[u + 1] - tb.uoff[u]) * ng - 1) mbar_arrive(&empty_g[s]);
       }
-      if (last && lane == 0) {
-        // Lane 0 stores the block's h rows of every pair of the unit itself,
-        // so the release orders exactly its own stores before the count.
-        __threadfence_block();  // the other warps' staged h (counted above)
-        #pragma unroll 1
-        for (int i = tb.uoff[u]; i < tb.uoff[u + 1]; ++i) {
-          const int p = tb.upairs[i] & 0xffff;
-          #pragma unroll 1
-          for (int q = 0; q < rg_rows; ++q) a.hbuf[(size_t)p * a.I + n0 + q] = hst[(size_t)p * a.rgu + q];
-        }
-        red_release_gpu_add(&cnt[u], 1);
-      }
-      __syncwarp();
     }
-  }
-  // The last down item of this warp (its last counter poll).
-  int last_u = -1, last_r = -1;
-  #pragma unroll 1
-  for (int u = 0, s = 0; u < U && nd > 0; ++u, s = (s + 1 == a.Sd) ? 0 : s + 1) {
-    if (!tb.blk[u]) continue;
-    #pragma unroll 1
-    for (int r = (warp - s * nd) & (kWarps - 1); r < nd; r += kWarps) {
-      last_u = u;
-      last_r = r;
-    }
-  }
-  if (!FAST && last_u < 0) bar_arrive(kBarPolled, kThreads);
-  int gd[NCH];
-#pragma unroll
-  for (int it = 0; it < NCH; ++it) gd[it] = (32 * (lane + 32 * it)) / a.g;
-  const int nchh = a.I / 32;
-  #pragma unroll 1
-  for (int u = 0, s = 0, fill = 0; u < U && nd > 0; ++u, s = (s + 1 == a.Sd) ? 0 : s + 1, fill += s == 0) {
-    if (!tb.blk[u]) continue;
-    #pragma unroll 1
-    for (int r = (warp - s * nd) & (kWarps - 1); r < nd; r += kWarps) {
-      // h of unit u complete in every block (bounded acquire poll; one
-      // token: the producer warp copied it into shared memory).
-      bool ok = true;
-      if (FAST) {
-        ok = __all_sync(0xffffffffu, wait_phase(&hfull[s], 0, abort_flag, a.ws));
-      } else if (lane == 0) {
-        unsigned tries = 0;
-        while (ld_acquire_gpu(&cnt[u]) < cnt_target) {
-          if (*abort_flag || ++tries > kSpinTries) {
-            if (!*abort_flag) {
-              *abort_flag = 1;
-              atomicOr(a.ws, 4);
-            }
-            ok = false;
-            break;
-          }
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!FAST && u == last_u && r == last_r) bar_arrive(kBarPolled, kThreads);
-      const bool landed = __all_sync(0xffffffffu, wait_phase(&full_d[s], fill & 1, abort_flag, a.ws));
-      ok = ok && landed;
-      const int r0 = r * kDownRows;
-      const uint8_t* stg = ring_d + (size_t)s * a.sd + (size_t)r0 * a.off.d_row;
+    // ---- every block's h rows are out (grid barrier, bounded) --------------
+    // Thread 0 releases the block's stores (after the block barrier) and
+    // waits until all G blocks have; the second barrier passes that on.
+    bar_sync(kBarGate, kWarps * 32);
+    if (tid == 0) {
+      int32_t* gbar = a.ws + kCntBase;
+      __threadfence();
+      red_release_gpu_add(gbar, 1);
+      unsigned tries = 0;
       #pragma unroll 1
-      for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
-        const int p = tb.upairs[i] & 0xffff;
-        const int nr = min(kDownRows, rd_rows - r0);
-        if (FAST)
-          down_rows<NCH, true>(stg, nr, a.off, hsm + (size_t)u * a.I, nchh, lane, gd, part + (size_t)p * a.rdn + r0);
-        else
-          down_rows<NCH, false>(stg, nr, a.off, a.hbuf + (size_t)p * a.I, nchh, lane, gd, part + (size_t)p * a.rdn + r0);
+      while (ld_acquire_gpu(gbar) < a.G) {
+        if (*abort_flag) break;
+        if (++tries > kSpinTries) {
+          *abort_flag = 1;
+          atomicOr(a.ws, 4);
+          break;
+        }
+      }
+      __threadfence();
+    }
+    bar_sync(kBarGate, kWarps * 32);
+    // ---- down: item i of unit u is (pairs kPairsDown * (i / nd) ..., row group i % nd)
+    const int ND = nd > 0 ? tb.dio[U] : 0;
+    u = 0;
+    #pragma unroll 1
+    for (int j = warp; j < ND && ok; j += kWarps) {
+      while (tb.dio[u + 1] <= j) ++u;
+      const int i = j - tb.dio[u], c = i / nd, r = i - c * nd;
+      const int pk = u / a.dpack, q = Ug + pk, s = q % a.Sg, lap = q / a.Sg;
+      ok = __all_sync(full, wait_fill(fillno, s, lap, abort_flag, a.ws) &&
+                                wait_phase(&full_g[s], lap & 1, abort_flag, a.ws));
+      if (!ok) break;
+      const int r0 = r * kDownRows;
+      const uint8_t* stg = ring_g + (size_t)s * a.sg + (size_t)(u - pk * a.dpack) * a.sd + (size_t)r0 * a.off.d_row;
+      const int i0 = tb.uoff[u] + c * kPairsDown, i1 = min(tb.uoff[u + 1], i0 + kPairsDown);
+      #pragma unroll 1
+      for (int ii = i0; ii < i1; ++ii) {
+        const int p = tb.upairs[ii] & 0xffff;
+        down_rows<NCH, false>(stg, min(kDownRows, rd_rows - r0), a.off, a.hbuf + (size_t)p * a.I, nchh, lane, gd,
+                              part + (size_t)p * a.rdn + r0);
       }
       __syncwarp();
-      if (lane == 0 && landed) mbar_arrive(&empty_d[s]);
+      if (lane == 0) {
+        __threadfence_block();
+        const int ua = pk * a.dpack, ub = min(U, ua + a.dpack);
+        if (atomicAdd(&tb.fdone[q], 1) == tb.dio[ub] - tb.dio[ua] - 1) mbar_arrive(&empty_g[s]);
+      }
     }
   }
   bar_sync(kBarCompute, kThreads);
@@ -1144,56 +1245,65 @@ cudaError_t launch_stream2(int dev, const StreamParams& a, cudaStream_t st) {
 
 constexpr size_t kSmemBudget = 227 * 1024;
 
-// Shared-memory carve-up: [ring_g | ring_d] (also the routing scratch) | x |
-// part | tables | barriers. Returns false when the shape does not fit.
+// Shared-memory carve-up: ring(s) (also the routing scratch) | x | part |
+// h staging | h copies | tables | barriers. Returns false when the shape
+// does not fit.
 bool carve(StreamParams& a) {
-  const int Umax = std::min(a.P, a.E);
   const size_t xbytes = (size_t)a.T * a.H * 2 + (size_t)a.T * (a.H / 32) * 8;
   const size_t partb = (size_t)a.P * a.rdn * 4;
-  const size_t hstb = (size_t)a.P * a.rgu * 2;
   const size_t tabb = tables_bytes(a.P, a.E);
-  // One routed token: the complete h of each pick is copied into shared
-  // memory for the down projection.
-  const bool want_fast = a.T == 1 && a.logits != nullptr && a.k <= kMaxRing;
-  const size_t hsmb = want_fast ? (size_t)a.k * a.I * 2 : 0;
-
+  const size_t barb = 6 * kMaxRing * 8;
+  const uint32_t sgu = align16((uint32_t)a.rgu * a.off.gu_row), sdn = align16((uint32_t)a.rdn * a.off.d_row);
   auto r16 = [](size_t v) { return (v + 15) & ~(size_t)15; };
-  const size_t fixed = r16(xbytes) + r16(partb) + r16(hstb) + r16(hsmb) + r16(tabb) + 5 * kMaxRing * 8;
-  if (fixed + a.sg + a.sd > kSmemBudget) return false;
-  const size_t ring = kSmemBudget - fixed;
-  int Sg = std::min(Umax, kMaxRing), Sd = std::min(Umax, kMaxRing);
-  if ((size_t)Sg * a.sg + (size_t)Sd * a.sd > ring) {
-    // Split the ring budget: about two thirds of the bytes to the gate/up ring.
-    Sg = (int)std::min<size_t>(Sg, std::max<size_t>(1, (ring * 2 / 3) / a.sg));
-    Sd = (int)std::min<size_t>(Sd, std::max<size_t>(1, (ring - (size_t)Sg * a.sg) / a.sd));
-    if ((size_t)Sg * a.sg + (size_t)Sd * a.sd > ring) return false;
+  auto place = [&](size_t ringb, size_t hstb, size_t hsmb) {
+    size_t o = r16(ringb);
+    a.o_x = (uint32_t)o;
+    o += r16(xbytes);
+    a.o_part = (uint32_t)o;
+    o += r16(partb);
+    a.o_hst = (uint32_t)o;
+    o += r16(hstb);
+    a.o_hsm = (uint32_t)o;
+    o += r16(hsmb);
+    a.o_small = (uint32_t)o;
+    o += r16(tabb);
+    a.o_bar = (uint32_t)o;
+    o += barb;
+    a.smem = (uint32_t)o;
+    return o <= kSmemBudget;
+  };
+  // One routed token: each of the k picks gets its own stage in both rings
+  // (filled once), h is staged per block and each pick's complete h is
+  // copied into shared memory for the down rows.
+  a.fast1 = 0;
+  a.dpack = 1;
+  if (a.T == 1 && a.logits != nullptr && a.k <= kMaxFastK) {
+    const size_t ringb = std::max((size_t)a.k * (sgu + sdn),
+                                  (size_t)route_candidates(a.E, std::min(a.k, 32)) * 12 + (size_t)a.k * 4);
+    if (place(ringb, (size_t)a.P * a.rgu * 2, (size_t)a.k * a.I * 2)) {
+      a.fast1 = 1;
+      a.Sg = a.Sd = a.k;
+      a.sg = sgu;
+      a.sd = sdn;
+      a.o_ring_d = (uint32_t)((size_t)a.k * sgu);
+      return true;
+    }
   }
-  a.Sg = Sg;
-  a.Sd = Sd;
-  // One routed token whose k picks all have their own stages: the producer
-  // warp routes and streams; gate/up items of one row spread the last
-  // expert's rows over more warps.
-  a.fast1 = (want_fast && a.k <= Sg && a.k <= Sd) ? 1 : 0;
-  size_t ringb = (size_t)Sg * a.sg + (size_t)Sd * a.sd;
-  if (a.fast1) ringb = std::max(ringb, (size_t)route_candidates(a.E, std::min(a.k, 32)) * 12 + (size_t)a.k * 4);
-  else ringb = std::max(ringb, (size_t)a.T * a.E * 4);  // routing scratch
-  size_t o = r16(ringb);
-  a.o_ring_d = (uint32_t)((size_t)Sg * a.sg);
-  a.o_x = (uint32_t)o;
-  o += r16(xbytes);
-  a.o_part = (uint32_t)o;
-  o += r16(partb);
-  a.o_hst = (uint32_t)o;
-  o += r16(hstb);
-  a.o_hsm = (uint32_t)o;
-  o += r16(hsmb);
-
-  a.o_small = (uint32_t)o;
-  o += r16(tabb);
-  a.o_bar = (uint32_t)o;
-  o += 5 * kMaxRing * 8;
-  if (o > kSmemBudget) return false;
-  a.smem = (uint32_t)o;
+  // Batched: one ring of S stages; a stage holds one unit's gate/up rows or
+  // the down rows of dpack units.
+  const size_t fixed = r16(xbytes) + r16(partb) + r16(tabb) + barb;
+  const int dpack = std::max<int>(1, (int)(sgu / sdn));
+  const uint32_t sst = align16(std::max<uint32_t>(sgu, (uint32_t)dpack * sdn));
+  if (fixed + sst > kSmemBudget) return false;
+  const int S = (int)std::min<size_t>(kMaxRing, (kSmemBudget - fixed) / sst);
+  const size_t ringb = std::max((size_t)S * sst, a.logits ? (size_t)a.T * a.E * 4 : 0);  // routing scratch
+  if (!place(ringb, 0, 0)) return false;
+  a.Sg = S;
+  a.Sd = 0;
+  a.sg = sst;
+  a.sd = sdn;
+  a.dpack = dpack;
+  a.o_ring_d = 0;
   return true;
 }
 
@@ -1225,8 +1335,6 @@ int fused_forward_routed(const ForwardArgs& fa, const float* logits, int renorm,
   a.hbuf = reinterpret_cast<__half*>(ws + ws_scratch_offset(a.P));
   a.rgu = (a.I + a.G - 1) / a.G;
   a.rdn = (a.H + a.G - 1) / a.G;
-  a.sg = align16((uint32_t)a.rgu * fa.off.gu_row);
-  a.sd = align16((uint32_t)a.rdn * fa.off.d_row);
   if (!carve(a)) return fail(MOE_ERR_UNSUPPORTED, "streamed decode: shapes exceed shared memory");
   cudaError_t e;
   cudaStream_t st = fa.stream;
