@@ -54,7 +54,6 @@ constexpr int kMaxE = 1024;                   // experts (in-block tables)
 constexpr int kMaxRing = 32;                  // stages per ring
 constexpr int kMaxFastK = 16;                 // one routed token: picks that each get their own stages
 constexpr int kDownRows = 8;                  // rows per down work item
-constexpr int kPairsDown = 2;                 // batched: pairs per down work item
 constexpr unsigned kMbarTries = 50000;        // ~1 s (20 us suspend hint per try)
 constexpr unsigned kIdleTries = 16000000;     // ~1 s of idle producer loop iterations
 constexpr unsigned kSpinTries = 2000000;      // ~1 s of counter polls (one L2 round trip each)
@@ -82,6 +81,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(20000u) : "memory");
+  return ok != 0;
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -168,8 +176,6 @@ struct Tables {
   int32_t* uoff;        // [P+1] first sorted pair of each unit
   int32_t* upairs;      // [P] pairs sorted by unit
   int32_t* udone;       // [P] one token: gate/up items finished per unit (this block)
-  int32_t* gio;         // [P+1] batched: first gate/up item of each unit
-  int32_t* dio;         // [P+1] batched: first down item of each unit
   int32_t* fdone;       // [2P] batched: items finished per ring fill
   int32_t* ecnt;        // [E] pairs per expert, then first sorted position
   int32_t* eunit;       // [E] unit of each expert
@@ -180,7 +186,7 @@ struct Tables {
 };
 
 __host__ __device__ inline size_t tables_bytes(int P, int E) {
-  return (size_t)P * 8 + ((size_t)P * 11 + 3 + (size_t)E * 4 + 8) * 4;
+  return (size_t)P * 8 + ((size_t)P * 9 + 1 + (size_t)E * 4 + 8) * 4;
 }
 
 __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) {
@@ -194,9 +200,7 @@ __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) 
   t.uoff = t.uexp + a.P;
   t.upairs = t.uoff + a.P + 1;
   t.udone = t.upairs + a.P;
-  t.gio = t.udone + a.P;
-  t.dio = t.gio + a.P + 1;
-  t.fdone = t.dio + a.P + 1;
+  t.fdone = t.udone + a.P;
   t.ecnt = t.fdone + 2 * a.P;
   t.eunit = t.ecnt + a.E;
   t.eslot = t.eunit + a.E;
@@ -441,22 +445,38 @@ __device__ void route_one_token(const StreamParams& a, const Tables& tb, uint8_t
   __syncthreads();
 }
 
-// Batched routing: warp t routes token t from its logits in shared memory
-// (lane l looks at experts l, l + 32, ...). Round r picks the best expert
-// that ranks after round r-1's pick, so no taken mask is needed; the
-// selection and the softmax arithmetic are moe_route's (sum over all E per
-// lane in index order, then a butterfly). A token with NaN/+inf logits, or
-// with every logit -inf, gets ids -1 and weights 0.
+// Order-preserving key of a finite or infinite FP32 value (larger value,
+// larger key; -0 and +0 share the key of +0, as they compare equal).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Batched routing: warp t routes token t. Lane l holds experts l + 32 j
+// (j < NJ, NJ >= E/32) in registers and keeps its best CD not yet picked
+// in a small sorted cache (rank order: logit desc, index asc). Round r takes
+// the best cache head of the warp -- the largest key by one warp reduction,
+// the smallest index among equal keys by another -- and the owning lane
+// pops it, refilling its cache from its registers when it runs dry. This is
+// moe_route's selection; the softmax arithmetic is moe_route's too (sum over
+// j per lane, then a butterfly). A token with NaN/+inf logits, or with
+// every logit -inf, gets ids -1 and weights 0.
+template <int NJ>
 __device__ void route_token_warp(const StreamParams& a, const Tables& tb, const float* lg, int t) {
   const int lane = threadIdx.x & 31, E = a.E, k = a.k;
   const unsigned full = 0xffffffffu;
+  float v[NJ];
   bool bad = false;
-  int ninf = 0;
-#pragma unroll 4
-  for (int e = lane; e < E; e += 32) {
-    const float v = lg[e];
-    bad |= isnan(v) || v == INFINITY;
-    ninf += v == -INFINITY;
+  int ninf = 0, mine_n = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? lg[e] : -INFINITY;
+    if (e < E) {
+      bad |= isnan(v[j]) || v[j] == INFINITY;
+      ninf += v[j] == -INFINITY;
+      ++mine_n;
+    }
   }
   bad = __any_sync(full, bad);
   ninf = __reduce_add_sync(full, ninf);
@@ -467,46 +487,91 @@ __device__ void route_token_warp(const StreamParams& a, const Tables& tb, const 
     }
     return;
   }
-  float prev_v = INFINITY, my_v = 0.0f;
-  int prev_i = -1, my_i = -1;
-#pragma unroll 1
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-#pragma unroll 4
-    for (int e = lane; e < E; e += 32) {
-      const float v = lg[e];
-      if (ranks_before(prev_v, prev_i, v, e) && ranks_before(v, e, bv, bi)) {
-        bv = v;
-        bi = e;
-      }
+  constexpr int CD = NJ < 2 ? NJ : 2;
+  float cv[CD];
+  int ci[CD];
+  // The lane's best CD elements that rank after (lv, li).
+  auto fill = [&](float lv, int li) {
+#pragma unroll
+    for (int c = 0; c < CD; ++c) {
+      cv[c] = -INFINITY;
+      ci[c] = INT_MAX;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(full, bv, o);
-      const int oi = __shfl_xor_sync(full, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && ranks_before(lv, li, v[j], e)) {
+        bool b[CD];
+#pragma unroll
+        for (int c = 0; c < CD; ++c) b[c] = ranks_before(v[j], e, cv[c], ci[c]);
+#pragma unroll
+        for (int c = CD - 1; c >= 1; --c) {
+          if (b[c - 1]) {
+            cv[c] = cv[c - 1];
+            ci[c] = ci[c - 1];
+          } else if (b[c]) {
+            cv[c] = v[j];
+            ci[c] = e;
+          }
+        }
+        if (b[0]) {
+          cv[0] = v[j];
+          ci[0] = e;
+        }
       }
     }
+  };
+  fill(INFINITY, -1);
+  int taken = 0;
+  float my_v = 0.0f;
+  int my_i = -1;
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    const bool has = ci[0] != INT_MAX;
+    const uint32_t key = has ? order_key(cv[0]) : 0u;  // every real key is above 0
+    const uint32_t kmax = __reduce_max_sync(full, key);
+    const uint32_t win = __reduce_min_sync(full, (has && key == kmax) ? (uint32_t)ci[0] : 0xffffffffu);
+    const float wv = __shfl_sync(full, cv[0], (int)(win & 31));
     if (lane == r) {
-      my_v = bv;
-      my_i = bi;
+      my_v = wv;
+      my_i = (int)win;
     }
-    prev_v = bv;
-    prev_i = bi;
+    if (has && (uint32_t)ci[0] == win) {
+      const float pv = cv[0];
+      ++taken;
+#pragma unroll
+      for (int c = 0; c + 1 < CD; ++c) {
+        cv[c] = cv[c + 1];
+        ci[c] = ci[c + 1];
+      }
+      cv[CD - 1] = -INFINITY;
+      ci[CD - 1] = INT_MAX;
+      if (ci[0] == INT_MAX && taken < mine_n) fill(pv, (int)win);
+    }
   }
   const float m = __shfl_sync(full, my_v, 0);
   float s_all = 0.0f;
-#pragma unroll 4
-  for (int e = lane; e < E; e += 32) s_all += expf(lg[e] - m);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) s_all += expf(v[j] - m);  // pads give 0
   s_all = warp_sum(s_all);
   const float mine = lane < k ? expf(my_v - m) : 0.0f;
   const float s_sel = warp_sum(mine);
   if (lane < k) {
     tb.ids[t * k + lane] = my_i;
     tb.w[t * k + lane] = mine / (a.renorm ? s_sel : s_all);
+  }
+}
+
+__device__ void route_tokens_warps(const StreamParams& a, const Tables& tb, const float* lgT) {
+  const int warp = threadIdx.x >> 5, nj = (a.E + 31) / 32;
+  #pragma unroll 1
+  for (int t = warp; t < a.T; t += kThreads / 32) {
+    const float* lg = lgT + (size_t)t * a.E;
+    if (nj <= 2) route_token_warp<2>(a, tb, lg, t);
+    else if (nj <= 4) route_token_warp<4>(a, tb, lg, t);
+    else if (nj <= 8) route_token_warp<8>(a, tb, lg, t);
+    else if (nj <= 16) route_token_warp<16>(a, tb, lg, t);
+    else route_token_warp<32>(a, tb, lg, t);
   }
 }
 
@@ -674,6 +739,88 @@ __device__ __forceinline__ void down_rows(const uint8_t* stg, int nrows, const B
   if ((lane & 3) == 0 && q < nrows) part_row[q] = w1;
 }
 
+// 16 FP16 values of h (two 16-byte words read through L2: h was written by
+// other SMs).
+__device__ __forceinline__ void load_piece(const __half* src, uint4 (&r)[2]) {
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0].x), "=r"(r[0].y), "=r"(r[0].z), "=r"(r[0].w) : "l"(src) : "memory");
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[1].x), "=r"(r[1].y), "=r"(r[1].z), "=r"(r[1].w) : "l"(src + 8) : "memory");
+}
+
+// The 16 values of load_piece as the scaled pairs of dot16_scaled (one
+// power-of-two scale for the piece); returns their sum, and 2^(24-s) in back.
+__device__ __forceinline__ float scale_piece(const uint4 (&r)[2], half2 (&xp)[8], float& back) {
+  float v[16];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const __half* e = reinterpret_cast<const __half*>(&r[q]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * q + i] = __half2float(e[i]);
+  }
+  float sum = 0.0f, amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    sum += v[i];
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const int sh = chunk_shift(amax);
+  scaled_perm8(v, sh, xp);
+  scaled_perm8(v + 8, sh, xp + 4);
+  back = pow2f(24 - sh);
+  return sum;
+}
+
+// Batched path: the block's down rows [0, nrows) of one pair, from the
+// stage's rows (stg, row 0): part_row[q] = (W_d h)[m0 + q]. Lane l holds h
+// pieces pc = l + 32 it (16 values each) as scaled pairs; rows go 8 at a
+// time, each row's sum over the pieces finished by the reduce-scatter
+// butterfly of down_rows.
+template <int NP>
+__device__ __forceinline__ void down_pair_rows(const uint8_t* stg, int nrows, const BlockOffsets& off, int npc,
+                                               int lane, const int* gp, const half2 (&hr)[NP][8],
+                                               const float* hsum, const float* hback, float* part_row) {
+  const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+  #pragma unroll 1
+  for (int q0 = 0; q0 < nrows; q0 += kDownRows) {
+    float v[kDownRows];
+#pragma unroll
+    for (int q = 0; q < kDownRows; ++q) {
+      v[q] = 0.0f;
+      if (q0 + q < nrows) {
+        const uint8_t* row = stg + (size_t)(q0 + q) * off.d_row;
+        const uint32_t* sz = reinterpret_cast<const uint32_t*>(row + off.d_sz);  // (s, z) per group
+#pragma unroll
+        for (int it = 0; it < NP; ++it) {
+          const int pc = lane + 32 * it;
+          if (pc < npc) {
+            const uint2 w = *reinterpret_cast<const uint2*>(row + off.d_q + 8 * pc);
+            const float2 s2 = __half22float2(u32_as_h2(sz[gp[it]]));
+            const float d = dot16_scaled(w.x, w.y, hr[it]) * hback[it];
+            v[q] += s2.x * (d - s2.y * hsum[it]);
+          }
+        }
+      }
+    }
+    float w4[4], w2[2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float keep = b4 ? v[4 + q] : v[q], send = b4 ? v[q] : v[4 + q];
+      w4[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float keep = b3 ? w4[2 + q] : w4[q], send = b3 ? w4[q] : w4[2 + q];
+      w2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+    w1 += __shfl_xor_sync(0xffffffffu, w1, 1);
+    const int q = q0 + 4 * b4 + 2 * b3 + b2;
+    if ((lane & 3) == 0 && q < nrows) part_row[q] = w1;
+  }
+}
+
 // Batched path: wait (bounded) until the producer has issued fill `lap` of
 // stage s, so that the stage's mbarrier is at that fill's phase.
 __device__ __forceinline__ bool wait_fill(const int32_t* fillno, int s, int lap, volatile int32_t* abort_flag,
@@ -788,8 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     }
     __syncthreads();
     if (a.logits) {
-      #pragma unroll 1
-      for (int t = warp; t < a.T; t += kThreads / 32) route_token_warp(a, tb, lgT + (size_t)t * a.E, t);
+      route_tokens_warps(a, tb, lgT);
     } else {
       #pragma unroll 1
       for (int p = tid; p < a.P; p += kThreads) {
@@ -821,10 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       tb.punit[p] = u;
     }
     __syncthreads();
-    // Units (experts with pairs, ascending id) and their work items, by one
-    // warp with exclusive scans: per unit, a gate/up item for every (pair,
-    // row group) and a down item for every (group of kPairsDown pairs,
-    // 8-row group).
+    // Units: experts with pairs, in ascending id (one warp, exclusive scans).
     if (warp == 0) {
       const int per = (a.E + 31) / 32;
       const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
@@ -862,38 +1005,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
         tb.misc[0] = U;
         tb.uoff[U] = sp;
       }
-      __syncwarp();
-      const int per2 = (U + 31) / 32;
-      const int u0 = min(U, lane * per2), u1 = min(U, u0 + per2);
-      int gi = 0, di = 0;
-      #pragma unroll 1
-      for (int v = u0; v < u1; ++v) {
-        const int n = tb.uoff[v + 1] - tb.uoff[v];
-        gi += n * ng;
-        di += nd * ((n + kPairsDown - 1) / kPairsDown);
-      }
-      int sg = gi, sd = di;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int vg = __shfl_up_sync(0xffffffffu, sg, o), vd = __shfl_up_sync(0xffffffffu, sd, o);
-        if (lane >= o) {
-          sg += vg;
-          sd += vd;
-        }
-      }
-      int g = sg - gi, d = sd - di;
-      #pragma unroll 1
-      for (int v = u0; v < u1; ++v) {
-        const int n = tb.uoff[v + 1] - tb.uoff[v];
-        tb.gio[v] = g;
-        tb.dio[v] = d;
-        g += n * ng;
-        d += nd * ((n + kPairsDown - 1) / kPairsDown);
-      }
-      if (lane == 31) {
-        tb.gio[U] = sg;
-        tb.dio[U] = sd;
-      }
     }
     __syncthreads();
     // Pairs under their unit. Atomic cursors: the order of a unit's pairs
@@ -914,41 +1025,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     // Fill q goes to stage q % S once the stage's previous fill is consumed;
     // the down fills need nothing but a free stage, so they stream while the
     // last gate/up rows are computed and while the blocks meet.
-    if (warp == kProducer && lane == 0) {
+    if (warp == kProducer) {
       const int U = tb.misc[0];
       const int Ug = ng > 0 ? U : 0, Q = Ug + (nd > 0 ? (U + a.dpack - 1) / a.dpack : 0);
       const uint32_t gbytes = (uint32_t)rg_rows * a.off.gu_row, dbytes = (uint32_t)rd_rows * a.off.d_row;
+      const int B = min(32, a.Sg);  // fills in one window: distinct stages
       int q = 0;
+      // Each round the lanes look at fills q .. q+B-1; the leading run of
+      // fills whose stages are free is issued at once, lane i issuing fill
+      // q+i (a bulk copy takes a thread a few hundred ns to issue; lanes
+      // issue side by side). If fill q's stage is still busy, wait for it.
       #pragma unroll 1
-      for (int s = 0, lap = 0; q < Q; ++q) {
-        if (lap > 0 && !wait_phase(&empty_g[s], (lap - 1) & 1, abort_flag, a.ws)) break;
-        uint8_t* dst = ring_g + (size_t)s * a.sg;
-        if (q < Ug) {
-          mbar_arrive_expect_tx(&full_g[s], gbytes);
-          bulk_g2s(dst, tb.blk[q] + (size_t)n0 * a.off.gu_row, gbytes, &full_g[s]);
-        } else {
-          const int u0 = (q - Ug) * a.dpack, u1 = min(U, u0 + a.dpack);
-          mbar_arrive_expect_tx(&full_g[s], (uint32_t)(u1 - u0) * dbytes);
-          #pragma unroll 1
-          for (int u = u0; u < u1; ++u)
-            bulk_g2s(dst + (size_t)(u - u0) * a.sd, tb.blk[u] + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes,
-                     &full_g[s]);
+      while (q < Q) {
+        const int qq = q + lane, s = qq % a.Sg, lap = qq / a.Sg;
+        const bool ready = lane < B && qq < Q && (lap == 0 || mbar_test(&empty_g[s], (lap - 1) & 1));
+        const unsigned m = __ballot_sync(0xffffffffu, ready);
+        const int n = m == 0xffffffffu ? 32 : __ffs(~m) - 1;
+        if (n == 0) {
+          const int s0 = q % a.Sg, lap0 = q / a.Sg;
+          if (!__all_sync(0xffffffffu, wait_phase(&empty_g[s0], (lap0 - 1) & 1, abort_flag, a.ws))) break;
+          continue;
         }
-        *(volatile int32_t*)&fillno[s] = lap + 1;
-        if (++s == a.Sg) {
-          s = 0;
-          ++lap;
+        if (lane < n) {
+          uint8_t* dst = ring_g + (size_t)s * a.sg;
+          if (qq < Ug) {
+            mbar_arrive_expect_tx(&full_g[s], gbytes);
+            bulk_g2s(dst, tb.blk[qq] + (size_t)n0 * a.off.gu_row, gbytes, &full_g[s]);
+          } else {
+            const int u0 = (qq - Ug) * a.dpack, u1 = min(U, u0 + a.dpack);
+            mbar_arrive_expect_tx(&full_g[s], (uint32_t)(u1 - u0) * dbytes);
+            #pragma unroll 1
+            for (int u = u0; u < u1; ++u)
+              bulk_g2s(dst + (size_t)(u - u0) * a.sd, tb.blk[u] + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes,
+                       &full_g[s]);
+          }
+          *(volatile int32_t*)&fillno[s] = lap + 1;
         }
+        __syncwarp();
+        q += n;
       }
       // Before the block may exit, every copy it issued has landed (bounded):
       // no fill follows the last one of each stage, so its parity is final.
       #pragma unroll 1
-      for (int s = 0; s < a.Sg && s < q; ++s) {
+      for (int s = lane; s < a.Sg && s < q; s += 32) {
         const int last = s + a.Sg * ((q - 1 - s) / a.Sg);
         #pragma unroll 1
         for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_g[s], (last / a.Sg) & 1); ++i) {
         }
       }
+      __syncwarp();
     }
   }
   const int U = tb.misc[0];
@@ -1090,23 +1215,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     int gq[NCX];
 #pragma unroll
     for (int it = 0; it < NCX; ++it) gq[it] = (32 * (lane + 32 * it)) / a.g;
-    int gd[NCH];
-#pragma unroll
-    for (int it = 0; it < NCH; ++it) gd[it] = (32 * (lane + 32 * it)) / a.g;
-    const int nchh = a.I / 32;
     bool ok = true;
-    // ---- gate/up: item i of unit u is (pair i / ng, row group i % ng) -------
-    const int NG = ng > 0 ? tb.gio[U] : 0;
+    // ---- gate/up: item j is (pair j / ng, row group j % ng) of the sorted
+    // pairs (unit u's pairs sit at uoff[u] ..)
+    const int NG = tb.uoff[U] * ng;
     int u = 0;
     #pragma unroll 1
     for (int j = warp; j < NG; j += kWarps) {
-      while (tb.gio[u + 1] <= j) ++u;
-      const int i = j - tb.gio[u], c = i / ng, r = i - c * ng;
+      const int c = j / ng, r = j - c * ng;
+      while (tb.uoff[u + 1] <= c) ++u;
       const int s = u % a.Sg, lap = u / a.Sg;
       ok = __all_sync(full, wait_fill(fillno, s, lap, abort_flag, a.ws) &&
                                 wait_phase(&full_g[s], lap & 1, abort_flag, a.ws));
       if (!ok) break;
-      const int pr = tb.upairs[tb.uoff[u] + c], p = pr & 0xffff, t = pr >> 16;
+      const int pr = tb.upairs[c], p = pr & 0xffff, t = pr >> 16;
       const int ra = r * kGateRows;
       const int nrows = min(kGateRows, rg_rows - ra);
       float acc[2 * kGateRows];
@@ -1124,12 +1246,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       }
     }
     // ---- every block's h rows are out (grid barrier, bounded) --------------
-    // Thread 0 releases the block's stores (after the block barrier) and
-    // waits until all G blocks have; the second barrier passes that on.
+    // Thread 0 releases the block's stores (ordered before it by the block
+    // barrier; the release is cumulative) and waits (acquire) until all G
+    // blocks have; the second barrier passes that on.
     bar_sync(kBarGate, kWarps * 32);
     if (tid == 0) {
       int32_t* gbar = a.ws + kCntBase;
-      __threadfence();
       red_release_gpu_add(gbar, 1);
       unsigned tries = 0;
       #pragma unroll 1
@@ -1141,34 +1263,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
           break;
         }
       }
-      __threadfence();
     }
     bar_sync(kBarGate, kWarps * 32);
-    // ---- down: item i of unit u is (pairs kPairsDown * (i / nd) ..., row group i % nd)
-    const int ND = nd > 0 ? tb.dio[U] : 0;
+    // ---- down: item j is the pair at sorted position j (all of the
+    // block's rows); the next item's h is loaded while this one computes.
+    constexpr int NP = 2 * NCH;  // 16-value pieces of h per lane
+    const int npc = a.I / 16;
+    int gp[NP];
+#pragma unroll
+    for (int it = 0; it < NP; ++it) gp[it] = (16 * (lane + 32 * it)) / a.g;
+    const int ND = nd > 0 ? tb.uoff[U] : 0;
+    uint4 nxt[NP][2];
+    auto fetch = [&](int jj) {
+      const __half* h = a.hbuf + (size_t)(tb.upairs[jj] & 0xffff) * a.I;
+#pragma unroll
+      for (int it = 0; it < NP; ++it)
+        if (lane + 32 * it < npc) load_piece(h + 16 * (lane + 32 * it), nxt[it]);
+    };
+    if (warp < ND && ok) fetch(warp);
     u = 0;
     #pragma unroll 1
     for (int j = warp; j < ND && ok; j += kWarps) {
-      while (tb.dio[u + 1] <= j) ++u;
-      const int i = j - tb.dio[u], c = i / nd, r = i - c * nd;
+      half2 hr[NP][8];
+      float hsum[NP], hback[NP];
+#pragma unroll
+      for (int it = 0; it < NP; ++it)
+        if (lane + 32 * it < npc) hsum[it] = scale_piece(nxt[it], hr[it], hback[it]);
+      if (j + kWarps < ND) fetch(j + kWarps);
+      while (tb.uoff[u + 1] <= j) ++u;
       const int pk = u / a.dpack, q = Ug + pk, s = q % a.Sg, lap = q / a.Sg;
       ok = __all_sync(full, wait_fill(fillno, s, lap, abort_flag, a.ws) &&
                                 wait_phase(&full_g[s], lap & 1, abort_flag, a.ws));
       if (!ok) break;
-      const int r0 = r * kDownRows;
-      const uint8_t* stg = ring_g + (size_t)s * a.sg + (size_t)(u - pk * a.dpack) * a.sd + (size_t)r0 * a.off.d_row;
-      const int i0 = tb.uoff[u] + c * kPairsDown, i1 = min(tb.uoff[u + 1], i0 + kPairsDown);
-      #pragma unroll 1
-      for (int ii = i0; ii < i1; ++ii) {
-        const int p = tb.upairs[ii] & 0xffff;
-        down_rows<NCH, false>(stg, min(kDownRows, rd_rows - r0), a.off, a.hbuf + (size_t)p * a.I, nchh, lane, gd,
-                              part + (size_t)p * a.rdn + r0);
-      }
+      const int p = tb.upairs[j] & 0xffff;
+      down_pair_rows<NP>(ring_g + (size_t)s * a.sg + (size_t)(u - pk * a.dpack) * a.sd, rd_rows, a.off, npc, lane,
+                         gp, hr, hsum, hback, part + (size_t)p * a.rdn);
       __syncwarp();
       if (lane == 0) {
         __threadfence_block();
         const int ua = pk * a.dpack, ub = min(U, ua + a.dpack);
-        if (atomicAdd(&tb.fdone[q], 1) == tb.dio[ub] - tb.dio[ua] - 1) mbar_arrive(&empty_g[s]);
+        if (atomicAdd(&tb.fdone[q], 1) == tb.uoff[ub] - tb.uoff[ua] - 1) mbar_arrive(&empty_g[s]);
       }
     }
   }

@@ -282,3 +282,26 @@ def test_layer_forward_one_token_ties_and_bad(row):
 ])
 def test_layer_forward_one_token_shapes(shape, E, k, renorm):
     _layer_forward_case(shape, E, k, renorm, 1, 46)
+
+
+def _routing_rows(E, k, seed):
+    # Token 0: one lane's experts (5, 37, 69, ...) hold the largest logits, so
+    # one warp lane owns every pick; token 1: a few values only, +0/-0 mixed
+    # (ties by index); token 2: fewer finite logits than k, the rest -inf;
+    # token 3: normal logits.
+    r = np.random.default_rng([seed, 5])
+    lg = r.standard_normal((4, E)).astype(np.float32)
+    own = np.arange(5, E, 32)
+    lg[0, own] = 10.0 + np.arange(len(own))[::-1]
+    lg[1] = r.choice(np.array([-0.0, 0.0, 1.0, 2.0], dtype=np.float32), size=E)
+    lg[2] = -np.inf
+    lg[2, r.choice(E, size=max(1, k // 2), replace=False)] = r.standard_normal(max(1, k // 2))
+    return lg
+
+
+@pytest.mark.parametrize("E,k", [(64, 8), (100, 12), (512, 10), (1024, 32)])
+def test_layer_forward_batched_routing_edges(E, k):
+    # Several tokens routed inside the kernels (one warp per token): picks by
+    # (logit desc, index asc) whatever lane holds them, ties by index.
+    lg = _routing_rows(E, k, 47)
+    _layer_forward_case((256, 128, 64), E, k, False, 4, 47, logits=lg)
