@@ -180,13 +180,11 @@ struct Tables {
   int32_t* ecnt;        // [E] pairs per expert, then first sorted position
   int32_t* eunit;       // [E] unit of each expert
   int32_t* eslot;       // [E] copy of slot_of
-  float* lg;            // [E] logits of the token routed by the producer warp
-  int32_t* misc;        // [0] units, [1] abort, [3] token without a routing, [4] -inf logits,
-                        // [5] one token: bit u set when unit u's h copy was issued
+  int32_t* misc;        // [0] units, [1] abort, [5] one token: bit u set when unit u's h copy was issued
 };
 
 __host__ __device__ inline size_t tables_bytes(int P, int E) {
-  return (size_t)P * 8 + ((size_t)P * 9 + 1 + (size_t)E * 4 + 8) * 4;
+  return (size_t)P * 8 + ((size_t)P * 9 + 1 + (size_t)E * 3 + 8) * 4;
 }
 
 __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) {
@@ -204,8 +202,7 @@ __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) 
   t.ecnt = t.fdone + 2 * a.P;
   t.eunit = t.ecnt + a.E;
   t.eslot = t.eunit + a.E;
-  t.lg = reinterpret_cast<float*>(t.eslot + a.E);
-  t.misc = reinterpret_cast<int32_t*>(t.lg + a.E);
+  t.misc = t.eslot + a.E;
   return t;
 }
 
@@ -333,117 +330,21 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
-__device__ __forceinline__ void bar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Named barriers, non-aligned forms: arrivals are counted per thread, so a
+// warp may reach them diverged (the .aligned bar.sync / bar.arrive would
+// require a converged warp); callers reconverge first all the same.
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // Named barriers (0 is __syncthreads).
 constexpr int kBarCompute = 1;  // before the combine: compute warps (and, batched, the producer) wait
 constexpr int kBarTables = 2;   // producer arrives with the routing tables, compute warps wait
 constexpr int kBarGate = 3;     // batched: the compute warps around the grid barrier
 constexpr int kBarPolled = 4;   // exchange warp arrives after its last counter poll, producer waits (64)
-
-// "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
-// experts of the token. The whole block routes one token in two stages, the
-// same selection as moe_route (top-k by (logit desc, index asc)):
-//   1. warp w ranks the experts of 32-expert segment w (w + 17, ...) among
-//      themselves; each segment's best min(k, 32) are candidates (every pick
-//      is among its own segment's best k);
-//   2. each candidate counts the candidates that rank before it: its count
-//      is its rank among all E experts when it is below k.
-// Four block barriers; the logits and the slot table go to shared memory
-// on the way. On return tb.ids[0..k) and pv[0..k) hold the picks and their
-// logits (tb.misc[3] set: the token has NaN/+inf logits, or all -inf).
-__host__ __device__ inline int route_candidates(int E, int k) { return (((E + 31) / 32) * k + 3) & ~3; }
-
-__device__ void route_one_token(const StreamParams& a, const Tables& tb, uint8_t* scratch, float* pv,
-                                uint4* xs4, float* xsum, float* xback) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int E = a.E, k = a.k, kk = min(k, 32), nseg = (E + 31) / 32, C = nseg * kk;
-  const int C4 = route_candidates(E, kk);  // candidates padded to whole 16-byte groups
-  float* cv = reinterpret_cast<float*>(scratch);
-  int32_t* ci = reinterpret_cast<int32_t*>(cv + C4);
-  int32_t* crank = ci + C4;
-  const int nchx = a.H / 32;
-  bool bad = false;
-  int ninf = 0;
-#pragma unroll 1
-  for (int e = tid; e < E; e += kThreads) {
-    const float v = __ldcg(a.logits + e);
-    tb.lg[e] = v;
-    tb.eslot[e] = __ldcg(a.slot_of + e);
-    bad |= isnan(v) || v == INFINITY;
-    ninf += v == -INFINITY;
-  }
-#pragma unroll 1
-  for (int c = tid; c < C4; c += kThreads) {
-    cv[c] = -INFINITY;
-    ci[c] = INT_MAX;
-    crank[c] = 0;
-  }
-#pragma unroll 1
-  for (int cc = tid; cc < nchx; cc += kThreads) stage_x_chunk(a.x, xs4, xsum, xback, cc);
-  bad = __any_sync(0xffffffffu, bad);
-  ninf = __reduce_add_sync(0xffffffffu, ninf);
-  if (lane == 0) {
-    if (bad) atomicOr(&tb.misc[3], 1);
-    if (ninf) atomicAdd(&tb.misc[4], ninf);
-  }
-  __syncthreads();
-  if (tb.misc[3] || tb.misc[4] == E) {
-    if (tid == 0) tb.misc[3] = 1;
-    __syncthreads();
-    __syncthreads();
-    __syncthreads();
-    return;
-  }
-#pragma unroll 1
-  for (int seg = warp; seg < nseg; seg += kThreads / 32) {
-    const int e = 32 * seg + lane;
-    if (e < E) {
-      const float v = tb.lg[e];
-      int lrank = 0;
-      const int e1 = min(E, 32 * seg + 32);
-#pragma unroll 4
-      for (int j = 32 * seg; j < e1; ++j) lrank += ranks_before(tb.lg[j], j, v, e);
-      if (lrank < kk) {
-        cv[seg * kk + lrank] = v;
-        ci[seg * kk + lrank] = e;
-      }
-    }
-  }
-  __syncthreads();
-  // Candidate c's comparisons are split over `parts` threads (c, part), each
-  // reading 4 candidates per 16-byte load; the partial counts are added.
-  const int parts = max(1, min(8, kThreads / C));
-  const int span = ((C4 / 4 + parts - 1) / parts) * 4;
-#pragma unroll 1
-  for (int t = tid; t < C * parts; t += kThreads) {
-    const int part = t / C, c = t - part * C;
-    const float v = cv[c];
-    const int i = ci[c];
-    if (i == INT_MAX) continue;
-    int cnt = 0;
-    const int j1 = min(C4, (part + 1) * span);
-#pragma unroll 2
-    for (int j = part * span; j < j1; j += 4) {
-      const float4 v4 = *reinterpret_cast<const float4*>(cv + j);
-      const int4 i4 = *reinterpret_cast<const int4*>(ci + j);
-      cnt += ranks_before(v4.x, i4.x, v, i) + ranks_before(v4.y, i4.y, v, i) + ranks_before(v4.z, i4.z, v, i) +
-             ranks_before(v4.w, i4.w, v, i);
-    }
-    if (cnt) atomicAdd(&crank[c], cnt);
-  }
-  __syncthreads();
-#pragma unroll 1
-  for (int c = tid; c < C; c += kThreads) {
-    const int rank = crank[c];
-    if (ci[c] != INT_MAX && rank < k) {
-      tb.ids[rank] = ci[c];
-      pv[rank] = cv[c];
-    }
-  }
-  __syncthreads();
-}
 
 // Order-preserving key of a finite or infinite FP32 value (larger value,
 // larger key; -0 and +0 share the key of +0, as they compare equal).
@@ -452,41 +353,20 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Batched routing: warp t routes token t. Lane l holds experts l + 32 j
-// (j < NJ, NJ >= E/32) in registers and keeps its best CD not yet picked
-// in a small sorted cache (rank order: logit desc, index asc). Round r takes
-// the best cache head of the warp -- the largest key by one warp reduction,
-// the smallest index among equal keys by another -- and the owning lane
-// pops it, refilling its cache from its registers when it runs dry. This is
-// moe_route's selection; the softmax arithmetic is moe_route's too (sum over
-// j per lane, then a butterfly). A token with NaN/+inf logits, or with
-// every logit -inf, gets ids -1 and weights 0.
+// Top-k of one token in one warp: lane l holds experts l + 32 j (j < NJ,
+// NJ >= E/32) in registers, pads (e >= E) are never picked. Each lane keeps
+// its best CD not yet picked in a small sorted cache (rank order: logit
+// desc, index asc); round r takes the best cache head of the warp -- the
+// largest key by one warp reduction, the smallest index among equal keys by
+// another -- and the owning lane pops it, refilling its cache from its
+// registers when it runs dry. Lane r < k returns pick r (value, expert).
+// This is moe_route's selection (top-k by (logit desc, index asc)).
 template <int NJ>
-__device__ void route_token_warp(const StreamParams& a, const Tables& tb, const float* lg, int t) {
-  const int lane = threadIdx.x & 31, E = a.E, k = a.k;
+__device__ __forceinline__ void warp_topk(const float (&v)[NJ], int E, int k, int lane, float& my_v, int& my_i) {
   const unsigned full = 0xffffffffu;
-  float v[NJ];
-  bool bad = false;
-  int ninf = 0, mine_n = 0;
+  int mine_n = 0;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = e < E ? lg[e] : -INFINITY;
-    if (e < E) {
-      bad |= isnan(v[j]) || v[j] == INFINITY;
-      ninf += v[j] == -INFINITY;
-      ++mine_n;
-    }
-  }
-  bad = __any_sync(full, bad);
-  ninf = __reduce_add_sync(full, ninf);
-  if (bad || ninf == E) {
-    if (lane < k) {
-      tb.ids[t * k + lane] = -1;
-      tb.w[t * k + lane] = 0.0f;
-    }
-    return;
-  }
+  for (int j = 0; j < NJ; ++j) mine_n += lane + 32 * j < E;
   constexpr int CD = NJ < 2 ? NJ : 2;
   float cv[CD];
   int ci[CD];
@@ -523,8 +403,8 @@ __device__ void route_token_warp(const StreamParams& a, const Tables& tb, const 
   };
   fill(INFINITY, -1);
   int taken = 0;
-  float my_v = 0.0f;
-  int my_i = -1;
+  my_v = 0.0f;
+  my_i = -1;
 #pragma unroll 1
   for (int r = 0; r < k; ++r) {
     const bool has = ci[0] != INT_MAX;
@@ -549,16 +429,64 @@ __device__ void route_token_warp(const StreamParams& a, const Tables& tb, const 
       if (ci[0] == INT_MAX && taken < mine_n) fill(pv, (int)win);
     }
   }
-  const float m = __shfl_sync(full, my_v, 0);
+}
+
+// A token's logits in registers (lane l: experts l + 32 j, pads -inf);
+// returns false for a token without a routing (NaN/+inf logits, or every
+// logit -inf).
+template <int NJ>
+__device__ __forceinline__ bool load_token_logits(const float* lg, int E, int lane, bool smem, float (&v)[NJ]) {
+  bool bad = false;
+  int ninf = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? (smem ? lg[e] : __ldcg(lg + e)) : -INFINITY;
+    if (e < E) {
+      bad |= isnan(v[j]) || v[j] == INFINITY;
+      ninf += v[j] == -INFINITY;
+    }
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  ninf = __reduce_add_sync(0xffffffffu, ninf);
+  return !bad && ninf != E;
+}
+
+// The softmax weight of lane r's pick (lane < k), with moe_route's
+// arithmetic: sum over all E of exp(logit - max) per lane in j order (pads
+// give 0), a butterfly, then the pick's share of all E (or of the k picks).
+template <int NJ>
+__device__ __forceinline__ float pick_weight(const float (&v)[NJ], int k, int renorm, int lane, float my_v) {
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
   float s_all = 0.0f;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) s_all += expf(v[j] - m);  // pads give 0
+  for (int j = 0; j < NJ; ++j) s_all += expf(v[j] - m);
   s_all = warp_sum(s_all);
   const float mine = lane < k ? expf(my_v - m) : 0.0f;
   const float s_sel = warp_sum(mine);
+  return mine / (renorm ? s_sel : s_all);
+}
+
+// Batched routing: warp t routes token t from its logits in shared memory
+// (ids -1 and weights 0 for a token without a routing).
+template <int NJ>
+__device__ void route_token_warp(const StreamParams& a, const Tables& tb, const float* lg, int t) {
+  const int lane = threadIdx.x & 31, k = a.k;
+  float v[NJ];
+  if (!load_token_logits<NJ>(lg, a.E, lane, true, v)) {
+    if (lane < k) {
+      tb.ids[t * k + lane] = -1;
+      tb.w[t * k + lane] = 0.0f;
+    }
+    return;
+  }
+  float my_v;
+  int my_i;
+  warp_topk<NJ>(v, a.E, k, lane, my_v, my_i);
+  const float wq = pick_weight<NJ>(v, k, a.renorm, lane, my_v);
   if (lane < k) {
     tb.ids[t * k + lane] = my_i;
-    tb.w[t * k + lane] = mine / (a.renorm ? s_sel : s_all);
+    tb.w[t * k + lane] = wq;
   }
 }
 
@@ -575,27 +503,31 @@ __device__ void route_tokens_warps(const StreamParams& a, const Tables& tb, cons
   }
 }
 
-// Producer warp after route_one_token: lane j < k resolves pick j's expert
-// block, the warp writes the tables the compute warps read (units are the
-// picks in choice order; every unit has its own stage in both rings) and
-// releases them; lane 0 then issues the copies. The softmax weights follow, with the
-// arithmetic of moe_route (sum over all E per lane in index order, then a
-// butterfly), and are released to the combine.
-__device__ void producer_one_token(const StreamParams& a, const Tables& tb, const float* pv, uint64_t* full_g,
+// "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
+// experts of the token (moe_route's definition). One routed token: the
+// producer warp routes it on its own (warp_topk) while the other warps
+// stage the activations. Lane j < k then resolves pick j's expert block, the
+// warp writes the tables the compute warps read (units are the picks in
+// choice order; every unit has its own stage in both rings) and releases
+// them; lane 0 issues the gate/up copies, lanes the down copies; the
+// softmax weights follow (pick_weight) and are released to the combine.
+template <int NJ>
+__device__ void producer_one_token(const StreamParams& a, const Tables& tb, const float* lgs, uint64_t* full_g,
                                    uint64_t* full_d, uint8_t* ring_g, uint8_t* ring_d, int n0, int rg_rows,
                                    int m0, int rd_rows, bool writer) {
   const int lane = threadIdx.x & 31;
   const int E = a.E, k = a.k;
   const uint32_t gbytes = (uint32_t)rg_rows * a.off.gu_row, dbytes = (uint32_t)rd_rows * a.off.d_row;
-  const bool ok = tb.misc[3] == 0;
-  // The picks' logits live in the ring, which the copies below overwrite.
-  const float m = ok ? pv[0] : 0.0f;
-  const float my_v = (ok && lane < k) ? pv[lane] : 0.0f;
+  float v[NJ];  // from shared memory (lgs lies in the ring: read before any copy is issued)
+  const bool ok = load_token_logits<NJ>(lgs, E, lane, true, v);
+  float my_v = 0.0f;
+  int my_i = -1;
+  if (ok) warp_topk<NJ>(v, E, k, lane, my_v, my_i);
   const uint8_t* blk = nullptr;
   int id = -1;
   if (lane < k) {
     if (ok) {
-      id = tb.ids[lane];
+      id = my_i;
       const int sl = tb.eslot[id];
       blk = (sl >= 0 && sl < a.n_slots) ? a.pool + (size_t)sl * a.block_bytes : nullptr;
       if (!blk && writer) atomicOr(a.ws, 1);
@@ -632,16 +564,7 @@ __device__ void producer_one_token(const StreamParams& a, const Tables& tb, cons
     mbar_arrive_expect_tx(&full_d[lane], dbytes);
     bulk_g2s(ring_d + (size_t)lane * a.sd, blk + a.off.d_offset + (size_t)m0 * a.off.d_row, dbytes, &full_d[lane]);
   }
-  float wq = 0.0f;
-  if (ok) {
-    float s_all = 0.0f;
-#pragma unroll 4
-    for (int e = lane; e < E; e += 32) s_all += expf(tb.lg[e] - m);
-    s_all = warp_sum(s_all);
-    const float mine = lane < k ? expf(my_v - m) : 0.0f;
-    const float s_sel = warp_sum(mine);
-    wq = mine / (a.renorm ? s_sel : s_all);
-  }
+  const float wq = ok ? pick_weight<NJ>(v, k, a.renorm, lane, my_v) : 0.0f;
   if (lane < k) {
     tb.w[lane] = wq;
     if (writer && a.wts_out) a.wts_out[lane] = wq;
@@ -885,8 +808,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     }
     for (int s = 0; s < kMaxRing; ++s) fillno[s] = 0;
     tb.misc[1] = 0;
-    tb.misc[3] = 0;
-    tb.misc[4] = 0;
     tb.misc[5] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -894,14 +815,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
   griddep_wait();  // x, logits / ids and slot_of come from earlier work
 
   if constexpr (FAST) {
-    // ---- one token routed in the block: see route_one_token ----------------
-    // Routing scratch in the rings (no copy is issued before the picks).
-    float* pv = reinterpret_cast<float*>(sm) + 3 * route_candidates(a.E, min(a.k, 32));
-    route_one_token(a, tb, sm, pv, xs4, xsum, xback);
+    // ---- one token: the producer warp routes and streams ------------------
+    // The token's logits (into the ring, before any copy) and the slot table
+    // go to shared memory first, one load per thread.
+    float* lgs = reinterpret_cast<float*>(ring_g);
+    #pragma unroll 2
+    for (int e = tid; e < a.E; e += kThreads) {
+      lgs[e] = __ldcg(a.logits + e);
+      tb.eslot[e] = __ldcg(a.slot_of + e);
+    }
+    __syncthreads();
     if (warp == kProducer) {
-      producer_one_token(a, tb, pv, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
+      const int nj = (a.E + 31) / 32;
+      if (nj <= 2) producer_one_token<2>(a, tb, lgs, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
+      else if (nj <= 8) producer_one_token<8>(a, tb, lgs, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
+      else if (nj <= 16) producer_one_token<16>(a, tb, lgs, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
+      else producer_one_token<32>(a, tb, lgs, full_g, full_d, ring_g, ring_d, n0, rg_rows, m0, rd_rows, writer);
       bar_arrive(kBarCompute, kThreads);  // weights ready for the combine
     } else {
+      // The other warps stage the activations, then wait for the tables.
+      const int i0 = warp < kProducer ? tid : tid - 32;
+      #pragma unroll 1
+      for (int cc = i0; cc < nchx; cc += kThreads - 32) stage_x_chunk(a.x, xs4, xsum, xback, cc);
+      __syncwarp();
       bar_sync(kBarTables, kThreads);
     }
     griddep_launch_dependents();
@@ -1082,6 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     // One token: the exchange warp polls the other blocks and copies each
     // unit's complete h into shared memory (the batched path meets the
     // other blocks once, in the compute warps).
+    __syncwarp();
     bar_arrive(kBarCompute, kThreads);
     if constexpr (FAST) {
       prefetch_one_token(a, tb, hsm, hfull, U, cnt_target, abort_flag);
@@ -1245,6 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
         if (atomicAdd(&tb.fdone[u], 1) == (tb.uoff[u + 1] - tb.uoff[u]) * ng - 1) mbar_arrive(&empty_g[s]);
       }
     }
+    __syncwarp();
     // ---- every block's h rows are out (grid barrier, bounded) --------------
     // Thread 0 releases the block's stores (ordered before it by the block
     // barrier; the release is cumulative) and waits (acquire) until all G
@@ -1264,6 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
         }
       }
     }
+    __syncwarp();
     bar_sync(kBarGate, kWarps * 32);
     // ---- down: item j is the pair at sorted position j (all of the
     // block's rows); the next item's h is loaded while this one computes.
@@ -1306,6 +1245,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       }
     }
   }
+  __syncwarp();
   bar_sync(kBarCompute, kThreads);
   // y[t][m0 + r] = sum_j w[t][j] * part[t*k + j][r] (+ y_shared), in j order.
   #pragma unroll 1
@@ -1412,8 +1352,7 @@ bool carve(StreamParams& a) {
   a.fast1 = 0;
   a.dpack = 1;
   if (a.T == 1 && a.logits != nullptr && a.k <= kMaxFastK) {
-    const size_t ringb = std::max((size_t)a.k * (sgu + sdn),
-                                  (size_t)route_candidates(a.E, std::min(a.k, 32)) * 12 + (size_t)a.k * 4);
+    const size_t ringb = std::max((size_t)a.k * (sgu + sdn), (size_t)a.E * 4);  // also the token's logits
     if (place(ringb, (size_t)a.P * a.rgu * 2, (size_t)a.k * a.I * 2)) {
       a.fast1 = 1;
       a.Sg = a.Sd = a.k;
