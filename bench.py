@@ -38,10 +38,24 @@ from int4_routed_expert_moe_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer decode tokens/s (expert-weight HBM GB/s in roofline)"
 METRIC_PREFILL = "MoE-layer prefill tokens/s (tensor-core TFLOP/s in roofline)"
-# DRAM bytes (read + written) of one launch of the decode kernel per
-# workload, from an ncu capture of the current kernel build; a workload
-# without an entry reports null.
-DECODE_DRAM_BYTES = {}
+# DRAM bytes (read + written) per algorithmic byte of one layer call, from
+# ncu captures (dram__bytes_read.sum + dram__bytes_write.sum) of the current
+# kernel build on a parity-test layer of the workload's shape; the bench
+# scales them by its own calls' algorithmic bytes (distinct experts x block
+# bytes). A workload without an entry reports null.
+DECODE_DRAM_RATIO = {
+    # decode_stream_kernel, one OLMoE layer, T = 1: 26,857,216 B for 8 experts
+    "olmoe_decode": 26_857_216 / 26_738_688,
+    # decode_stream_kernel, 512 experts, T = 1: 16,833,536 B for 10 experts
+    "large_fanout_b1": 16_833_536 / 16_711_680,
+    # decode_stream_kernel, 512 experts, T = 16: 145,658,880 + 3,502,080 B for 87 experts
+    "large_fanout_b16": (145_658_880 + 3_502_080) / 145_391_616,
+    # grouped path, 512 experts, T = 256 (route, sort, gather, two GEMMs, combine):
+    # 686,131,648 B for 377 experts
+    "large_fanout_b256": 686_131_648 / 630_030_336,
+}
+TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of a parity-test layer of this shape "
+                  "(current kernel build), scaled to this call by its distinct-expert bytes")
 # Prefill: DRAM bytes of the gate/up and down grouped GEMMs of one layer call
 # from an ncu capture (gate/up 159.45 MB read + 5.10 MB written, down 79.77 +
 # 8.18 MB).
@@ -348,12 +362,12 @@ def decode_roofline(wl, step_ms, peak, peak_src):
     launch_s = step_ms / 1e3 / wl.L
     assert wl.L * launch_s * 1e3 <= step_ms * (1 + 1e-9)
     achieved = bytes_per_launch / launch_s / 1e9
-    traffic = DECODE_DRAM_BYTES.get(wl.name)
+    ratio = DECODE_DRAM_RATIO.get(wl.name)
+    traffic = int(round(ratio * wl.expert_bytes_per_step() / wl.L)) if ratio else None
     return {"bound": "hbm", "kernel": "decode_stream_kernel (routing, gate/up + SwiGLU, down + combine; one layer)",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": traffic,
-            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the current "
-                              "kernel on this workload" if traffic else "not captured for this kernel build",
+            "traffic_source": TRAFFIC_SOURCE if traffic else "not captured for this kernel build",
             "bytes_per_launch": int(bytes_per_launch), "avg_launch_us": round(launch_s * 1e6, 3),
             "peak_source": peak_src,
             "timing": "CUDA events over the timed region on the launching stream; launch time = step time / layers"}
@@ -730,13 +744,16 @@ def run_fanout(args, world, rank, T):
                        "kernel": ("decode_stream_kernel, one layer" if streamed else
                                   "moe_layer_forward grouped path (route, sort, gather, 2 GEMMs, combine), one layer"),
                        "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                       "frac": round(achieved / peak, 4), "traffic": None,
-                       "traffic_source": "not captured for this kernel build",
+                       "frac": round(achieved / peak, 4),
+                       "traffic": (int(round(DECODE_DRAM_RATIO[f"large_fanout_b{T}"] * bytes_step / L))
+                                   if f"large_fanout_b{T}" in DECODE_DRAM_RATIO else None),
+                       "traffic_source": (TRAFFIC_SOURCE if f"large_fanout_b{T}" in DECODE_DRAM_RATIO
+                                          else "not captured for this kernel build"),
                        "bytes_per_launch": int(bytes_step / L), "avg_launch_us": round(launch_s * 1e6, 3),
                        "bytes_rule": "distinct experts of each layer x expert block bytes, from the timed steps' ids",
                        "peak_source": peak_src,
                        "timing": "CUDA events over the timed region; layer time = step time / layers"}
-    out["gpu_launches"] = L * K * (1 if streamed else 7)
+    out["gpu_launches"] = L * K * (1 if streamed else 6)  # grouped: route, sort, gather, 2 GEMMs, combine
     out["clocks"] = clocks
     return out
 

@@ -29,9 +29,12 @@ inline BlockOffsets offsets_of(const BlockLayout& b) {
 }
 
 // The workspace starts with a 256-byte header; its first int32 is the sticky
-// error word, the second the fused decode kernel's exit counter. Then come the
-// fused kernel's per-pair counters [P] (256-byte rounded); every path keeps
-// its scratch after them, so counters stay zero between calls of any path.
+// error word, the second the streamed decode kernel's exit counter (blocks
+// counted out). Then come that kernel's counters, [P] int32 (256-byte
+// rounded): one per unit (distinct expert) for one routed token, the grid
+// barrier's counter in the first word for several tokens. The last block out
+// zeroes them, and every path keeps its scratch after them, so they stay zero
+// between calls of any path.
 constexpr size_t kWorkspaceHeader = 256;
 inline size_t ws_scratch_offset(int P) { return kWorkspaceHeader + (((size_t)P * 4 + 255) / 256) * 256; }
 
