@@ -1030,12 +1030,21 @@ def device_info():
     return info
 
 
+# Arm "CPU part" numbers of /proc/cpuinfo (implementer 0x41) seen on these hosts.
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+             "0xd49": "Arm Neoverse N2"}
+
+
 def cpu_model():
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu part")):
+                key = line.lower()
+                if key.startswith("model name"):
                     return line.split(":", 1)[1].strip()
+                if key.startswith("cpu part"):
+                    part = line.split(":", 1)[1].strip()
+                    return f"{ARM_PARTS[part]} (CPU part {part})" if part in ARM_PARTS else f"CPU part {part}"
     except OSError:
         pass
     return "unknown"

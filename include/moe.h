@@ -237,10 +237,13 @@ int moe_expert_forward_zero_copy(const moe_expert_shape* shape, const void* x, i
  * The same result as moe_route(logits, ...) followed by
  * moe_expert_forward(...): the router picks each token's experts and their
  * weights ("02 / A solução") and the chosen INT4 experts run on x. On the
- * GEMV path, when T * E * E <= 262144, the routing runs inside the expert
- * kernels (every block ranks the logits itself, fixed-order reductions), so
- * no separate routing kernel or id round trip sits between the layer's input
- * and its weight stream; otherwise moe_route runs first.
+ * GEMV path (MOE_PATH_GEMV, or MOE_PATH_AUTO at T <= 16 and T*k <= 256) with
+ * the streamed decode kernel's limits (H <= 4096, inter <= 2048, E <= 1024)
+ * the routing runs inside that kernel: every block picks the same experts
+ * with moe_route's selection and fixed-order softmax (one token: the block's
+ * producer warp; several: a warp per token), so no separate routing kernel
+ * or id round trip sits between the layer's input and its weight stream;
+ * otherwise moe_route runs first.
  * logits  device fp32 [T][E]; ids / weights device out [T][k] (the routing
  * used, as moe_route defines it: NaN/+inf/all -inf tokens get ids -1).
  * Other arguments as moe_expert_forward; limits as moe_route.

@@ -267,7 +267,8 @@ __device__ __forceinline__ void stage_x_chunk(const __half* __restrict__ src, ui
 // the warp sum: s * (sum_c q_c x_c - z * sum_c x_c) over the lane's chunks
 // cc = lane + 32 it. The activation chunk is loaded once for all rows; the
 // rows' dot products are independent chains. acc = (g0, u0, g1, u1, ...).
-constexpr int kGateRows = 4;  // rows per gate/up work item
+constexpr int kGateRows = 4;  // rows per gate/up work item (at most)
+constexpr int kFastRows = 4;  // one routed token: rows per gate/up work item
 template <int NC>
 __device__ __forceinline__ void gate_up_rows(const uint8_t* row0, int nrows, const BlockOffsets& off, int nch,
                                              int lane, const int* gq, const uint4* xs4, const float* xsum,
@@ -769,7 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
   const int n0 = (int)(((long long)c * a.I) / a.G), n1 = (int)(((long long)(c + 1) * a.I) / a.G);
   const int m0 = (int)(((long long)c * a.H) / a.G), m1 = (int)(((long long)(c + 1) * a.H) / a.G);
   const int rg_rows = n1 - n0, rd_rows = m1 - m0;
-  const int ng = (rg_rows + kGateRows - 1) / kGateRows;   // gate/up items per unit
+  constexpr int kRows = FAST ? kFastRows : kGateRows;
+  const int ng = (rg_rows + kRows - 1) / kRows;            // gate/up items per unit
   const int nd = (rd_rows + kDownRows - 1) / kDownRows;   // down items per unit
   uint8_t* ring_g = sm;
   uint8_t* ring_d = sm + a.o_ring_d;
@@ -1075,8 +1077,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       #pragma unroll 1
       for (int r = (warp - s * ng) & (kWarps - 1); r < ng; r += kWarps) {
         const bool ok = __all_sync(0xffffffffu, wait_phase(&full_g[s], fill & 1, abort_flag, a.ws));
-        const int ra = r * kGateRows;
-        const int nrows = min(kGateRows, rg_rows - ra);
+        const int ra = r * kFastRows;
+        const int nrows = min(kFastRows, rg_rows - ra);
         const uint8_t* rowa = ring_g + (size_t)s * a.sg + (size_t)ra * a.off.gu_row;
         #pragma unroll 1
         for (int i = tb.uoff[u]; i < tb.uoff[u + 1] && ok; ++i) {
