@@ -459,12 +459,14 @@ def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0, prefetch=0):
     ws = torch.zeros(moe.moe_forward_workspace_bytes(ps.shape, 1, k, E, moe.MOE_PATH_GEMV), dtype=torch.uint8,
                      device=dev)
     ids_host = torch.empty((k,), dtype=torch.int32).pin_memory()
+    id_trace = [[] for _ in range(L)]  # every step's ids per layer, as the manager saw them
 
     def step(s):
         for l in range(L):
             moe.moe_route(ps.logits[s, l], k, ps.wl["renorm"], ids[l], w[l])
             ids_host.copy_(ids[l].view(-1), non_blocking=True)
             torch.cuda.current_stream().synchronize()  # the step's ids reach the host
+            id_trace[l].append(ids_host.numpy().tolist())
             moe.moe_residency_prepare(h, l, ids_host.numpy())
             x = ps.x0[s] if l == 0 else y[l - 1]
             moe.moe_expert_forward(ps.shape, x, ids[l], w[l], E, pool[l], slot_of[l], C + prefetch, None, y[l],
@@ -498,6 +500,7 @@ def partial_copy(moe, ps, C, policy, K, W, world, steps_from=0, prefetch=0):
         moe.moe_residency_destroy(h)
     hits, misses = st1["hits"] - st0["hits"], st1["misses"] - st0["misses"]
     return {"ms": ms, "wall_s": wall, "hits": hits, "misses": misses, "pinned": pinned,
+            "id_trace": id_trace, "total_hits": st1["hits"], "total_misses": st1["misses"],
             "bytes_out": st1["h2d_bytes"] - st0["h2d_bytes"], "launches_per_step": L * 7,
             "prefetched": st1["prefetched"] - st0["prefetched"],
             "prefetch_copies": st1["prefetch_copies"] - st0["prefetch_copies"]}
@@ -657,7 +660,35 @@ def run_partial(args, world, rank):
     out["time_model"] = time_model_line(full, low, main_run, K, Ktm, E, lo)
     if args.mode == "copy":
         out["time_model"]["copy_engine_gbs"] = round(copy_engine_gbs(ps), 2)
+        if rank == 0:
+            out["residency_oracle"] = residency_oracle_timing(ps, C, args.policy, args.prefetch, main_run)
     out["gpu_launches"] = main_run["launches_per_step"] * K
+    return out
+
+
+def residency_oracle_timing(ps, C, policy, spares, run):
+    """The oracle's residency simulator (the decision model the library
+    implements) on the run's full id trace -- every layer, warm-up and timed
+    steps -- single-threaded on the host, with its hit and miss totals beside
+    the library's. With spare slots the library also served prefetches the
+    trace does not hold, so only the time is reported."""
+    from oracle import moe_oracle
+    pinned = run["pinned"]
+    profile = ps.profile() if policy == "pinned" else None
+    t0 = time.perf_counter()
+    hits = misses = 0
+    for l, steps in enumerate(run["id_trace"]):
+        r = moe_oracle.residency_sim(steps, ps.E, C, 0, ps.wl["decay"], policy,
+                                     None if profile is None else profile[l], pinned)
+        hits += r["hits"]
+        misses += r["misses"]
+    dt = time.perf_counter() - t0
+    n_steps = sum(len(st) for st in run["id_trace"])
+    out = {"layers": len(run["id_trace"]), "layer_steps": n_steps, "seconds": round(dt, 3), "cores": 1,
+           "layer_steps_per_s": round(n_steps / dt, 1), "kind": "oracle"}
+    if not spares:
+        out.update({"hits": hits, "misses": misses,
+                    "matches_library": hits == run["total_hits"] and misses == run["total_misses"]})
     return out
 
 
