@@ -51,6 +51,7 @@ constexpr int kExchange = kWarps + 1;
 constexpr int kMaxT = 16;                     // tokens per call
 constexpr int kMaxP = 256;                    // (token, choice) pairs per call
 constexpr int kMaxE = 1024;                   // experts (in-block tables)
+static_assert(kMaxE <= 2 * kThreads, "the batched unit scan takes two experts per thread");
 constexpr int kMaxRing = 32;                  // stages per ring
 constexpr int kMaxFastK = 16;                 // one routed token: picks that each get their own stages
 constexpr int kDownRows = 8;                  // rows per down work item
@@ -865,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
     }
     #pragma unroll 1
     for (int q = tid; q < 2 * a.P; q += kThreads) tb.fdone[q] = 0;
-    #pragma unroll 1
+    #pragma unroll 2
     for (int i = tid; i < a.T * nchx; i += kThreads) {
       const int t = i / nchx, cc = i - t * nchx;
       stage_x_chunk(a.x + (size_t)t * a.H, xs4 + (size_t)t * nchx * 4, xsum + (size_t)t * nchx,
@@ -905,16 +906,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       tb.punit[p] = u;
     }
     __syncthreads();
-    // Units: experts with pairs, in ascending id (one warp, exclusive scans).
-    if (warp == 0) {
-      const int per = (a.E + 31) / 32;
-      const int e0 = min(a.E, lane * per), e1 = min(a.E, e0 + per);
-      int nu = 0, np = 0;
-      #pragma unroll 1
-      for (int e = e0; e < e1; ++e) {
-        nu += tb.ecnt[e] > 0;
-        np += tb.ecnt[e];
-      }
+    // Units: experts with pairs, in ascending id, by a block-wide exclusive
+    // scan (thread i takes experts 2i and 2i + 1; E <= 2 * kThreads).
+    {
+      int32_t* wsum = reinterpret_cast<int32_t*>(sm);  // [2][warps], in the routing scratch (read already)
+      constexpr int kW = kThreads / 32;
+      const int e0 = 2 * tid;
+      const int c0 = e0 < a.E ? tb.ecnt[e0] : 0, c1 = e0 + 1 < a.E ? tb.ecnt[e0 + 1] : 0;
+      const int nu = (c0 > 0) + (c1 > 0), np = c0 + c1;
       int su = nu, sp = np;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -924,10 +923,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
           sp += vp;
         }
       }
-      int u = su - nu, pos = sp - np;
+      if (lane == 31) {
+        wsum[warp] = su;
+        wsum[kW + warp] = sp;
+      }
+      __syncthreads();
       #pragma unroll 1
-      for (int e = e0; e < e1; ++e) {
-        const int n = tb.ecnt[e];
+      for (int w = 0; w < warp; ++w) {
+        su += wsum[w];
+        sp += wsum[kW + w];
+      }
+      int u = su - nu, pos = sp - np;
+      #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h, n = h ? c1 : c0;
+        if (e >= a.E) break;
         tb.eunit[e] = n > 0 ? u : -1;
         if (n > 0) {
           tb.uexp[u] = e;
@@ -938,10 +948,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
           pos += n;
         }
       }
-      const int U = __shfl_sync(0xffffffffu, su, 31);
-      if (lane == 31) {
-        tb.misc[0] = U;
-        tb.uoff[U] = sp;
+      if (tid == kThreads - 1) {
+        tb.misc[0] = su;
+        tb.uoff[su] = sp;
       }
     }
     __syncthreads();
