@@ -305,3 +305,26 @@ def test_layer_forward_batched_routing_edges(E, k):
     # (logit desc, index asc) whatever lane holds them, ties by index.
     lg = _routing_rows(E, k, 47)
     _layer_forward_case((256, 128, 64), E, k, False, 4, 47, logits=lg)
+
+
+def test_one_token_h_words_across_calls_and_paths():
+    # One token's h crosses the blocks as words marked with a per-call
+    # counter: a sequence of one-token calls on one workspace, with a
+    # several-token call (FP16 h in the same bytes) in between, must each use
+    # only its own words.
+    shape, E, k = (2048, 1024, 128), 64, 8
+    lp = LayerPool(moe, 48, 0, shape, E)
+    dev = torch.device("cuda")
+    ws = torch.zeros(moe.moe_forward_workspace_bytes(shape, 2, k, E, 1), dtype=torch.uint8, device=dev)
+    for i, T in enumerate([1, 2, 1, 1, 2, 1]):
+        x16 = synth.activations(48, 10 + i, T, shape[0])
+        lg = synth.logits_normal(48, 20 + i, T, E)
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        y = torch.empty((T, shape[0]), dtype=torch.float16, device=dev)
+        moe.moe_layer_forward(shape, torch.from_numpy(x16).to(dev), torch.from_numpy(lg).to(dev), k, False, ids, w,
+                              lp.pool, lp.slot_of, E, None, y, ws, 1)
+        assert moe.moe_workspace_flags(ws) == 0
+        ref = moe_oracle.moe_layer(x16, lg, lp.arrays, k, False, shape[2])
+        ok, err, bound = tol_ok(y.float().cpu().numpy(), ref["y"])
+        assert ok, (i, T, err, bound)
