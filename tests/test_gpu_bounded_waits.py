@@ -3,15 +3,13 @@
 Every wait of the kernel gives up after about a second: the block sets bit 2
 of the workspace error word, stops waiting, lets its own copies land and
 exits, and the last block out still zeroes the counters. The tests make one
-wait run out without any fault: the grid barrier's counter, which every
-block releases into between the gate/up and the down items, starts far
-below zero, so the count the waiters expect never comes. The call must come
+wait run out without any fault: a counter that every block releases into
+starts far below zero, so the count the waiters expect never comes -- the
+grid barrier's counter of the several-token schedule (4 tokens, and one
+token with 17 picks, which takes that schedule), and the per-unit counters
+that one token's exchange warps poll before copying h. The call must come
 back with bit 2 set, the counters zeroed, and the next call on the same
-workspace must be correct. (The single-token schedule of up to 16 picks has
-no counter: its blocks poll each other's marked h words, which every block
-writes itself, so nothing outside the kernel can withhold them; its polls
-end on the same bound and abort path, read in the code. One token with 17
-picks takes the grid-barrier schedule and is tested here.)
+workspace must be correct.
 """
 import numpy as np
 import pytest
@@ -28,7 +26,7 @@ moe = binding() if torch.cuda.is_available() else None
 
 SHAPE = (2048, 1024, 128)  # the OLMoE expert shape
 E = 64
-CNT_BASE = 64  # workspace word of the grid barrier's counter
+CNT_BASE = 64  # workspace word of the kernel's first counter
 
 
 @pytest.fixture(scope="module")
@@ -45,8 +43,8 @@ def _call(lp, x, lg, ws, T, K):
     return y
 
 
-@pytest.mark.parametrize("T,K", [(4, 8), (1, 17)])
-def test_decode_wait_expires_and_workspace_recovers(pool, T, K):
+@pytest.mark.parametrize("T,K,counters", [(4, 8, 1), (1, 17, 1), (1, 8, 8)])
+def test_decode_wait_expires_and_workspace_recovers(pool, T, K, counters):
     dev = torch.device("cuda")
     x16 = synth.activations(pool.seed, 5, T, SHAPE[0])
     lg16 = synth.logits_normal(pool.seed, 6, T, E)
@@ -54,7 +52,7 @@ def test_decode_wait_expires_and_workspace_recovers(pool, T, K):
     ws = torch.zeros(moe.moe_forward_workspace_bytes(SHAPE, T, K, E, moe.MOE_PATH_GEMV), dtype=torch.uint8,
                      device=dev)
     words = ws.view(torch.int32)
-    n = 1
+    n = counters  # the grid barrier's counter, or one counter per unit (one token, <= 16 picks)
     words[CNT_BASE:CNT_BASE + n] = -(1 << 30)  # a release count nobody reaches
     _call(pool, x, lg, ws, T, K)
     torch.cuda.synchronize()
