@@ -44,12 +44,12 @@ METRIC_PREFILL = "MoE-layer prefill tokens/s (tensor-core TFLOP/s in roofline)"
 # scales them by its own calls' algorithmic bytes (distinct experts x block
 # bytes). A workload without an entry reports null.
 DECODE_DRAM_RATIO = {
-    # decode_stream_kernel, one OLMoE layer, T = 1: 26,857,216 B for 8 experts
-    "olmoe_decode": 26_857_216 / 26_738_688,
+    # decode_stream_kernel, one OLMoE layer, T = 1: 26,856,704 B for 8 experts
+    "olmoe_decode": 26_856_704 / 26_738_688,
     # decode_stream_kernel, 512 experts, T = 1: 16,833,536 B for 10 experts
     "large_fanout_b1": 16_833_536 / 16_711_680,
-    # decode_stream_kernel, 512 experts, T = 16: 145,658,880 + 3,502,080 B for 87 experts
-    "large_fanout_b16": (145_658_880 + 3_502_080) / 145_391_616,
+    # decode_stream_kernel, 512 experts, T = 16: 145,656,576 + 3,329,536 B for 87 experts
+    "large_fanout_b16": (145_656_576 + 3_329_536) / 145_391_616,
     # grouped path, 512 experts, T = 256 (route, sort, gather, two GEMMs, combine):
     # 686,131,648 B for 377 experts
     "large_fanout_b256": 686_131_648 / 630_030_336,
