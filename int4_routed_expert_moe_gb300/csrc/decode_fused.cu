@@ -221,14 +221,6 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
   return false;
 }
 
-// "Horizon RunMap -- Prévia Técnica", "02 / A solução": the router picks the
-// experts of each token: top-k by (logit desc, index asc), softmax over all
-// E, renormalised over the k when asked -- moe_route's definition. A token
-// with NaN/+inf logits or all -inf gets ids -1 and weights 0. a ranks before
-// b in (value desc, index asc); -0 == +0 by IEEE compare.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
 
 // The activations of a token in shared memory as the scaled pairs of
 // dot16_scaled, 64 bytes per 32-element chunk; piece i (16 bytes) of chunk
@@ -347,91 +339,6 @@ constexpr int kBarCompute = 1;  // before the combine: compute warps (and, batch
 constexpr int kBarTables = 2;   // producer arrives with the routing tables, compute warps wait
 constexpr int kBarGate = 3;     // batched: the compute warps around the grid barrier
 constexpr int kBarPolled = 4;   // exchange warp arrives after its last counter poll, producer waits (64)
-
-// Order-preserving key of a finite or infinite FP32 value (larger value,
-// larger key; -0 and +0 share the key of +0, as they compare equal).
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Top-k of one token in one warp: lane l holds experts l + 32 j (j < NJ,
-// NJ >= E/32) in registers, pads (e >= E) are never picked. Each lane keeps
-// its best CD not yet picked in a small sorted cache (rank order: logit
-// desc, index asc); round r takes the best cache head of the warp -- the
-// largest key by one warp reduction, the smallest index among equal keys by
-// another -- and the owning lane pops it, refilling its cache from its
-// registers when it runs dry. Lane r < k returns pick r (value, expert).
-// This is moe_route's selection (top-k by (logit desc, index asc)).
-template <int NJ>
-__device__ __forceinline__ void warp_topk(const float (&v)[NJ], int E, int k, int lane, float& my_v, int& my_i) {
-  const unsigned full = 0xffffffffu;
-  int mine_n = 0;
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) mine_n += lane + 32 * j < E;
-  constexpr int CD = NJ < 2 ? NJ : 2;
-  float cv[CD];
-  int ci[CD];
-  // The lane's best CD elements that rank after (lv, li).
-  auto fill = [&](float lv, int li) {
-#pragma unroll
-    for (int c = 0; c < CD; ++c) {
-      cv[c] = -INFINITY;
-      ci[c] = INT_MAX;
-    }
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && ranks_before(lv, li, v[j], e)) {
-        bool b[CD];
-#pragma unroll
-        for (int c = 0; c < CD; ++c) b[c] = ranks_before(v[j], e, cv[c], ci[c]);
-#pragma unroll
-        for (int c = CD - 1; c >= 1; --c) {
-          if (b[c - 1]) {
-            cv[c] = cv[c - 1];
-            ci[c] = ci[c - 1];
-          } else if (b[c]) {
-            cv[c] = v[j];
-            ci[c] = e;
-          }
-        }
-        if (b[0]) {
-          cv[0] = v[j];
-          ci[0] = e;
-        }
-      }
-    }
-  };
-  fill(INFINITY, -1);
-  int taken = 0;
-  my_v = 0.0f;
-  my_i = -1;
-#pragma unroll 1
-  for (int r = 0; r < k; ++r) {
-    const bool has = ci[0] != INT_MAX;
-    const uint32_t key = has ? order_key(cv[0]) : 0u;  // every real key is above 0
-    const uint32_t kmax = __reduce_max_sync(full, key);
-    const uint32_t win = __reduce_min_sync(full, (has && key == kmax) ? (uint32_t)ci[0] : 0xffffffffu);
-    const float wv = __shfl_sync(full, cv[0], (int)(win & 31));
-    if (lane == r) {
-      my_v = wv;
-      my_i = (int)win;
-    }
-    if (has && (uint32_t)ci[0] == win) {
-      const float pv = cv[0];
-      ++taken;
-#pragma unroll
-      for (int c = 0; c + 1 < CD; ++c) {
-        cv[c] = cv[c + 1];
-        ci[c] = ci[c + 1];
-      }
-      cv[CD - 1] = -INFINITY;
-      ci[CD - 1] = INT_MAX;
-      if (ci[0] == INT_MAX && taken < mine_n) fill(pv, (int)win);
-    }
-  }
-}
 
 // A token's logits in registers (lane l: experts l + 32 j, pads -inf);
 // returns false for a token without a routing (NaN/+inf logits, or every

@@ -10,14 +10,9 @@
 namespace moe {
 namespace {
 
-// a ranks before b in (value desc, index asc); -0 == +0 by IEEE compare.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// One warp per token. Lane l holds elements l, l+32, ... (PER_LANE of them).
-// Round r picks the best element that ranks after round r-1's pick, so no
-// "taken" mask is needed; k rounds give the k picks in order.
+// One warp per token. Lane l holds elements l, l+32, ... (PER_LANE of them);
+// warp_topk picks the k best in order (per-lane cache of its best elements,
+// warp reductions for the best of the round).
 template <int PER_LANE>
 __global__ void __launch_bounds__(128) route_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
@@ -44,7 +39,7 @@ __global__ void __launch_bounds__(128) route_kernel(
     }
     v[i] = x;
   }
-  // Pad elements (e >= E) rank after every real one: index INT_MAX.
+  // Pad elements (e >= E) are never picked and add 0 to the softmax sum.
   const unsigned full = 0xffffffffu;
   bad = __any_sync(full, bad);
   int total_ninf = n_neg_inf;
@@ -60,39 +55,9 @@ __global__ void __launch_bounds__(128) route_kernel(
     return;
   }
 
-  float prev_v = INFINITY;
-  int prev_i = -1;
   float my_v = 0.0f;
   int my_i = -1;
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int e = lane + 32 * i;
-      const int idx = e < E ? e : INT_MAX;
-      const bool after_prev = ranks_before(prev_v, prev_i, v[i], idx);
-      if (after_prev && ranks_before(v[i], idx, bv, bi)) {
-        bv = v[i];
-        bi = idx;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(full, bv, o);
-      const int oi = __shfl_xor_sync(full, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == r) {
-      my_v = bv;
-      my_i = bi;
-    }
-    prev_v = bv;
-    prev_i = bi;
-  }
+  warp_topk<PER_LANE>(v, E, k, lane, my_v, my_i);  // lane r < k: pick r
 
   // Softmax over all E in FP32, shifted by the top logit.
   const float m = __shfl_sync(full, my_v, 0);

@@ -6,9 +6,10 @@
 // One block of 32 warps. Warp w owns the contiguous pair segment
 // [w*seg, (w+1)*seg). Pass 1 counts, per warp and expert, the pairs of the
 // segment (warp match instead of atomics). Pass 2 turns the counts into
-// per-warp starting positions (prefix over warps, then an exclusive scan over
-// experts). Pass 3 re-walks each segment in order and scatters; ranks inside a
-// 32-pair chunk come from the match mask, so the order is stable.
+// per-warp starting positions (prefix over warps, then a block-wide exclusive
+// scan over experts, a thread per expert). Pass 3 re-walks each segment in
+// order and scatters; ranks inside a 32-pair chunk come from the match mask,
+// so the order is stable.
 #include "common.h"
 #include "device.cuh"
 #include "kernels.h"
@@ -24,15 +25,21 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
   extern __shared__ __align__(16) int32_t sm[];
   int32_t* cnt = sm;                          // [kSortWarps][E]
   int32_t* total = sm + kSortWarps * E;       // [E + 1]
+  int32_t* slot = total + E + 1;              // [E] copy of slot_of (tile list / id check only)
+  int32_t* wsc = slot + E;                    // [2][kSortWarps] warp sums of the expert scans
   griddep_wait();
   griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < kSortWarps * E; i += blockDim.x) cnt[i] = 0;
+  if (tl.tiles)
+    for (int e = tid; e < E; e += blockDim.x) slot[e] = tl.slot_of[e];
   __syncthreads();
   const int seg = (P + kSortWarps - 1) / kSortWarps;
   const int p0 = warp * seg, p1 = min(P, p0 + seg);
   const unsigned lt_mask = (1u << lane) - 1u;
-  // Pass 1: per-warp histogram.
+  // Pass 1: per-warp histogram (rounds unrolled, so that their id loads are
+  // in flight together).
+#pragma unroll 4
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     int e = -1;
@@ -49,7 +56,7 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
         const int raw = ids[p];
         if (raw != -1 && (raw < 0 || raw >= E)) bad_id = 1;
         else if (raw >= 0) {
-          const int sl = tl.slot_of[raw];
+          const int sl = slot[raw];
           no_slot = sl < 0 || sl >= tl.n_slots;
         }
       }
@@ -59,63 +66,67 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
     __syncwarp();
   }
   __syncthreads();
-  // Pass 2a: per expert, exclusive prefix over warps; totals per expert.
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < kSortWarps; ++w) {
-      const int c = cnt[w * E + e];
-      cnt[w * E + e] = run;
-      run += c;
+  // Pass 2 (thread e = expert e, E <= blockDim): the exclusive prefix of the
+  // expert's counts over the warps (in place), then block-wide exclusive
+  // scans over experts of the totals (the experts' first sorted positions)
+  // and of the tile counts (tile list: every resident expert with pairs,
+  // tiles of up to tile_n consecutive sorted pairs: slot, first position,
+  // pairs, expert).
+  {
+    int tot = 0, tc = 0, sl = -1;
+    if (tid < E) {
+      for (int w = 0; w < kSortWarps; ++w) {
+        const int c = cnt[w * E + tid];
+        cnt[w * E + tid] = tot;
+        tot += c;
+      }
+      if (tl.tiles) {
+        sl = slot[tid];
+        if (tot > 0 && sl >= 0 && sl < tl.n_slots) tc = (tot + tl.tile_n - 1) / tl.tile_n;
+      }
     }
-    total[e] = run;
-  }
-  __syncthreads();
-  // Pass 2b: exclusive scan of totals over experts (one warp, E <= 1024).
-  if (warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int v = e < E ? total[e] : 0;
-      int incl = v;
+    int it = tot, ic = tc;  // inclusive within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, it, o), b = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) {
+        it += a;
+        ic += b;
+      }
+    }
+    if (lane == 31) {
+      wsc[warp] = it;
+      wsc[kSortWarps + warp] = ic;
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of the warp sums
+      const int a = wsc[lane], b = wsc[kSortWarps + lane];
+      int ia = a, ib = b;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (e < E) total[e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) total[E] = carry;
-    // Tile list: every resident expert with pairs, tiles of up to tile_n
-    // consecutive sorted pairs (slot, first position, pairs, expert).
-    if (tl.tiles) {
-      __syncwarp();  // total[] of every lane visible to the warp
-      int tcarry = 0;
-      for (int base = 0; base < E; base += 32) {
-        const int e = base + lane;
-        int tc = 0, sl = -1, o0 = 0, ne = 0;
-        if (e < E) {
-          o0 = total[e];
-          ne = (e + 1 < E ? total[e + 1] : carry) - o0;
-          sl = tl.slot_of[e];
-          if (ne > 0 && sl >= 0 && sl < tl.n_slots) tc = (ne + tl.tile_n - 1) / tl.tile_n;
+        const int na = __shfl_up_sync(0xffffffffu, ia, o), nb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+          ia += na;
+          ib += nb;
         }
-        int incl = tc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        for (int i = 0; i < tc; ++i)
-          tl.tiles[tcarry + incl - tc + i] = make_int4(sl, o0 + i * tl.tile_n, min(tl.tile_n, ne - i * tl.tile_n), e);
-        tcarry += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (lane == 0) *tl.n_tiles = tcarry;
+      wsc[lane] = ia - a;
+      wsc[kSortWarps + lane] = ib - b;
     }
+    __syncthreads();
+    const int first = wsc[warp] + it - tot, tfirst = wsc[kSortWarps + warp] + ic - tc;
+    if (tid < E) total[tid] = first;
+    if (tid == E - 1) {
+      total[E] = first + tot;
+      if (tl.tiles) *tl.n_tiles = tfirst + tc;
+    }
+    for (int i = 0; i < tc; ++i)
+      tl.tiles[tfirst + i] = make_int4(sl, first + i * tl.tile_n, min(tl.tile_n, tot - i * tl.tile_n), tid);
   }
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) offsets[e] = total[e];
   // Pass 3: stable scatter.
+#pragma unroll 4
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     int e = -1;
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(kSortWarps * 32) token_sort_kernel(
 
 int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
                       int32_t* pair_tok, int32_t* pair_j, cudaStream_t st, const SortTiles* tiles) {
-  const size_t smem = (size_t)(kSortWarps * E + E + 1) * sizeof(int32_t);
+  const size_t smem = (size_t)(kSortWarps * E + 2 * E + 1 + 2 * kSortWarps) * sizeof(int32_t);
   cudaError_t e = cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort smem attr: %s", cudaGetErrorString(e));
   cudaLaunchConfig_t cfg = {};
