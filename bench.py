@@ -51,8 +51,8 @@ DECODE_DRAM_RATIO = {
     # decode_stream_kernel, 512 experts, T = 16: 145,656,576 + 3,329,536 B for 87 experts
     "large_fanout_b16": (145_656_576 + 3_329_536) / 145_391_616,
     # grouped path, 512 experts, T = 256 (route, sort, gather, two GEMMs, combine):
-    # 686,131,648 B for 377 experts
-    "large_fanout_b256": 686_131_648 / 630_030_336,
+    # 685,785,856 B for 377 experts
+    "large_fanout_b256": 685_785_856 / 630_030_336,
 }
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of a parity-test layer of this shape "
                   "(current kernel build), scaled to this call by its distinct-expert bytes")
