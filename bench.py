@@ -51,15 +51,15 @@ DECODE_DRAM_RATIO = {
     # decode_stream_kernel, 512 experts, T = 16: 145,656,576 + 3,329,536 B for 87 experts
     "large_fanout_b16": (145_656_576 + 3_329_536) / 145_391_616,
     # grouped path, 512 experts, T = 256 (route, sort, gather, two GEMMs, combine):
-    # 685,785,856 B for 377 experts
-    "large_fanout_b256": 685_785_856 / 630_030_336,
+    # 686,125,824 B for 377 experts
+    "large_fanout_b256": 686_125_824 / 630_030_336,
 }
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of a parity-test layer of this shape "
                   "(current kernel build), scaled to this call by its distinct-expert bytes")
 # Prefill: DRAM bytes of the gate/up and down grouped GEMMs of one layer call
-# from an ncu capture (gate/up 159.45 MB read + 5.10 MB written, down 79.77 +
-# 8.18 MB).
-PREFILL_GEMM_DRAM_BYTES = 252_505_088
+# from an ncu capture (gate/up 159.47 MB read + 5.84 MB written, down 79.77 +
+# 8.05 MB).
+PREFILL_GEMM_DRAM_BYTES = 253_141_504
 
 
 def parse():

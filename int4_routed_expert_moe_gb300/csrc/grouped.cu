@@ -75,11 +75,13 @@ constexpr int BK = 64;   // K elements per pipeline step (one 128-byte swizzle r
 constexpr int BN = 128;  // sorted pairs per tile at most (MMA N)
 // Warp roles: 0 codes TMA, 1 TMEM + MMA issue (accumulator 0), 2 activation
 // TMA, 3 MMA issue (accumulator 1), 4..19 expand codes to FP16 and run the
-// epilogue. One thread issues a tcgen05.mma about every 120 cycles whatever
-// its N, so two issuing threads with an accumulator each double the rate at
-// the small N of a single expert's pairs. The expansion is a chain of short
-// dependent steps per warp; sixteen expand warps (four per SM sub-partition)
-// keep the issue slots busy.
+// epilogue. At the small N of one expert's pairs an issuing thread needs
+// about as long per MMA as the tensor pipe (~54 cycles against 32 at N = 64),
+// so two issuing warps with an accumulator each keep the pipe fed; each runs
+// its loop converged with one elected lane issuing (a lone issuing lane
+// loses half its rate to the expand warps on its scheduler). The expansion
+// is a chain of short dependent steps per warp; sixteen expand warps (four
+// per SM sub-partition) keep the issue slots busy.
 constexpr int kDqWarps = 16;
 constexpr int kThreads = (4 + kDqWarps) * 32;
 constexpr uint32_t kCodeBytes = BM * 32;      // codes of 128 rows x 64 elements
@@ -319,43 +321,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_aborted(b)) drain(b.x_full, G::SX, issued);
     }
   } else if (warp == 1 || warp == 3) {
-    if (lane == 0) {
-      // Issuer p owns accumulator p: the gate (p = 0) or up (p = 1)
-      // projection, or for the down projection the K slices kk = p, p + 2.
-      const int p = warp == 1 ? 0 : 1;
-      for (int w = blockIdx.x, li = 0; w < n_items && !is_aborted(b); w += gridDim.x, ++li) {
-        const Item it = item_of(a, w, rblocks);
-        const uint32_t idesc = tc::idesc_f16(BM, it.nmma);
-        // The previous item's epilogue has read the accumulators.
-        if (li > 0 && !tc::bar_wait(b.acc_empty, (li - 1) & 1)) {
-          abort_block(b, a.flags);
+    // Issuer p owns accumulator p: the gate (p = 0) or up (p = 1)
+    // projection, or for the down projection the K slices kk = p, p + 2.
+    // The whole warp runs the loop (waits, descriptors) and one elected lane
+    // issues: descriptors from values fixed before the loop plus one add, one
+    // wait per step (a_full also stands for the activation tile, see the
+    // expand warps), the abort flag read once per item.
+    const int p = warp == 1 ? 0 : 1;
+    const uint32_t d_tmem = tmem + (uint32_t)(p * BN);
+    const uint64_t xdesc0 = tc::sw128_desc(tc::smem_addr(sm + G::offX));
+    constexpr uint32_t kXDescStep = kXBytes >> 4;  // descriptor address units per activation stage
+    const uint32_t a_tmem0 = tmem + G::colA(0, NPROJ == 2 ? p : 0);
+    constexpr uint32_t kAColStep = G::colA(1, 0) - G::colA(0, 0);
+    for (int w = blockIdx.x, li = 0; w < n_items && !__any_sync(0xffffffffu, is_aborted(b)); w += gridDim.x, ++li) {
+      const Item it = item_of(a, w, rblocks);
+      const uint32_t idesc = tc::idesc_f16(BM, it.nmma);
+      // The previous item's epilogue has read the accumulators.
+      if (li > 0 && !tc::bar_wait_warp(b.acc_empty, (li - 1) & 1)) {
+        if (lane == 0) abort_block(b, a.flags);
+        break;
+      }
+      tc::tc_fence_after();
+      bool ok = true;
+      for (int kt = 0; kt < KT; ++kt) {
+        const int g = li * KT + kt, sa = g % G::SA;
+        if (!tc::bar_wait_warp(&b.a_full[sa], (g / G::SA) & 1)) {
+          ok = false;
           break;
         }
         tc::tc_fence_after();
-        for (int kt = 0; kt < KT; ++kt) {
-          const int g = li * KT + kt, sa = g % G::SA;
-          if (!tc::bar_wait(&b.a_full[sa], (g / G::SA) & 1) || !tc::bar_wait(&b.x_full[sa], (g / G::SX) & 1)) {
-            abort_block(b, a.flags);
-            break;
-          }
-          if (is_aborted(b)) break;
-          tc::tc_fence_after();
-          const uint32_t xbase = tc::smem_addr(sm + G::offX + (size_t)sa * kXBytes);
+        const uint64_t xd = xdesc0 + (uint64_t)(sa * kXDescStep);  // 128-byte-swizzled tile, 1024-aligned
+        const uint32_t at = a_tmem0 + (uint32_t)sa * kAColStep;
+        if (tc::elect_one()) {
           if (NPROJ == 2) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, p) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
-                             kt > 0 || kk > 0);
+              tc::mma_f16_ta(d_tmem, at + kk * 8, xd + 2 * kk, idesc, kt > 0 || kk > 0);
           } else {
 #pragma unroll
-            for (int kk = p; kk < BK / 16; kk += 2)
-              tc::mma_f16_ta(tmem + p * BN, tmem + G::colA(sa, 0) + kk * 8, tc::sw128_desc(xbase + kk * 32), idesc,
-                             kt > 0 || kk > p);
+            for (int kk = 0; kk < BK / 16; kk += 2)
+              tc::mma_f16_ta(d_tmem, at + (kk + p) * 8, xd + 2 * (kk + p), idesc, kt > 0 || kk > 0);
           }
           tc::mma_commit(&b.a_empty[sa]);
         }
-        tc::mma_commit(b.acc_full);
+        __syncwarp();
       }
+      if (!ok) {
+        if (lane == 0) abort_block(b, a.flags);
+        break;
+      }
+      if (tc::elect_one()) tc::mma_commit(b.acc_full);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // Expand: warp w owns the TMEM lanes of its quarter (rows 32 (w % 4) ..
@@ -416,6 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tmem_st_wait();
         tc::tc_fence_before();
+        // Lane 0 of the step's quarter-0 warp also waits for the step's
+        // activation tile before its arrival, so a complete a_full phase means
+        // both operands are in place (the issuers wait on a_full alone).
+        bool xin = true;
+        if (q4 == 0 && lane == 0) xin = tc::bar_wait(&b.x_full[sa], (g / G::SX) & 1);
+        if (!__shfl_sync(0xffffffffu, xin, 0)) {
+          abort_block(b, a.flags);
+          ok = false;
+          break;
+        }
         __syncwarp();
         if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
       }

@@ -107,26 +107,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       produce_tiles<2, kGuStages>(c, sm, kGuStage, kGuN * BK * 2, &map_wg, &map_wu, &map_x, row0, tok0, KT, a.flags);
   } else if (warp == 1 || warp == 3) {
-    if (lane == 0) {  // issuer p: the gate (p = 0) or up (p = 1) projection
-      const int p = warp == 1 ? 0 : 1;
-      const uint32_t idesc = tc::idesc_f16(BM, nmma);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kGuStages;
-        if (!tc::bar_wait(&c.tma_full[s], (kt / kGuStages) & 1)) {
-          tc::set_abort(c, a.flags);
-          break;
-        }
-        if (tc::aborted(c)) break;
-        tc::tc_fence_after();
-        const uint32_t base = tc::smem_addr(sm + (size_t)s * kGuStage);
+    // Issuer p: the gate (p = 0) or up (p = 1) projection. The whole warp
+    // runs the loop, one elected lane issues.
+    const int p = warp == 1 ? 0 : 1;
+    const uint32_t idesc = tc::idesc_f16(BM, nmma);
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % kGuStages;
+      if (!tc::bar_wait_warp(&c.tma_full[s], (kt / kGuStages) & 1)) {
+        if (lane == 0) tc::set_abort(c, a.flags);
+        break;
+      }
+      if (__any_sync(0xffffffffu, tc::aborted(c))) break;
+      tc::tc_fence_after();
+      const uint32_t base = tc::smem_addr(sm + (size_t)s * kGuStage);
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           tc::mma_f16(tmem + p * kGuN, tc::sw128_desc(base + p * kWTile + kk * 32),
                       tc::sw128_desc(base + 2 * kWTile + kk * 32), idesc, kt > 0 || kk > 0);
         tc::mma_commit(&c.empty[s]);
       }
-      tc::mma_commit(c.acc_full);
+      __syncwarp();
     }
+    if (tc::elect_one()) tc::mma_commit(c.acc_full);
+    __syncwarp();
   } else if (warp >= 4) {
     const bool ok = tc::bar_wait(c.acc_full, 0);
     if (!ok) tc::set_abort(c, a.flags);
@@ -175,26 +179,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       produce_tiles<1, kDnStages>(c, sm, kDnStage, kDnN * BK * 2, &map_wd, nullptr, &map_h, row0, tok0, KT, a.flags);
   } else if (warp == 1 || warp == 3) {
-    if (lane == 0) {  // issuer p: the K slices kk = p, p + 2 of every step, into accumulator p
-      const int p = warp == 1 ? 0 : 1;
-      const uint32_t idesc = tc::idesc_f16(BM, nmma);
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kDnStages;
-        if (!tc::bar_wait(&c.tma_full[s], (kt / kDnStages) & 1)) {
-          tc::set_abort(c, a.flags);
-          break;
-        }
-        if (tc::aborted(c)) break;
-        tc::tc_fence_after();
-        const uint32_t base = tc::smem_addr(sm + (size_t)s * kDnStage);
+    // Issuer p: the K slices kk = p, p + 2 of every step, into accumulator p.
+    // The whole warp runs the loop, one elected lane issues.
+    const int p = warp == 1 ? 0 : 1;
+    const uint32_t idesc = tc::idesc_f16(BM, nmma);
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % kDnStages;
+      if (!tc::bar_wait_warp(&c.tma_full[s], (kt / kDnStages) & 1)) {
+        if (lane == 0) tc::set_abort(c, a.flags);
+        break;
+      }
+      if (__any_sync(0xffffffffu, tc::aborted(c))) break;
+      tc::tc_fence_after();
+      const uint32_t base = tc::smem_addr(sm + (size_t)s * kDnStage);
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = p; kk < BK / 16; kk += 2)
           tc::mma_f16(tmem + p * kDnN, tc::sw128_desc(base + kk * 32), tc::sw128_desc(base + kWTile + kk * 32), idesc,
                       kt > 0 || kk > p);
         tc::mma_commit(&c.empty[s]);
       }
-      tc::mma_commit(c.acc_full);
+      __syncwarp();
     }
+    if (tc::elect_one()) tc::mma_commit(c.acc_full);
+    __syncwarp();
   } else if (warp >= 4) {
     const bool ok = tc::bar_wait(c.acc_full, 0);
     if (!ok) tc::set_abort(c, a.flags);

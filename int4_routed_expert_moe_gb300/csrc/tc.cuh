@@ -171,6 +171,23 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
+// One lane of a converged warp: true in exactly one active lane. An issuing
+// loop run by the whole warp, with the tcgen05 operations under this
+// predicate, keeps its warp-uniform operands uniform; the same loop run by a
+// lone lane issues at about half the rate once other warps load its
+// scheduler (measured on GB300: 4 MMAs + commit of N = 64 in 294 cycles
+// against 576).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pr;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(pr));
+  return pr != 0;
+}
+// Bounded wait by every lane of a converged warp, with one verdict for all.
+__device__ __forceinline__ bool bar_wait_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, bar_wait(bar, parity));
+}
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
