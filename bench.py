@@ -44,22 +44,22 @@ METRIC_PREFILL = "MoE-layer prefill tokens/s (tensor-core TFLOP/s in roofline)"
 # scales them by its own calls' algorithmic bytes (distinct experts x block
 # bytes). A workload without an entry reports null.
 DECODE_DRAM_RATIO = {
-    # decode_stream_kernel, one OLMoE layer, T = 1: 26,856,704 B for 8 experts
-    "olmoe_decode": 26_856_704 / 26_738_688,
-    # decode_stream_kernel, 512 experts, T = 1: 16,833,536 B for 10 experts
-    "large_fanout_b1": 16_833_536 / 16_711_680,
-    # decode_stream_kernel, 512 experts, T = 16: 145,656,576 + 3,329,536 B for 87 experts
-    "large_fanout_b16": (145_656_576 + 3_329_536) / 145_391_616,
+    # decode_stream_kernel, one OLMoE layer, T = 1: 26,856,960 B for 8 experts
+    "olmoe_decode": 26_856_960 / 26_738_688,
+    # decode_stream_kernel, 512 experts, T = 1: 16,834,304 B for 10 experts
+    "large_fanout_b1": 16_834_304 / 16_711_680,
+    # decode_stream_kernel, 512 experts, T = 16: 145,702,912 + 3,361,536 B for 87 experts
+    "large_fanout_b16": (145_702_912 + 3_361_536) / 145_391_616,
     # grouped path, 512 experts, T = 256 (route, sort, gather, two GEMMs, combine):
-    # 686,125,824 B for 377 experts
-    "large_fanout_b256": 686_125_824 / 630_030_336,
+    # 686,300,672 B for 377 experts
+    "large_fanout_b256": 686_300_672 / 630_030_336,
 }
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of a parity-test layer of this shape "
                   "(current kernel build), scaled to this call by its distinct-expert bytes")
 # Prefill: DRAM bytes of the gate/up and down grouped GEMMs of one layer call
-# from an ncu capture (gate/up 159.47 MB read + 5.84 MB written, down 79.77 +
-# 8.05 MB).
-PREFILL_GEMM_DRAM_BYTES = 253_141_504
+# from an ncu capture (gate/up 159.48 MB read + 6.29 MB written, down 79.79 +
+# 8.20 MB).
+PREFILL_GEMM_DRAM_BYTES = 253_761_536
 
 
 def parse():

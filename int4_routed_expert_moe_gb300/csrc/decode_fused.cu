@@ -55,7 +55,7 @@ static_assert(kMaxE <= 2 * kThreads, "the batched unit scan takes two experts pe
 constexpr int kMaxRing = 32;                  // stages per ring
 constexpr int kMaxFastK = 16;                 // one routed token: picks that each get their own stages
 constexpr int kDownRows = 8;                  // rows per down work item
-constexpr unsigned kMbarTries = 50000;        // ~1 s (20 us suspend hint per try)
+constexpr unsigned long long kWaitNs = 1000000000ull;  // bound of one mbarrier wait: ~1 s of global time
 constexpr unsigned kIdleTries = 16000000;     // ~1 s of idle producer loop iterations
 constexpr unsigned kSpinTries = 2000000;      // ~1 s of counter polls (one L2 round trip each)
 constexpr int kCntBase = 64;                  // workspace word of unit counter 0
@@ -74,15 +74,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// try_wait with a suspend-time hint: the thread sleeps until the phase
-// completes or about 20 us pass.
+// try_wait without a suspend-time hint: the thread waits at most a short,
+// hardware-defined window for the phase (a 20 us hint measured 0.7 % slower
+// at the OLMoE decode shape: the hand-offs of one layer are short waits).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(20000u) : "memory");
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long v;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(v));
+  return v;
+}
+// Bounded wait for a phase (about kWaitNs), no abort check: copies landing
+// before a block exits.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  #pragma unroll 1
+  while (global_ns() - t0 < kWaitNs)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 // Non-blocking test of a phase.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
@@ -211,11 +227,13 @@ __device__ __forceinline__ Tables tables_of(const StreamParams& a, uint8_t* sm) 
 // already aborted. Returns false (and marks the abort) on expiry.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
                                            int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
   #pragma unroll 1
-  for (unsigned i = 0; i < kMbarTries; ++i) {
+  do {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-  }
+  } while (global_ns() - t0 < kWaitNs);
   *abort_flag = 1;
   atomicOr(err, 4);
   return false;
@@ -923,9 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
       #pragma unroll 1
       for (int s = lane; s < a.Sg && s < q; s += 32) {
         const int last = s + a.Sg * ((q - 1 - s) / a.Sg);
-        #pragma unroll 1
-        for (unsigned i = 0; i < kMbarTries && !mbar_try_wait(&full_g[s], (last / a.Sg) & 1); ++i) {
-        }
+        mbar_wait_bounded(&full_g[s], (last / a.Sg) & 1);
       }
       __syncwarp();
     }
@@ -956,15 +972,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
         #pragma unroll 1
         for (int u = 0; u < U; ++u) {
           if (!tb.blk[u]) continue;
-          #pragma unroll 1
-          for (unsigned i = 0; ng > 0 && i < kMbarTries && !mbar_try_wait(&full_g[u], 0); ++i) {
-          }
-          #pragma unroll 1
-          for (unsigned i = 0; nd > 0 && i < kMbarTries && !mbar_try_wait(&full_d[u], 0); ++i) {
-          }
-          #pragma unroll 1
-          for (unsigned i = 0; ((tb.misc[5] >> u) & 1) && i < kMbarTries && !mbar_try_wait(&hfull[u], 0); ++i) {
-          }
+          if (ng > 0) mbar_wait_bounded(&full_g[u], 0);
+          if (nd > 0) mbar_wait_bounded(&full_d[u], 0);
+          if ((tb.misc[5] >> u) & 1) mbar_wait_bounded(&hfull[u], 0);
         }
       }
       if (atom_add_acq_rel_gpu(&a.ws[1], 1) == a.G - 1) {

@@ -83,21 +83,26 @@ constexpr int BN = 128;  // sorted pairs per tile at most (MMA N)
 // is a chain of short dependent steps per warp; sixteen expand warps (four
 // per SM sub-partition) keep the issue slots busy.
 constexpr int kDqWarps = 16;
-constexpr int kThreads = (4 + kDqWarps) * 32;
+// The down kernel has four more warps (20..23) for its epilogue: its items are
+// short (K = I), so it keeps two accumulators and the next item's MMAs run
+// while these warps write the previous item's rows.
+constexpr int kEpiWarps = 4;
+template <int NPROJ>
+constexpr int kThreadsOf = (4 + kDqWarps + (NPROJ == 1 ? kEpiWarps : 0)) * 32;
 constexpr uint32_t kCodeBytes = BM * 32;      // codes of 128 rows x 64 elements
 constexpr uint32_t kSzBytes = BM * 32;        // 32 bytes of scale/zero entries per row
 constexpr uint32_t kXBytes = BN * BK * 2;     // activation tile, up to 128 pairs
 
 // Ring geometry per kernel (NPROJ = 2: gate and up; 1: down). Two rings:
-// codes in shared memory (freed as soon as the expand warps hold them in
-// registers), and per step an activation tile in shared memory plus the
-// expanded FP16 weights in tensor memory (freed together, by one commit per
-// issuing thread, when the MMAs reading them complete). Keeping the expanded
-// operand out of shared memory leaves its bandwidth to the TMA writes and the
-// activation reads of the MMAs.
+// codes and scale/zero entries in shared memory (freed as soon as the expand
+// warps hold them in registers), and per step an activation tile in shared
+// memory plus the expanded FP16 weights in tensor memory (freed together, by
+// one commit per issuing warp, when the MMAs reading them complete). Keeping
+// the expanded operand out of shared memory leaves its bandwidth to the TMA
+// writes and the activation reads of the MMAs.
 template <int NPROJ>
 struct Geo {
-  static constexpr int SC = 8;
+  static constexpr int SC = NPROJ == 2 ? 12 : 16;  // code stages: 144 / 128 KB in flight per SM
   static constexpr int SA = 4;
   static constexpr int SX = SA;
   static constexpr uint32_t kC = NPROJ * kCodeBytes + kSzBytes;
@@ -181,7 +186,7 @@ struct GemmParams {
 };
 
 struct Bars {
-  uint64_t *c_full, *c_empty, *x_full, *a_full, *a_empty, *acc_full, *acc_empty;
+  uint64_t *c_full, *c_empty, *x_full, *a_full, *a_empty, *acc_full, *acc_empty, *handoff;
   uint32_t* tmem_slot;
   int* abort;
 };
@@ -195,8 +200,9 @@ __device__ __forceinline__ Bars bars_at(uint8_t* p) {
   b.x_full = q; q += G::SX;
   b.a_full = q; q += G::SA;
   b.a_empty = q; q += G::SA;
-  b.acc_full = q; q += 1;
-  b.acc_empty = q; q += 1;
+  b.acc_full = q; q += 2;
+  b.acc_empty = q; q += 2;
+  b.handoff = q; q += 2;
   b.tmem_slot = reinterpret_cast<uint32_t*>(q);
   b.abort = reinterpret_cast<int*>(b.tmem_slot + 1);
   return b;
@@ -237,7 +243,7 @@ __device__ __forceinline__ Item item_of(const GemmParams& a, int w, int rblocks)
 }
 
 template <int NPROJ>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<NPROJ>, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
                         const GemmParams a) {
   using G = Geo<NPROJ>;
@@ -260,10 +266,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < G::SA; ++s) {
       tc::bar_init(&b.x_full[s], 1);
       tc::bar_init(&b.a_full[s], 4);
-      tc::bar_init(&b.a_empty[s], 2);  // one commit per issuing thread
+      tc::bar_init(&b.a_empty[s], NPROJ == 2 ? 2 : 1);  // one commit per issuing warp that reads the step
     }
-    tc::bar_init(b.acc_full, 2);
-    tc::bar_init(b.acc_empty, kDqWarps);
+    if (NPROJ == 2) {  // one accumulator pair; the expand warps run the epilogue
+      tc::bar_init(&b.acc_full[0], 2);
+      tc::bar_init(&b.acc_empty[0], kDqWarps);
+    } else {  // two accumulators, items alternating; the epilogue warps free them
+      for (int p = 0; p < 2; ++p) {
+        tc::bar_init(&b.acc_full[p], 1);
+        tc::bar_init(&b.acc_empty[p], kEpiWarps);
+        tc::bar_init(&b.handoff[p], 1);
+      }
+    }
     *b.abort = 0;
     tc::bar_init_fence();
   }
@@ -321,8 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_aborted(b)) drain(b.x_full, G::SX, issued);
     }
   } else if (warp == 1 || warp == 3) {
-    // Issuer p owns accumulator p: the gate (p = 0) or up (p = 1)
-    // projection, or for the down projection the K slices kk = p, p + 2.
+    // Issuing warp p owns accumulator p. Gate/up: the gate (p = 0) or up
+    // (p = 1) projection of every item. Down: the items li with li % 2 == p,
+    // all four K slices of each step, so one item's MMAs run while the
+    // epilogue warps read the other accumulator; a warp starts its item once
+    // the other has issued the item before (handoff), so its waits on the
+    // step barriers, which complete once per step, are never a phase ahead.
     // The whole warp runs the loop (waits, descriptors) and one elected lane
     // issues: descriptors from values fixed before the loop plus one add, one
     // wait per step (a_full also stands for the activation tile, see the
@@ -334,10 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t a_tmem0 = tmem + G::colA(0, NPROJ == 2 ? p : 0);
     constexpr uint32_t kAColStep = G::colA(1, 0) - G::colA(0, 0);
     for (int w = blockIdx.x, li = 0; w < n_items && !__any_sync(0xffffffffu, is_aborted(b)); w += gridDim.x, ++li) {
+      if (NPROJ == 1 && (li & 1) != p) continue;
       const Item it = item_of(a, w, rblocks);
       const uint32_t idesc = tc::idesc_f16(BM, it.nmma);
-      // The previous item's epilogue has read the accumulators.
-      if (li > 0 && !tc::bar_wait_warp(b.acc_empty, (li - 1) & 1)) {
+      // The epilogue has read this accumulator's previous item.
+      const int use = NPROJ == 2 ? li : (li >> 1);  // this accumulator's use count
+      uint64_t* acc_full = &b.acc_full[NPROJ == 2 ? 0 : p];
+      uint64_t* acc_empty = &b.acc_empty[NPROJ == 2 ? 0 : p];
+      if (NPROJ == 1 && li > 0 && !tc::bar_wait_warp(&b.handoff[p ^ 1], ((li - 1) >> 1) & 1)) {
+        if (lane == 0) abort_block(b, a.flags);
+        break;
+      }
+      if (use > 0 && !tc::bar_wait_warp(acc_empty, (use - 1) & 1)) {
         if (lane == 0) abort_block(b, a.flags);
         break;
       }
@@ -353,15 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t xd = xdesc0 + (uint64_t)(sa * kXDescStep);  // 128-byte-swizzled tile, 1024-aligned
         const uint32_t at = a_tmem0 + (uint32_t)sa * kAColStep;
         if (tc::elect_one()) {
-          if (NPROJ == 2) {
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc::mma_f16_ta(d_tmem, at + kk * 8, xd + 2 * kk, idesc, kt > 0 || kk > 0);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; kk += 2)
-              tc::mma_f16_ta(d_tmem, at + (kk + p) * 8, xd + 2 * (kk + p), idesc, kt > 0 || kk > 0);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16_ta(d_tmem, at + kk * 8, xd + 2 * kk, idesc, kt > 0 || kk > 0);
           tc::mma_commit(&b.a_empty[sa]);
         }
         __syncwarp();
@@ -370,10 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) abort_block(b, a.flags);
         break;
       }
-      if (tc::elect_one()) tc::mma_commit(b.acc_full);
+      if (tc::elect_one()) {
+        tc::mma_commit(acc_full);
+        if (NPROJ == 1) tc::bar_arrive(&b.handoff[p]);  // this item's MMAs are all issued
+      }
       __syncwarp();
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4 + kDqWarps) {
     // Expand: warp w owns the TMEM lanes of its quarter (rows 32 (w % 4) ..
     // +31) and every fourth step (global step g = j (mod 4), j = (w - 4) / 4),
     // so four steps are expanded at once; lane t owns row 32 (w % 4) + t, all
@@ -446,51 +469,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
       }
       if (!ok) break;
+      if (NPROJ == 1) continue;  // the epilogue warps take the down items
       // Epilogue of this item: TMEM lanes of this warp's quarter, the
       // 16-column chunks ci = j4, j4 + 4, ... of the live columns; then
       // release the accumulators.
-      const bool got = tc::bar_wait(b.acc_full, li & 1);
+      const bool got = tc::bar_wait(&b.acc_full[0], li & 1);
       if (!got) abort_block(b, a.flags);
       tc::tc_fence_after();
       const int row = it.row0 + r;
       const bool live = got && !is_aborted(b) && row < a.rows;
       for (int c0 = 16 * j4; c0 < it.nmma; c0 += 64) {
-        if (NPROJ == 2) {
-          float gv[16], uv[16];
-          tc::tmem_ld16(tlane + (uint32_t)c0, gv);
-          tc::tmem_ld16(tlane + (uint32_t)(BN + c0), uv);
-          tc::tmem_ld_wait();
-          if (live) {
-            const int prow = (row & ~7) | kperm_pos(row & 7);
+        float gv[16], uv[16];
+        tc::tmem_ld16(tlane + (uint32_t)c0, gv);
+        tc::tmem_ld16(tlane + (uint32_t)(BN + c0), uv);
+        tc::tmem_ld_wait();
+        if (live) {
+          const int prow = (row & ~7) | kperm_pos(row & 7);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < it.n)
-                a.h_sorted[(size_t)(it.pos0 + c0 + j) * a.rows + prow] =
-                    __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
-          }
-        } else {
-          // Output pair index of column c0 + lane (lanes 0..15), shared by shuffles.
-          int qi = 0;
-          if (lane < 16 && c0 + lane < it.n) {
-            const int pos = it.pos0 + c0 + lane;
-            qi = a.pair_tok[pos] * a.k + a.pair_j[pos];
-          }
-          float dv[16], ev[16];
-          tc::tmem_ld16(tlane + (uint32_t)c0, dv);
-          tc::tmem_ld16(tlane + (uint32_t)(BN + c0), ev);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) dv[j] += ev[j];  // even + odd K slices, fixed order
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int q = __shfl_sync(0xffffffffu, qi, j);
-            if (live && c0 + j < it.n) a.pair_out[(size_t)q * a.rows + row] = dv[j] * kInvAScale;
-          }
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < it.n)
+              a.h_sorted[(size_t)(it.pos0 + c0 + j) * a.rows + prow] =
+                  __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
         }
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::bar_arrive(b.acc_empty);
+      if (lane == 0) tc::bar_arrive(&b.acc_empty[0]);
+      if (!got) break;
+    }
+  } else if (NPROJ == 1) {
+    // Down epilogue (warps 20..23): warp q owns the TMEM lanes of quarter q.
+    // Per item: the output pair index of each column (lane l holds columns
+    // l, l + 32, l + 64, l + 96), read before the accumulator is ready; then
+    // the FP32 rows of the item's pairs, and the accumulator released.
+    const int q4 = warp & 3;
+    const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
+    for (int w = blockIdx.x, li = 0; w < n_items; w += gridDim.x, ++li) {
+      const Item it = item_of(a, w, rblocks);
+      static_assert(BN == 128, "four 32-column groups per accumulator");
+      int qcol[BN / 32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col = lane + 32 * c;
+        qcol[c] = 0;
+        if (col < it.n) qcol[c] = a.pair_tok[it.pos0 + col] * a.k + a.pair_j[it.pos0 + col];
+      }
+      const int pb = li & 1;
+      const bool got = tc::bar_wait_warp(&b.acc_full[pb], (li >> 1) & 1);
+      if (!got && lane == 0) abort_block(b, a.flags);
+      tc::tc_fence_after();
+      const int row = it.row0 + 32 * q4 + lane;
+      const bool live = got && !is_aborted(b) && row < a.rows;
+      for (int c0 = 0; c0 < it.nmma; c0 += 16) {
+        float dv[16];
+        tc::tmem_ld16(tlane + (uint32_t)(pb * BN + c0), dv);
+        tc::tmem_ld_wait();
+        const int qsrc = (c0 >> 5) == 0 ? qcol[0] : (c0 >> 5) == 1 ? qcol[1] : (c0 >> 5) == 2 ? qcol[2] : qcol[3];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int q = __shfl_sync(0xffffffffu, qsrc, (c0 & 31) + j);
+          if (live && c0 + j < it.n) a.pair_out[(size_t)q * a.rows + row] = dv[j] * kInvAScale;
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&b.acc_empty[pb]);
       if (!got) break;
     }
   }
@@ -504,61 +547,101 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- small kernels -------------------------------------------------------------
 // X_sorted[pos] = x[pair_tok[pos]], each 8-element chunk in operand K order.
-__global__ void grouped_gather_kernel(const __half* __restrict__ x, int H, const int32_t* __restrict__ offsets,
-                                      int E, const int32_t* __restrict__ pair_tok, __half* __restrict__ xs) {
+// A warp per sorted row (rows pos < offsets[E] hold valid pairs): the row's
+// token is read once and the row's 16-byte chunks are loaded side by side.
+constexpr int kGatherWarps = 8;
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    grouped_gather_kernel(const __half* __restrict__ x, int H, const int32_t* __restrict__ offsets, int E,
+                          const int32_t* __restrict__ pair_tok, __half* __restrict__ xs) {
   const int pv = offsets[E];
   const int cpr = H / 8;
-  const long long total = (long long)pv * cpr;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int pos = (int)(i / cpr), ch = (int)(i - (long long)pos * cpr);
+  const int lane = threadIdx.x & 31;
+  for (int pos = blockIdx.x * kGatherWarps + (threadIdx.x >> 5); pos < pv; pos += gridDim.x * kGatherWarps) {
     const int t = pair_tok[pos];
-    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + 8 * ch);
-    const unsigned short* e = reinterpret_cast<const unsigned short*>(&v);
-    uint4 o;
-    o.x = (uint32_t)e[0] | ((uint32_t)e[4] << 16);
-    o.y = (uint32_t)e[1] | ((uint32_t)e[5] << 16);
-    o.z = (uint32_t)e[2] | ((uint32_t)e[6] << 16);
-    o.w = (uint32_t)e[3] | ((uint32_t)e[7] << 16);
-    *reinterpret_cast<uint4*>(xs + (size_t)pos * H + 8 * ch) = o;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)pos * H);
+#pragma unroll 4
+    for (int ch = lane; ch < cpr; ch += 32) {
+      const uint4 v = src[ch];
+      const unsigned short* e = reinterpret_cast<const unsigned short*>(&v);
+      uint4 o;
+      o.x = (uint32_t)e[0] | ((uint32_t)e[4] << 16);
+      o.y = (uint32_t)e[1] | ((uint32_t)e[5] << 16);
+      o.z = (uint32_t)e[2] | ((uint32_t)e[6] << 16);
+      o.w = (uint32_t)e[3] | ((uint32_t)e[7] << 16);
+      dst[ch] = o;
+    }
   }
 }
 
 // y[t][m] = sum_j w[t][j] * pair_out[t*k + j][m] (+ y_shared), j in order;
-// pairs whose expert is not usable contribute nothing.
-__global__ void grouped_combine_kernel(const float* __restrict__ pair_out, const int32_t* __restrict__ ids,
-                                       const float* __restrict__ w, const int32_t* __restrict__ slot_of,
-                                       int n_slots, int E, int T, int k, int H, const __half* __restrict__ y_shared,
-                                       __half* __restrict__ y) {
-  const int cpr = H / 8;
-  const long long total = (long long)T * cpr;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / cpr), m0 = 8 * (int)(i - (long long)t * cpr);
+// pairs whose expert is not usable contribute nothing. A warp per (token,
+// 256-column segment): lanes j < k resolve choice j's usability and weight
+// once, then every lane loads its 8 columns of all the token's usable pair
+// rows (up to 8 rows in flight) before adding them in j order.
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(kCombineWarps * 32, 2)
+    grouped_combine_kernel(const float* __restrict__ pair_out, const int32_t* __restrict__ ids,
+                           const float* __restrict__ w, const int32_t* __restrict__ slot_of, int n_slots, int E,
+                           int T, int k, int H, const __half* __restrict__ y_shared, __half* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int segs = (H + 255) / 256;
+  const long long units = (long long)T * segs;
+  for (long long u = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5); u < units;
+       u += (long long)gridDim.x * kCombineWarps) {
+    const int t = (int)(u / segs), m0 = (int)(u - (long long)t * segs) * 256 + 8 * lane;
+    const bool mv = m0 < H;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < k; ++j) {
-      const int q = t * k + j;
-      const int e = ids[q];
-      if (e < 0 || e >= E) continue;
-      const int s = slot_of[e];
-      if (s < 0 || s >= n_slots) continue;
-      const float wj = w[q];
-      const float4* src = reinterpret_cast<const float4*>(pair_out + (size_t)q * H + m0);
-      const float4 v0 = src[0], v1 = src[1];
-      acc[0] += wj * v0.x; acc[1] += wj * v0.y; acc[2] += wj * v0.z; acc[3] += wj * v0.w;
-      acc[4] += wj * v1.x; acc[5] += wj * v1.y; acc[6] += wj * v1.z; acc[7] += wj * v1.w;
-    }
-    if (y_shared) {
-      const uint4 ys = *reinterpret_cast<const uint4*>(y_shared + (size_t)t * H + m0);
-      const __half* e = reinterpret_cast<const __half*>(&ys);
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      // choice j0 + lane: usable, and its weight
+      bool use = false;
+      float wl = 0.0f;
+      if (j0 + lane < k) {
+        const int q = t * k + j0 + lane;
+        const int e = ids[q];
+        if (e >= 0 && e < E) {
+          const int s = slot_of[e];
+          use = s >= 0 && s < n_slots;
+        }
+        wl = w[q];
+      }
+      const unsigned um = __ballot_sync(0xffffffffu, use);
+      const int nj = min(32, k - j0);
+      for (int jb = 0; jb < nj; jb += 8) {
+        float4 v[8][2];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] += __half2float(e[c]);
-    }
-    uint4 o;
-    __half* oh = reinterpret_cast<__half*>(&o);
+        for (int d = 0; d < 8; ++d) {
+          const int j = jb + d;
+          if (j < nj && ((um >> j) & 1u) && mv) {
+            const float4* src = reinterpret_cast<const float4*>(pair_out + (size_t)(t * k + j0 + j) * H + m0);
+            v[d][0] = src[0];
+            v[d][1] = src[1];
+          }
+        }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) oh[c] = __float2half_rn(acc[c]);
-    *reinterpret_cast<uint4*>(y + (size_t)t * H + m0) = o;
+        for (int d = 0; d < 8; ++d) {
+          const int j = jb + d;
+          const float wj = __shfl_sync(0xffffffffu, wl, j & 31);
+          if (j < nj && ((um >> j) & 1u) && mv) {
+            acc[0] += wj * v[d][0].x; acc[1] += wj * v[d][0].y; acc[2] += wj * v[d][0].z; acc[3] += wj * v[d][0].w;
+            acc[4] += wj * v[d][1].x; acc[5] += wj * v[d][1].y; acc[6] += wj * v[d][1].z; acc[7] += wj * v[d][1].w;
+          }
+        }
+      }
+    }
+    if (mv) {
+      if (y_shared) {
+        const uint4 ys = *reinterpret_cast<const uint4*>(y_shared + (size_t)t * H + m0);
+        const __half* e = reinterpret_cast<const __half*>(&ys);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] += __half2float(e[c]);
+      }
+      uint4 o;
+      __half* oh = reinterpret_cast<__half*>(&o);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) oh[c] = __float2half_rn(acc[c]);
+      *reinterpret_cast<uint4*>(y + (size_t)t * H + m0) = o;
+    }
   }
 }
 
@@ -629,7 +712,7 @@ int grouped_forward(const ForwardArgs& a) {
   stl.flags = flags;
   int rc = launch_token_sort(a.ids, P, a.k, a.E, offsets, pair_tok, pair_j, st, &stl);
   if (rc != MOE_OK) return rc;
-  grouped_gather_kernel<<<4 * 152, 256, 0, st>>>(a.x, a.H, offsets, a.E, pair_tok, xs);
+  grouped_gather_kernel<<<8 * 152, kGatherWarps * 32, 0, st>>>(a.x, a.H, offsets, a.E, pair_tok, xs);
   if ((rc = check_launch("grouped gather")) != MOE_OK) return rc;
 
   // Tensor maps: expert sections of the pool (bytes; rows; slots) and the
@@ -693,7 +776,7 @@ int grouped_forward(const ForwardArgs& a) {
   const int n_sm = num_sms();
   if (n_sm <= 0) return fail(MOE_ERR_CUDA, "device query failed");
   const int gu_items = ((a.I + BM - 1) / BM) * w.max_tiles, dn_items = ((a.H + BM - 1) / BM) * w.max_tiles;
-  grouped_gemm_kernel<2><<<std::min(n_sm, gu_items), kThreads, Geo<2>::smem, st>>>(m_gu, m_x, gu);
+  grouped_gemm_kernel<2><<<std::min(n_sm, gu_items), kThreadsOf<2>, Geo<2>::smem, st>>>(m_gu, m_x, gu);
   if ((rc = check_launch("grouped gate/up GEMM")) != MOE_OK) return rc;
   GemmParams dn = gp;
   dn.rows = a.H;
@@ -701,9 +784,9 @@ int grouped_forward(const ForwardArgs& a) {
   dn.q0 = a.off.d_q;
   dn.sz = a.off.d_sz;
   dn.pair_out = pair_out;
-  grouped_gemm_kernel<1><<<std::min(n_sm, dn_items), kThreads, Geo<1>::smem, st>>>(m_dn, m_h, dn);
+  grouped_gemm_kernel<1><<<std::min(n_sm, dn_items), kThreadsOf<1>, Geo<1>::smem, st>>>(m_dn, m_h, dn);
   if ((rc = check_launch("grouped down GEMM")) != MOE_OK) return rc;
-  grouped_combine_kernel<<<4 * 152, 256, 0, st>>>(pair_out, a.ids, a.weights, a.slot_of, a.n_slots, a.E, a.T,
+  grouped_combine_kernel<<<8 * 152, kCombineWarps * 32, 0, st>>>(pair_out, a.ids, a.weights, a.slot_of, a.n_slots, a.E, a.T,
                                                   a.k, a.H, a.y_shared, a.y);
   return check_launch("grouped combine");
 }

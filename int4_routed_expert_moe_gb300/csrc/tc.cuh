@@ -30,12 +30,13 @@ __device__ __forceinline__ void bar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
 }
+// try_wait without a suspend-time hint (a short, hardware-defined window).
 __device__ __forceinline__ bool bar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(20000u) : "memory");
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
 // Non-blocking test of a phase.
@@ -47,14 +48,22 @@ __device__ __forceinline__ bool bar_test(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait (about one second at most); false when it gave up. A phase
-// that has already completed is taken without the suspending wait.
-constexpr unsigned kWaitTries = 50000;
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t v;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(v));
+  return v;
+}
+// Bounded wait (about one second of global time at most); false when it gave
+// up. A phase that has already completed is taken at the first test.
+constexpr uint64_t kWaitNs = 1000000000ull;
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
   if (bar_test(bar, parity)) return true;
-  for (unsigned i = 0; i < kWaitTries; ++i)
-    if (bar_try_wait(bar, parity)) return true;
-  return false;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (bar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
 }
 
 // ---- TMA tensor loads (tile mode), completion counted on an mbarrier ------
