@@ -51,15 +51,15 @@ DECODE_DRAM_RATIO = {
     # decode_stream_kernel, 512 experts, T = 16: 145,702,912 + 3,361,536 B for 87 experts
     "large_fanout_b16": (145_702_912 + 3_361_536) / 145_391_616,
     # grouped path, 512 experts, T = 256 (route, sort, gather, two GEMMs, combine):
-    # 686,300,672 B for 377 experts
-    "large_fanout_b256": 686_300_672 / 630_030_336,
+    # 686,205,184 B for 377 experts
+    "large_fanout_b256": 686_205_184 / 630_030_336,
 }
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of a parity-test layer of this shape "
                   "(current kernel build), scaled to this call by its distinct-expert bytes")
 # Prefill: DRAM bytes of the gate/up and down grouped GEMMs of one layer call
-# from an ncu capture (gate/up 159.48 MB read + 6.29 MB written, down 79.79 +
-# 8.20 MB).
-PREFILL_GEMM_DRAM_BYTES = 253_761_536
+# from an ncu capture (gate/up 159.49 MB read + 5.61 MB written, down 79.79 +
+# 6.74 MB).
+PREFILL_GEMM_DRAM_BYTES = 251_635_456
 
 
 def parse():

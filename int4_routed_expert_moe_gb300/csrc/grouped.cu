@@ -287,53 +287,53 @@ __global__ void __launch_bounds__(kThreadsOf<NPROJ>, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *b.tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {  // codes and scale/zero entries of each item's rows
-      int issued = 0;
-      for (int w = blockIdx.x, li = 0; w < n_items && !is_aborted(b); w += gridDim.x, ++li) {
-        const Item it = item_of(a, w, rblocks);
-        for (int kt = 0; kt < KT; ++kt) {
-          const int g = li * KT + kt, s = g % G::SC;
-          if (g >= G::SC && !tc::bar_wait(&b.c_empty[s], ((g / G::SC) - 1) & 1)) {
-            abort_block(b, a.flags);
-            break;
-          }
-          if (is_aborted(b)) break;
-          uint8_t* st = sm + G::offC + (size_t)s * G::kC;
-          const int k0 = kt * BK;
-          const int gb = (k0 / a.g) / G::kGAlign * G::kGAlign;
-          tc::bar_expect_tx(&b.c_full[s], G::kC);
-          tc::tma_load_3d(st, &map_w, (int)a.q0 + k0 / 2, it.row0, it.slot, &b.c_full[s]);
-          if (NPROJ == 2) tc::tma_load_3d(st + kCodeBytes, &map_w, (int)a.q1 + k0 / 2, it.row0, it.slot, &b.c_full[s]);
-          tc::tma_load_3d(st + NPROJ * kCodeBytes, &map_w, (int)(a.sz + G::kSzEntry * gb), it.row0, it.slot,
-                          &b.c_full[s]);
-          issued = g + 1;
+  if (warp == 0 || warp == 2) {
+    // TMA producers, each a whole warp running its loop (waits, addresses)
+    // with one elected lane issuing the copies: a lone lane's loop loses
+    // issue slots to the expand warps on its scheduler. Warp 0: codes and
+    // scale/zero entries of each item's rows; warp 2: the activation tile of
+    // each step (64 sorted pairs per load).
+    const bool codes = warp == 0;
+    uint64_t* full = codes ? b.c_full : b.x_full;
+    uint64_t* empty = codes ? b.c_empty : b.a_empty;
+    const int S = codes ? G::SC : G::SX;
+    int issued = 0;
+    for (int w = blockIdx.x, li = 0; w < n_items && !__any_sync(0xffffffffu, is_aborted(b)); w += gridDim.x, ++li) {
+      const Item it = item_of(a, w, rblocks);
+      const uint32_t xbytes = (it.n > 64 ? 2u : 1u) * 64u * BK * 2u;
+      bool ok = true;
+      for (int kt = 0; kt < KT; ++kt) {
+        const int g = li * KT + kt, s = g % S;
+        if (g >= S && !tc::bar_wait_warp(&empty[s], ((g / S) - 1) & 1)) {
+          ok = false;
+          break;
         }
-      }
-      if (is_aborted(b)) drain(b.c_full, G::SC, issued);
-    }
-  } else if (warp == 2) {
-    if (lane == 0) {  // activation tile of each item: 64 sorted pairs per load
-      int issued = 0;
-      for (int w = blockIdx.x, li = 0; w < n_items && !is_aborted(b); w += gridDim.x, ++li) {
-        const Item it = item_of(a, w, rblocks);
-        const uint32_t bytes = (it.n > 64 ? 2u : 1u) * 64u * BK * 2u;
-        for (int kt = 0; kt < KT; ++kt) {
-          const int g = li * KT + kt, s = g % G::SX;
-          if (g >= G::SX && !tc::bar_wait(&b.a_empty[s], ((g / G::SX) - 1) & 1)) {
-            abort_block(b, a.flags);
-            break;
+        const int k0 = kt * BK;
+        if (tc::elect_one()) {
+          if (codes) {
+            uint8_t* st = sm + G::offC + (size_t)s * G::kC;
+            const int gb = (int)__umulhi((uint32_t)k0, a.g_magic) / G::kGAlign * G::kGAlign;  // floor(k0 / g), aligned
+            tc::bar_expect_tx(&full[s], G::kC);
+            tc::tma_load_3d(st, &map_w, (int)a.q0 + k0 / 2, it.row0, it.slot, &full[s]);
+            if (NPROJ == 2) tc::tma_load_3d(st + kCodeBytes, &map_w, (int)a.q1 + k0 / 2, it.row0, it.slot, &full[s]);
+            tc::tma_load_3d(st + NPROJ * kCodeBytes, &map_w, (int)(a.sz + G::kSzEntry * gb), it.row0, it.slot,
+                            &full[s]);
+          } else {
+            uint8_t* st = sm + G::offX + (size_t)s * kXBytes;
+            tc::bar_expect_tx(&full[s], xbytes);
+            tc::tma_load_2d(st, &map_b, k0, it.pos0, &full[s]);
+            if (it.n > 64) tc::tma_load_2d(st + 64 * BK * 2, &map_b, k0, it.pos0 + 64, &full[s]);
           }
-          if (is_aborted(b)) break;
-          uint8_t* st = sm + G::offX + (size_t)s * kXBytes;
-          tc::bar_expect_tx(&b.x_full[s], bytes);
-          tc::tma_load_2d(st, &map_b, kt * BK, it.pos0, &b.x_full[s]);
-          if (it.n > 64) tc::tma_load_2d(st + 64 * BK * 2, &map_b, kt * BK, it.pos0 + 64, &b.x_full[s]);
-          issued = g + 1;
         }
+        __syncwarp();
+        issued = g + 1;
       }
-      if (is_aborted(b)) drain(b.x_full, G::SX, issued);
+      if (!ok) {
+        if (lane == 0) abort_block(b, a.flags);
+        break;
+      }
     }
+    if (lane == 0 && is_aborted(b)) drain(full, S, issued);
   } else if (warp == 1 || warp == 3) {
     // Issuing warp p owns accumulator p. Gate/up: the gate (p = 0) or up
     // (p = 1) projection of every item. Down: the items li with li % 2 == p,
@@ -404,7 +404,39 @@ __global__ void __launch_bounds__(kThreadsOf<NPROJ>, 1)
     const int q4 = warp & 3, j4 = (warp - 4) >> 2;
     const int r = 32 * q4 + lane;
     const uint32_t tlane = tmem + ((uint32_t)(32 * q4) << 16);
+    // Gate/up epilogue of item e_li: TMEM lanes of this warp's quarter, the
+    // 16-column chunks j4, j4 + 4, ... of the live columns; then release the
+    // accumulators. Each warp runs it after expanding its first step of the
+    // next item, so the next item's first four steps are ready when the
+    // accumulators are.
+    auto epilogue = [&](const Item& e, int e_li) -> bool {
+      const bool got = tc::bar_wait(&b.acc_full[0], e_li & 1);
+      if (!got) abort_block(b, a.flags);
+      tc::tc_fence_after();
+      const int row = e.row0 + r;
+      const bool live = got && !is_aborted(b) && row < a.rows;
+      for (int c0 = 16 * j4; c0 < e.nmma; c0 += 64) {
+        float gv[16], uv[16];
+        tc::tmem_ld16(tlane + (uint32_t)c0, gv);
+        tc::tmem_ld16(tlane + (uint32_t)(BN + c0), uv);
+        tc::tmem_ld_wait();
+        if (live) {
+          const int prow = (row & ~7) | kperm_pos(row & 7);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < e.n)
+              a.h_sorted[(size_t)(e.pos0 + c0 + j) * a.rows + prow] =
+                  __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&b.acc_empty[0]);
+      return got;
+    };
     bool ok = true;
+    Item prev{};
+    int prev_li = -1;  // item whose epilogue this warp still owes (gate/up)
     for (int w = blockIdx.x, li = 0; w < n_items && ok; w += gridDim.x, ++li) {
       const Item it = item_of(a, w, rblocks);
       const int g0 = li * KT;
@@ -467,36 +499,19 @@ __global__ void __launch_bounds__(kThreadsOf<NPROJ>, 1)
         }
         __syncwarp();
         if (lane == 0) tc::bar_arrive(&b.a_full[sa]);
+        if (NPROJ == 2 && prev_li >= 0) {
+          ok = epilogue(prev, prev_li);
+          prev_li = -1;
+          if (!ok) break;
+        }
       }
       if (!ok) break;
       if (NPROJ == 1) continue;  // the epilogue warps take the down items
-      // Epilogue of this item: TMEM lanes of this warp's quarter, the
-      // 16-column chunks ci = j4, j4 + 4, ... of the live columns; then
-      // release the accumulators.
-      const bool got = tc::bar_wait(&b.acc_full[0], li & 1);
-      if (!got) abort_block(b, a.flags);
-      tc::tc_fence_after();
-      const int row = it.row0 + r;
-      const bool live = got && !is_aborted(b) && row < a.rows;
-      for (int c0 = 16 * j4; c0 < it.nmma; c0 += 64) {
-        float gv[16], uv[16];
-        tc::tmem_ld16(tlane + (uint32_t)c0, gv);
-        tc::tmem_ld16(tlane + (uint32_t)(BN + c0), uv);
-        tc::tmem_ld_wait();
-        if (live) {
-          const int prow = (row & ~7) | kperm_pos(row & 7);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < it.n)
-              a.h_sorted[(size_t)(it.pos0 + c0 + j) * a.rows + prow] =
-                  __float2half_rn(silu_fast(gv[j] * kInvAScale) * (uv[j] * kInvAScale));
-        }
-      }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::bar_arrive(&b.acc_empty[0]);
-      if (!got) break;
+      if (prev_li >= 0 && !(ok = epilogue(prev, prev_li))) break;  // this warp had no step in item li
+      prev = it;
+      prev_li = li;
     }
+    if (NPROJ == 2 && ok && prev_li >= 0) epilogue(prev, prev_li);
   } else if (NPROJ == 1) {
     // Down epilogue (warps 20..23): warp q owns the TMEM lanes of quarter q.
     // Per item: the output pair index of each column (lane l holds columns

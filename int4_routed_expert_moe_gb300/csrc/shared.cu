@@ -46,27 +46,32 @@ struct SharedParams {
 };
 
 // Producer: per K step the weight tile(s) at row0 and the token tile at tok0.
+// The whole warp runs the loop and one elected lane issues the copies.
 template <int NW, int STAGES>
 __device__ __forceinline__ void produce_tiles(const tc::Ctrl& c, uint8_t* sm, uint32_t stage_bytes,
                                               uint32_t tok_bytes, const CUtensorMap* w0, const CUtensorMap* w1,
                                               const CUtensorMap* tok, int row0, int tok0, int KT, int32_t* flags) {
+  const int lane = threadIdx.x & 31;
   int issued = 0;
   for (int kt = 0; kt < KT; ++kt) {
     const int s = kt % STAGES;
-    if (kt >= STAGES && !tc::bar_wait(&c.empty[s], ((kt / STAGES) - 1) & 1)) {
-      tc::set_abort(c, flags);
+    if (kt >= STAGES && !tc::bar_wait_warp(&c.empty[s], ((kt / STAGES) - 1) & 1)) {
+      if (lane == 0) tc::set_abort(c, flags);
       break;
     }
-    if (tc::aborted(c)) break;
+    if (__any_sync(0xffffffffu, tc::aborted(c))) break;
     uint8_t* st = sm + (size_t)s * stage_bytes;
     const int k0 = kt * BK;
-    tc::bar_expect_tx(&c.tma_full[s], NW * kWTile + tok_bytes);
-    tc::tma_load_2d(st, w0, k0, row0, &c.tma_full[s]);
-    if (NW == 2) tc::tma_load_2d(st + kWTile, w1, k0, row0, &c.tma_full[s]);
-    tc::tma_load_2d(st + NW * kWTile, tok, k0, tok0, &c.tma_full[s]);
+    if (tc::elect_one()) {
+      tc::bar_expect_tx(&c.tma_full[s], NW * kWTile + tok_bytes);
+      tc::tma_load_2d(st, w0, k0, row0, &c.tma_full[s]);
+      if (NW == 2) tc::tma_load_2d(st + kWTile, w1, k0, row0, &c.tma_full[s]);
+      tc::tma_load_2d(st + NW * kWTile, tok, k0, tok0, &c.tma_full[s]);
+    }
+    __syncwarp();
     issued = kt + 1;
   }
-  if (tc::aborted(c)) tc::drain_loads(c, STAGES, issued);
+  if (lane == 0 && tc::aborted(c)) tc::drain_loads(c, STAGES, issued);
 }
 
 __device__ __forceinline__ void setup_bars(const tc::Ctrl& c, int stages) {
@@ -104,8 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *c.tmem_slot;
   if (warp == 0) {
-    if (lane == 0)
-      produce_tiles<2, kGuStages>(c, sm, kGuStage, kGuN * BK * 2, &map_wg, &map_wu, &map_x, row0, tok0, KT, a.flags);
+    produce_tiles<2, kGuStages>(c, sm, kGuStage, kGuN * BK * 2, &map_wg, &map_wu, &map_x, row0, tok0, KT, a.flags);
   } else if (warp == 1 || warp == 3) {
     // Issuer p: the gate (p = 0) or up (p = 1) projection. The whole warp
     // runs the loop, one elected lane issues.
@@ -176,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *c.tmem_slot;
   if (warp == 0) {
-    if (lane == 0)
-      produce_tiles<1, kDnStages>(c, sm, kDnStage, kDnN * BK * 2, &map_wd, nullptr, &map_h, row0, tok0, KT, a.flags);
+    produce_tiles<1, kDnStages>(c, sm, kDnStage, kDnN * BK * 2, &map_wd, nullptr, &map_h, row0, tok0, KT, a.flags);
   } else if (warp == 1 || warp == 3) {
     // Issuer p: the K slices kk = p, p + 2 of every step, into accumulator p.
     // The whole warp runs the loop, one elected lane issues.
