@@ -255,9 +255,8 @@ int moe_layer_forward(const moe_expert_shape* shape, const void* x, const float*
 /* ---- routed layer without any device allocation --------------------------
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory: plugins and serving runtimes whose host
- * framework owns every device allocation and forbids extra ones, deployments
- * with a fixed, pre-planned memory budget, and code running inside another
- * component's CUDA stream capture, where cudaMalloc is not permitted.
+ * framework owns every device allocation and forbids extra ones, and
+ * deployments with a fixed, pre-planned memory budget.
  * Same arguments and result as moe_layer_forward on the MOE_PATH_GEMV path,
  * minus the workspace: the scratch it needs (a header with the error word and
  * the kernel's counters, then the FP16 SwiGLU intermediate of every
@@ -270,10 +269,10 @@ int moe_layer_forward(const moe_expert_shape* shape, const void* x, const float*
  * below come first); H <= 4096, inter <= 2048, T <= 16, T*k <= 256 and
  * E <= 1024 (the streamed decode kernel), else MOE_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture. The cached address belongs to the device's current
- * context: after cudaDeviceReset the library must be reloaded (or the process
- * restarted) before this call is used again on that device.
+ * (cudaGetSymbolAddress) and caches it. The cached address belongs to the
+ * device's current context: after cudaDeviceReset the library must be
+ * reloaded (or the process restarted) before this call is used again on that
+ * device. Nothing is stated here about capturing this call in a CUDA graph.
  * Every call shares the one array: calls that overlap on the GPU (different
  * streams, or other threads) race and corrupt each other's results; order
  * them on one stream. Each call keeps its error word (bit 0: an id without a

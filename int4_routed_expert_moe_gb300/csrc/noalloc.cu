@@ -1,10 +1,8 @@
 // A routed-layer entry point for callers that cannot allocate device memory.
 //
 // moe_layer_forward needs a caller-provided workspace. Some callers cannot
-// provide one: code that runs inside another component's CUDA stream
-// capture (cudaMalloc is not permitted while a stream is being captured),
-// plugins and serving runtimes whose host framework owns every device
-// allocation and forbids extra ones, and deployments with a fixed,
+// provide one: plugins and serving runtimes whose host framework owns every
+// device allocation and forbids extra ones, and deployments with a fixed,
 // pre-planned memory budget. moe_layer_forward_noalloc serves them from a
 // fixed scratch array compiled into the library.
 #include <mutex>

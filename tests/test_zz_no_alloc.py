@@ -1,9 +1,9 @@
 """moe_layer_forward_noalloc against moe_layer_forward (needs a GB300).
 
 The no-allocation entry point serves callers that cannot allocate device
-memory (inside another component's stream capture, under a host framework
-that owns all allocations, or with a fixed memory budget): its scratch is a
-fixed array inside the library instead of a caller workspace. Two calls in
+memory (under a host framework that owns all allocations, or with a fixed
+memory budget): its scratch is a fixed array inside the library instead of
+a caller workspace. Two calls in
 a row on different inputs must each match the workspace entry point within
 the tolerance the parity tests use. This file is collected last so that a
 failure here comes after every other test has run."""
