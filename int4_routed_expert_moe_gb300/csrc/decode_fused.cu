@@ -1191,7 +1191,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_stream_kernel(const Stream
 }
 
 // ---- host side ----------------------------------------------------------------
-constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 int g_num_sms[kMaxDevices] = {0};
 // Per device: the largest dynamic shared memory already granted to each kernel
@@ -1309,6 +1308,8 @@ bool carve(StreamParams& a) {
 }
 
 }  // namespace
+
+int current_device_sms(int* dev, int* sms) { return device_sms(dev, sms); }
 
 size_t fused_workspace_bytes(int H, int I, int T, int k) {
   (void)H;

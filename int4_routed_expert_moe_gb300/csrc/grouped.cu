@@ -683,17 +683,9 @@ GroupedWs grouped_ws(int H, int I, int T, int k, int E) {
   return w;
 }
 
-bool g_attr_done = false;
-int g_num_sms = 0;
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      g_num_sms = -1;
-  }
-  return g_num_sms;
-}
+// Per device: the GEMM kernels' shared-memory attribute has been set.
+std::mutex g_attr_mutex;
+bool g_attr_set[kMaxDevices] = {};
 
 }  // namespace
 
@@ -765,12 +757,17 @@ int grouped_forward(const ForwardArgs& a) {
                                 CU_TENSOR_MAP_SWIZZLE_128B)) != MOE_OK)
       return rc;
   }
-  if (!g_attr_done) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)Geo<2>::smem));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)Geo<1>::smem));
-    g_attr_done = true;
+  int dev = 0, n_sm = 0;
+  if ((rc = current_device_sms(&dev, &n_sm)) != MOE_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    if (!g_attr_set[dev]) {
+      MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Geo<2>::smem));
+      MOE_CUDA_TRY(cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Geo<1>::smem));
+      g_attr_set[dev] = true;
+    }
   }
   GemmParams gp = {};
   gp.tiles = tiles;
@@ -788,8 +785,6 @@ int grouped_forward(const ForwardArgs& a) {
   gu.q1 = a.off.gu_q_up;
   gu.sz = a.off.gu_sz;
   gu.h_sorted = hs;
-  const int n_sm = num_sms();
-  if (n_sm <= 0) return fail(MOE_ERR_CUDA, "device query failed");
   const int gu_items = ((a.I + BM - 1) / BM) * w.max_tiles, dn_items = ((a.H + BM - 1) / BM) * w.max_tiles;
   grouped_gemm_kernel<2><<<std::min(n_sm, gu_items), kThreadsOf<2>, Geo<2>::smem, st>>>(m_gu, m_x, gu);
   if ((rc = check_launch("grouped gate/up GEMM")) != MOE_OK) return rc;

@@ -75,6 +75,11 @@ struct SortTiles {
 int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
                       int32_t* pair_tok, int32_t* pair_j, cudaStream_t st, const SortTiles* tiles);
 
+// The current device's index and SM count (the count cached per device).
+// MOE_OK, or an error status for a failed query or an index >= kMaxDevices.
+constexpr int kMaxDevices = 64;
+int current_device_sms(int* dev, int* sms);
+
 // Fused one-kernel decode path (persistent, one block per SM).
 size_t fused_workspace_bytes(int H, int I, int T, int k);
 int fused_forward(const ForwardArgs& a);

@@ -12,6 +12,7 @@
 //   2. down: per (128 rows of H, 128 tokens) two accumulators over the even
 //      and odd 16-element K slices, added in the epilogue; y stored as FP16.
 #include <algorithm>
+#include <mutex>
 
 #include "common.h"
 #include "device.cuh"
@@ -229,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::gemm_teardown(tmem, 2 * kDnN);
 }
 
-bool g_attr_done = false;
+// Per device: the kernels' shared-memory attribute has been set.
+std::mutex g_attr_mutex;
+bool g_attr_set[kMaxDevices] = {};
 
 int fp16_map(CUtensorMap* m, const void* base, int inner, int outer, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)inner, (uint64_t)outer};
@@ -275,12 +278,17 @@ extern "C" int moe_shared_forward(const void* x, int T, int H, int Is, const voi
   if ((rc = moe::fp16_map(&m_x, x, H, T, moe::kGuN)) != MOE_OK) return rc;
   if ((rc = moe::fp16_map(&m_wd, wd, Is, H, moe::BM)) != MOE_OK) return rc;
   if ((rc = moe::fp16_map(&m_h, h, Is, T, moe::kDnN)) != MOE_OK) return rc;
-  if (!moe::g_attr_done) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(moe::shared_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)moe::kGuSmem));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(moe::shared_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)moe::kDnSmem));
-    moe::g_attr_done = true;
+  int dev = 0, n_sm = 0;
+  if ((rc = moe::current_device_sms(&dev, &n_sm)) != MOE_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lock(moe::g_attr_mutex);
+    if (!moe::g_attr_set[dev]) {
+      MOE_CUDA_TRY(cudaFuncSetAttribute(moe::shared_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)moe::kGuSmem));
+      MOE_CUDA_TRY(cudaFuncSetAttribute(moe::shared_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)moe::kDnSmem));
+      moe::g_attr_set[dev] = true;
+    }
   }
   moe::SharedParams p;
   p.T = T;

@@ -14,6 +14,8 @@
 // (a warp multisplit), and a lane's rank is the number of them below it, so
 // the order is stable. The ids of the first kCachedRounds chunks of a segment
 // stay in registers between the passes.
+#include <mutex>
+
 #include "common.h"
 #include "device.cuh"
 #include "kernels.h"
@@ -203,8 +205,21 @@ int launch_token_sort(const int32_t* ids, int P, int k, int E, int32_t* offsets,
                       int32_t* pair_tok, int32_t* pair_j, cudaStream_t st, const SortTiles* tiles) {
   const size_t smem =
       (size_t)(kSortWarps * E + 2 * E + 1 + 2 * kSortWarps + (P <= kStagedPairs ? 2 * P : 0)) * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort smem attr: %s", cudaGetErrorString(e));
+  int dev = 0, n_sm = 0;
+  int rc = current_device_sms(&dev, &n_sm);
+  if (rc != MOE_OK) return rc;
+  cudaError_t e;
+  {
+    // Per device, the largest dynamic shared memory granted so far.
+    static std::mutex mu;
+    static int granted[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (granted[dev] < (int)smem) {
+      e = cudaFuncSetAttribute(token_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "token_sort smem attr: %s", cudaGetErrorString(e));
+      granted[dev] = (int)smem;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(kSortWarps * 32);
