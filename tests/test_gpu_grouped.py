@@ -52,6 +52,8 @@ def test_grouped_tiny_layer(zero, shared):
     ((320, 192, 64), 4, 2, 150),     # H and I not multiples of 128 (partial row blocks), odd group count
     ((256, 128, 32), 2, 1, 300),     # g = 32 (two groups per K step); ~150 pairs per expert: two tiles
     ((1024, 512, 128), 8, 2, 513),   # tiles of 128 and ragged tails
+    ((128, 256, 64), 8, 2, 100),     # 2 gate/up K steps per item: some expand warps own no step of an item
+    ((192, 128, 64), 4, 2, 90),      # 3 gate/up K steps, 2 down K steps per item
     ((2048, 1408, 128), 8, 4, 96),   # Qwen-like expert shape: 11 row blocks of 128, down K of 22 steps
 ])
 def test_grouped_shapes(shape, E, k, T):
